@@ -1,0 +1,533 @@
+/*
+ * oracle.c -- plain fp64 CPU restatement of attention-score-driven prompt
+ * KV-cache compression (SnapKV observation-window scoring, ZigZagKV MBA /
+ * LMBA layer budgets, per-head top-K, K/V compaction, ThinK key-channel
+ * magnitude pruning).
+ *
+ * TEST INFRASTRUCTURE ONLY.  The test-suite, the package smoke check and the
+ * benchmark's CPU-baseline leg call this file; the CUDA library neither links
+ * nor calls it and the two share no code.  It is deliberately slow and
+ * direct: one loop per definition, library qsort for sorting, no blocking.
+ *
+ * Sources (page title, section):
+ *  [SNAP]       ZigZagKV/SnapKV blog post "ZigZagKV, KVCache 80% compression
+ *               near-lossless" (dis.qidao123.com), section "SnapKV": the last
+ *               window's queries score every prefix token, the scores are
+ *               averaged over the window rows per head, each head keeps its
+ *               top-K prefix tokens plus every token of the last window.
+ *  [ZZ-MBA]     same post, section "ZigZagKV's new observations": MBA is the
+ *               fewest KV entries whose attention reaches 90% of the total
+ *               attention score over the n tokens in the cache; LMBA is the
+ *               mean of MBA over the heads of a layer.
+ *  [ZZ-ALLOC]   same post, section "ZigZagKV space allocation": the total
+ *               budget is split across layers in proportion to LMBA, with a
+ *               minimum size reserved for every layer.
+ *  [ZZ-SEL]     same post, section "ZigZagKV token selection": selection is
+ *               SnapKV's, with each head's K set by its quota.
+ *  [THINK-ATT]  "ThinK: Thinner Key Cache by Query-Driven Pruning", section
+ *               "Method details", attention equation softmax(Q K^T / sqrt(D)) V.
+ *  [THINK-MAG]  same page, "Magnitude-based pruning": M_{n,d} = ||K[n,:,d]||_p;
+ *               keep floor((1-lambda) D) channels per head, Top_T of M.
+ *  [THINK-IMPL] same page, "Implementation of THINK": recent tokens are not
+ *               pruned.
+ *
+ * Readings where the pages are silent or garbled:
+ *  - GQA: query head h belongs to KV head h / G (G = H_q / H_kv); the score
+ *    of a KV head is the mean over its G query heads and W window rows.
+ *  - Causal mask inside the window: window row i sits at position P+i
+ *    (P = T-W) and sees keys 0..P+i.
+ *  - MBA is taken per KV head over all T scores (prefix and window); the
+ *    mass is exact fixed point u_j = floor(c_j * 2^56) and "reaches" means
+ *    den * (sum of the m largest u) >= num * (sum of all u).
+ *  - Budgets count prefix tokens only; the W window rows are always kept.
+ *  - Split: B_l = floor + largest-remainder share of (total - L*floor) by
+ *    S_l = sum_k MBA_{l,k} (LMBA up to the common factor H_kv), ties to the
+ *    lower layer; budgets above the prefix length P are capped and the excess
+ *    is re-split over the uncapped layers until none exceeds P.
+ *  - Top-K ties go to the lower token index; kept rows are written in
+ *    ascending position order, then the window rows in order.
+ *  - ThinK uses p = 2 over the kept prefix rows only (window rows stay
+ *    full width); channel ties go to the lower channel index.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+    int32_t n_layers, n_q_heads, n_kv_heads, head_dim, seq_len, window;
+    int32_t dtype; /* 0: fp32, 1: bf16 */
+} ora_shape;
+
+int ora_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void ora_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* Exact widening of one stored element to fp64. bf16 is the top half of an
+ * IEEE binary32, so shifting it up 16 bits gives the identical value. */
+static double ora_elem(const void *base, int64_t i, int dtype)
+{
+    if (dtype == 0) return (double)((const float *)base)[i];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static int ora_shape_ok(const ora_shape *s)
+{
+    if (!s) return 0;
+    if (s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1) return 0;
+    if (s->n_q_heads % s->n_kv_heads) return 0;
+    if (s->head_dim < 1 || s->window < 1 || s->seq_len <= s->window) return 0;
+    if (s->dtype != 0 && s->dtype != 1) return 0;
+    return 1;
+}
+
+/* ---------------------------------------------------------------------------
+ * a1. Observation-window score of one (layer, KV head)   [SNAP], [THINK-ATT]
+ *
+ * For every query head h of the group and window row i (position t = P+i):
+ *   x_j = (q_{h,i} . k_j) / sqrt(D)              for j = 0..t
+ *   p_j = exp(x_j - max x) / sum_{j'<=t} exp(x_j' - max x)
+ *   c_j += p_j / (G * W)
+ * so c is the mean attention row over the G*W window queries; c sums to 1.
+ * ------------------------------------------------------------------------- */
+int ora_score_unit(const ora_shape *s, const void *q, const void *k,
+                   int layer, int kv_head, double *c)
+{
+    if (!ora_shape_ok(s) || layer < 0 || layer >= s->n_layers ||
+        kv_head < 0 || kv_head >= s->n_kv_heads)
+        return -1;
+    const int64_t D = s->head_dim, T = s->seq_len, W = s->window;
+    const int64_t Hq = s->n_q_heads, Hkv = s->n_kv_heads, G = Hq / Hkv;
+    const int64_t P = T - W;
+    const double rows = (double)(G * W);
+    const double root_d = sqrt((double)D);
+    const int64_t k_base = ((int64_t)layer * Hkv + kv_head) * T * D;
+    double *x = (double *)malloc(sizeof(double) * (size_t)T);
+    double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!x || !qr) { free(x); free(qr); return -2; }
+    for (int64_t j = 0; j < T; ++j) c[j] = 0.0;
+    for (int64_t g = 0; g < G; ++g) {
+        const int64_t h = (int64_t)kv_head * G + g;
+        for (int64_t i = 0; i < W; ++i) {
+            const int64_t q_base = (((int64_t)layer * Hq + h) * W + i) * D;
+            for (int64_t d = 0; d < D; ++d) qr[d] = ora_elem(q, q_base + d, s->dtype);
+            const int64_t t = P + i;
+            double mu = -INFINITY;
+            for (int64_t j = 0; j <= t; ++j) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d)
+                    dot += qr[d] * ora_elem(k, k_base + j * D + d, s->dtype);
+                x[j] = dot / root_d;
+                if (x[j] > mu) mu = x[j];
+            }
+            double z = 0.0;
+            for (int64_t j = 0; j <= t; ++j) {
+                x[j] = exp(x[j] - mu);
+                z += x[j];
+            }
+            for (int64_t j = 0; j <= t; ++j) c[j] += x[j] / z / rows;
+        }
+    }
+    free(x);
+    free(qr);
+    return 0;
+}
+
+/* a1 over all (layer, KV head) units; scores laid out [L][H_kv][T]. */
+int ora_score(const ora_shape *s, const void *q, const void *k, double *scores)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t units = (int64_t)s->n_layers * s->n_kv_heads;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t u = 0; u < units; ++u) {
+        int l = (int)(u / s->n_kv_heads), h = (int)(u % s->n_kv_heads);
+        if (ora_score_unit(s, q, k, l, h, scores + u * s->seq_len) != 0) bad = 1;
+    }
+    return bad ? -2 : 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * a2. MBA of one head                                        [ZZ-MBA]
+ *
+ * Mass in exact fixed point: u_j = floor(c_j * 2^56) (c_j in [0,1]).  With the
+ * u sorted in descending order and U = sum u, MBA is the smallest m with
+ *   den * sum_{r<m} u_(r) >= num * U        (num/den = 9/10 on the pages).
+ * Returns -1 for a score outside [0,1] or NaN.
+ * ------------------------------------------------------------------------- */
+static int ora_cmp_u64_desc(const void *a, const void *b)
+{
+    uint64_t x = *(const uint64_t *)a, y = *(const uint64_t *)b;
+    return (x < y) - (x > y);
+}
+
+int64_t ora_mba(int64_t n, const double *c, uint32_t num, uint32_t den)
+{
+    if (n < 0 || den == 0 || num > den) return -1;
+    uint64_t *u = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(n ? n : 1));
+    if (!u) return -2;
+    for (int64_t j = 0; j < n; ++j) {
+        if (!(c[j] >= 0.0 && c[j] <= 1.0)) { free(u); return -1; }
+        u[j] = (uint64_t)floor(ldexp(c[j], 56));
+    }
+    qsort(u, (size_t)n, sizeof(uint64_t), ora_cmp_u64_desc);
+    unsigned __int128 total = 0;
+    for (int64_t j = 0; j < n; ++j) total += u[j];
+    const unsigned __int128 need = (unsigned __int128)num * total;
+    unsigned __int128 run = 0;
+    int64_t m = 0;
+    while ((unsigned __int128)den * run < need) {
+        run += u[m];
+        ++m;
+    }
+    free(u);
+    return m;
+}
+
+int ora_mba_all(const ora_shape *s, const double *scores, uint32_t num, uint32_t den,
+                int32_t *mba)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t units = (int64_t)s->n_layers * s->n_kv_heads;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t u = 0; u < units; ++u) {
+        int64_t m = ora_mba(s->seq_len, scores + u * s->seq_len, num, den);
+        if (m < 0) bad = 1;
+        mba[u] = (int32_t)m;
+    }
+    return bad ? -1 : 0;
+}
+
+/* Same as ora_mba_all on fp32 scores (widened exactly). */
+int ora_mba_all_f32(const ora_shape *s, const float *scores, uint32_t num, uint32_t den,
+                    int32_t *mba)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t n = (int64_t)s->n_layers * s->n_kv_heads * s->seq_len;
+    double *c = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!c) return -2;
+    for (int64_t i = 0; i < n; ++i) c[i] = (double)scores[i];
+    int r = ora_mba_all(s, c, num, den, mba);
+    free(c);
+    return r;
+}
+
+/* ---------------------------------------------------------------------------
+ * a3. Layer budgets                                          [ZZ-ALLOC]
+ *
+ * Largest-remainder split of R units over the eligible entries in proportion
+ * to w (equal weights if the eligible weights sum to zero).  Each entry gets
+ * floor(R w_l / sum w); the units left over go one each to the largest
+ * remainders R w_l mod sum w, ties to the lower index.
+ * ------------------------------------------------------------------------- */
+static void ora_split(int n, const int64_t *w, const unsigned char *eligible,
+                      int64_t R, int64_t *add)
+{
+    int64_t sumw = 0;
+    int any = 0;
+    for (int l = 0; l < n; ++l)
+        if (eligible[l]) { sumw += w[l]; any = 1; }
+    for (int l = 0; l < n; ++l) add[l] = 0;
+    if (!any || R <= 0) return;
+    const int equal = (sumw == 0);
+    if (equal)
+        for (int l = 0; l < n; ++l) sumw += eligible[l] ? 1 : 0;
+    int64_t *rem = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+    unsigned char *given = (unsigned char *)calloc((size_t)n, 1);
+    int64_t handed = 0;
+    for (int l = 0; l < n; ++l) {
+        rem[l] = -1;
+        if (!eligible[l]) continue;
+        const __int128 prod = (__int128)R * (equal ? 1 : w[l]);
+        add[l] = (int64_t)(prod / sumw);
+        rem[l] = (int64_t)(prod % sumw);
+        handed += add[l];
+    }
+    for (int64_t left = R - handed; left > 0; --left) {
+        int best = -1;
+        for (int l = 0; l < n; ++l)
+            if (eligible[l] && !given[l] && (best < 0 || rem[l] > rem[best])) best = l;
+        given[best] = 1;
+        add[best] += 1;
+    }
+    free(rem);
+    free(given);
+}
+
+/* mba: [L][H_kv]; budget: [L].  Returns -1 for invalid arguments. */
+int ora_budget(int L, int Hkv, const int32_t *mba, int64_t prefix, int64_t total,
+               int64_t floor_, int32_t *budget)
+{
+    if (L < 1 || Hkv < 1 || prefix < 1 || floor_ < 0 || floor_ > prefix ||
+        total < (int64_t)L * floor_)
+        return -1;
+    if (total >= (int64_t)L * prefix) {
+        for (int l = 0; l < L; ++l) budget[l] = (int32_t)prefix;
+        return 0;
+    }
+    int64_t *S = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    int64_t *B = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    int64_t *add = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    unsigned char *elig = (unsigned char *)malloc((size_t)L);
+    for (int l = 0; l < L; ++l) {
+        S[l] = 0;
+        for (int k = 0; k < Hkv; ++k) S[l] += mba[(int64_t)l * Hkv + k];
+        elig[l] = 1;
+    }
+    ora_split(L, S, elig, total - (int64_t)L * floor_, add);
+    for (int l = 0; l < L; ++l) B[l] = floor_ + add[l];
+    for (;;) {
+        int64_t excess = 0;
+        for (int l = 0; l < L; ++l)
+            if (B[l] > prefix) { excess += B[l] - prefix; B[l] = prefix; }
+        if (excess == 0) break;
+        for (int l = 0; l < L; ++l) elig[l] = (unsigned char)(B[l] < prefix);
+        ora_split(L, S, elig, excess, add);
+        for (int l = 0; l < L; ++l) B[l] += add[l];
+    }
+    for (int l = 0; l < L; ++l) budget[l] = (int32_t)B[l];
+    free(S); free(B); free(add); free(elig);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * a4. Per-head top-K of the prefix                           [SNAP], [ZZ-SEL]
+ *
+ * Order the prefix positions by (score descending, position ascending), keep
+ * the first min(B, P), and return them in ascending position order.
+ * ------------------------------------------------------------------------- */
+typedef struct { double v; int64_t j; } ora_item;
+
+static int ora_cmp_item(const void *a, const void *b)
+{
+    const ora_item *x = (const ora_item *)a, *y = (const ora_item *)b;
+    if (x->v != y->v) return (x->v < y->v) ? 1 : -1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+static int ora_cmp_i32(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+static int64_t ora_kept(int64_t budget, int64_t prefix)
+{
+    return budget < 0 ? 0 : (budget > prefix ? prefix : budget);
+}
+
+int64_t ora_topk(int64_t P, const double *c, int64_t B, int32_t *idx)
+{
+    const int64_t n = ora_kept(B, P);
+    ora_item *it = (ora_item *)malloc(sizeof(ora_item) * (size_t)(P ? P : 1));
+    if (!it) return -2;
+    for (int64_t j = 0; j < P; ++j) { it[j].v = c[j]; it[j].j = j; }
+    qsort(it, (size_t)P, sizeof(ora_item), ora_cmp_item);
+    for (int64_t r = 0; r < n; ++r) idx[r] = (int32_t)it[r].j;
+    qsort(idx, (size_t)n, sizeof(int32_t), ora_cmp_i32);
+    free(it);
+    return n;
+}
+
+/* idx: [L][H_kv][k_max]; entries past the kept count are left untouched. */
+int ora_topk_all(const ora_shape *s, const double *scores, const int32_t *budget,
+                 int64_t k_max, int32_t *idx)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t T = s->seq_len, P = T - s->window, Hkv = s->n_kv_heads;
+    for (int l = 0; l < s->n_layers; ++l)
+        if (ora_kept(budget[l], P) > k_max) return -1;
+    const int64_t units = (int64_t)s->n_layers * Hkv;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t u = 0; u < units; ++u) {
+        if (ora_topk(P, scores + u * T, budget[u / Hkv], idx + u * k_max) < 0) bad = 1;
+    }
+    return bad ? -2 : 0;
+}
+
+int ora_topk_all_f32(const ora_shape *s, const float *scores, const int32_t *budget,
+                     int64_t k_max, int32_t *idx)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t n = (int64_t)s->n_layers * s->n_kv_heads * s->seq_len;
+    double *c = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!c) return -2;
+    for (int64_t i = 0; i < n; ++i) c[i] = (double)scores[i];
+    int r = ora_topk_all(s, c, budget, k_max, idx);
+    free(c);
+    return r;
+}
+
+/* ---------------------------------------------------------------------------
+ * a5. Compaction                                             [SNAP]
+ *
+ * Layer l of the output holds [H_kv][n_l + W][D] with n_l = min(B_l, P): the
+ * kept prefix rows in ascending position order, then the W window rows.
+ * Layers follow each other; layer l starts at row H_kv * sum_{l'<l}(n_l'+W).
+ * Returns the number of rows written per tensor, or -1.
+ * ------------------------------------------------------------------------- */
+int64_t ora_compact_rows(const ora_shape *s, const int32_t *budget)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t P = (int64_t)s->seq_len - s->window;
+    int64_t rows = 0;
+    for (int l = 0; l < s->n_layers; ++l)
+        rows += (int64_t)s->n_kv_heads * (ora_kept(budget[l], P) + s->window);
+    return rows;
+}
+
+int64_t ora_compact(const ora_shape *s, const void *src, const int32_t *idx,
+                    const int32_t *budget, int64_t k_max, void *out)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t T = s->seq_len, W = s->window, P = T - W, Hkv = s->n_kv_heads;
+    const size_t row_bytes = (size_t)s->head_dim * (s->dtype == 0 ? 4 : 2);
+    const unsigned char *in = (const unsigned char *)src;
+    unsigned char *o = (unsigned char *)out;
+    int64_t row = 0;
+    for (int l = 0; l < s->n_layers; ++l) {
+        const int64_t n = ora_kept(budget[l], P);
+        if (n > k_max) return -1;
+        for (int64_t h = 0; h < Hkv; ++h) {
+            const int64_t head = (int64_t)l * Hkv + h;
+            const int32_t *sel = idx + head * k_max;
+            for (int64_t r = 0; r < n + W; ++r) {
+                const int64_t t = r < n ? (int64_t)sel[r] : P + (r - n);
+                if (t < 0 || t >= T) return -1;
+                memcpy(o + (size_t)row * row_bytes, in + (size_t)(head * T + t) * row_bytes,
+                       row_bytes);
+                ++row;
+            }
+        }
+    }
+    return row;
+}
+
+/* ---------------------------------------------------------------------------
+ * a6. ThinK magnitude channel pruning                        [THINK-MAG]
+ *
+ * keep = floor((1 - lambda) * D).  Per (layer, KV head): M_d = sum over the
+ * n_l kept prefix rows of K_out[r][d]^2 (the squared l2 norm ranks the same
+ * channels as the norm), order channels by (M desc, d asc), keep the first
+ * `keep`, list them ascending, and copy those channels of the kept prefix
+ * rows into K_pruned.  The window rows are left full width [THINK-IMPL].
+ * K_pruned layer l holds [H_kv][n_l][keep] starting at element
+ * H_kv * keep * sum_{l'<l} n_l'.
+ * ------------------------------------------------------------------------- */
+int32_t ora_keep_channels(double lambda, int32_t D)
+{
+    return (int32_t)floor((1.0 - lambda) * (double)D);
+}
+
+typedef struct { double m; int32_t d; } ora_chan;
+
+static int ora_cmp_chan(const void *a, const void *b)
+{
+    const ora_chan *x = (const ora_chan *)a, *y = (const ora_chan *)b;
+    if (x->m != y->m) return (x->m < y->m) ? 1 : -1;
+    return (x->d > y->d) - (x->d < y->d);
+}
+
+int ora_channel_prune(const ora_shape *s, const void *k_out, const int32_t *budget,
+                      double lambda, int32_t *chan, double *norms, void *k_pruned)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t D = s->head_dim, W = s->window, P = (int64_t)s->seq_len - W;
+    const int64_t Hkv = s->n_kv_heads, L = s->n_layers;
+    const int32_t keep = ora_keep_channels(lambda, (int32_t)D);
+    if (keep < 1 || keep > D) return -1;
+    const size_t es = s->dtype == 0 ? 4 : 2;
+    int64_t *in_row = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    int64_t *out_el = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    int64_t ir = 0, oe = 0;
+    for (int64_t l = 0; l < L; ++l) {
+        in_row[l] = ir;
+        out_el[l] = oe;
+        const int64_t n = ora_kept(budget[l], P);
+        ir += Hkv * (n + W);
+        oe += Hkv * n * keep;
+    }
+    const int64_t units = L * Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < units; ++u) {
+        const int64_t l = u / Hkv, h = u % Hkv;
+        const int64_t n = ora_kept(budget[l], P);
+        const int64_t row0 = in_row[l] + h * (n + W);
+        ora_chan *ch = (ora_chan *)malloc(sizeof(ora_chan) * (size_t)D);
+        for (int64_t d = 0; d < D; ++d) {
+            double m = 0.0;
+            for (int64_t r = 0; r < n; ++r) {
+                const double x = ora_elem(k_out, (row0 + r) * D + d, s->dtype);
+                m += x * x;
+            }
+            ch[d].m = m;
+            ch[d].d = (int32_t)d;
+            if (norms) norms[u * D + d] = m;
+        }
+        qsort(ch, (size_t)D, sizeof(ora_chan), ora_cmp_chan);
+        int32_t *sel = chan + u * keep;
+        for (int32_t i = 0; i < keep; ++i) sel[i] = ch[i].d;
+        qsort(sel, (size_t)keep, sizeof(int32_t), ora_cmp_i32);
+        if (k_pruned) {
+            const unsigned char *src = (const unsigned char *)k_out;
+            unsigned char *dst = (unsigned char *)k_pruned;
+            const int64_t o0 = out_el[l] + h * n * keep;
+            for (int64_t r = 0; r < n; ++r)
+                for (int32_t i = 0; i < keep; ++i)
+                    memcpy(dst + (size_t)(o0 + r * keep + i) * es,
+                           src + (size_t)((row0 + r) * D + sel[i]) * es, es);
+        }
+        free(ch);
+    }
+    free(in_row);
+    free(out_el);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * The whole path for one prompt: score -> MBA -> budgets -> top-K -> compact
+ * (-> channel prune when lambda >= 0).  Output buffers as above; scores are
+ * returned in fp64.  Returns 0, or a negative code from the failing step.
+ * ------------------------------------------------------------------------- */
+int ora_compress(const ora_shape *s, const void *q, const void *k, const void *v,
+                 uint32_t num, uint32_t den, int64_t total, int64_t floor_,
+                 double lambda, int64_t k_max,
+                 double *scores, int32_t *mba, int32_t *budget, int32_t *idx,
+                 void *k_out, void *v_out, int32_t *chan, void *k_pruned)
+{
+    int r;
+    if ((r = ora_score(s, q, k, scores)) != 0) return r;
+    if ((r = ora_mba_all(s, scores, num, den, mba)) != 0) return r;
+    if ((r = ora_budget(s->n_layers, s->n_kv_heads, mba, (int64_t)s->seq_len - s->window,
+                        total, floor_, budget)) != 0)
+        return r;
+    if ((r = ora_topk_all(s, scores, budget, k_max, idx)) != 0) return r;
+    if (ora_compact(s, k, idx, budget, k_max, k_out) < 0) return -3;
+    if (ora_compact(s, v, idx, budget, k_max, v_out) < 0) return -3;
+    if (lambda >= 0.0)
+        if ((r = ora_channel_prune(s, k_out, budget, lambda, chan, NULL, k_pruned)) != 0)
+            return r;
+    return 0;
+}

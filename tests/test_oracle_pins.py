@@ -1,0 +1,394 @@
+"""Pins for the fp64 CPU oracle, each against something other than the oracle.
+
+Every test here checks the oracle against a fact the method pages or the
+mathematics fix: a library routine the definition reduces to, a closed form,
+an invariant, or brute-force enumeration on tiny inputs.  A dropped term,
+wrong sign, wrong index or transposed operand anywhere in the oracle fails at
+least one of them (see the comment on each test).
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_inputs(L, Hq, Hkv, D, T, W, seed, dtype="f32", scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (scale * torch.randn(L, Hq, W, D, generator=g)).float()
+    k = torch.randn(L, Hkv, T, D, generator=g).float()
+    if dtype == "bf16":
+        q, k = q.bfloat16(), k.bfloat16()
+    return q, k
+
+
+# --------------------------------------------------------------------------- a1
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_score_equals_library_attention(seed):
+    """The mean attention row of the window queries equals what torch's own
+    scaled-dot-product attention returns when V is the identity (so the output
+    IS the probability matrix), with the causal window mask and GQA mapping
+    expanded explicitly.  Catches: wrong scale (1/D vs 1/sqrt(D)), mask offset
+    (j<=i instead of j<=P+i), GQA mapping (h % H_kv instead of h // G), mean
+    over the wrong axis, missing normalisation."""
+    L, Hq, Hkv, D, T, W = 2, 4, 2, 8, 37, 5
+    q, k = _rand_inputs(L, Hq, Hkv, D, T, W, seed, scale=2.0)
+    s = O.shape_of(L, Hq, Hkv, D, T, W, "f32")
+    c = O.score(s, q, k)
+    G, P = Hq // Hkv, T - W
+    kk = k.double().repeat_interleave(G, dim=1)                 # [L][Hq][T][D]
+    eye = torch.eye(T, dtype=torch.float64).expand(L, Hq, T, T)
+    pos = torch.arange(T)
+    mask = pos[None, :] <= (P + torch.arange(W))[:, None]       # [W][T]
+    probs = torch.nn.functional.scaled_dot_product_attention(
+        q.double(), kk, eye, attn_mask=mask)                    # [L][Hq][W][T]
+    ref = probs.view(L, Hkv, G, W, T).mean(dim=(2, 3)).numpy()
+    np.testing.assert_allclose(c, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_score_single_row_is_softmax():
+    """W=1, G=1: the score is one textbook softmax row over all T keys."""
+    L, H, D, T = 1, 3, 16, 50
+    q, k = _rand_inputs(L, H, H, D, T, 1, 7)
+    s = O.shape_of(L, H, H, D, T, 1, "f32")
+    c = O.score(s, q, k)
+    for h in range(H):
+        logits = (k[0, h].double() @ q[0, h, 0].double()).numpy() / math.sqrt(D)
+        np.testing.assert_allclose(c[0, h], scipy.special.softmax(logits), rtol=1e-12)
+
+
+def test_score_equal_keys_closed_form():
+    """All keys equal: window row i attends uniformly to its P+i+1 visible
+    keys, so c_j = (1/W) sum_{i : j <= P+i} 1/(P+i+1)."""
+    L, H, D, T, W = 1, 2, 4, 20, 6
+    q, _ = _rand_inputs(L, H, H, D, T, W, 3)
+    k = torch.ones(L, H, T, D) * 0.37
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    c = O.score(s, q, k)
+    P = T - W
+    want = np.array([sum(1.0 / (P + i + 1) for i in range(W) if j <= P + i) / W
+                     for j in range(T)])
+    for h in range(H):
+        np.testing.assert_allclose(c[0, h], want, rtol=1e-13)
+
+
+def test_score_rows_sum_to_one_and_bf16_widening_is_exact():
+    """Each softmax row sums to 1, so the window mean sums to 1; bf16 bytes
+    decode to exactly the fp32 values they round to."""
+    L, Hq, Hkv, D, T, W = 1, 4, 1, 16, 64, 8
+    q, k = _rand_inputs(L, Hq, Hkv, D, T, W, 11, dtype="bf16")
+    sb = O.shape_of(L, Hq, Hkv, D, T, W, "bf16")
+    sf = O.shape_of(L, Hq, Hkv, D, T, W, "f32")
+    cb = O.score(sb, q, k)
+    cf = O.score(sf, q.float(), k.float())
+    assert np.array_equal(cb, cf)
+    np.testing.assert_allclose(cb.sum(axis=-1), 1.0, rtol=0, atol=1e-13)
+
+
+def test_score_unit_matches_all():
+    L, Hq, Hkv, D, T, W = 2, 6, 3, 8, 30, 4
+    q, k = _rand_inputs(L, Hq, Hkv, D, T, W, 5)
+    s = O.shape_of(L, Hq, Hkv, D, T, W, "f32")
+    c = O.score(s, q, k)
+    assert np.array_equal(O.score_unit(s, q, k, 1, 2), c[1, 2])
+
+
+# --------------------------------------------------------------------------- a2
+def _mba_bruteforce(c, num, den):
+    """Fewest entries whose sum reaches num/den of the total, by enumerating
+    every subset in exact rational arithmetic (no sorting)."""
+    fr = [Fraction(x) for x in c]
+    need = Fraction(num, den) * sum(fr)
+    for m in range(0, len(c) + 1):
+        for sub in itertools.combinations(range(len(c)), m):
+            if sum((fr[j] for j in sub), Fraction(0)) >= need:
+                return m
+    raise AssertionError
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_mba_bruteforce_subsets(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 12))
+    c = rng.dirichlet(np.full(n, 0.3 + seed % 3))
+    num, den = [(9, 10), (1, 2), (3, 4)][seed % 3]
+    assert O.mba(c, num, den) == _mba_bruteforce(c, num, den)
+
+
+def test_mba_special_cases():
+    # one-hot: a single token holds all the mass
+    assert O.mba(np.eye(1, 40, 17).ravel()) == 1
+    # uniform over n tokens: ceil(0.9 n) of them are needed
+    for n in (1, 7, 10, 33, 1000):
+        assert O.mba(np.full(n, 1.0 / n)) == math.ceil(0.9 * n)
+    # "reaches" is inclusive: 1/2 + 1/4 is exactly 3/4 of the mass
+    assert O.mba(np.array([0.25, 0.5, 0.25]), 3, 4) == 2
+    # dyadic masses: 1/2+1/4+1/8 = 0.875 < 0.9, all four are needed
+    assert O.mba(np.array([0.125, 0.5, 0.125, 0.25])) == 4
+    # no mass at all needs no tokens
+    assert O.mba(np.zeros(5)) == 0
+
+
+def test_mba_permutation_invariant_and_rejects_bad_scores():
+    rng = np.random.default_rng(4)
+    c = rng.dirichlet(np.ones(300))
+    m = O.mba(c)
+    for _ in range(3):
+        assert O.mba(rng.permutation(c)) == m
+    with pytest.raises(ValueError):
+        O.mba(np.array([0.5, -0.1, 0.6]))
+    with pytest.raises(ValueError):
+        O.mba(np.array([0.5, np.nan]))
+
+
+# --------------------------------------------------------------------------- a3
+def _hamilton_ok(S, R, a):
+    """a is a largest-remainder apportionment of R by weights S: every entry
+    is floor or ceil of its exact quota and sum(|a-q|) is minimal over all
+    non-negative integer vectors summing to R (checked by enumeration)."""
+    tot = sum(S) or len(S)
+    w = S if sum(S) else [1] * len(S)
+    q = [Fraction(R * x, tot) for x in w]
+    best = None
+    for vec in itertools.product(range(R + 1), repeat=len(S)):
+        if sum(vec) != R:
+            continue
+        dev = sum(abs(v - qq) for v, qq in zip(vec, q))
+        if best is None or dev < best[0]:
+            best = (dev, [vec])
+        elif dev == best[0]:
+            best[1].append(vec)
+    return tuple(a) in best[1], max(best[1])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_budget_bruteforce_largest_remainder(seed):
+    rng = np.random.default_rng(100 + seed)
+    L = int(rng.integers(1, 5))
+    H = int(rng.integers(1, 3))
+    mba = rng.integers(0, 9, size=(L, H)).astype(np.int32)
+    floor = int(rng.integers(0, 3))
+    R = int(rng.integers(0, 10))
+    total = L * floor + R
+    P = 10_000                                   # no cap
+    b = O.budget(mba, P, total, floor)
+    a = [int(x) - floor for x in b]
+    S = [int(x) for x in mba.sum(axis=1)]
+    ok, lex_max = _hamilton_ok(S, R, a)
+    assert ok, (S, R, a)
+    # remainder ties go to the lower layer: the lexicographically largest
+    # optimum
+    assert tuple(a) == lex_max
+
+
+def test_budget_invariants_random():
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        L = int(rng.integers(1, 40))
+        H = int(rng.integers(1, 9))
+        P = int(rng.integers(1, 500))
+        floor = int(rng.integers(0, P + 1))
+        total = int(rng.integers(L * floor, L * P + 50))
+        mba = rng.integers(0, 2 * P, size=(L, H)).astype(np.int32)
+        b = O.budget(mba, P, total, floor)
+        assert b.min() >= floor and b.max() <= P
+        assert b.sum() == min(total, L * P)
+
+
+def test_budget_worked_examples():
+    with open(os.path.join(GOLDEN, "budget_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        got = O.budget(np.array(c["mba"], dtype=np.int32), c["prefix"], c["total"], c["floor"])
+        assert got.tolist() == c["budget"], c["why"]
+
+
+def test_budget_equal_lmba_and_errors():
+    mba = np.full((8, 4), 17, dtype=np.int32)
+    assert O.budget(mba, 1000, 8 * 300, 100).tolist() == [300] * 8
+    # 2403 = 8*300 + 3 spare tokens go to the three lowest layers
+    assert O.budget(mba, 1000, 2403, 100).tolist() == [301] * 3 + [300] * 5
+    # total >= L*P keeps everything
+    assert O.budget(mba, 50, 10**6, 10).tolist() == [50] * 8
+    with pytest.raises(ValueError):
+        O.budget(mba, 1000, 8 * 100 - 1, 100)      # below the floors
+    with pytest.raises(ValueError):
+        O.budget(mba, 50, 1000, 51)                # floor above the prefix
+
+
+# --------------------------------------------------------------------------- a4
+def _topk_bruteforce(c, B):
+    """Among all B-subsets, the largest exact score sum; among those, the
+    lexicographically smallest sorted index tuple (lowest indices win ties)."""
+    fr = [Fraction(x) for x in c]
+    best = None
+    for sub in itertools.combinations(range(len(c)), B):
+        key = (sum((fr[j] for j in sub), Fraction(0)), tuple(-j for j in sub))
+        if best is None or key > best[0]:
+            best = (key, sub)
+    return list(best[1])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_topk_bruteforce(seed):
+    rng = np.random.default_rng(200 + seed)
+    P = int(rng.integers(1, 11))
+    B = int(rng.integers(0, P + 1))
+    # few distinct values so that ties are common
+    c = rng.integers(0, 4, size=P).astype(np.float64) / 7.0
+    assert O.topk(c, P, B).tolist() == _topk_bruteforce(c, B)
+
+
+def test_topk_special_cases():
+    P = 100
+    assert O.topk(np.full(P, 0.01), P, 10).tolist() == list(range(10))
+    c = np.full(P, 1e-3)
+    c[73] = 0.5
+    assert 73 in O.topk(c, P, 1).tolist()
+    assert O.topk(np.random.default_rng(0).random(P), P, 500).tolist() == list(range(P))
+    assert O.topk(np.random.default_rng(0).random(P), P, 0).tolist() == []
+    got = O.topk(np.random.default_rng(1).random(P), P, 30)
+    assert np.all(np.diff(got) > 0)
+
+
+# --------------------------------------------------------------------------- a5
+def test_compact_equals_fancy_indexing():
+    L, H, D, T, W = 3, 2, 8, 40, 5
+    P = T - W
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((L, H, T, D)).astype(np.float32)
+    bud = np.array([4, 0, 35], dtype=np.int32)
+    k_max = 35
+    idx = np.full((L, H, k_max), -1, dtype=np.int32)
+    for l in range(L):
+        for h in range(H):
+            idx[l, h, : bud[l]] = np.sort(rng.choice(P, bud[l], replace=False))
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    out = O.compact(s, x, idx, bud, k_max)
+    want = np.concatenate([
+        np.concatenate([x[l, h, idx[l, h, : bud[l]]], x[l, h, P:]])
+        for l in range(L) for h in range(H)])
+    assert out.shape[0] == H * int((bud + W).sum())
+    assert np.array_equal(out, want)
+
+
+# --------------------------------------------------------------------------- a6
+def test_keep_channels_formula():
+    # the 128K workload: 40% of 128 key channels pruned keeps floor(76.8) = 76
+    assert O.keep_channels(0.4, 128) == 76
+    assert O.keep_channels(0.5, 128) == 64
+    assert O.keep_channels(0.0, 128) == 128
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_channel_prune_bruteforce(seed):
+    """For D <= 8, the kept channels are the keep-subset with the largest
+    total squared norm, lowest channel indices winning ties; norms equal
+    numpy's l2 norm squared; pruned rows are the kept rows' chosen columns."""
+    rng = np.random.default_rng(300 + seed)
+    L, H, D, T, W = 2, 2, 6, 12, 3
+    P = T - W
+    lam = [0.3, 0.5, 0.17][seed % 3]
+    keep = O.keep_channels(lam, D)
+    bud = np.array([int(rng.integers(0, P + 1)) for _ in range(L)], dtype=np.int32)
+    rows = H * int((bud + W).sum())
+    k_out = (rng.integers(-3, 4, size=(rows, D)) / 2.0).astype(np.float32)
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    chan, norms, kp = O.channel_prune(s, k_out, bud, lam)
+    r0, o0 = 0, 0
+    for l in range(L):
+        n = int(bud[l])
+        for h in range(H):
+            blk = k_out[r0: r0 + n]
+            np.testing.assert_allclose(norms[l, h], np.linalg.norm(blk.astype(np.float64), axis=0) ** 2,
+                                       rtol=1e-15, atol=0)
+            fr = [Fraction(float(x)) for x in norms[l, h]]
+            best = max(itertools.combinations(range(D), keep),
+                       key=lambda sub: (sum((fr[d] for d in sub), Fraction(0)), tuple(-d for d in sub)))
+            assert chan[l, h].tolist() == list(best)
+            got = kp[o0: o0 + n * keep].reshape(n, keep)
+            assert np.array_equal(got, blk[:, list(best)])
+            r0 += n + W
+            o0 += n * keep
+
+
+def test_channel_prune_keeps_outlier_channels():
+    """Keys with 4 channels scaled x8 (the Llama-shaped generators): those
+    channels carry far more magnitude and must be among the kept 76."""
+    from eviction_kvc_score_gb300 import workloads as wk
+    wl = wk.LLAMA3_8B_LAYER.scaled(n_layers=2, seq_len=1024, n_q_heads=8, n_kv_heads=2)
+    x = wk.make_inputs(wl, 17)
+    k = x["k"]
+    L, H, T, D, W = wl.n_layers, wl.n_kv_heads, wl.seq_len, wl.head_dim, wl.window
+    P = T - W
+    bud = np.array([300, 500], dtype=np.int32)
+    idx = np.zeros((L, H, 500), dtype=np.int32)
+    for l in range(L):
+        for h in range(H):
+            idx[l, h, : bud[l]] = np.arange(bud[l])
+    s = O.shape_of(L, 8, H, D, T, W, "bf16")
+    k_out = O.compact(s, k, idx, bud, 500)
+    chan, _, _ = O.channel_prune(s, k_out, bud, 0.4)
+    kf = k.float()
+    for l in range(L):
+        for h in range(H):
+            outl = torch.topk(kf[l, h, :P].abs().mean(0), 4).indices.tolist()
+            assert set(outl) <= set(chan[l, h].tolist())
+
+
+# --------------------------------------------------------------------- end to end
+def test_tiny_planted_keys_are_selected():
+    """The tiny MHA workload plants 4 keys per head equal to 3x the head's mean
+    window query; with this seed each lands in its head's top-128.  A much
+    stronger plant (logit far above every random one) must always be kept."""
+    from eviction_kvc_score_gb300 import workloads as wk
+    wl = wk.TINY
+    x = wk.make_inputs(wl, wk.seed_for(0))
+    s = O.shape_of(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len,
+                   wl.window, wl.dtype)
+    c = O.score(s, x["q"], x["k"])
+    P = wl.prefix_len
+    for h in range(wl.n_kv_heads):
+        sel = set(O.topk(c[0, h, :P], P, wl.per_head_budget).tolist())
+        assert set(x["planted"][0, h].tolist()) <= sel
+    k2 = x["k"].clone()
+    qm = x["q"][0].mean(dim=1)                     # [H][D]
+    for h in range(wl.n_kv_heads):
+        k2[0, h, 400] = 40.0 * qm[h]
+    c2 = O.score(s, x["q"], k2)
+    for h in range(wl.n_kv_heads):
+        assert 400 in O.topk(c2[0, h, :P], P, 1).tolist()
+
+
+def test_compress_chains_the_steps():
+    from eviction_kvc_score_gb300 import workloads as wk
+    wl = wk.ZIGZAG_32K.scaled(n_layers=3, seq_len=300, window=16, n_q_heads=4,
+                              n_kv_heads=2, head_dim=16, total_budget=3 * 40,
+                              layer_floor=8, think_lambda=0.25)
+    x = wk.make_inputs(wl, 21)
+    s = O.shape_of(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len,
+                   wl.window, wl.dtype)
+    total, floor = wl.budget_args()
+    out = O.compress(s, x["q"], x["k"], x["v"], total, floor, wl.k_max, lam=wl.think_lambda)
+    c = O.score(s, x["q"], x["k"])
+    assert np.array_equal(out["scores"], c)
+    m = O.mba_all(s, c)
+    assert np.array_equal(out["mba"], m)
+    b = O.budget(m, wl.prefix_len, total, floor)
+    assert np.array_equal(out["budget"], b) and b.sum() == total
+    idx = O.topk_all(s, c, b, wl.k_max)
+    for l in range(wl.n_layers):
+        assert np.array_equal(out["idx"][l, :, : b[l]], idx[l, :, : b[l]])
+    assert np.array_equal(out["k_out"], O.compact(s, x["k"], idx, b, wl.k_max))
+    assert np.array_equal(out["v_out"], O.compact(s, x["v"], idx, b, wl.k_max))
+    chan, _, kp = O.channel_prune(s, out["k_out"], b, wl.think_lambda)
+    assert np.array_equal(out["chan"], chan) and np.array_equal(out["k_pruned"], kp)
