@@ -1,0 +1,442 @@
+"""Benchmark: prompt tokens compressed per second on the 32K-token
+Llama-3-8B-shaped ZigZagKV workload (32 layers x 8 KV heads, GQA 4, D=128,
+W=128, bf16, total budget 32*2048, floor 256).
+
+One step = one pass of the whole path over one prompt:
+  kvc_score -> kvc_mba_budget -> kvc_topk_select -> kvc_compact
+(+ kvc_channel_prune on the workload with ThinK).  Inputs are resident in HBM
+before timing; K and V (2 GiB each) exceed the 129 MB L2, so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun every rank compresses its own prompt (independent problems,
+no collective on the data path): weak scaling, value = all ranks' tokens /
+max-over-ranks time.  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from eviction_kvc_score_gb300 import workloads as wk  # noqa: E402
+
+METRIC = "prompt tokens compressed/sec (score+budget+select+gather); % of HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# kernels each C-ABI call launches
+LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
+            "kvc_channel_prune": 1}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
+    ap.add_argument("--workload", default=wk.ZIGZAG_32K.name,
+                    choices=sorted(wk.WORKLOADS) + ["ragged_mistral_batch"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_list(name, rank):
+    if name == "ragged_mistral_batch":
+        return wk.ragged_mistral_batch(wk.seed_for(3, rank))
+    return [wk.WORKLOADS[name]]
+
+
+def algorithmic_bytes(wl, budget):
+    """Each input read once, each output written once (scores count as an
+    output): K, Q_obs, scores, indices, kept K/V rows read, compacted V
+    written, compacted (or pruned) K written."""
+    s = wl.elt_size
+    L, Hq, H, T, W, D = (wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.seq_len, wl.window,
+                         wl.head_dim)
+    P = T - W
+    keep = None
+    if wl.think_lambda is not None:
+        import math
+        keep = int(math.floor((1.0 - wl.think_lambda) * D))
+    total = 0
+    for b in budget:
+        n = max(0, min(int(b), P))
+        total += H * T * D * s + Hq * W * D * s + 4 * H * T + 4 * H * n
+        total += 2 * H * (n + W) * D * s + H * (n + W) * D * s
+        total += H * (n * keep + W * D) * s if keep else H * (n + W) * D * s
+    return total
+
+
+def score_flops(wl):
+    """Two contraction passes over the window rows (row statistics, then the
+    normalised column sums): 2 * (2 * H_q * W * D * T) per layer."""
+    return 2 * 2 * wl.n_q_heads * wl.window * wl.head_dim * wl.seq_len * wl.n_layers
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel_src):
+    """DRAM bytes per launch recorded by an ncu capture of this exact kernel
+    source (profiles/score_traffic.txt); None if absent or stale."""
+    p = os.path.join(ROOT, "profiles", "score_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    rec = {}
+    for ln in open(p):
+        if "=" in ln and not ln.lstrip().startswith("#"):
+            k, v = ln.split("=", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("kernel_src_sha256_16") != h:
+        return None
+    try:
+        return float(rec["traffic_bytes_per_step_score"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_setup(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, None
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    world = int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, dist
+
+
+def aggregate(ms_local, tokens_local, dist, device=None):
+    """Max time and summed tokens over ranks (host-side reduction of two
+    scalars; the data path has no collective)."""
+    if dist is None:
+        return ms_local, tokens_local
+    t = torch.tensor([ms_local, tokens_local], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[1])
+
+
+# ----------------------------------------------------------------- our arm
+def run_kvc(args):
+    from eviction_kvc_score_gb300 import kvc
+    rank, world, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wls = workload_list(args.workload, rank)
+    stream = torch.cuda.current_stream()
+    jobs = []
+    for i, wl in enumerate(wls):
+        x = wk.make_inputs(wl, wk.seed_for(2, 100 * rank + i), device=dev)
+        total, floor = wl.budget_args()
+        b = kvc.alloc_buffers(kvc.shape_of(wl), total, wl.k_max, lam=wl.think_lambda)
+        jobs.append((wl, x, b, total, floor))
+    torch.cuda.synchronize()
+
+    def step(score_ev=None):
+        for wl, x, b, total, floor in jobs:
+            if score_ev is not None:
+                score_ev[0].record(stream)
+            kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
+            if score_ev is not None:
+                score_ev[1].record(stream)
+            kvc.kvc_mba_budget(b.shape, b.scores, wl.mass_num, wl.mass_den, total, floor,
+                               b.mba, b.budget, b.ws)
+            kvc.kvc_topk_select(b.shape, b.scores, b.budget, b.k_max, b.idx, b.ws)
+            kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
+                            b.v_out, b.ws)
+            if wl.think_lambda is not None:
+                kvc.kvc_channel_prune(b.shape, b.k_out, b.budget, wl.think_lambda, b.chan,
+                                      b.k_pruned, b.ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for _, _, b, _, _ in jobs:
+        st = kvc.kvc_workspace_status(b.ws)
+        if st:
+            raise RuntimeError(f"device status {st:#x} after warm-up")
+
+    single = len(jobs) == 1
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)] if single else [None] * args.steps
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev0[i].record(stream)
+            step(sev[i])
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms_local = sum(step_ms) / len(step_ms)
+    tokens_local = float(sum(wl.seq_len for wl in wls))
+    ms, tokens = aggregate(ms_local, tokens_local, dist, dev)
+    value = tokens / (ms / 1e3)
+
+    pk, pk_src = peaks()
+    budgets = [b.budget.cpu().tolist() for _, _, b, _, _ in jobs]
+    alg_bytes = sum(algorithmic_bytes(wl, bud) for (wl, *_), bud in zip(jobs, budgets))
+    hbm_frac = alg_bytes / (ms_local / 1e3) / (pk["hbm_gbs"] * 1e9)
+    roof = None
+    if single:
+        wl = jobs[0][0]
+        score_ms = statistics.mean(a.elapsed_time(b) for a, b in sev)
+        flops = score_flops(wl)
+        achieved = flops / (score_ms / 1e3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        traffic = traffic_for(os.path.join(ROOT, "eviction_kvc_score_gb300", "csrc", "score_tc.cu"))
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "kvc_score (stats + merge + column-mean launches)",
+                "ms_per_launch": round(score_ms, 4), "flops_per_launch": flops,
+                "peak_source": f"{pk_src} bf16_tflops_sustained"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if jobs[0][0].dtype == "bf16" else "f32", "data": "synthetic (seeded generators)",
+        "config": {"workload": args.workload, "layers": jobs[0][0].n_layers,
+                   "q_heads": jobs[0][0].n_q_heads, "kv_heads": jobs[0][0].n_kv_heads,
+                   "head_dim": jobs[0][0].head_dim,
+                   "seq_len": [wl.seq_len for wl in wls] if not single else wls[0].seq_len,
+                   "window": jobs[0][0].window, "think_lambda": jobs[0][0].think_lambda,
+                   "l2": "inputs larger than the 129 MB L2 (K and V resident in HBM); no flush",
+                   "parallelism": f"replica x{world} (one prompt per GPU)"},
+        "hbm_roofline": {"algorithmic_bytes_per_step": alg_bytes,
+                         "achieved_gbs": round(alg_bytes / (ms_local / 1e3) / 1e9, 1),
+                         "peak_gbs": pk["hbm_gbs"], "frac": round(hbm_frac, 4),
+                         "peak_source": pk_src},
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * sum(LAUNCHES[k] for k in LAUNCHES
+                                         if k != "kvc_channel_prune" or wls[0].think_lambda
+                                         is not None) * len(jobs),
+        "wall_s_timed": round(t_wall, 3),
+    }
+    out["e2e"] = run_e2e(args, jobs, stream) if args.e2e_steps > 0 else None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(jobs[0][0], jobs[0][1])
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, jobs, stream):
+    """Same metric through the public API with HOST buffers: every step copies
+    the prompt's Q_obs, K, V from pinned host memory, runs the path and reads
+    the compacted K/V, indices and budgets back."""
+    from eviction_kvc_score_gb300 import kvc
+    host = []
+    for wl, x, b, total, floor in jobs:
+        hin = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v")}
+        hout = {"k_out": torch.empty_like(b.k_out, device="cpu").pin_memory(),
+                "v_out": torch.empty_like(b.v_out, device="cpu").pin_memory(),
+                "idx": torch.empty_like(b.idx, device="cpu").pin_memory(),
+                "budget": torch.empty_like(b.budget, device="cpu").pin_memory()}
+        if wl.think_lambda is not None:
+            hout["k_pruned"] = torch.empty_like(b.k_pruned, device="cpu").pin_memory()
+        host.append((hin, hout))
+    h2d = sum(t.numel() * t.element_size() for hin, _ in host for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for _, hout in host for t in hout.values())
+
+    def e2e_step():
+        for (wl, x, b, total, floor), (hin, hout) in zip(jobs, host):
+            for kname in ("q", "k", "v"):
+                x[kname].copy_(hin[kname], non_blocking=True)
+            kvc.compress(b, x["q"], x["k"], x["v"], total, floor, wl.mass_num, wl.mass_den,
+                         lam=wl.think_lambda)
+            hout["budget"].copy_(b.budget, non_blocking=True)
+            hout["idx"].copy_(b.idx, non_blocking=True)
+            hout["k_out"].copy_(b.k_out, non_blocking=True)
+            hout["v_out"].copy_(b.v_out, non_blocking=True)
+            if "k_pruned" in hout:
+                hout["k_pruned"].copy_(b.k_pruned, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.e2e_steps
+    tokens = sum(wl.seq_len for wl, *_ in jobs)
+    return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+
+
+# ----------------------------------------------------------------- oracle arm
+def _oracle_run(wl, x, n):
+    """The fp64 oracle's whole path (score, MBA, budget, top-K, compact, ThinK
+    if any) on the first n layers of the prompt, the total budget scaled to
+    those layers.  Returns wall seconds."""
+    from oracle import oracle as O
+    total, floor = wl.budget_args()
+    sub = wl.scaled(n_layers=n, total_budget=max(n * floor, total * n // wl.n_layers)
+                    if wl.total_budget is not None else None)
+    st, sf = sub.budget_args()
+    s = O.shape_of(n, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len, wl.window, wl.dtype)
+    q, k, v = (x[name][:n].cpu() for name in ("q", "k", "v"))
+    t0 = time.perf_counter()
+    O.compress(s, q, k, v, st, sf, sub.k_max, wl.mass_num, wl.mass_den, lam=wl.think_lambda)
+    return time.perf_counter() - t0
+
+
+def _sample_desc(wl, n, dt):
+    return (f"first {n} of {wl.n_layers} layers of one {wl.seq_len}-token prompt "
+            f"({n * wl.n_kv_heads} (layer, KV head) units), whole path in fp64, "
+            f"{dt:.2f} s wall per sample, scaled to the prompt by {wl.n_layers}/{n}")
+
+
+def cpu_baseline(wl, x, target_s=15.0):
+    """The oracle as it stands, timed on this host's cores on a bounded sample
+    of the workload (layers doubled until one sample takes about target_s/4),
+    scaled to tokens/s of the whole prompt."""
+    from oracle import oracle as O
+    n, spent = 1, 0.0
+    while True:
+        dt = _oracle_run(wl, x, n)
+        spent += dt
+        if dt * 4 >= target_s or n >= wl.n_layers or spent + 2 * dt > target_s:
+            break
+        n = min(wl.n_layers, 2 * n)
+    return {"value": round(wl.seq_len / (dt * wl.n_layers / n), 3), "unit": "tokens/s",
+            "cores": O.num_threads(), "kind": "oracle", "sample": _sample_desc(wl, n, dt)}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle, each step one fixed bounded sample
+    (the first layer of the prompt)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    O.build()
+    wl = workload_list(args.workload, 0)[0]
+    n = 1   # only the sampled layers are generated
+    x = wk.make_inputs(wl.scaled(n_layers=n), wk.seed_for(2), device="cpu")
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = _oracle_run(wl, x, n)
+        if i >= args.warmup:
+            times.append(dt)
+    per_prompt_s = statistics.mean(times) * wl.n_layers / n
+    val = wl.seq_len / per_prompt_s
+    out = {"impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(per_prompt_s * 1e3, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded generators)",
+           "config": {"workload": args.workload, "layers": wl.n_layers,
+                      "q_heads": wl.n_q_heads, "kv_heads": wl.n_kv_heads,
+                      "head_dim": wl.head_dim, "seq_len": wl.seq_len, "window": wl.window,
+                      "think_lambda": wl.think_lambda},
+           "cpu_baseline": {"value": round(val, 3), "unit": "tokens/s", "cores": O.num_threads(),
+                            "kind": "oracle", "sample": _sample_desc(wl, n, statistics.mean(times))},
+           "e2e": {"value": round(val, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvc(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,279 @@
+// api.cu -- the extern "C" entry points of libkvc: argument validation,
+// workspace layout and dispatch to the kernels.  Nothing here allocates
+// device memory; every launch goes to the caller's stream.
+#include "kvc_internal.cuh"
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+namespace kvc {
+
+namespace {
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct DeviceInfo {
+    int sms = 0;
+    int major = 0;
+};
+
+DeviceInfo device_info() {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DeviceInfo{};
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev].sms == 0) {
+        cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&cache[dev].major, cudaDevAttrComputeCapabilityMajor, dev);
+    }
+    return cache[dev];
+}
+
+bool shape_ok(const kvc_shape *s, const char *fn) {
+    if (!s) return fail(KVC_ERR_INVALID_ARG, "%s: shape is NULL", fn), false;
+    if (s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1)
+        return fail(KVC_ERR_INVALID_ARG, "%s: layers and heads must be >= 1", fn), false;
+    if (s->n_q_heads % s->n_kv_heads)
+        return fail(KVC_ERR_INVALID_ARG, "%s: n_q_heads %% n_kv_heads != 0", fn), false;
+    if (s->head_dim < 1 || s->head_dim > 256)
+        return fail(KVC_ERR_INVALID_ARG, "%s: head_dim must be in 1..256", fn), false;
+    if (s->window < 1 || s->seq_len <= s->window)
+        return fail(KVC_ERR_INVALID_ARG, "%s: need 1 <= window < seq_len", fn), false;
+    if (s->dtype != KVC_F32 && s->dtype != KVC_BF16)
+        return fail(KVC_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, s->dtype), false;
+    if ((int64_t)s->n_layers * s->n_kv_heads > (1 << 30))
+        return fail(KVC_ERR_INVALID_ARG, "%s: too many heads", fn), false;
+    return true;
+}
+
+bool tc_eligible(const kvc_shape &s) {
+    const int G = s.n_q_heads / s.n_kv_heads;
+    return s.dtype == KVC_BF16 && (s.head_dim == 64 || s.head_dim == 128) &&
+           (int64_t)G * s.window <= kMaxRowsTC && device_info().major >= 10;
+}
+
+// "auto" (default), "simt" or "tc", from KVC_SCORE_IMPL.
+int score_impl_choice() {
+    const char *e = getenv("KVC_SCORE_IMPL");
+    if (!e || !*e || !strcmp(e, "auto")) return 0;
+    if (!strcmp(e, "simt")) return 1;
+    if (!strcmp(e, "tc")) return 2;
+    return -1;
+}
+
+ScoreSplit make_split(const kvc_shape &s, bool tc) {
+    ScoreSplit sp;
+    const int G = s.n_q_heads / s.n_kv_heads;
+    sp.n_units = (int64_t)s.n_layers * s.n_kv_heads;
+    sp.tiles_per_unit = (s.seq_len + kTileKeys - 1) / kTileKeys;
+    sp.n_tiles = sp.n_units * sp.tiles_per_unit;
+    const int sms = device_info().sms > 0 ? device_info().sms : 148;
+    const int64_t want = tc ? sms : 4LL * sms;
+    sp.grid = (int)(sp.n_tiles < want ? sp.n_tiles : want);
+    sp.rows = G * s.window;
+    sp.rows_pad = (sp.rows + 127) / 128 * 128;
+    int mx = 1;
+    for (int64_t u = 0; u < sp.n_units; ++u) {
+        const int64_t a = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit);
+        const int64_t b = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit + sp.tiles_per_unit - 1);
+        if (b - a + 1 > mx) mx = (int)(b - a + 1);
+    }
+    sp.max_slots = mx;
+    return sp;
+}
+
+struct WsLayout {
+    size_t partial_off, partial_bytes;
+    size_t bias_off, bias_bytes;
+    size_t total;
+};
+
+WsLayout ws_layout(const kvc_shape &s) {
+    const ScoreSplit a = make_split(s, true), b = make_split(s, false);
+    const int slots = a.max_slots > b.max_slots ? a.max_slots : b.max_slots;
+    WsLayout w;
+    w.partial_off = kWsHeader;
+    w.partial_bytes = align256((size_t)a.n_units * slots * a.rows_pad * sizeof(float2));
+    w.bias_off = w.partial_off + w.partial_bytes;
+    w.bias_bytes = align256((size_t)a.n_units * a.rows_pad * sizeof(float));
+    w.total = w.bias_off + w.bias_bytes;
+    return w;
+}
+
+bool ws_ok(void *ws, size_t ws_bytes, size_t need, const char *fn) {
+    if (!ws) return fail(KVC_ERR_WORKSPACE, "%s: workspace is NULL", fn), false;
+    if (ws_bytes < need)
+        return fail(KVC_ERR_WORKSPACE, "%s: workspace has %zu bytes, needs %zu", fn, ws_bytes, need),
+               false;
+    if (reinterpret_cast<uintptr_t>(ws) % 256)
+        return fail(KVC_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", fn), false;
+    return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+uint32_t *status_word(void *ws) { return static_cast<uint32_t *>(ws); }
+
+}  // namespace
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+size_t kvc_workspace_size(const kvc_shape *shape, int32_t k_max) {
+    (void)k_max;
+    if (!shape_ok(shape, "kvc_workspace_size")) return 0;
+    return ws_layout(*shape).total;
+}
+
+int kvc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!ws || ws_bytes < kWsHeader) return fail(KVC_ERR_WORKSPACE, "kvc_workspace_init: bad workspace");
+    cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_workspace_init: %s", cudaGetErrorString(e));
+    return KVC_OK;
+}
+
+int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!ws || ws_bytes < kWsHeader || !status)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_workspace_status: bad arguments");
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_workspace_status: %s", cudaGetErrorString(e));
+    *status = v;
+    return KVC_OK;
+}
+
+int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *scores, void *ws,
+              size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_score")) return KVC_ERR_INVALID_ARG;
+    if (!q_obs || !k || !scores) return fail(KVC_ERR_INVALID_ARG, "kvc_score: NULL tensor");
+    if (!aligned16(q_obs) || !aligned16(k))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_score: q_obs and k must be 16-byte aligned");
+    const kvc_shape &s = *shape;
+    const WsLayout w = ws_layout(s);
+    if (!ws_ok(ws, ws_bytes, w.total, "kvc_score")) return KVC_ERR_WORKSPACE;
+    const int choice = score_impl_choice();
+    if (choice < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_score: KVC_SCORE_IMPL must be auto, simt or tc");
+    const bool can_tc = tc_eligible(s);
+    if (choice == 2 && !can_tc)
+        return fail(KVC_ERR_UNSUPPORTED, "kvc_score: tensor-core path needs bf16, head_dim 64/128, "
+                                         "G*W <= 512 and an sm_100-family device");
+    const bool tc = can_tc && choice != 1;
+    const ScoreSplit sp = make_split(s, tc);
+    ScoreArgs a;
+    a.q = q_obs;
+    a.k = k;
+    a.scores = scores;
+    a.partial = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.partial_off);
+    a.neg_bias = reinterpret_cast<float *>(static_cast<char *>(ws) + w.bias_off);
+    a.status = status_word(ws);
+    return tc ? launch_score_tc(s, sp, a, device_info().sms, stream) : launch_score_simt(s, sp, a, stream);
+}
+
+int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_num, uint32_t mass_den,
+                   int64_t total_budget, int32_t layer_floor, int32_t *mba, int32_t *budget, void *ws,
+                   size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_mba_budget")) return KVC_ERR_INVALID_ARG;
+    const kvc_shape &s = *shape;
+    if (!scores || !mba || !budget) return fail(KVC_ERR_INVALID_ARG, "kvc_mba_budget: NULL tensor");
+    if (mass_den == 0 || mass_num > mass_den)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_mba_budget: need 0 < mass_den and mass_num <= mass_den");
+    const int64_t P = (int64_t)s.seq_len - s.window;
+    if (layer_floor < 0 || layer_floor > P)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_mba_budget: layer_floor must be in [0, T-W]");
+    if (total_budget < (int64_t)s.n_layers * layer_floor)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_mba_budget: total_budget below n_layers * layer_floor");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_mba_budget")) return KVC_ERR_WORKSPACE;
+    int rc = launch_mba(s, scores, mass_num, mass_den, mba, status_word(ws), stream);
+    if (rc) return rc;
+    return launch_budget(s, mba, total_budget, layer_floor, budget, stream);
+}
+
+int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *budget, int32_t k_max,
+                    int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_topk_select")) return KVC_ERR_INVALID_ARG;
+    if (!scores || !budget || !idx) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: NULL tensor");
+    if (k_max < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: k_max must be >= 1");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_topk_select")) return KVC_ERR_WORKSPACE;
+    return launch_topk(*shape, scores, budget, k_max, idx, status_word(ws), stream);
+}
+
+int kvc_compact(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
+                const int32_t *budget, int32_t k_max, void *k_out, void *v_out, int64_t out_rows,
+                void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_compact")) return KVC_ERR_INVALID_ARG;
+    if (!k || !v || !idx || !budget || !k_out || !v_out)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact: NULL tensor");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact: tensors must be 16-byte aligned");
+    if (k_max < 1 || out_rows < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_compact: bad k_max/out_rows");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_compact")) return KVC_ERR_WORKSPACE;
+    return launch_compact(*shape, k, v, idx, budget, k_max, k_out, v_out, out_rows, status_word(ws),
+                          stream);
+}
+
+int32_t kvc_keep_channels(double lambda, int32_t head_dim) {
+    if (!(lambda >= 0.0 && lambda < 1.0) || head_dim < 1) return 0;
+    return (int32_t)std::floor((1.0 - lambda) * (double)head_dim);
+}
+
+int kvc_channel_prune(const kvc_shape *shape, const void *k_out, const int32_t *budget, double lambda,
+                      int32_t *chan, void *k_pruned, int64_t pruned_elems, void *ws, size_t ws_bytes,
+                      cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_channel_prune")) return KVC_ERR_INVALID_ARG;
+    if (!k_out || !budget || !chan || !k_pruned)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: NULL tensor");
+    const int32_t keep = kvc_keep_channels(lambda, shape->head_dim);
+    if (keep < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: lambda keeps no channel");
+    if (pruned_elems < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: bad pruned_elems");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_channel_prune")) return KVC_ERR_WORKSPACE;
+    return launch_channel_prune(*shape, k_out, budget, keep, chan, k_pruned, pruned_elems,
+                                status_word(ws), stream);
+}
+
+const char *kvc_status_string(int status) {
+    switch (status) {
+        case KVC_OK: return "ok";
+        case KVC_ERR_INVALID_ARG: return "invalid argument";
+        case KVC_ERR_UNSUPPORTED: return "unsupported";
+        case KVC_ERR_CUDA: return "CUDA error";
+        case KVC_ERR_TIMEOUT: return "device wait timed out";
+        case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+const char *kvc_last_error(void) { return g_err; }
+
+}  // extern "C"

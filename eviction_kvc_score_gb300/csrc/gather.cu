@@ -1,0 +1,250 @@
+// gather.cu -- K/V compaction and ThinK magnitude channel pruning.
+//
+// Compaction (blog post "ZigZagKV, KVCache 80% compression near-lossless",
+// section "SnapKV": the kept tokens are the top-K plus every token of the
+// last window): for head (l,k) the output block holds the n_l kept prefix
+// rows in ascending position order, then the W window rows.  The copy is
+// pure data movement: each thread moves 16-byte vectors, consecutive threads
+// write consecutive addresses, reads are whole rows gathered by index.
+//
+// ThinK ("ThinK: Thinner Key Cache by Query-Driven Pruning", "Magnitude-based
+// pruning", "Implementation of THINK"): per head, M_d = ||K[:, d]||_2^2 over
+// the kept prefix rows, keep the floor((1-lambda) D) largest channels (ties to
+// the lower d), copy them for the prefix rows; window rows stay full width.
+// Sums of squares run in a float-float pair (error-free products via FMA and
+// TwoSum additions), about 44 significant bits, so the channel order matches
+// an fp64 sum except for channels equal to within ~1e-13.
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kRowsPerBlock = 64;
+
+__device__ __forceinline__ int64_t kept(int32_t b, int P) {
+    return b < 0 ? 0 : (b > P ? P : b);
+}
+
+// Row offset of layer l in the packed output (in rows), computed from the
+// device budgets.
+__device__ __forceinline__ int64_t layer_row_offset(const int32_t *budget, int l, int Hkv, int P,
+                                                    int W) {
+    int64_t off = 0;
+    for (int i = 0; i < l; ++i) off += (int64_t)Hkv * (kept(budget[i], P) + W);
+    return off;
+}
+
+template <typename V>
+__global__ void __launch_bounds__(kCopyThreads)
+    compact_kernel(const V *__restrict__ k, const V *__restrict__ v, const int32_t *__restrict__ idx,
+                   const int32_t *__restrict__ budget, int T, int W, int Hkv, int k_max,
+                   int vec_per_row, V *__restrict__ k_out, V *__restrict__ v_out, int64_t out_rows,
+                   uint32_t *status) {
+    __shared__ int64_t s_row0;
+    __shared__ int s_n;
+    const int head = blockIdx.x;
+    const int l = head / Hkv, h = head % Hkv;
+    const int P = T - W;
+    if (threadIdx.x == 0) {
+        int64_t n = kept(budget[l], P);
+        if (n > k_max) n = k_max;   // reported by the top-K step
+        s_n = (int)n;
+        s_row0 = layer_row_offset(budget, l, Hkv, P, W) + (int64_t)h * (kept(budget[l], P) + W);
+    }
+    __syncthreads();
+    const int n = s_n;
+    const int64_t row0 = s_row0;
+    const int rows = n + W;
+    const int32_t *sel = idx + (int64_t)head * k_max;
+    const V *ks = k + (int64_t)head * T * vec_per_row;
+    const V *vs = v + (int64_t)head * T * vec_per_row;
+    for (int rb = blockIdx.y * kRowsPerBlock; rb < rows; rb += gridDim.y * kRowsPerBlock) {
+        const int rend = min(rows, rb + kRowsPerBlock);
+        const int total = (rend - rb) * vec_per_row;
+        for (int i = threadIdx.x; i < total; i += kCopyThreads) {
+            const int r = rb + i / vec_per_row;
+            const int e = i % vec_per_row;
+            const int64_t orow = row0 + r;
+            if (orow >= out_rows) {
+                set_status(status, KVC_DEV_OUT_CAPACITY);
+                continue;
+            }
+            const int t = r < n ? sel[r] : P + (r - n);
+            if (t < 0 || t >= T) {
+                set_status(status, KVC_DEV_BAD_BUDGET);
+                continue;
+            }
+            k_out[orow * vec_per_row + e] = ks[(int64_t)t * vec_per_row + e];
+            v_out[orow * vec_per_row + e] = vs[(int64_t)t * vec_per_row + e];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ ThinK
+struct FF {   // unevaluated sum hi + lo
+    float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    e += a.lo + b.lo;
+    FF r;
+    two_sum(s, e, r.hi, r.lo);
+    return r;
+}
+
+__device__ __forceinline__ FF ff_add_sq(FF a, float x) {
+    const float p = x * x;
+    const float pe = fmaf(x, x, -p);   // exact product error
+    float s, e;
+    two_sum(a.hi, p, s, e);
+    e += a.lo + pe;
+    FF r;
+    two_sum(s, e, r.hi, r.lo);
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_f(const T *p, int64_t i);
+template <>
+__device__ __forceinline__ float ld_f<float>(const float *p, int64_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+
+constexpr int kPruneThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kPruneThreads)
+    channel_prune_kernel(const T *__restrict__ k_out, const int32_t *__restrict__ budget, int T_len,
+                         int W, int Hkv, int D, int keep, int32_t *__restrict__ chan,
+                         T *__restrict__ k_pruned, int64_t pruned_elems, uint32_t *status) {
+    __shared__ FF part[kPruneThreads];
+    __shared__ double m[256];
+    __shared__ int sel[256];
+    __shared__ int flag[256];
+    __shared__ int64_t s_row0, s_o0;
+    __shared__ int s_n;
+    const int head = blockIdx.x;
+    const int l = head / Hkv, h = head % Hkv;
+    const int P = T_len - W;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        const int64_t n = kept(budget[l], P);
+        s_n = (int)n;
+        s_row0 = layer_row_offset(budget, l, Hkv, P, W) + (int64_t)h * (n + W);
+        int64_t o = 0;
+        for (int i = 0; i < l; ++i) o += kept(budget[i], P);
+        s_o0 = ((int64_t)Hkv * o + (int64_t)h * n) * keep;
+    }
+    __syncthreads();
+    const int n = s_n;
+    const int64_t row0 = s_row0;
+    // 1. per-channel sums of squares: thread = (channel, row group)
+    const int groups = kPruneThreads / D;
+    const int d = tid % D, g = tid / D;
+    FF acc = {0.f, 0.f};
+    if (g < groups)
+        for (int r = g; r < n; r += groups) acc = ff_add_sq(acc, ld_f(k_out, (row0 + r) * D + d));
+    part[tid] = acc;
+    __syncthreads();
+    if (tid < D) {
+        FF tot = part[tid];
+        for (int gg = 1; gg < groups; ++gg) tot = ff_add(tot, part[gg * D + tid]);
+        m[tid] = (double)tot.hi + (double)tot.lo;
+    }
+    __syncthreads();
+    // 2. rank channels by (M desc, d asc); keep the first `keep`, ascending
+    if (tid < D) {
+        const double mine = m[tid];
+        int rank = 0;
+        for (int o = 0; o < D; ++o) rank += (m[o] > mine) || (m[o] == mine && o < tid);
+        flag[tid] = rank < keep;
+    }
+    __syncthreads();
+    if (tid < D && flag[tid]) {
+        int pos = 0;
+        for (int o = 0; o < tid; ++o) pos += flag[o];
+        sel[pos] = tid;
+        chan[(int64_t)head * keep + pos] = tid;
+    }
+    __syncthreads();
+    // 3. copy the kept channels of the prefix rows
+    const int64_t o0 = s_o0;
+    const int64_t total = (int64_t)n * keep;
+    for (int64_t i = tid; i < total; i += kPruneThreads) {
+        const int64_t r = i / keep;
+        const int c = (int)(i % keep);
+        if (o0 + i >= pruned_elems) {
+            set_status(status, KVC_DEV_OUT_CAPACITY);
+            break;
+        }
+        k_pruned[o0 + i] = k_out[(row0 + r) * D + sel[c]];
+    }
+}
+
+}  // namespace
+
+int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
+                   const int32_t *budget, int32_t k_max, void *k_out, void *v_out, int64_t out_rows,
+                   uint32_t *status, cudaStream_t st) {
+    const size_t es = s.dtype == KVC_F32 ? 4 : 2;
+    const size_t row_bytes = es * (size_t)s.head_dim;
+    const int heads = s.n_layers * s.n_kv_heads;
+    const int max_rows = k_max + s.window;
+    dim3 grid(heads, (unsigned)min(32, (max_rows + kRowsPerBlock - 1) / kRowsPerBlock));
+    if (row_bytes % 16 == 0) {
+        compact_kernel<uint4><<<grid, kCopyThreads, 0, st>>>(
+            (const uint4 *)k, (const uint4 *)v, idx, budget, s.seq_len, s.window, s.n_kv_heads,
+            k_max, (int)(row_bytes / 16), (uint4 *)k_out, (uint4 *)v_out, out_rows, status);
+    } else if (row_bytes % 4 == 0) {
+        compact_kernel<uint32_t><<<grid, kCopyThreads, 0, st>>>(
+            (const uint32_t *)k, (const uint32_t *)v, idx, budget, s.seq_len, s.window,
+            s.n_kv_heads, k_max, (int)(row_bytes / 4), (uint32_t *)k_out, (uint32_t *)v_out,
+            out_rows, status);
+    } else {
+        compact_kernel<uint16_t><<<grid, kCopyThreads, 0, st>>>(
+            (const uint16_t *)k, (const uint16_t *)v, idx, budget, s.seq_len, s.window,
+            s.n_kv_heads, k_max, (int)(row_bytes / 2), (uint16_t *)k_out, (uint16_t *)v_out,
+            out_rows, status);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_compact: launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
+
+int launch_channel_prune(const kvc_shape &s, const void *k_out, const int32_t *budget, int32_t keep,
+                         int32_t *chan, void *k_pruned, int64_t pruned_elems, uint32_t *status,
+                         cudaStream_t st) {
+    const int heads = s.n_layers * s.n_kv_heads;
+    if (s.dtype == KVC_F32) {
+        channel_prune_kernel<float><<<heads, kPruneThreads, 0, st>>>(
+            (const float *)k_out, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim, keep, chan,
+            (float *)k_pruned, pruned_elems, status);
+    } else {
+        channel_prune_kernel<__nv_bfloat16><<<heads, kPruneThreads, 0, st>>>(
+            (const __nv_bfloat16 *)k_out, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim,
+            keep, chan, (__nv_bfloat16 *)k_pruned, pruned_elems, status);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_channel_prune: launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
+
+}  // namespace kvc

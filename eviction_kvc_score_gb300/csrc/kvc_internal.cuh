@@ -1,0 +1,279 @@
+// kvc_internal.cuh -- definitions shared by the libkvc translation units:
+// workspace layout, the score-pass work split, and thin inline-PTX wrappers
+// for the sm_100-family async machinery (mbarrier, TMA, tcgen05/TMEM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+// ---------------------------------------------------------------- constants
+constexpr int kTileKeys = 128;          // keys per score tile (MMA M or N)
+constexpr int kMaxRowsTC = 512;         // G*W handled by the tensor-core path
+constexpr size_t kWsHeader = 256;       // status word + padding
+constexpr double kLog2e = 1.4426950408889634;
+
+// Every pipeline wait gives up after this many nanoseconds of %globaltimer,
+// sets KVC_DEV_TIMEOUT and lets the kernel unwind.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// ---------------------------------------------------------------- score split
+// The score passes walk the flat sequence of (unit, key-tile) pairs, unit =
+// (layer, KV head), in unit-major order.  CTA c of a grid of g owns tiles
+// [floor(N c / g), floor(N (c+1) / g)).  Pass 1 leaves one partial (max, sum)
+// per row for every (unit, CTA touching it) in slot c - first_cta(unit).
+struct ScoreSplit {
+    int64_t n_units;       // L * H_kv
+    int64_t tiles_per_unit;
+    int64_t n_tiles;       // n_units * tiles_per_unit
+    int grid;              // CTAs
+    int max_slots;         // partial slots per unit
+    int rows;              // G * W
+    int rows_pad;          // rows rounded up to 128
+};
+
+__host__ __device__ inline int64_t split_begin(int64_t n, int g, int64_t c) {
+    return (n * c) / g;
+}
+__host__ __device__ inline int64_t split_cta_of(int64_t n, int g, int64_t t) {
+    return ((int64_t)g * (t + 1) - 1) / n;
+}
+
+// ---------------------------------------------------------------- status word
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
+    atomicOr(status, bits);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false (and
+// records KVC_DEV_TIMEOUT / raises the CTA abort flag) if the limit passes,
+// or immediately if another thread of the CTA already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_status(status, KVC_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait used only while unwinding: bounded, ignores the abort flag.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tiled load; c0 is the innermost coordinate (must be a multiple of
+// 16 bytes' worth of elements).
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *bar, void *dst, int c0,
+                                            int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand stored in the
+// 128-byte swizzled layout that TMA writes for a box whose inner extent is
+// 128 bytes: 8-row groups of 1024 bytes (stride-dimension offset 1024).
+// Bits: [0,14) start>>4, [16,30) leading offset>>4 (unused for this layout),
+// [32,46) stride offset>>4, [46,48) descriptor version 1, [61,64) layout 2 =
+// 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B, fp32 accumulator,
+// both operands K-major: [4,6) D format (1 = f32), [7,10) A format (1 =
+// bf16), [10,13) B format (1 = bf16), [17,23) N>>3, [24,29) M>>4.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive columns of 32-bit TMEM cells -> 32 registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Hardware base-2 exponential (PTX ex2.approx.ftz.f32; ex2(-inf) = +0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- host side
+struct ScoreArgs {
+    const void *q;
+    const void *k;
+    float *scores;
+    float2 *partial;   // [units][max_slots][rows_pad] (running max, sum), log2 units
+    float *neg_bias;   // [units][rows_pad] = -(max + log2(sum)), -inf for pad rows
+    uint32_t *status;
+};
+
+int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, int num_sms,
+                    cudaStream_t st);
+int launch_score_simt(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
+                      cudaStream_t st);
+int launch_score_merge(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
+                       cudaStream_t st);
+int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
+               uint32_t *status, cudaStream_t st);
+int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,
+                  int32_t *budget, cudaStream_t st);
+int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int32_t k_max,
+                int32_t *idx, uint32_t *status, cudaStream_t st);
+int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
+                   const int32_t *budget, int32_t k_max, void *k_out, void *v_out,
+                   int64_t out_rows, uint32_t *status, cudaStream_t st);
+int launch_channel_prune(const kvc_shape &s, const void *k_out, const int32_t *budget, int32_t keep,
+                         int32_t *chan, void *k_pruned, int64_t pruned_elems, uint32_t *status,
+                         cudaStream_t st);
+
+void set_error(const char *fmt, ...);
+
+}  // namespace kvc

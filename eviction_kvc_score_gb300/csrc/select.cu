@@ -1,0 +1,424 @@
+// select.cu -- ZigZagKV MBA, layer budgets and per-head top-K.
+//
+// MBA (blog post "ZigZagKV, KVCache 80% compression near-lossless", section
+// "ZigZagKV's new observations"): the fewest tokens whose scores reach 90%
+// of a head's attention mass.  Mass is exact fixed point u = floor(c*2^56),
+// so the count does not depend on summation order.  Instead of sorting, a
+// three-pass MSB radix select over the fp32 bit patterns (non-negative floats
+// order like their bit patterns) keeps, per digit bucket, the count and the
+// u-sum, and descends into the bucket where the running mass from the top
+// first reaches the threshold.  The exact crossing value v* and the mass
+// above it then give the count in closed form.
+//
+// Budgets (same post, "ZigZagKV space allocation"): integer proportional
+// split with a floor and largest remainders, capped at the prefix length.
+//
+// Top-K (same post, "SnapKV" / "ZigZagKV token selection"): radix select of
+// the B-th largest prefix score, then an ordered block-wide compaction that
+// keeps everything above it and the lowest-index ties, writing positions in
+// ascending order.
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kSelThreads = 1024;
+// Digits of the 32-bit key, most significant first: bits 31..21, 20..10, 9..0.
+__device__ __forceinline__ int digit_bits(int pass) { return pass == 2 ? 10 : 11; }
+
+__device__ __forceinline__ int digit_of(uint32_t key, int pass) {
+    return (int)((key >> (pass == 0 ? 21 : pass == 1 ? 10 : 0)) & (pass == 2 ? 0x3FFu : 0x7FFu));
+}
+
+// Does key lie inside the bucket chosen by the earlier passes?
+__device__ __forceinline__ bool in_prefix(uint32_t key, int pass, uint32_t prefix) {
+    if (pass == 0) return true;
+    return (key >> (pass == 1 ? 21 : 10)) == prefix;
+}
+
+__device__ __forceinline__ unsigned long long fixed56(float c) {
+    return (unsigned long long)(ldexp((double)c, 56));
+}
+
+// ------------------------------------------------------------------ MBA
+__global__ void __launch_bounds__(kSelThreads)
+    mba_kernel(const float *__restrict__ scores, int T, uint32_t num, uint32_t den,
+               int32_t *__restrict__ mba, uint32_t *status) {
+    __shared__ uint32_t cnt[2048];
+    __shared__ unsigned long long msum[2048];
+    __shared__ unsigned long long s_total, s_sum_gt;
+    __shared__ long long s_cnt_gt;
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_bad, s_done;
+    const float *c = scores + (int64_t)blockIdx.x * T;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_sum_gt = 0;
+        s_cnt_gt = 0;
+        s_prefix = 0;
+        s_bad = 0;
+        s_done = 0;
+    }
+    for (int pass = 0; pass < 3; ++pass) {
+        const int nb = 1 << digit_bits(pass);
+        for (int d = tid; d < nb; d += kSelThreads) {
+            cnt[d] = 0;
+            msum[d] = 0;
+        }
+        __syncthreads();
+        const uint32_t prefix = s_prefix;
+        for (int j = tid; j < T; j += kSelThreads) {
+            const float v = c[j];
+            const uint32_t key = __float_as_uint(v);
+            if (pass == 0 && !(v >= 0.f && v <= 1.f)) s_bad = 1;
+            if (in_prefix(key, pass, prefix) && key <= 0x3F800000u) {   // 0 <= v <= 1
+                const int d = digit_of(key, pass);
+                atomicAdd(&cnt[d], 1u);
+                atomicAdd(&msum[d], fixed56(v));
+            }
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // Warp 0: lane L sums the buckets [nb - (L+1)*per, nb - L*per), so
+            // lane order runs from the largest digit down.
+            const int per = nb / 32;
+            const int lo = nb - (tid + 1) * per;
+            unsigned long long ls = 0;
+            long long lc = 0;
+            for (int d = lo; d < lo + per; ++d) {
+                ls += msum[d];
+                lc += cnt[d];
+            }
+            if (pass == 0) {
+                unsigned long long tot = ls;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+                if (tid == 0) {
+                    s_total = tot;
+                    // sum of the scores above 16 (or invalid values) would
+                    // overflow the exact comparisons below
+                    if (s_bad || tot > (1ull << 60)) s_bad = 1;
+                    if (s_bad || (unsigned __int128)num * tot == 0) s_done = 1;
+                }
+                __syncwarp();
+            }
+            if (!s_done) {
+                const unsigned __int128 need = (unsigned __int128)num * s_total;
+                // inclusive scan of the lane sums from lane 0 (largest digits)
+                unsigned long long incl = ls;
+                long long incl_c = lc;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long a = __shfl_up_sync(0xffffffffu, incl, o);
+                    const long long b = __shfl_up_sync(0xffffffffu, incl_c, o);
+                    if (tid >= o) {
+                        incl += a;
+                        incl_c += b;
+                    }
+                }
+                const unsigned long long base = s_sum_gt;
+                const bool reach = (unsigned __int128)den * (base + incl) >= need;
+                const unsigned mask = __ballot_sync(0xffffffffu, reach);
+                const int L = __ffs(mask) - 1;   // first lane whose range reaches
+                if (tid == L) {
+                    unsigned long long run = base + incl - ls;   // mass above my range
+                    long long runc = s_cnt_gt + incl_c - lc;
+                    int chosen = lo;
+                    for (int d = lo + per - 1; d >= lo; --d) {
+                        if ((unsigned __int128)den * (run + msum[d]) >= need) {
+                            chosen = d;
+                            break;
+                        }
+                        run += msum[d];
+                        runc += cnt[d];
+                    }
+                    s_sum_gt = run;
+                    s_cnt_gt = runc;
+                    s_prefix = (prefix << digit_bits(pass)) | (uint32_t)chosen;
+                }
+            }
+        }
+        __syncthreads();
+        if (s_done) break;
+    }
+    if (tid == 0) {
+        if (s_bad) {
+            set_status(status, KVC_DEV_BAD_SCORE);
+            mba[blockIdx.x] = 0;
+        } else if (s_done) {
+            mba[blockIdx.x] = 0;
+        } else {
+            // s_prefix is now the exact crossing value v*; every element above
+            // it is counted in s_cnt_gt / s_sum_gt; ties at v* each carry u*.
+            const unsigned long long ustar = fixed56(__uint_as_float(s_prefix));
+            const unsigned __int128 need = (unsigned __int128)num * s_total;
+            const unsigned __int128 have = (unsigned __int128)den * s_sum_gt;
+            const unsigned __int128 step = (unsigned __int128)den * ustar;
+            const long long k = (long long)((need - have + step - 1) / step);
+            mba[blockIdx.x] = (int32_t)(s_cnt_gt + k);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ budgets
+// One thread; L <= 1024 layers.  Largest-remainder split of R over the
+// eligible layers by weight S (equal weights if they sum to 0), ties to the
+// lower layer.
+__device__ void lr_split(int L, const long long *S, const unsigned char *elig, long long R,
+                         long long *add, long long *rem, unsigned char *given) {
+    long long sumw = 0;
+    int n_el = 0;
+    for (int l = 0; l < L; ++l) {
+        add[l] = 0;
+        given[l] = 0;
+        if (elig[l]) {
+            sumw += S[l];
+            ++n_el;
+        }
+    }
+    if (n_el == 0 || R <= 0) return;
+    const bool equal = sumw == 0;
+    if (equal) sumw = n_el;
+    long long handed = 0;
+    for (int l = 0; l < L; ++l) {
+        rem[l] = -1;
+        if (!elig[l]) continue;
+        const unsigned __int128 prod = (unsigned __int128)R * (unsigned long long)(equal ? 1 : S[l]);
+        add[l] = (long long)(prod / (unsigned long long)sumw);
+        rem[l] = (long long)(prod % (unsigned long long)sumw);
+        handed += add[l];
+    }
+    for (long long left = R - handed; left > 0; --left) {
+        int best = -1;
+        for (int l = 0; l < L; ++l)
+            if (elig[l] && !given[l] && (best < 0 || rem[l] > rem[best])) best = l;
+        given[best] = 1;
+        add[best] += 1;
+    }
+}
+
+constexpr int kMaxLayers = 1024;
+
+__global__ void budget_kernel(const int32_t *__restrict__ mba, int L, int Hkv, long long P,
+                              long long total, long long floor_, int32_t *__restrict__ budget) {
+    __shared__ long long S[kMaxLayers], B[kMaxLayers], add[kMaxLayers], rem[kMaxLayers];
+    __shared__ unsigned char elig[kMaxLayers], given[kMaxLayers];
+    if (threadIdx.x != 0) return;
+    if (total >= (long long)L * P) {
+        for (int l = 0; l < L; ++l) budget[l] = (int32_t)P;
+        return;
+    }
+    for (int l = 0; l < L; ++l) {
+        long long acc = 0;
+        for (int k = 0; k < Hkv; ++k) acc += mba[(int64_t)l * Hkv + k];
+        S[l] = acc;
+        elig[l] = 1;
+    }
+    lr_split(L, S, elig, total - (long long)L * floor_, add, rem, given);
+    for (int l = 0; l < L; ++l) B[l] = floor_ + add[l];
+    while (true) {
+        long long excess = 0;
+        for (int l = 0; l < L; ++l)
+            if (B[l] > P) {
+                excess += B[l] - P;
+                B[l] = P;
+            }
+        if (excess == 0) break;
+        for (int l = 0; l < L; ++l) elig[l] = B[l] < P;
+        lr_split(L, S, elig, excess, add, rem, given);
+        for (int l = 0; l < L; ++l) B[l] += add[l];
+    }
+    for (int l = 0; l < L; ++l) budget[l] = (int32_t)B[l];
+}
+
+// ------------------------------------------------------------------ top-K
+// Block-wide exclusive scan of one uint32 per thread (1024 threads).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tot, uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t a = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += a;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = warp_tot[lane];
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t a = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += a;
+        }
+        warp_tot[lane] = wi - w;   // exclusive
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const uint32_t r = warp_tot[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    topk_kernel(const float *__restrict__ scores, int T, int P, int Hkv,
+                const int32_t *__restrict__ budget, int k_max, int32_t *__restrict__ idx,
+                uint32_t *status) {
+    __shared__ uint32_t cnt[2048];
+    __shared__ uint32_t warp_tot[32];
+    __shared__ uint32_t s_total;
+    __shared__ uint32_t s_prefix;
+    __shared__ long long s_cnt_gt;
+    __shared__ int s_bad;
+    const int head = blockIdx.x;
+    const int l = head / Hkv;
+    const int tid = threadIdx.x;
+    const float *c = scores + (int64_t)head * T;
+    int32_t *out = idx + (int64_t)head * k_max;
+    long long B = budget[l];
+    if (B < 0) {
+        if (tid == 0) set_status(status, KVC_DEV_BAD_BUDGET);
+        B = 0;
+    }
+    if (B > P) B = P;
+    if (B > k_max) {
+        if (tid == 0) set_status(status, KVC_DEV_BAD_BUDGET);
+        B = k_max;
+    }
+    if (B == 0) return;
+    if (B == P) {
+        for (int j = tid; j < P; j += kSelThreads) out[j] = j;
+        return;
+    }
+    if (tid == 0) {
+        s_prefix = 0;
+        s_cnt_gt = 0;
+        s_bad = 0;
+    }
+    for (int pass = 0; pass < 3; ++pass) {
+        const int nb = 1 << digit_bits(pass);
+        for (int d = tid; d < nb; d += kSelThreads) cnt[d] = 0;
+        __syncthreads();
+        const uint32_t prefix = s_prefix;
+        for (int j = tid; j < P; j += kSelThreads) {
+            const float v = c[j];
+            const uint32_t key = __float_as_uint(v);
+            if (pass == 0 && !(v >= 0.f)) s_bad = 1;
+            if (in_prefix(key, pass, prefix)) atomicAdd(&cnt[digit_of(key, pass)], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            const int per = nb / 32;
+            const int lo = nb - (tid + 1) * per;
+            long long lc = 0;
+            for (int d = lo; d < lo + per; ++d) lc += cnt[d];
+            long long incl = lc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long a = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += a;
+            }
+            const long long base = s_cnt_gt;
+            const unsigned mask = __ballot_sync(0xffffffffu, base + incl >= B);
+            const int L = __ffs(mask) - 1;
+            if (tid == L) {
+                long long run = base + incl - lc;
+                int chosen = lo;
+                for (int d = lo + per - 1; d >= lo; --d) {
+                    if (run + cnt[d] >= B) {
+                        chosen = d;
+                        break;
+                    }
+                    run += cnt[d];
+                }
+                s_cnt_gt = run;
+                s_prefix = (prefix << digit_bits(pass)) | (uint32_t)chosen;
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0 && s_bad) set_status(status, KVC_DEV_BAD_SCORE);
+    const uint32_t vstar = s_prefix;
+    const long long need_eq = B - s_cnt_gt;   // >= 1
+    // Ordered compaction: position of a kept j is G(j) + min(E(j), need_eq)
+    // with G/E the numbers of elements above / equal to v* before j.
+    long long g_before = 0, e_before = 0;
+    for (int base = 0; base < P; base += 4 * kSelThreads) {
+        const int j0 = base + 4 * tid;
+        uint32_t gt[4], eq[4];
+        uint32_t ng = 0, ne = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = j0 + i;
+            const uint32_t key = j < P ? __float_as_uint(c[j]) : 0u;
+            gt[i] = (j < P) && key > vstar;
+            eq[i] = (j < P) && key == vstar;
+            ng += gt[i];
+            ne += eq[i];
+        }
+        const uint32_t packed = block_excl_scan(ng | (ne << 16), warp_tot, &s_total);
+        long long G = g_before + (packed & 0xFFFFu);
+        long long E = e_before + (packed >> 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (gt[i] || (eq[i] && E < need_eq)) {
+                const long long pos = G + (E < need_eq ? E : need_eq);
+                out[pos] = j0 + i;
+            }
+            G += gt[i];
+            E += eq[i];
+        }
+        const uint32_t tot = s_total;
+        g_before += tot & 0xFFFFu;
+        e_before += tot >> 16;
+        if (g_before + (e_before < need_eq ? e_before : need_eq) >= B) break;
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
+               uint32_t *status, cudaStream_t st) {
+    const int heads = s.n_layers * s.n_kv_heads;
+    mba_kernel<<<heads, kSelThreads, 0, st>>>(scores, s.seq_len, num, den, mba, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_mba_budget: MBA launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
+
+int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,
+                  int32_t *budget, cudaStream_t st) {
+    if (s.n_layers > kMaxLayers) {
+        set_error("kvc_mba_budget: at most %d layers", kMaxLayers);
+        return KVC_ERR_UNSUPPORTED;
+    }
+    budget_kernel<<<1, 32, 0, st>>>(mba, s.n_layers, s.n_kv_heads,
+                                    (long long)s.seq_len - s.window, (long long)total,
+                                    (long long)floor_, budget);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_mba_budget: budget launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
+
+int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int32_t k_max,
+                int32_t *idx, uint32_t *status, cudaStream_t st) {
+    const int heads = s.n_layers * s.n_kv_heads;
+    topk_kernel<<<heads, kSelThreads, 0, st>>>(scores, s.seq_len, s.seq_len - s.window,
+                                                s.n_kv_heads, budget, k_max, idx, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_topk_select: launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
+
+}  // namespace kvc

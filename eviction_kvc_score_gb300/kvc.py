@@ -1,0 +1,222 @@
+"""Python binding of libkvc (include/kvc.h): argument marshalling only.
+
+Every function here forwards device pointers, sizes and the current CUDA
+stream to the C ABI; all compression work runs in the library's CUDA kernels.
+There is no CPU fallback: importing this module raises if libkvc.so has not
+been built, and calls raise KvcError on any non-zero status.
+
+Tensors are torch tensors on the GPU (torch provides device memory and
+streams only).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libkvc.so is missing at {LIB_PATH}: build it with "
+        "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+
+_lib = C.CDLL(LIB_PATH)
+
+KVC_OK = 0
+KVC_F32, KVC_BF16 = 0, 1
+DEV_TIMEOUT, DEV_BAD_SCORE, DEV_BAD_BUDGET, DEV_OUT_CAPACITY = 0x1, 0x2, 0x4, 0x8
+
+
+class KvcError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+class KvcShape(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("n_q_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("seq_len", C.c_int32), ("window", C.c_int32),
+                ("dtype", C.c_int32)]
+
+
+_p, _sz, _i32, _i64, _u32, _d = C.c_void_p, C.c_size_t, C.c_int32, C.c_int64, C.c_uint32, C.c_double
+_sp = C.POINTER(KvcShape)
+_SIGS = {
+    "kvc_workspace_size": (_sz, [_sp, _i32]),
+    "kvc_workspace_init": (C.c_int, [_p, _sz, _p]),
+    "kvc_workspace_status": (C.c_int, [_p, _sz, C.POINTER(_u32), _p]),
+    "kvc_score": (C.c_int, [_sp, _p, _p, _p, _p, _sz, _p]),
+    "kvc_mba_budget": (C.c_int, [_sp, _p, _u32, _u32, _i64, _i32, _p, _p, _p, _sz, _p]),
+    "kvc_topk_select": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
+    "kvc_compact": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
+    "kvc_channel_prune": (C.c_int, [_sp, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
+    "kvc_keep_channels": (_i32, [_d, _i32]),
+    "kvc_status_string": (C.c_char_p, [C.c_int]),
+    "kvc_last_error": (C.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def _check(fn, rc):
+    if rc != KVC_OK:
+        raise KvcError(fn, rc, _lib.kvc_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libkvc takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libkvc takes contiguous tensors")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def shape(n_layers, n_q_heads, n_kv_heads, head_dim, seq_len, window, dtype) -> KvcShape:
+    if isinstance(dtype, torch.dtype):
+        dt = KVC_F32 if dtype == torch.float32 else KVC_BF16
+    else:
+        dt = KVC_F32 if dtype in ("f32", KVC_F32) else KVC_BF16
+    return KvcShape(n_layers, n_q_heads, n_kv_heads, head_dim, seq_len, window, dt)
+
+
+def shape_of(wl) -> KvcShape:
+    """KvcShape of a workloads.Workload."""
+    return shape(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len, wl.window,
+                 wl.dtype)
+
+
+# --- the C ABI, one Python function per entry point -------------------------
+
+def kvc_workspace_size(s: KvcShape, k_max: int = 0) -> int:
+    n = _lib.kvc_workspace_size(C.byref(s), int(k_max))
+    if n == 0:
+        raise KvcError("kvc_workspace_size", -1, _lib.kvc_last_error().decode())
+    return n
+
+
+def kvc_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check("kvc_workspace_init", _lib.kvc_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
+
+
+def kvc_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    out = _u32(0)
+    _check("kvc_workspace_status",
+           _lib.kvc_workspace_status(_ptr(ws), ws.numel(), C.byref(out), _stream(stream)))
+    return out.value
+
+
+def kvc_score(s: KvcShape, q_obs, k, scores, ws, stream=None) -> None:
+    _check("kvc_score", _lib.kvc_score(C.byref(s), _ptr(q_obs), _ptr(k), _ptr(scores), _ptr(ws),
+                                       ws.numel(), _stream(stream)))
+
+
+def kvc_mba_budget(s: KvcShape, scores, mass_num: int, mass_den: int, total_budget: int,
+                   layer_floor: int, mba, budget, ws, stream=None) -> None:
+    _check("kvc_mba_budget", _lib.kvc_mba_budget(
+        C.byref(s), _ptr(scores), int(mass_num), int(mass_den), int(total_budget),
+        int(layer_floor), _ptr(mba), _ptr(budget), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def kvc_topk_select(s: KvcShape, scores, budget, k_max: int, idx, ws, stream=None) -> None:
+    _check("kvc_topk_select", _lib.kvc_topk_select(
+        C.byref(s), _ptr(scores), _ptr(budget), int(k_max), _ptr(idx), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def kvc_compact(s: KvcShape, k, v, idx, budget, k_max: int, k_out, v_out, ws, stream=None) -> None:
+    _check("kvc_compact", _lib.kvc_compact(
+        C.byref(s), _ptr(k), _ptr(v), _ptr(idx), _ptr(budget), int(k_max), _ptr(k_out),
+        _ptr(v_out), k_out.shape[0], _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def kvc_channel_prune(s: KvcShape, k_out, budget, lam: float, chan, k_pruned, ws,
+                      stream=None) -> None:
+    _check("kvc_channel_prune", _lib.kvc_channel_prune(
+        C.byref(s), _ptr(k_out), _ptr(budget), float(lam), _ptr(chan), _ptr(k_pruned),
+        k_pruned.numel(), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def kvc_keep_channels(lam: float, head_dim: int) -> int:
+    return int(_lib.kvc_keep_channels(float(lam), int(head_dim)))
+
+
+def kvc_status_string(code: int) -> str:
+    return _lib.kvc_status_string(int(code)).decode()
+
+
+def kvc_last_error() -> str:
+    return _lib.kvc_last_error().decode()
+
+
+# --- buffers for one prompt -------------------------------------------------
+
+@dataclass
+class Buffers:
+    """Device buffers for the whole path on one prompt shape.  Output row
+    capacity is sized for the largest packed result the budgets allow:
+    H_kv * (min(total, L*P) + L*W) rows."""
+    shape: KvcShape
+    k_max: int
+    ws: torch.Tensor
+    scores: torch.Tensor
+    mba: torch.Tensor
+    budget: torch.Tensor
+    idx: torch.Tensor
+    k_out: torch.Tensor
+    v_out: torch.Tensor
+    chan: Optional[torch.Tensor] = None
+    k_pruned: Optional[torch.Tensor] = None
+    keep: int = 0
+
+
+def alloc_buffers(s: KvcShape, total_budget: int, k_max: int, lam: Optional[float] = None,
+                  device="cuda") -> Buffers:
+    L, H, T, W, D = s.n_layers, s.n_kv_heads, s.seq_len, s.window, s.head_dim
+    P = T - W
+    dt = torch.float32 if s.dtype == KVC_F32 else torch.bfloat16
+    ws_bytes = kvc_workspace_size(s, k_max)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    kept_rows = min(int(total_budget), L * P)
+    rows = H * (kept_rows + L * W)
+    b = Buffers(
+        shape=s, k_max=int(k_max), ws=ws,
+        scores=torch.empty((L, H, T), dtype=torch.float32, device=device),
+        mba=torch.empty((L, H), dtype=torch.int32, device=device),
+        budget=torch.empty(L, dtype=torch.int32, device=device),
+        idx=torch.empty((L, H, max(1, int(k_max))), dtype=torch.int32, device=device),
+        k_out=torch.empty((rows, D), dtype=dt, device=device),
+        v_out=torch.empty((rows, D), dtype=dt, device=device))
+    if lam is not None:
+        b.keep = kvc_keep_channels(lam, D)
+        b.chan = torch.empty((L, H, max(1, b.keep)), dtype=torch.int32, device=device)
+        b.k_pruned = torch.empty(max(1, H * kept_rows * b.keep), dtype=dt, device=device)
+    kvc_workspace_init(ws)
+    return b
+
+
+def compress(b: Buffers, q_obs, k, v, total_budget: int, layer_floor: int, mass_num: int = 9,
+             mass_den: int = 10, lam: Optional[float] = None, stream=None) -> None:
+    """Enqueue the whole path: score -> MBA/budget -> top-K -> compact
+    (-> channel prune when lam is given).  Asynchronous on `stream`."""
+    s = b.shape
+    kvc_score(s, q_obs, k, b.scores, b.ws, stream)
+    kvc_mba_budget(s, b.scores, mass_num, mass_den, total_budget, layer_floor, b.mba, b.budget,
+                   b.ws, stream)
+    kvc_topk_select(s, b.scores, b.budget, b.k_max, b.idx, b.ws, stream)
+    kvc_compact(s, k, v, b.idx, b.budget, b.k_max, b.k_out, b.v_out, b.ws, stream)
+    if lam is not None:
+        kvc_channel_prune(s, b.k_out, b.budget, lam, b.chan, b.k_pruned, b.ws, stream)

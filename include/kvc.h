@@ -1,0 +1,186 @@
+/*
+ * kvc.h -- C ABI of libkvc: attention-score-driven prompt KV-cache
+ * compression on one GB300 GPU (sm_103a).
+ *
+ * The method, in the pages' terms:
+ *  1. Observation-window scoring (SnapKV; blog post "ZigZagKV, KVCache 80%
+ *     compression near-lossless", section "SnapKV"): the last W prompt
+ *     tokens' queries attend to all T prompt keys; each KV head's attention
+ *     rows are averaged over its window rows and its GQA query heads into one
+ *     importance value per token.  Attention is softmax(Q K^T / sqrt(D))
+ *     ("ThinK: Thinner Key Cache by Query-Driven Pruning", section "Method
+ *     details").
+ *  2. ZigZagKV budgets (same blog post, sections "ZigZagKV's new
+ *     observations" and "ZigZagKV space allocation"): each head's MBA is the
+ *     fewest tokens whose scores reach 90% of the attention mass; a layer's
+ *     LMBA is the mean over its heads; the total budget is split across
+ *     layers in proportion to LMBA with a per-layer floor.
+ *  3. Selection (same post, sections "SnapKV" and "ZigZagKV token
+ *     selection"): each head keeps its layer's budget of highest-scoring
+ *     prefix tokens plus every window token; the kept K/V rows are gathered
+ *     into a compacted cache.
+ *  4. ThinK magnitude pruning (ThinK page, "Magnitude-based pruning"): keep
+ *     floor((1-lambda) D) key channels per head with the largest l2 norm over
+ *     the kept prefix rows; window (recent) rows are not pruned ("Implementation
+ *     of THINK").
+ *
+ * Conventions (all entry points):
+ *  - Every tensor argument is a DEVICE pointer owned by the caller,
+ *    contiguous in the layout stated below.  The library never allocates
+ *    device memory; scratch lives in a caller-provided workspace of
+ *    kvc_workspace_size() bytes, zeroed once with kvc_workspace_init().
+ *  - Work is enqueued on `stream` and is asynchronous.  Argument errors are
+ *    detected on the host before anything is launched and returned as a
+ *    negative kvc_status; kvc_last_error() then holds a message.
+ *  - Data-dependent errors found by a kernel (a score outside [0,1], a
+ *    budget larger than k_max, an output buffer too small, a pipeline wait
+ *    that timed out) are OR-ed into a status word inside the workspace and
+ *    read back with kvc_workspace_status().  Launch failures return
+ *    KVC_ERR_CUDA.
+ *  - Calls sharing one workspace must be ordered on one stream; distinct
+ *    workspaces may run concurrently.
+ *
+ * Layouts (row-major, innermost last):
+ *  q_obs   [L][H_q][W][D]   window queries; query head h belongs to KV head
+ *                           h / (H_q / H_kv)
+ *  k, v    [L][H_kv][T][D]  prompt keys / values; window = last W positions
+ *  scores  [L][H_kv][T]     fp32, sums to 1 per head
+ *  mba     [L][H_kv]        int32
+ *  budget  [L]              int32, prefix tokens kept per head of layer l
+ *  idx     [L][H_kv][k_max] int32, ascending kept prefix positions; entries
+ *                           at and after n_l = min(budget[l], T-W) untouched
+ *  k_out, v_out             packed: layer l holds [H_kv][n_l + W][D] (kept
+ *                           rows ascending, then the W window rows); layer l
+ *                           starts at row H_kv * sum_{l'<l} (n_l' + W)
+ *  chan    [L][H_kv][keep]  int32, ascending kept key channels
+ *  k_pruned packed: layer l holds [H_kv][n_l][keep], starting at element
+ *                           H_kv * keep * sum_{l'<l} n_l'
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_INVALID_ARG = -1,  /* bad shape, pointer, size or alignment */
+    KVC_ERR_UNSUPPORTED = -2,  /* valid request this build cannot serve */
+    KVC_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+    KVC_ERR_TIMEOUT = -4,      /* reserved: a device wait gave up */
+    KVC_ERR_WORKSPACE = -5     /* workspace missing or smaller than required */
+} kvc_status;
+
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
+
+/* Device status bits, OR-ed into the workspace status word by kernels. */
+#define KVC_DEV_TIMEOUT      0x1u  /* a pipeline wait exceeded its limit */
+#define KVC_DEV_BAD_SCORE    0x2u  /* a score was negative, NaN or > 1, or
+                                      the scores of a head summed above 16 */
+#define KVC_DEV_BAD_BUDGET   0x4u  /* min(budget[l], T-W) exceeded k_max or
+                                      budget[l] was negative; clamped */
+#define KVC_DEV_OUT_CAPACITY 0x8u  /* packed output larger than the buffer;
+                                      rows past the end were not written */
+
+typedef struct {
+    int32_t n_layers;    /* L >= 1 */
+    int32_t n_q_heads;   /* H_q >= 1, a multiple of H_kv */
+    int32_t n_kv_heads;  /* H_kv >= 1 */
+    int32_t head_dim;    /* D, 1..256 (tensor-core path: 64 or 128, bf16) */
+    int32_t seq_len;     /* T > W */
+    int32_t window;      /* W >= 1, observation window = last W tokens */
+    int32_t dtype;       /* kvc_dtype of q_obs, k, v */
+} kvc_shape;
+
+/* Bytes of workspace the calls below need for `shape` on the CURRENT device
+ * (the score pass splits work by the device's SM count).  Returns 0 for an
+ * invalid shape.  k_max is accepted for future use and may be 0. */
+size_t kvc_workspace_size(const kvc_shape *shape, int32_t k_max);
+
+/* Zero the workspace (status word included).  Call once after allocating
+ * it; kernels only OR bits into the status word afterwards. */
+int kvc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronise `stream` and return the device status word of `ws` (the OR of
+ * KVC_DEV_* bits since the last kvc_workspace_init) in *status. */
+int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status,
+                         cudaStream_t stream);
+
+/* a1 -- observation-window scores (SnapKV scoring, causal inside the window,
+ * GQA-averaged):
+ *   scores[l][k][j] = 1/(G W) * sum_{g<G, i<W} softmax_j( q_{kG+g,i} . k_j / sqrt(D) )
+ * with row i (position T-W+i) seeing keys j <= T-W+i only; scores of keys a
+ * row cannot see are zero for that row.  Computed with fp32 accumulation;
+ * bf16 inputs with D in {64,128} and G*W <= 512 run on the tcgen05 tensor
+ * cores, everything else on a CUDA-core fp32 path.  q_obs and k must be
+ * 16-byte aligned.  Uses the workspace for per-row softmax statistics. */
+int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *scores,
+              void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* a2 + a3 -- ZigZagKV budgets.
+ * mba[l][k] = smallest m with mass_den * (sum of the m largest u) >=
+ *             mass_num * (sum of all u), u_j = floor(scores[l][k][j] * 2^56),
+ *             over all T tokens (0 for an all-zero head);
+ * budget[l] = layer_floor + largest-remainder share of
+ *             (total_budget - L*layer_floor) by S_l = sum_k mba[l][k]
+ *             (equal shares if every S_l is 0), remainder ties to the lower
+ *             layer, then capped at T-W with the excess re-split over the
+ *             layers still below T-W until none exceeds it.  If total_budget
+ *             >= L*(T-W) every layer gets T-W.
+ * Requires 0 <= layer_floor <= T-W, total_budget >= L*layer_floor,
+ * 0 < mass_den, mass_num <= mass_den.  Scores must lie in [0,1] and sum to
+ * at most 16 per head (KVC_DEV_BAD_SCORE otherwise). */
+int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_num,
+                   uint32_t mass_den, int64_t total_budget, int32_t layer_floor,
+                   int32_t *mba, int32_t *budget, void *ws, size_t ws_bytes,
+                   cudaStream_t stream);
+
+/* a4 -- per-head top-K of the prefix.  For head (l,k) keep
+ * n_l = min(max(budget[l],0), T-W) prefix positions j < T-W with the largest
+ * scores, ties to the lower position, written ascending to idx[l][k][0..n_l).
+ * budget is a DEVICE array (e.g. from kvc_mba_budget, or filled by the
+ * caller with a uniform SnapKV budget).  n_l > k_max sets KVC_DEV_BAD_BUDGET
+ * and keeps only k_max. */
+int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *budget,
+                    int32_t k_max, int32_t *idx, void *ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* a5 -- compaction.  Gathers, for every head, rows idx[l][k][0..n_l) and then
+ * the W window rows T-W..T-1 of k and v into k_out / v_out (packed layout
+ * above).  out_rows is the capacity of each output in rows of D elements;
+ * the rows needed are H_kv * sum_l (n_l + W).  k, v, k_out and v_out must be
+ * 16-byte aligned. */
+int kvc_compact(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
+                const int32_t *budget, int32_t k_max, void *k_out, void *v_out,
+                int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* a6 -- ThinK magnitude pruning of the compacted keys.  keep =
+ * kvc_keep_channels(lambda, D).  Per head: M_d = sum over its n_l kept
+ * prefix rows of k_out[r][d]^2 (accumulated in a float-float pair, about 44
+ * significant bits), the `keep` channels with the largest M_d (ties to the
+ * lower d) are written ascending to chan, and those channels of the prefix
+ * rows are copied to k_pruned (packed layout above; pruned_elems is its
+ * capacity in elements).  Window rows stay full width in k_out. */
+int kvc_channel_prune(const kvc_shape *shape, const void *k_out, const int32_t *budget,
+                      double lambda, int32_t *chan, void *k_pruned, int64_t pruned_elems,
+                      void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* floor((1 - lambda) * head_dim) computed in double; 0 if lambda is outside
+ * [0,1). */
+int32_t kvc_keep_channels(double lambda, int32_t head_dim);
+
+const char *kvc_status_string(int status);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char *kvc_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */
