@@ -51,6 +51,7 @@ _SIGS = {
     "kvc_workspace_init": (C.c_int, [_p, _sz, _p]),
     "kvc_workspace_status": (C.c_int, [_p, _sz, C.POINTER(_u32), _p]),
     "kvc_score": (C.c_int, [_sp, _p, _p, _p, _p, _sz, _p]),
+    "kvc_score_noalloc": (C.c_int, [_sp, _p, _p, _p, _p, _p]),
     "kvc_mba_budget": (C.c_int, [_sp, _p, _u32, _u32, _i64, _i32, _p, _p, _p, _sz, _p]),
     "kvc_topk_select": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
     "kvc_compact": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
@@ -122,6 +123,15 @@ def kvc_workspace_status(ws: torch.Tensor, stream=None) -> int:
 def kvc_score(s: KvcShape, q_obs, k, scores, ws, stream=None) -> None:
     _check("kvc_score", _lib.kvc_score(C.byref(s), _ptr(q_obs), _ptr(k), _ptr(scores), _ptr(ws),
                                        ws.numel(), _stream(stream)))
+
+
+def kvc_score_noalloc(s: KvcShape, q_obs, k, scores, dev_status=None, stream=None) -> None:
+    """kvc_score without a workspace, for callers that may not allocate device
+    memory: scratch comes from a fixed array inside the library (see kvc.h).
+    Calls that overlap on the GPU race on that array; keep them on one
+    stream."""
+    _check("kvc_score_noalloc", _lib.kvc_score_noalloc(
+        C.byref(s), _ptr(q_obs), _ptr(k), _ptr(scores), _ptr(dev_status), _stream(stream)))
 
 
 def kvc_mba_budget(s: KvcShape, scores, mass_num: int, mass_den: int, total_budget: int,

@@ -26,9 +26,10 @@
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer owned by the caller,
- *    contiguous in the layout stated below.  The library never allocates
- *    device memory; scratch lives in a caller-provided workspace of
- *    kvc_workspace_size() bytes, zeroed once with kvc_workspace_init().
+ *    contiguous in the layout stated below.  No call allocates device
+ *    memory; scratch lives in a caller-provided workspace of
+ *    kvc_workspace_size() bytes, zeroed once with kvc_workspace_init()
+ *    (kvc_score_noalloc alone uses a fixed array inside the library).
  *  - Work is enqueued on `stream` and is asynchronous.  Argument errors are
  *    detected on the host before anything is launched and returned as a
  *    negative kvc_status; kvc_last_error() then holds a message.
@@ -121,6 +122,25 @@ int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status,
  * 16-byte aligned.  Uses the workspace for per-row softmax statistics. */
 int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *scores,
               void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* kvc_score for callers that cannot allocate device memory (no counterpart in
+ * the method pages; it exists for integration only).  Some hosts give a
+ * plugin just its input and output buffers -- no workspace -- and forbid
+ * cudaMalloc because their own allocator already holds the device memory
+ * and an allocation would synchronise the device mid-schedule.  This call
+ * computes exactly what kvc_score computes, with the same kernels, but keeps
+ * its scratch in a fixed 8 MiB array inside the library's device memory
+ * (held by every GPU that loads the library until the process exits).
+ * Shapes whose scratch exceeds 8 MiB return KVC_ERR_UNSUPPORTED (the 32K and
+ * 128K Llama-3-8B-shaped prompts need 2.5 MiB).  dev_status is an
+ * optional DEVICE uint32 that is zeroed and then receives the KVC_DEV_* bits
+ * (NULL: they go to a word inside the array).  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress) and should be
+ * made outside any stream capture.  All calls share the array: calls that
+ * overlap on the GPU race and give undefined scores, so order them on one
+ * stream.  Allocates nothing. */
+int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, const void *k, float *scores,
+                      uint32_t *dev_status, cudaStream_t stream);
 
 /* a2 + a3 -- ZigZagKV budgets.
  * mba[l][k] = smallest m with mass_den * (sum of the m largest u) >=
