@@ -44,11 +44,13 @@ LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_comp
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvc", choices=["kvc", "reference"])
     ap.add_argument("--workload", default=wk.ZIGZAG_32K.name,
                     choices=sorted(wk.WORKLOADS) + ["ragged_mistral_batch"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run the workload with this many layers")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -63,10 +65,20 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_list(name, rank):
+def workload_list(name, rank, layers=0):
     if name == "ragged_mistral_batch":
-        return wk.ragged_mistral_batch(wk.seed_for(3, rank))
-    return [wk.WORKLOADS[name]]
+        wls = wk.ragged_mistral_batch(wk.seed_for(3, rank))
+    else:
+        wls = [wk.WORKLOADS[name]]
+    if layers:
+        out = []
+        for wl in wls:
+            kw = {"n_layers": layers}
+            if wl.total_budget is not None:
+                kw["total_budget"] = wl.total_budget * layers // wl.n_layers
+            out.append(wl.scaled(**kw))
+        wls = out
+    return wls
 
 
 def algorithmic_bytes(wl, budget):
@@ -203,7 +215,7 @@ def run_kvc(args):
     from eviction_kvc_score_gb300 import kvc
     rank, world, dist = dist_setup(args.gpus)
     dev = torch.device("cuda", torch.cuda.current_device())
-    wls = workload_list(args.workload, rank)
+    wls = workload_list(args.workload, rank, args.layers)
     stream = torch.cuda.current_stream()
     jobs = []
     for i, wl in enumerate(wls):
@@ -284,7 +296,8 @@ def run_kvc(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if jobs[0][0].dtype == "bf16" else "f32", "data": "synthetic (seeded generators)",
-        "config": {"workload": args.workload, "layers": jobs[0][0].n_layers,
+        "config": {"workload": args.workload + (f" ({args.layers} layers)" if args.layers else ""),
+                   "layers": jobs[0][0].n_layers,
                    "q_heads": jobs[0][0].n_q_heads, "kv_heads": jobs[0][0].n_kv_heads,
                    "head_dim": jobs[0][0].head_dim,
                    "seq_len": [wl.seq_len for wl in wls] if not single else wls[0].seq_len,

@@ -16,7 +16,7 @@
 //           epilogue thread owns one TMEM lane = one query row and keeps an
 //           online (max, sum) over its CTA's keys -> per-CTA partials;
 //   merge   (score_simt.cu) combines the partials into nb_r = -(m_r + log2 l_r);
-//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 256 query rows): each
+//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 128 query rows): each
 //           epilogue thread owns one key and sums 2^(x_rj + nb_r) over the
 //           query rows in registers -- the column sum needs no cross-lane
 //           reduction in this orientation.
@@ -24,8 +24,14 @@
 // Both passes are persistent: CTA c owns a contiguous run of (unit, key
 // tile) pairs, keeps the unit's Q block resident in shared memory and streams
 // K tiles with TMA through an mbarrier ring.  Warp roles: warp 0 TMA
-// producer, warp 1 MMA issuer (and TMEM owner), warps 2-5 epilogue.  Every
-// wait is bounded (kvc_internal.cuh).
+// producer, warp 1 MMA issuer (and TMEM owner), warps 2-9 epilogue in two
+// warpgroups.  TMEM holds four 128-column accumulator slots; each MMA job
+// fills one 128 x 128 slot and the warpgroups take alternate jobs, so one
+// computes while the other waits for its TMEM load or its next MMA.  Each
+// thread keeps eight independent max / sum chains, and the epilogue has one
+// copy of its inner loop (the window's causal mask is applied by setting
+// invisible logits to -inf first) so that it fits the instruction cache.
+// Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
 #include <cstdio>
@@ -36,8 +42,8 @@ namespace kvc {
 
 namespace {
 
-constexpr int kThreads = 192;     // 6 warps
-constexpr int kEpiThreads = 128;  // warps 2..5
+constexpr int kThreads = 320;     // 10 warps: producer, MMA, 2 x 4 epilogue
+constexpr int kEpi = 256;         // epilogue threads
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 
@@ -66,9 +72,10 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 struct Smem {
     uint8_t *q;        // [KH][rows_pad][128 B], 128-byte swizzled (TMA)
     uint8_t *k;        // [stages][KH][128 keys][128 B]
-    float *nb;         // [rows_pad] (pass 2)
-    int *wr;           // [rows_pad] window position of each row (pass 2)
-    uint64_t *full, *empty, *q_full, *q_empty, *t_full, *t_empty, *drain;
+    float *red;        // [2][128] pass-2 partial column sums handed WG1 -> WG0
+    float *nb;         // [rows_pad] pass-2 row biases of the current unit
+    uint64_t *full, *empty, *q_full, *q_empty, *t_full, *t_empty, *c_full, *c_empty;
+    uint64_t *nb_ready, *nb_done, *drain;
     uint32_t *tmem_base;
     volatile int *abort_flag;
 };
@@ -81,10 +88,10 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
     b += (size_t)KH * p.rows_pad * 128;
     s.k = b;
     b += (size_t)p.stages * KH * kBoxBytes;
+    s.red = reinterpret_cast<float *>(b);
+    b += 2 * 128 * sizeof(float);
     s.nb = reinterpret_cast<float *>(b);
     b += (size_t)p.rows_pad * sizeof(float);
-    s.wr = reinterpret_cast<int *>(b);
-    b += (size_t)p.rows_pad * sizeof(int);
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
     s.full = bars;
     s.empty = bars + p.stages;
@@ -92,7 +99,11 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
     s.q_empty = s.q_full + 1;
     s.t_full = s.q_empty + 1;   // 4
     s.t_empty = s.t_full + 4;   // 4
-    s.drain = s.t_empty + 4;
+    s.c_full = s.t_empty + 4;   // 2
+    s.c_empty = s.c_full + 2;   // 2
+    s.nb_ready = s.c_empty + 2;
+    s.nb_done = s.nb_ready + 1;
+    s.drain = s.nb_done + 1;
     s.tmem_base = reinterpret_cast<uint32_t *>(s.drain + 1);
     s.abort_flag = reinterpret_cast<volatile int *>(s.tmem_base + 1);
     return s;
@@ -100,8 +111,8 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
 
 template <int KH>
 size_t smem_bytes(int rows_pad, int stages) {
-    return 1024 + (size_t)KH * rows_pad * 128 + (size_t)stages * KH * kBoxBytes +
-           (size_t)rows_pad * 8 + (size_t)(2 * stages + 11) * 8 + 16;
+    return 1024 + (size_t)KH * rows_pad * 128 + (size_t)stages * KH * kBoxBytes + 2 * 128 * 4 +
+           (size_t)rows_pad * 4 + (size_t)(2 * stages + 17) * 8 + 16;
 }
 
 // Barrier set-up, TMEM allocation; returns the TMEM base column address.
@@ -116,8 +127,14 @@ __device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p) {
         mbar_init(s.q_empty, 1);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s.t_full[i], 1);
-            mbar_init(&s.t_empty[i], 4);  // one arrive per epilogue warp
+            mbar_init(&s.t_empty[i], 4);  // one arrive per warp of the owning warpgroup
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.c_full[i], 128);
+            mbar_init(&s.c_empty[i], 128);
+        }
+        mbar_init(s.nb_ready, kEpi);
+        mbar_init(s.nb_done, kEpi);
         mbar_init(s.drain, 1);
         *s.abort_flag = 0;
         fence_barrier_init();
@@ -179,6 +196,126 @@ __device__ __forceinline__ void mma_drain(const Smem &s) {
     mbar_drain(s.drain, 0);
 }
 
+// MMA issuer (one thread).  For every K tile: njob jobs of 128 x 128 fp32
+// accumulators into TMEM slot (job % 4).  Pass 1 (KEYS_AS_B): A = Q row block
+// jb, B = the K tile.  Pass 2: A = the K tile, B = Q rows 128 jb ...
+template <int KH, bool KEYS_AS_B>
+__device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int64_t t0, int64_t t1,
+                           int njob) {
+    int stage = 0;
+    uint32_t phase = 0, q_loads = 0, job = 0;
+    bool ok = true;
+    for (int64_t t = t0; t < t1 && ok; ++t) {
+        const int jt = (int)(t % p.tiles_per_unit);
+        const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
+        if (t == t0 || jt == 0) {
+            if (!mbar_wait(s.q_full, q_loads & 1, s.abort_flag, p.status)) break;
+            ++q_loads;
+        }
+        if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int jb = 0; jb < njob; ++jb, ++job) {
+            const uint32_t slot = job & 3, use = job >> 2;
+            if (!mbar_wait(&s.t_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int n = KEYS_AS_B ? kTileKeys : min(128, p.n_pad - jb * 128);
+            const uint32_t idesc = idesc_bf16_f32(128, n);
+            const uint32_t d = tmem + slot * 128;
+#pragma unroll
+            for (int ks = 0; ks < KH * 4; ++ks) {
+                const int kh = ks >> 2, off = (ks & 3) * 32;
+                const uint32_t qa =
+                    smem_u32(s.q + ((size_t)kh * p.rows_pad + jb * 128) * 128) + off;
+                const uint32_t ka = smem_u32(s.k + ((size_t)stage * KH + kh) * kBoxBytes) + off;
+                const uint64_t a = sw128_kmajor_desc(KEYS_AS_B ? qa : ka);
+                const uint64_t b = sw128_kmajor_desc(KEYS_AS_B ? ka : qa);
+                tc_mma_bf16(d, a, b, idesc, ks > 0);
+            }
+            tc_commit(&s.t_full[slot]);
+        }
+        if (!ok) break;
+        tc_commit(&s.empty[stage]);
+        if (last) tc_commit(s.q_empty);
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+        }
+    }
+    mma_drain(s);
+}
+
+// Release a TMEM slot once this warp's loads from it have completed.
+__device__ __forceinline__ void release_slot(uint64_t *bar, int lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ void ld_wait_fence(float (&v)[32]) {
+    tmem_ld_wait();
+    reg_fence(v);
+}
+
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmax3(v[i], v[i + 8], v[i + 16]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], v[i + 24]);
+    return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// sum_i 2^(v_i * cs - ref) with packed f32x2 arithmetic
+__device__ __forceinline__ float expsum32(const float (&v)[32], float cs, float ref) {
+    const unsigned long long cs2 = f2_pack(cs, cs), nr2 = f2_pack(-ref, -ref);
+    unsigned long long s4[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), cs2, nr2), x0, x1);
+        s4[(i >> 1) & 3] = f2_add(s4[(i >> 1) & 3], f2_pack(ex2(x0), ex2(x1)));
+    }
+    float a, b;
+    f2_unpack(f2_add(f2_add(s4[0], s4[1]), f2_add(s4[2], s4[3])), a, b);
+    return a + b;
+}
+
+// Fold 32 logits (-inf = not visible) into a row's running (ref, sum), where
+// sum = sum_j 2^(x_j - ref).  The sum is taken against the current reference
+// while the chunk max is found in parallel; only when a logit exceeds the
+// reference by more than 2^64 is the chunk redone against a new reference.
+__device__ __forceinline__ void row_stats32(const float (&v)[32], float cs, float &ref, float &l) {
+    const float mx = max32(v) * cs;
+    if (mx == -INFINITY) return;
+    if (ref == -INFINITY) ref = mx;                 // first visible chunk of the row
+    if (mx <= ref + 64.f) {
+        l += expsum32(v, cs, ref);
+    } else {
+        l = l * ex2(ref - mx) + expsum32(v, cs, mx);
+        ref = mx;
+    }
+}
+
+// Add 2^(x * cs + nb[i]) for 32 query-row columns into packed partial sums.
+__device__ __forceinline__ void col_sums32(const float (&v)[32], const float *nb, float cs,
+                                           unsigned long long (&a4)[4]) {
+    const float4 *nb4 = reinterpret_cast<const float4 *>(nb);
+    const unsigned long long cs2 = f2_pack(cs, cs);
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 b4 = nb4[i4];
+        const int i = i4 * 4;
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), cs2, f2_pack(b4.x, b4.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(v[i + 2], v[i + 3]), cs2, f2_pack(b4.z, b4.w)), x2, x3);
+        a4[(i4 * 2) & 3] = f2_add(a4[(i4 * 2) & 3], f2_pack(ex2(x0), ex2(x1)));
+        a4[(i4 * 2 + 1) & 3] = f2_add(a4[(i4 * 2 + 1) & 3], f2_pack(ex2(x2), ex2(x3)));
+    }
+}
+
 // --------------------------------------------------------------- pass 1
 template <int KH>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -199,55 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             producer<KH>(s, p, &tq, &tk, t0, t1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, kTileKeys);
-            int stage = 0;
-            uint32_t phase = 0, q_loads = 0;
-            uint32_t job = 0;
-            bool ok = true;
-            for (int64_t t = t0; t < t1 && ok; ++t) {
-                const int jt = (int)(t % p.tiles_per_unit);
-                const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
-                if (t == t0 || jt == 0) {
-                    if (!mbar_wait(s.q_full, q_loads & 1, s.abort_flag, p.status)) break;
-                    ++q_loads;
-                }
-                if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
-                tc_fence_after();
-                for (int rb = 0; rb < nrb; ++rb, ++job) {
-                    const uint32_t slot = job & 3, use = job >> 2;
-                    if (!mbar_wait(&s.t_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d = tmem + slot * 128;
-#pragma unroll
-                    for (int ks = 0; ks < KH * 4; ++ks) {
-                        const int kh = ks >> 2, off = (ks & 3) * 32;
-                        const uint64_t a = sw128_kmajor_desc(
-                            smem_u32(s.q + ((size_t)kh * p.rows_pad + rb * 128) * 128) + off);
-                        const uint64_t b = sw128_kmajor_desc(
-                            smem_u32(s.k + ((size_t)stage * KH + kh) * kBoxBytes) + off);
-                        tc_mma_bf16(d, a, b, idesc, ks > 0);
-                    }
-                    tc_commit(&s.t_full[slot]);
-                }
-                if (!ok) break;
-                tc_commit(&s.empty[stage]);
-                if (last) tc_commit(s.q_empty);
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-            mma_drain(s);
-        }
+        if (lane == 0) mma_issuer<KH, true>(s, p, tmem, t0, t1, nrb);
     } else {
-        // Epilogue: TMEM lane quarter is fixed by warp id % 4.
+        // Epilogue.  Warpgroup ewg owns the row blocks rb with rb % 2 == ewg;
+        // a warp's TMEM lane quarter is fixed by its id % 4, so each thread
+        // owns one query row per row block (two at most: m0/l0, m1/l1).
         const int quarter = warp & 3;
+        const int ewg = (warp - 2) >> 2;
         const int row_in_blk = quarter * 32 + lane;
-        float m_run[4], l_run[4];
+        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
         uint32_t job = 0;
         bool ok = true;
         for (int64_t t = t0; t < t1 && ok; ++t) {
@@ -256,68 +353,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j0 = jt * kTileKeys;
             const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
             if (t == t0 || jt == 0) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    m_run[i] = -INFINITY;
-                    l_run[i] = 0.f;
-                }
+                m0 = m1 = -INFINITY;
+                l0 = l1 = 0.f;
             }
             const bool masked = j0 + kTileKeys - 1 > p.P;
-#pragma unroll
-            for (int rb = 0; rb < 4; ++rb) {
-                if (rb >= nrb) break;
-                const uint32_t slot = job & 3, use = job >> 2;
-                ++job;
+#pragma unroll 1
+            for (int rb = ewg; rb < nrb; rb += 2) {
+                const uint32_t jj = job + rb;
+                const uint32_t slot = jj & 3, use = jj >> 2;
                 if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 128;
-                float v[128];
-                tmem_ld32(taddr + 0, *reinterpret_cast<float(*)[32]>(&v[0]));
-                tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-                tmem_ld32(taddr + 64, *reinterpret_cast<float(*)[32]>(&v[64]));
-                tmem_ld32(taddr + 96, *reinterpret_cast<float(*)[32]>(&v[96]));
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.t_empty[slot]);
-
                 const int r = rb * 128 + row_in_blk;
-                float mx = -INFINITY, sum = 0.f, mnew;
-                if (!masked) {
+                // Largest column of this tile that row r may see.
+                const int lim = masked ? p.P + (r % p.W) - j0 : kTileKeys - 1;
+                float m = (rb >> 1) ? m1 : m0;
+                float l = (rb >> 1) ? l1 : l0;
+                // Four 32-column chunks, each TMEM load issued before the
+                // previous chunk is processed.
+                float va[32], vb[32];
+                tmem_ld32(taddr, va);
+                ld_wait_fence(va);
 #pragma unroll
-                    for (int i = 0; i < 128; ++i) mx = fmaxf(mx, v[i]);
-                    mnew = fmaxf(m_run[rb], mx * p.cs);
+                for (int q = 0; q < 4; q += 2) {
+                    tmem_ld32(taddr + (q + 1) * 32, vb);
+                    if (masked) {
 #pragma unroll
-                    for (int i = 0; i < 128; ++i) sum += ex2(fmaf(v[i], p.cs, -mnew));
-                } else {
-                    // Largest column of this tile that row r may see.
-                    const int lim = p.P + (r % p.W) - j0;
-#pragma unroll
-                    for (int i = 0; i < 128; ++i)
-                        if (i <= lim) mx = fmaxf(mx, v[i]);
-                    mnew = fmaxf(m_run[rb], mx * p.cs);
-                    if (mx > -INFINITY) {
-#pragma unroll
-                        for (int i = 0; i < 128; ++i)
-                            if (i <= lim) sum += ex2(fmaf(v[i], p.cs, -mnew));
+                        for (int i = 0; i < 32; ++i)
+                            if (q * 32 + i > lim) va[i] = -INFINITY;
                     }
+                    row_stats32(va, p.cs, m, l);
+                    ld_wait_fence(vb);
+                    if (q + 2 < 4) tmem_ld32(taddr + (q + 2) * 32, va);
+                    else release_slot(&s.t_empty[slot], lane);   // all four chunks loaded
+                    if (masked) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if ((q + 1) * 32 + i > lim) vb[i] = -INFINITY;
+                    }
+                    row_stats32(vb, p.cs, m, l);
+                    if (q + 2 < 4) ld_wait_fence(va);
                 }
-                if (mx > -INFINITY) {
-                    l_run[rb] = l_run[rb] * ex2(m_run[rb] - mnew) + sum;
-                    m_run[rb] = mnew;
+                if (rb >> 1) {
+                    m1 = m;
+                    l1 = l;
+                } else {
+                    m0 = m;
+                    l0 = l;
                 }
             }
+            job += nrb;
             if (!ok) break;
             if (last) {
                 const int64_t slot_u = c - split_cta_of(p.n_tiles, p.grid, (int64_t)u * p.tiles_per_unit);
                 float2 *dst = p.partial + ((int64_t)u * p.max_slots + slot_u) * p.rows_pad;
-#pragma unroll
-                for (int rb = 0; rb < 4; ++rb) {
+                for (int rb = ewg; rb < nrb; rb += 2) {
                     const int r = rb * 128 + row_in_blk;
-                    if (rb < nrb && r < p.rows) dst[r] = make_float2(m_run[rb], l_run[rb]);
+                    if (r < p.rows) dst[r] = (rb >> 1) ? make_float2(m1, l1) : make_float2(m0, l0);
                 }
             }
         }
@@ -328,6 +423,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Causal mask inside the window for pass 2: row r = g*W + w sees the key iff
+// w >= dj.  w advances with the column and wraps at W; it carries over
+// between consecutive chunks.
+__device__ __forceinline__ void mask_cols(float (&v)[32], int &w, int dj, int W) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (w < dj) v[i] = -INFINITY;
+        w = (w + 1 == W) ? 0 : w + 1;
     }
 }
 
@@ -342,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c = blockIdx.x;
     const int64_t t0 = split_begin(p.n_tiles, p.grid, c), t1 = split_begin(p.n_tiles, p.grid, c + 1);
-    const int nch = (p.n_pad + 255) / 256;
+    const int nch = (p.n_pad + 127) / 128;   // 128-row query chunks (MMA N)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -351,120 +457,111 @@ __global__ void __launch_bounds__(kThreads, 1)
             producer<KH>(s, p, &tq, &tk, t0, t1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, q_loads = 0;
-            uint32_t job = 0;
-            bool ok = true;
-            for (int64_t t = t0; t < t1 && ok; ++t) {
-                const int jt = (int)(t % p.tiles_per_unit);
-                const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
-                if (t == t0 || jt == 0) {
-                    if (!mbar_wait(s.q_full, q_loads & 1, s.abort_flag, p.status)) break;
-                    ++q_loads;
-                }
-                if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
-                tc_fence_after();
-                for (int nc = 0; nc < nch; ++nc, ++job) {
-                    const uint32_t slot = job & 1, use = job >> 1;
-                    if (!mbar_wait(&s.t_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int n = min(256, p.n_pad - nc * 256);
-                    const uint32_t idesc = idesc_bf16_f32(128, n);
-                    const uint32_t d = tmem + slot * 256;
-#pragma unroll
-                    for (int ks = 0; ks < KH * 4; ++ks) {
-                        const int kh = ks >> 2, off = (ks & 3) * 32;
-                        const uint64_t a = sw128_kmajor_desc(
-                            smem_u32(s.k + ((size_t)stage * KH + kh) * kBoxBytes) + off);
-                        const uint64_t b = sw128_kmajor_desc(
-                            smem_u32(s.q + ((size_t)kh * p.rows_pad + nc * 256) * 128) + off);
-                        tc_mma_bf16(d, a, b, idesc, ks > 0);
-                    }
-                    tc_commit(&s.t_full[slot]);
-                }
-                if (!ok) break;
-                tc_commit(&s.empty[stage]);
-                if (last) tc_commit(s.q_empty);
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-            mma_drain(s);
-        }
+        if (lane == 0) mma_issuer<KH, false>(s, p, tmem, t0, t1, nch);
     } else {
+        // Epilogue.  Each thread owns one key (its TMEM lane) and sums
+        // 2^(x + nb_r) over the query rows r of the chunks its warpgroup owns:
+        // chunk nc goes to warpgroup nc % 2 when a tile has several chunks
+        // (warpgroup 1 then hands its partial sum to warpgroup 0 through
+        // shared memory), otherwise whole tiles alternate between the two.
         const int quarter = warp & 3;
-        const int etid = threadIdx.x - 64;   // 0..127 over the epilogue warps
+        const int ewg = (warp - 2) >> 2;
+        const int etid = threadIdx.x - 64;
         const int key_in_tile = quarter * 32 + lane;
         const float rows_f = (float)p.rows;
-        uint32_t job = 0;
+        uint32_t job = 0, unit_changes = 0;
         bool ok = true;
-        float acc = 0.f;
         for (int64_t t = t0; t < t1 && ok; ++t) {
             const int u = (int)(t / p.tiles_per_unit);
             const int jt = (int)(t % p.tiles_per_unit);
             const int j0 = jt * kTileKeys;
+            const uint32_t tl = (uint32_t)(t - t0);
             if (t == t0 || jt == 0) {
-                named_bar_sync(1, kEpiThreads);
-                for (int r = etid; r < p.rows_pad; r += kEpiThreads) {
-                    s.nb[r] = p.neg_bias_in[(int64_t)u * p.rows_pad + r];
-                    s.wr[r] = r < p.rows ? r % p.W : p.W;
+                // stage the unit's row biases in shared memory: everyone is
+                // done with the previous unit's, then everyone sees the new
+                if (unit_changes > 0) {
+                    mbar_arrive(s.nb_done);
+                    if (!mbar_wait(s.nb_done, (unit_changes - 1) & 1, s.abort_flag, p.status)) break;
                 }
-                named_bar_sync(1, kEpiThreads);
+                for (int r = etid; r < p.rows_pad; r += kEpi)
+                    s.nb[r] = p.neg_bias_in[(int64_t)u * p.rows_pad + r];
+                mbar_arrive(s.nb_ready);
+                if (!mbar_wait(s.nb_ready, unit_changes & 1, s.abort_flag, p.status)) break;
+                ++unit_changes;
             }
             const int j = j0 + key_in_tile;
-            const int dj = j - p.P;   // row r sees key j iff wr[r] >= dj
+            const int dj = j - p.P;   // row r = g*W + w sees key j iff w >= dj
             const bool masked = j0 + kTileKeys - 1 > p.P;
+            unsigned long long a4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a4[i] = 0ull;   // (+0, +0) pairs
+#pragma unroll 1
             for (int nc = 0; nc < nch; ++nc) {
-                const uint32_t slot = job & 1, use = job >> 1;
-                ++job;
+                const uint32_t jj = job + nc;
+                const uint32_t slot = jj & 3, use = jj >> 2;
+                const int owner = nch >= 2 ? (nc & 1) : (int)(tl & 1);
+                if (owner != ewg) continue;
                 if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int n = min(256, p.n_pad - nc * 256);
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 256;
-                const float *nb = s.nb + nc * 256;
-                const int *wr = s.wr + nc * 256;
-                for (int cg = 0; cg < n; cg += 32) {
-                    float v[32];
-                    const int cnt = min(32, n - cg);
-                    if (cnt == 32) {
-                        tmem_ld32(taddr + cg, v);
-                    } else {
-                        tmem_ld16(taddr + cg, *reinterpret_cast<float(*)[16]>(&v[0]));
-                    }
-                    tmem_ld_wait();
-                    if (!masked) {
-                        if (cnt == 32) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) acc += ex2(fmaf(v[i], p.cs, nb[cg + i]));
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) acc += ex2(fmaf(v[i], p.cs, nb[cg + i]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (i < cnt) {
-                                const float e = ex2(fmaf(v[i], p.cs, nb[cg + i]));
-                                acc += (wr[cg + i] >= dj) ? e : 0.f;
-                            }
-                        }
-                    }
+                const int n = min(128, p.n_pad - nc * 128);
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 128;
+                const int nq = n / 32;           // full 32-column chunks
+                const int tail = n - nq * 32;     // 0 or 16 columns
+                const int r0 = nc * 128;
+                float va[32], vb[32];
+                int wq = masked ? r0 % p.W : 0;   // window position of the chunk's first row
+                // chunk loop, loads one chunk ahead
+                tmem_ld32(taddr, va);
+                ld_wait_fence(va);
+#pragma unroll 1
+                for (int q = 0; q < nq; q += 2) {
+                    const bool has_b = q + 1 < nq;
+                    if (has_b) tmem_ld32(taddr + (q + 1) * 32, vb);
+                    if (masked) mask_cols(va, wq, dj, p.W);
+                    col_sums32(va, s.nb + r0 + q * 32, p.cs, a4);
+                    if (!has_b) break;
+                    ld_wait_fence(vb);
+                    if (q + 2 < nq) tmem_ld32(taddr + (q + 2) * 32, va);
+                    if (masked) mask_cols(vb, wq, dj, p.W);
+                    col_sums32(vb, s.nb + r0 + (q + 1) * 32, p.cs, a4);
+                    if (q + 2 < nq) ld_wait_fence(va);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.t_empty[slot]);
+                if (tail) {
+                    // 16 leftover columns of a narrow last chunk (its other 16
+                    // TMEM columns hold no logits)
+                    tmem_ld32(taddr + nq * 32, va);
+                    ld_wait_fence(va);
+#pragma unroll
+                    for (int i = 16; i < 32; ++i) va[i] = -INFINITY;
+                    if (masked) mask_cols(va, wq, dj, p.W);
+                    col_sums32(va, s.nb + r0 + nq * 32, p.cs, a4);
+                }
+                release_slot(&s.t_empty[slot], lane);
             }
+            job += nch;
             if (!ok) break;
-            if (j < p.T) p.scores[(int64_t)u * p.T + j] = acc / rows_f;
-            acc = 0.f;
+            float acc, acc_hi;
+            f2_unpack(f2_add(f2_add(a4[0], a4[1]), f2_add(a4[2], a4[3])), acc, acc_hi);
+            acc += acc_hi;
+            if (nch >= 2) {
+                const uint32_t b = tl & 1, ub = tl >> 1;
+                float *red = s.red + b * 128;
+                if (ewg == 1) {
+                    if (!mbar_wait(&s.c_empty[b], (ub & 1) ^ 1, s.abort_flag, p.status)) break;
+                    red[key_in_tile] = acc;
+                    mbar_arrive(&s.c_full[b]);
+                } else {
+                    if (!mbar_wait(&s.c_full[b], ub & 1, s.abort_flag, p.status)) break;
+                    acc += red[key_in_tile];
+                    mbar_arrive(&s.c_empty[b]);
+                    if (j < p.T) p.scores[(int64_t)u * p.T + j] = acc / rows_f;
+                }
+            } else if ((int)(tl & 1) == ewg) {
+                if (j < p.T) p.scores[(int64_t)u * p.T + j] = acc / rows_f;
+            }
         }
     }
 

@@ -24,21 +24,34 @@ namespace kvc {
 namespace {
 
 constexpr int kSelThreads = 1024;
-// Digits of the 32-bit key, most significant first: bits 31..21, 20..10, 9..0.
-__device__ __forceinline__ int digit_bits(int pass) { return pass == 2 ? 10 : 11; }
+
+// A valid score is a non-negative float, so its sign bit is zero and its
+// bit pattern orders like its value.  Radix digits of that 31-bit key, most
+// significant first: bits 30..20 (exponent + 3 mantissa bits), 19..9, 8..0.
+__device__ __forceinline__ int digit_bits(int pass) { return pass == 2 ? 9 : 11; }
+__device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 20 : pass == 1 ? 9 : 0; }
 
 __device__ __forceinline__ int digit_of(uint32_t key, int pass) {
-    return (int)((key >> (pass == 0 ? 21 : pass == 1 ? 10 : 0)) & (pass == 2 ? 0x3FFu : 0x7FFu));
+    return (int)((key >> digit_shift(pass)) & ((1u << digit_bits(pass)) - 1u));
 }
 
 // Does key lie inside the bucket chosen by the earlier passes?
 __device__ __forceinline__ bool in_prefix(uint32_t key, int pass, uint32_t prefix) {
     if (pass == 0) return true;
-    return (key >> (pass == 1 ? 21 : 10)) == prefix;
+    return (key >> (pass == 1 ? 20 : 9)) == prefix;
 }
 
-__device__ __forceinline__ unsigned long long fixed56(float c) {
-    return (unsigned long long)(ldexp((double)c, 56));
+// floor(c * 2^56) for a float 0 <= c <= 1, from its bits with integer
+// operations only (exact): c = m * 2^(e-150) with the 24-bit significand m,
+// so c * 2^56 = m * 2^(e-94).
+__device__ __forceinline__ unsigned long long fixed56(uint32_t key) {
+    const int e = (int)(key >> 23);
+    if (e == 0) return 0;   // zero and subnormals: below 2^-126
+    const unsigned long long m = (key & 0x7FFFFFu) | 0x800000u;
+    const int sh = e - 94;
+    if (sh >= 0) return m << sh;   // sh <= 33 for c <= 1
+    if (sh <= -24) return 0;
+    return m >> (-sh);
 }
 
 // ------------------------------------------------------------------ MBA
@@ -75,7 +88,7 @@ __global__ void __launch_bounds__(kSelThreads)
             if (in_prefix(key, pass, prefix) && key <= 0x3F800000u) {   // 0 <= v <= 1
                 const int d = digit_of(key, pass);
                 atomicAdd(&cnt[d], 1u);
-                atomicAdd(&msum[d], fixed56(v));
+                atomicAdd(&msum[d], fixed56(key));
             }
         }
         __syncthreads();
@@ -151,85 +164,122 @@ __global__ void __launch_bounds__(kSelThreads)
         } else {
             // s_prefix is now the exact crossing value v*; every element above
             // it is counted in s_cnt_gt / s_sum_gt; ties at v* each carry u*.
-            const unsigned long long ustar = fixed56(__uint_as_float(s_prefix));
+            const unsigned long long ustar = fixed56(s_prefix);
             const unsigned __int128 need = (unsigned __int128)num * s_total;
             const unsigned __int128 have = (unsigned __int128)den * s_sum_gt;
             const unsigned __int128 step = (unsigned __int128)den * ustar;
-            const long long k = (long long)((need - have + step - 1) / step);
-            mba[blockIdx.x] = (int32_t)(s_cnt_gt + k);
+            if (step == 0 || have >= need) {
+                // unreachable for valid scores (the crossing bucket always
+                // carries mass); never divide by zero on corrupt input
+                set_status(status, KVC_DEV_BAD_SCORE);
+                mba[blockIdx.x] = (int32_t)s_cnt_gt;
+            } else {
+                const long long k = (long long)((need - have + step - 1) / step);
+                mba[blockIdx.x] = (int32_t)(s_cnt_gt + k);
+            }
         }
     }
 }
 
 // ------------------------------------------------------------------ budgets
-// One thread; L <= 1024 layers.  Largest-remainder split of R over the
-// eligible layers by weight S (equal weights if they sum to 0), ties to the
-// lower layer.
-__device__ void lr_split(int L, const long long *S, const unsigned char *elig, long long R,
-                         long long *add, long long *rem, unsigned char *given) {
-    long long sumw = 0;
-    int n_el = 0;
-    for (int l = 0; l < L; ++l) {
-        add[l] = 0;
-        given[l] = 0;
-        if (elig[l]) {
-            sumw += S[l];
-            ++n_el;
-        }
-    }
-    if (n_el == 0 || R <= 0) return;
-    const bool equal = sumw == 0;
-    if (equal) sumw = n_el;
-    long long handed = 0;
-    for (int l = 0; l < L; ++l) {
-        rem[l] = -1;
-        if (!elig[l]) continue;
-        const unsigned __int128 prod = (unsigned __int128)R * (unsigned long long)(equal ? 1 : S[l]);
-        add[l] = (long long)(prod / (unsigned long long)sumw);
-        rem[l] = (long long)(prod % (unsigned long long)sumw);
-        handed += add[l];
-    }
-    for (long long left = R - handed; left > 0; --left) {
-        int best = -1;
-        for (int l = 0; l < L; ++l)
-            if (elig[l] && !given[l] && (best < 0 || rem[l] > rem[best])) best = l;
-        given[best] = 1;
-        add[best] += 1;
+// One block, one thread per layer (L <= 1024).  Integer arithmetic only.
+constexpr int kMaxLayers = 1024;
+
+// floor(a*b/c) and the remainder, exact (64-bit when the product fits).
+__device__ __forceinline__ void muldiv(unsigned long long a, unsigned long long b,
+                                       unsigned long long c, unsigned long long &q,
+                                       unsigned long long &r) {
+    if (b == 0 || a <= ~0ull / b) {
+        const unsigned long long p = a * b;
+        q = p / c;
+        r = p % c;
+    } else {
+        const unsigned __int128 p = (unsigned __int128)a * b;
+        q = (unsigned long long)(p / c);
+        r = (unsigned long long)(p % c);
     }
 }
 
-constexpr int kMaxLayers = 1024;
+// Largest-remainder split of R over the eligible layers by weight S (equal
+// weights if the eligible weights sum to 0): every layer gets
+// floor(R S_l / sum S); the leftover units go one each to the largest
+// remainders, ties to the lower layer.  Returns the calling thread's share.
+__device__ long long lr_split(int L, const long long *S, const unsigned char *elig, long long R,
+                              long long *rem, unsigned long long *red) {
+    const int l = threadIdx.x;
+    const bool act = l < L;
+    if (l == 0) red[0] = red[1] = red[2] = 0;
+    __syncthreads();
+    const bool e = act && elig[l];
+    if (e) {
+        atomicAdd(&red[0], (unsigned long long)S[l]);
+        atomicAdd(&red[1], 1ull);
+    }
+    __syncthreads();
+    unsigned long long sumw = red[0];
+    const unsigned long long n_el = red[1];
+    if (n_el == 0 || R <= 0) {
+        __syncthreads();
+        return 0;
+    }
+    const bool equal = sumw == 0;
+    if (equal) sumw = n_el;
+    long long add = 0;
+    if (e) {
+        unsigned long long q, r;
+        muldiv((unsigned long long)R, equal ? 1ull : (unsigned long long)S[l], sumw, q, r);
+        add = (long long)q;
+        rem[l] = (long long)r;
+        atomicAdd(&red[2], q);
+    }
+    __syncthreads();
+    const long long left = R - (long long)red[2];
+    if (e && left > 0) {
+        long long rank = 0;
+        for (int o = 0; o < L; ++o)
+            rank += elig[o] && (rem[o] > rem[l] || (rem[o] == rem[l] && o < l));
+        if (rank < left) add += 1;
+    }
+    __syncthreads();
+    return add;
+}
 
-__global__ void budget_kernel(const int32_t *__restrict__ mba, int L, int Hkv, long long P,
-                              long long total, long long floor_, int32_t *__restrict__ budget) {
-    __shared__ long long S[kMaxLayers], B[kMaxLayers], add[kMaxLayers], rem[kMaxLayers];
-    __shared__ unsigned char elig[kMaxLayers], given[kMaxLayers];
-    if (threadIdx.x != 0) return;
+__global__ void __launch_bounds__(kMaxLayers)
+    budget_kernel(const int32_t *__restrict__ mba, int L, int Hkv, long long P, long long total,
+                  long long floor_, int32_t *__restrict__ budget) {
+    __shared__ long long S[kMaxLayers], rem[kMaxLayers];
+    __shared__ unsigned char elig[kMaxLayers];
+    __shared__ unsigned long long red[3];
+    const int l = threadIdx.x;
+    const bool act = l < L;
     if (total >= (long long)L * P) {
-        for (int l = 0; l < L; ++l) budget[l] = (int32_t)P;
+        if (act) budget[l] = (int32_t)P;
         return;
     }
-    for (int l = 0; l < L; ++l) {
+    if (act) {
         long long acc = 0;
         for (int k = 0; k < Hkv; ++k) acc += mba[(int64_t)l * Hkv + k];
         S[l] = acc;
         elig[l] = 1;
     }
-    lr_split(L, S, elig, total - (long long)L * floor_, add, rem, given);
-    for (int l = 0; l < L; ++l) B[l] = floor_ + add[l];
+    __syncthreads();
+    long long B = floor_ + lr_split(L, S, elig, total - (long long)L * floor_, rem, red);
     while (true) {
-        long long excess = 0;
-        for (int l = 0; l < L; ++l)
-            if (B[l] > P) {
-                excess += B[l] - P;
-                B[l] = P;
-            }
+        if (l == 0) red[0] = 0;
+        __syncthreads();
+        if (act && B > P) {
+            atomicAdd(&red[0], (unsigned long long)(B - P));
+            B = P;
+        }
+        __syncthreads();
+        const unsigned long long excess = red[0];
+        __syncthreads();
         if (excess == 0) break;
-        for (int l = 0; l < L; ++l) elig[l] = B[l] < P;
-        lr_split(L, S, elig, excess, add, rem, given);
-        for (int l = 0; l < L; ++l) B[l] += add[l];
+        if (act) elig[l] = B < P;
+        __syncthreads();
+        B += lr_split(L, S, elig, (long long)excess, rem, red);
     }
-    for (int l = 0; l < L; ++l) budget[l] = (int32_t)B[l];
+    if (act) budget[l] = (int32_t)B;
 }
 
 // ------------------------------------------------------------------ top-K
@@ -364,7 +414,7 @@ __global__ void __launch_bounds__(kSelThreads)
         for (int i = 0; i < 4; ++i) {
             if (gt[i] || (eq[i] && E < need_eq)) {
                 const long long pos = G + (E < need_eq ? E : need_eq);
-                out[pos] = j0 + i;
+                if (pos < B) out[pos] = j0 + i;   // always true for valid scores
             }
             G += gt[i];
             E += eq[i];
@@ -397,7 +447,7 @@ int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t
         set_error("kvc_mba_budget: at most %d layers", kMaxLayers);
         return KVC_ERR_UNSUPPORTED;
     }
-    budget_kernel<<<1, 32, 0, st>>>(mba, s.n_layers, s.n_kv_heads,
+    budget_kernel<<<1, (s.n_layers + 31) / 32 * 32, 0, st>>>(mba, s.n_layers, s.n_kv_heads,
                                     (long long)s.seq_len - s.window, (long long)total,
                                     (long long)floor_, budget);
     cudaError_t e = cudaGetLastError();
