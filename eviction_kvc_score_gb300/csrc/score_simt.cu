@@ -144,8 +144,11 @@ __global__ void __launch_bounds__(kSimtThreads)
     }
 }
 
-// Merge: nb_r = -(M + log2 sum_s l_s 2^(m_s - M)) over the unit's slots, in
-// fp64; pad rows get -inf so that they contribute nothing in pass 2.
+// Merge: nb_r = -(M + log2 sum_s l_s 2^(m_s - M)) over the unit's slots
+// (fp32: the few terms are within a factor 2^64 of each other and the result
+// needs ~1e-6 relative accuracy; fp64 runs at a small fraction of the fp32
+// rate on this GPU); pad rows get -inf so that they contribute nothing in
+// pass 2.
 __global__ void score_merge(const float2 *__restrict__ partial, float *__restrict__ neg_bias,
                             int64_t n_units, int64_t tiles_per_unit, int64_t n_tiles, int grid,
                             int max_slots, int rows, int rows_pad) {
@@ -160,14 +163,14 @@ __global__ void score_merge(const float2 *__restrict__ partial, float *__restric
     const int64_t first = split_cta_of(n_tiles, grid, u * tiles_per_unit);
     const int64_t last = split_cta_of(n_tiles, grid, u * tiles_per_unit + tiles_per_unit - 1);
     const float2 *pp = partial + u * max_slots * (int64_t)rows_pad + r;
-    double m = -INFINITY;
-    for (int64_t s = 0; s <= last - first; ++s) m = fmax(m, (double)pp[s * rows_pad].x);
-    double l = 0.0;
+    float m = -INFINITY;
+    for (int64_t s = 0; s <= last - first; ++s) m = fmaxf(m, pp[s * rows_pad].x);
+    float l = 0.f;
     for (int64_t s = 0; s <= last - first; ++s) {
         const float2 v = pp[s * rows_pad];
-        if (v.x > -INFINITY) l += (double)v.y * exp2((double)v.x - m);
+        if (v.x > -INFINITY) l += v.y * exp2f(v.x - m);
     }
-    neg_bias[i] = (float)(-(m + log2(l)));
+    neg_bias[i] = -(m + log2f(l));
 }
 
 template <typename T>

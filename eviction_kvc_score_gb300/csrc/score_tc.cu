@@ -27,10 +27,11 @@
 // producer, warp 1 MMA issuer (and TMEM owner), warps 2-9 epilogue in two
 // warpgroups.  TMEM holds four 128-column accumulator slots; each MMA job
 // fills one 128 x 128 slot and the warpgroups take alternate jobs, so one
-// computes while the other waits for its TMEM load or its next MMA.  Each
-// thread keeps eight independent max / sum chains, and the epilogue has one
-// copy of its inner loop (the window's causal mask is applied by setting
-// invisible logits to -inf first) so that it fits the instruction cache.
+// computes while the other waits for its TMEM load or its next MMA.  A job is
+// read from TMEM in two 64-column halves; each thread keeps eight independent
+// max / sum chains, and the epilogue has one copy of its inner loop (the
+// window's causal mask is applied by setting invisible logits to -inf first)
+// so that it fits the instruction cache.
 // Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
@@ -254,65 +255,62 @@ __device__ __forceinline__ void release_slot(uint64_t *bar, int lane) {
     if (lane == 0) mbar_arrive(bar);
 }
 
-__device__ __forceinline__ void ld_wait_fence(float (&v)[32]) {
+// 64 consecutive fp32 columns of this thread's TMEM lane -> v, completed.
+__device__ __forceinline__ void load_row64(uint32_t taddr, float (&v)[2][32]) {
+    tmem_ld32(taddr + 0, v[0]);
+    tmem_ld32(taddr + 32, v[1]);
     tmem_ld_wait();
-    reg_fence(v);
+    reg_fence(v[0]);
+    reg_fence(v[1]);
 }
 
-__device__ __forceinline__ float max32(const float (&v)[32]) {
-    float m[8];
+// Fold 64 logits (-inf = not visible) into a row's online (max, sum) in base
+// 2, with eight independent max and sum chains.
+__device__ __forceinline__ void row_stats64(const float (&v)[2][32], float cs, float &m_run,
+                                            float &l_run) {
+    float mx8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = fmax3(v[i], v[i + 8], v[i + 16]);
+    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(v[0][i], v[0][i + 8]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], v[i + 24]);
-    return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
-}
-
-// sum_i 2^(v_i * cs - ref) with packed f32x2 arithmetic
-__device__ __forceinline__ float expsum32(const float (&v)[32], float cs, float ref) {
-    const unsigned long long cs2 = f2_pack(cs, cs), nr2 = f2_pack(-ref, -ref);
-    unsigned long long s4[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), cs2, nr2), x0, x1);
-        s4[(i >> 1) & 3] = f2_add(s4[(i >> 1) & 3], f2_pack(ex2(x0), ex2(x1)));
-    }
-    float a, b;
-    f2_unpack(f2_add(f2_add(s4[0], s4[1]), f2_add(s4[2], s4[3])), a, b);
-    return a + b;
-}
-
-// Fold 32 logits (-inf = not visible) into a row's running (ref, sum), where
-// sum = sum_j 2^(x_j - ref).  The sum is taken against the current reference
-// while the chunk max is found in parallel; only when a logit exceeds the
-// reference by more than 2^64 is the chunk redone against a new reference.
-__device__ __forceinline__ void row_stats32(const float (&v)[32], float cs, float &ref, float &l) {
-    const float mx = max32(v) * cs;
+    for (int i = 16; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], v[i >> 5][i & 31]);
+    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
     if (mx == -INFINITY) return;
-    if (ref == -INFINITY) ref = mx;                 // first visible chunk of the row
-    if (mx <= ref + 64.f) {
-        l += expsum32(v, cs, ref);
-    } else {
-        l = l * ex2(ref - mx) + expsum32(v, cs, mx);
-        ref = mx;
+    const float mnew = fmaxf(m_run, mx * cs);
+    float s8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s8[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) s8[i & 7] += ex2(fmaf(v[i >> 5][i & 31], cs, -mnew));
+    const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+    l_run = l_run * ex2(m_run - mnew) + sum;
+    m_run = mnew;
+}
+
+// Add 2^(x * cs + nb[i]) for 64 query-row columns into eight partial sums.
+__device__ __forceinline__ void col_sums64(const float (&v)[2][32], const float *nb, float cs,
+                                           float (&a8)[8]) {
+    const float4 *nb4 = reinterpret_cast<const float4 *>(nb);
+#pragma unroll
+    for (int i4 = 0; i4 < 16; ++i4) {
+        const float4 b4 = nb4[i4];
+        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = i4 * 4 + e;
+            a8[i & 7] += ex2(fmaf(v[i >> 5][i & 31], cs, bb[e]));
+        }
     }
 }
 
-// Add 2^(x * cs + nb[i]) for 32 query-row columns into packed partial sums.
-__device__ __forceinline__ void col_sums32(const float (&v)[32], const float *nb, float cs,
-                                           unsigned long long (&a4)[4]) {
-    const float4 *nb4 = reinterpret_cast<const float4 *>(nb);
-    const unsigned long long cs2 = f2_pack(cs, cs);
+// Causal mask inside the window for pass 2: row r = g*W + w sees the key iff
+// w >= dj.  w advances with the column and wraps at W; it carries over
+// between consecutive chunks.
+__device__ __forceinline__ void mask_cols(float (&v)[32], int &w, int dj, int W) {
 #pragma unroll
-    for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 b4 = nb4[i4];
-        const int i = i4 * 4;
-        float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), cs2, f2_pack(b4.x, b4.y)), x0, x1);
-        f2_unpack(f2_fma(f2_pack(v[i + 2], v[i + 3]), cs2, f2_pack(b4.z, b4.w)), x2, x3);
-        a4[(i4 * 2) & 3] = f2_add(a4[(i4 * 2) & 3], f2_pack(ex2(x0), ex2(x1)));
-        a4[(i4 * 2 + 1) & 3] = f2_add(a4[(i4 * 2 + 1) & 3], f2_pack(ex2(x2), ex2(x3)));
+    for (int i = 0; i < 32; ++i) {
+        if (w < dj) v[i] = -INFINITY;
+        w = (w + 1 == W) ? 0 : w + 1;
     }
 }
 
@@ -372,30 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lim = masked ? p.P + (r % p.W) - j0 : kTileKeys - 1;
                 float m = (rb >> 1) ? m1 : m0;
                 float l = (rb >> 1) ? l1 : l0;
-                // Four 32-column chunks, each TMEM load issued before the
-                // previous chunk is processed.
-                float va[32], vb[32];
-                tmem_ld32(taddr, va);
-                ld_wait_fence(va);
-#pragma unroll
-                for (int q = 0; q < 4; q += 2) {
-                    tmem_ld32(taddr + (q + 1) * 32, vb);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[2][32];
+                    load_row64(taddr + h * 64, v);
+                    if (h == 1) release_slot(&s.t_empty[slot], lane);   // values are in registers
                     if (masked) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (q * 32 + i > lim) va[i] = -INFINITY;
+                        for (int i = 0; i < 64; ++i)
+                            if (h * 64 + i > lim) v[i >> 5][i & 31] = -INFINITY;
                     }
-                    row_stats32(va, p.cs, m, l);
-                    ld_wait_fence(vb);
-                    if (q + 2 < 4) tmem_ld32(taddr + (q + 2) * 32, va);
-                    else release_slot(&s.t_empty[slot], lane);   // all four chunks loaded
-                    if (masked) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if ((q + 1) * 32 + i > lim) vb[i] = -INFINITY;
-                    }
-                    row_stats32(vb, p.cs, m, l);
-                    if (q + 2 < 4) ld_wait_fence(va);
+                    row_stats64(v, p.cs, m, l);
                 }
                 if (rb >> 1) {
                     m1 = m;
@@ -423,17 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// Causal mask inside the window for pass 2: row r = g*W + w sees the key iff
-// w >= dj.  w advances with the column and wraps at W; it carries over
-// between consecutive chunks.
-__device__ __forceinline__ void mask_cols(float (&v)[32], int &w, int dj, int W) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        if (w < dj) v[i] = -INFINITY;
-        w = (w + 1 == W) ? 0 : w + 1;
     }
 }
 
@@ -492,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = j0 + key_in_tile;
             const int dj = j - p.P;   // row r = g*W + w sees key j iff w >= dj
             const bool masked = j0 + kTileKeys - 1 > p.P;
-            unsigned long long a4[4];
+            float a8[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a4[i] = 0ull;   // (+0, +0) pairs
+            for (int i = 0; i < 8; ++i) a8[i] = 0.f;
 #pragma unroll 1
             for (int nc = 0; nc < nch; ++nc) {
                 const uint32_t jj = job + nc;
@@ -508,44 +482,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int n = min(128, p.n_pad - nc * 128);
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 128;
-                const int nq = n / 32;           // full 32-column chunks
-                const int tail = n - nq * 32;     // 0 or 16 columns
-                const int r0 = nc * 128;
-                float va[32], vb[32];
-                int wq = masked ? r0 % p.W : 0;   // window position of the chunk's first row
-                // chunk loop, loads one chunk ahead
-                tmem_ld32(taddr, va);
-                ld_wait_fence(va);
+                const int nh = (n + 63) / 64;
 #pragma unroll 1
-                for (int q = 0; q < nq; q += 2) {
-                    const bool has_b = q + 1 < nq;
-                    if (has_b) tmem_ld32(taddr + (q + 1) * 32, vb);
-                    if (masked) mask_cols(va, wq, dj, p.W);
-                    col_sums32(va, s.nb + r0 + q * 32, p.cs, a4);
-                    if (!has_b) break;
-                    ld_wait_fence(vb);
-                    if (q + 2 < nq) tmem_ld32(taddr + (q + 2) * 32, va);
-                    if (masked) mask_cols(vb, wq, dj, p.W);
-                    col_sums32(vb, s.nb + r0 + (q + 1) * 32, p.cs, a4);
-                    if (q + 2 < nq) ld_wait_fence(va);
-                }
-                if (tail) {
-                    // 16 leftover columns of a narrow last chunk (its other 16
-                    // TMEM columns hold no logits)
-                    tmem_ld32(taddr + nq * 32, va);
-                    ld_wait_fence(va);
+                for (int h = 0; h < nh; ++h) {
+                    float v[2][32];
+                    load_row64(taddr + h * 64, v);
+                    if (h == nh - 1) release_slot(&s.t_empty[slot], lane);
+                    const int valid = n - h * 64;   // narrow last chunk: 16..48 columns
+                    if (valid < 64) {
 #pragma unroll
-                    for (int i = 16; i < 32; ++i) va[i] = -INFINITY;
-                    if (masked) mask_cols(va, wq, dj, p.W);
-                    col_sums32(va, s.nb + r0 + nq * 32, p.cs, a4);
+                        for (int i = 0; i < 64; ++i)
+                            if (i >= valid) v[i >> 5][i & 31] = -INFINITY;
+                    }
+                    const int r0 = nc * 128 + h * 64;
+                    if (masked) {
+                        int w = r0 % p.W;
+                        mask_cols(v[0], w, dj, p.W);
+                        mask_cols(v[1], w, dj, p.W);
+                    }
+                    col_sums64(v, s.nb + r0, p.cs, a8);
                 }
-                release_slot(&s.t_empty[slot], lane);
             }
             job += nch;
             if (!ok) break;
-            float acc, acc_hi;
-            f2_unpack(f2_add(f2_add(a4[0], a4[1]), f2_add(a4[2], a4[3])), acc, acc_hi);
-            acc += acc_hi;
+            float acc = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
             if (nch >= 2) {
                 const uint32_t b = tl & 1, ub = tl >> 1;
                 float *red = s.red + b * 128;

@@ -3,12 +3,12 @@
 // MBA (blog post "ZigZagKV, KVCache 80% compression near-lossless", section
 // "ZigZagKV's new observations"): the fewest tokens whose scores reach 90%
 // of a head's attention mass.  Mass is exact fixed point u = floor(c*2^56),
-// so the count does not depend on summation order.  Instead of sorting, a
-// three-pass MSB radix select over the fp32 bit patterns (non-negative floats
-// order like their bit patterns) keeps, per digit bucket, the count and the
-// u-sum, and descends into the bucket where the running mass from the top
-// first reaches the threshold.  The exact crossing value v* and the mass
-// above it then give the count in closed form.
+// so the count does not depend on summation order.  Instead of sorting, an
+// MSB radix select over the fp32 bit patterns (non-negative floats order like
+// their bit patterns) keeps, per digit bucket, the count and the u-mass, and
+// descends into the bucket where the running mass from the top first reaches
+// the threshold.  The exact crossing value v* and the mass above it then give
+// the count in closed form.
 //
 // Budgets (same post, "ZigZagKV space allocation"): integer proportional
 // split with a floor and largest remainders, capped at the prefix length.
@@ -17,6 +17,13 @@
 // the B-th largest prefix score, then an ordered block-wide compaction that
 // keeps everything above it and the lowest-index ties, writing positions in
 // ascending order.
+//
+// Histograms: one shared histogram per block with a 12-bit first digit
+// (exponent plus four mantissa bits, so a head's scores spread over many
+// buckets).  Within a warp the lanes that share the first active lane's digit
+// are added as one group (ballot + warp reductions), the rest one by one.
+// Only native 32-bit shared atomics are used: the exact 64-bit mass of a
+// bucket is a (hi, lo) word pair, lo's carry folded into hi.
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -24,12 +31,15 @@ namespace kvc {
 namespace {
 
 constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kBuckets = 4096;
+constexpr int kPasses = 3;
 
 // A valid score is a non-negative float, so its sign bit is zero and its
-// bit pattern orders like its value.  Radix digits of that 31-bit key, most
-// significant first: bits 30..20 (exponent + 3 mantissa bits), 19..9, 8..0.
-__device__ __forceinline__ int digit_bits(int pass) { return pass == 2 ? 9 : 11; }
-__device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 20 : pass == 1 ? 9 : 0; }
+// 31-bit pattern orders like its value.  Three radix digits, most significant
+// first: bits 30..19 (exponent and top mantissa bits), 18..9, 8..0.
+__device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 19 : pass == 1 ? 9 : 0; }
+__device__ __forceinline__ int digit_bits(int pass) { return pass == 0 ? 12 : pass == 1 ? 10 : 9; }
 
 __device__ __forceinline__ int digit_of(uint32_t key, int pass) {
     return (int)((key >> digit_shift(pass)) & ((1u << digit_bits(pass)) - 1u));
@@ -37,8 +47,7 @@ __device__ __forceinline__ int digit_of(uint32_t key, int pass) {
 
 // Does key lie inside the bucket chosen by the earlier passes?
 __device__ __forceinline__ bool in_prefix(uint32_t key, int pass, uint32_t prefix) {
-    if (pass == 0) return true;
-    return (key >> (pass == 1 ? 20 : 9)) == prefix;
+    return pass == 0 || (key >> digit_shift(pass - 1)) == prefix;
 }
 
 // floor(c * 2^56) for a float 0 <= c <= 1, from its bits with integer
@@ -54,18 +63,83 @@ __device__ __forceinline__ unsigned long long fixed56(uint32_t key) {
     return m >> (-sh);
 }
 
+// Called by all 32 lanes of one warp.  Walks the nb buckets from the largest
+// digit down and finds the first one at which the running total (base plus
+// everything above) reaches the target, as decided by reach(total).  Lane L
+// owns the buckets [nb-(L+1)per, nb-L*per); the lanes scan their range sums
+// and the first lane whose range reaches walks its own buckets.  That lane
+// stores the bucket, the total strictly above it and the count strictly above
+// it to *chosen, *above, *cabove (shared memory).
+template <typename V, typename VA, typename Reach>
+__device__ __forceinline__ void find_bucket(const VA *val, const uint32_t *cnt, int nb, V base,
+                                            long long cbase, Reach reach, int *chosen, V *above,
+                                            long long *cabove) {
+    const int lane = threadIdx.x & 31;
+    const int per = nb / 32;
+    const int lo = nb - (lane + 1) * per;
+    V ls = 0;
+    long long lc = 0;
+    for (int k = 0; k < per; ++k) {   // staggered order: no bank conflicts
+        const int d = lo + ((k + lane) & (per - 1));
+        ls += (V)val[d];
+        lc += cnt[d];
+    }
+    V incl = ls;
+    long long incl_c = lc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const V a = __shfl_up_sync(0xffffffffu, incl, o);
+        const long long b = __shfl_up_sync(0xffffffffu, incl_c, o);
+        if (lane >= o) {
+            incl += a;
+            incl_c += b;
+        }
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, reach(base + incl));
+    const int finder = mask ? __ffs(mask) - 1 : 31;   // no lane: corrupt input
+    if (lane == finder) {
+        V run = base + incl - ls;
+        long long runc = cbase + incl_c - lc;
+        int pick = lo;
+        for (int d = lo + per - 1; d >= lo; --d) {
+            if (reach(run + (V)val[d])) {
+                pick = d;
+                break;
+            }
+            run += (V)val[d];
+            runc += cnt[d];
+        }
+        *chosen = pick;
+        *above = run;
+        *cabove = runc;
+    }
+}
+
 // ------------------------------------------------------------------ MBA
+struct MbaSmem {
+    uint32_t cnt[kBuckets];
+    uint32_t lo[kBuckets];
+    uint32_t hi[kBuckets];
+    unsigned long long msum[kBuckets];
+};
+
+__device__ __forceinline__ void add_mass(MbaSmem &sm, int d, unsigned long long x) {
+    const uint32_t lo = (uint32_t)x;
+    const uint32_t old = atomicAdd(&sm.lo[d], lo);
+    atomicAdd(&sm.hi[d], (uint32_t)(x >> 32) + (old + lo < old ? 1u : 0u));
+}
+
 __global__ void __launch_bounds__(kSelThreads)
     mba_kernel(const float *__restrict__ scores, int T, uint32_t num, uint32_t den,
                int32_t *__restrict__ mba, uint32_t *status) {
-    __shared__ uint32_t cnt[2048];
-    __shared__ unsigned long long msum[2048];
+    extern __shared__ __align__(16) uint8_t sel_smem[];
+    MbaSmem &sm = *reinterpret_cast<MbaSmem *>(sel_smem);
     __shared__ unsigned long long s_total, s_sum_gt;
     __shared__ long long s_cnt_gt;
     __shared__ uint32_t s_prefix;
-    __shared__ int s_bad, s_done;
+    __shared__ int s_bad, s_done, s_chosen;
     const float *c = scores + (int64_t)blockIdx.x * T;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
         s_sum_gt = 0;
         s_cnt_gt = 0;
@@ -73,44 +147,60 @@ __global__ void __launch_bounds__(kSelThreads)
         s_bad = 0;
         s_done = 0;
     }
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = 0; pass < kPasses; ++pass) {
         const int nb = 1 << digit_bits(pass);
-        for (int d = tid; d < nb; d += kSelThreads) {
-            cnt[d] = 0;
-            msum[d] = 0;
+        for (int i = tid; i < nb; i += kSelThreads) {
+            sm.cnt[i] = 0;
+            sm.lo[i] = 0;
+            sm.hi[i] = 0;
         }
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        for (int j = tid; j < T; j += kSelThreads) {
-            const float v = c[j];
+        const int lane = tid & 31;
+        for (int base = 0; base < T; base += kSelThreads) {   // uniform trip count
+            const int j = base + tid;
+            const float v = j < T ? c[j] : 0.f;
             const uint32_t key = __float_as_uint(v);
-            if (pass == 0 && !(v >= 0.f && v <= 1.f)) s_bad = 1;
-            if (in_prefix(key, pass, prefix) && key <= 0x3F800000u) {   // 0 <= v <= 1
-                const int d = digit_of(key, pass);
-                atomicAdd(&cnt[d], 1u);
-                atomicAdd(&msum[d], fixed56(key));
+            if (pass == 0 && j < T && !(v >= 0.f && v <= 1.f)) s_bad = 1;
+            const bool valid = j < T && key <= 0x3F800000u && in_prefix(key, pass, prefix);
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            if (vmask == 0) continue;
+            // peel the first valid lane's digit: its lanes add as one group
+            const int d = digit_of(key, pass);
+            const int leader = __ffs(vmask) - 1;
+            const int dl = __shfl_sync(0xffffffffu, d, leader);
+            const bool same = valid && d == dl;
+            const unsigned smask = __ballot_sync(0xffffffffu, same);
+            const unsigned long long u = valid ? fixed56(key) : 0ull;
+            const unsigned long long us = same ? u : 0ull;
+            const unsigned s0 = __reduce_add_sync(0xffffffffu, (unsigned)(us & 0x7FFFu));
+            const unsigned s1 = __reduce_add_sync(0xffffffffu, (unsigned)((us >> 15) & 0x7FFFu));
+            const unsigned s2 = __reduce_add_sync(0xffffffffu, (unsigned)((us >> 30) & 0x7FFFu));
+            const unsigned s3 = __reduce_add_sync(0xffffffffu, (unsigned)(us >> 45));
+            if (lane == leader) {
+                atomicAdd(&sm.cnt[dl], (uint32_t)__popc(smask));
+                add_mass(sm, dl, (unsigned long long)s0 + ((unsigned long long)s1 << 15) +
+                                     ((unsigned long long)s2 << 30) + ((unsigned long long)s3 << 45));
+            }
+            if (valid && !same) {
+                atomicAdd(&sm.cnt[d], 1u);
+                add_mass(sm, d, u);
             }
         }
         __syncthreads();
-        if (tid < 32) {
-            // Warp 0: lane L sums the buckets [nb - (L+1)*per, nb - L*per), so
-            // lane order runs from the largest digit down.
-            const int per = nb / 32;
-            const int lo = nb - (tid + 1) * per;
-            unsigned long long ls = 0;
-            long long lc = 0;
-            for (int d = lo; d < lo + per; ++d) {
-                ls += msum[d];
-                lc += cnt[d];
-            }
+        for (int d = tid; d < nb; d += kSelThreads)
+            sm.msum[d] = ((unsigned long long)sm.hi[d] << 32) + sm.lo[d];
+        __syncthreads();
+        if (warp == 0) {
             if (pass == 0) {
-                unsigned long long tot = ls;
+                unsigned long long tot = 0;
+                for (int d = tid; d < nb; d += 32) tot += sm.msum[d];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
                 if (tid == 0) {
                     s_total = tot;
-                    // sum of the scores above 16 (or invalid values) would
-                    // overflow the exact comparisons below
+                    // a head whose scores sum above 16 (or hold invalid values)
+                    // would overflow the exact comparisons below
                     if (s_bad || tot > (1ull << 60)) s_bad = 1;
                     if (s_bad || (unsigned __int128)num * tot == 0) s_done = 1;
                 }
@@ -118,38 +208,12 @@ __global__ void __launch_bounds__(kSelThreads)
             }
             if (!s_done) {
                 const unsigned __int128 need = (unsigned __int128)num * s_total;
-                // inclusive scan of the lane sums from lane 0 (largest digits)
-                unsigned long long incl = ls;
-                long long incl_c = lc;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long a = __shfl_up_sync(0xffffffffu, incl, o);
-                    const long long b = __shfl_up_sync(0xffffffffu, incl_c, o);
-                    if (tid >= o) {
-                        incl += a;
-                        incl_c += b;
-                    }
-                }
-                const unsigned long long base = s_sum_gt;
-                const bool reach = (unsigned __int128)den * (base + incl) >= need;
-                const unsigned mask = __ballot_sync(0xffffffffu, reach);
-                const int L = __ffs(mask) - 1;   // first lane whose range reaches
-                if (tid == L) {
-                    unsigned long long run = base + incl - ls;   // mass above my range
-                    long long runc = s_cnt_gt + incl_c - lc;
-                    int chosen = lo;
-                    for (int d = lo + per - 1; d >= lo; --d) {
-                        if ((unsigned __int128)den * (run + msum[d]) >= need) {
-                            chosen = d;
-                            break;
-                        }
-                        run += msum[d];
-                        runc += cnt[d];
-                    }
-                    s_sum_gt = run;
-                    s_cnt_gt = runc;
-                    s_prefix = (prefix << digit_bits(pass)) | (uint32_t)chosen;
-                }
+                find_bucket<unsigned long long>(
+                    sm.msum, sm.cnt, nb, s_sum_gt, s_cnt_gt,
+                    [&](unsigned long long x) { return (unsigned __int128)den * x >= need; },
+                    &s_chosen, &s_sum_gt, &s_cnt_gt);
+                __syncwarp();
+                if (tid == 0) s_prefix = (prefix << digit_bits(pass)) | (uint32_t)s_chosen;
             }
         }
         __syncthreads();
@@ -283,7 +347,7 @@ __global__ void __launch_bounds__(kMaxLayers)
 }
 
 // ------------------------------------------------------------------ top-K
-// Block-wide exclusive scan of one uint32 per thread (1024 threads).
+// Block-wide exclusive scan of one uint32 per thread.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tot, uint32_t *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = v;
@@ -295,14 +359,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = warp_tot[lane];
+        const uint32_t w = lane < kSelWarps ? warp_tot[lane] : 0u;
         uint32_t wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t a = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += a;
         }
-        warp_tot[lane] = wi - w;   // exclusive
+        if (lane < kSelWarps) warp_tot[lane] = wi - w;   // exclusive
         if (lane == 31) *total = wi;
     }
     __syncthreads();
@@ -315,15 +379,15 @@ __global__ void __launch_bounds__(kSelThreads)
     topk_kernel(const float *__restrict__ scores, int T, int P, int Hkv,
                 const int32_t *__restrict__ budget, int k_max, int32_t *__restrict__ idx,
                 uint32_t *status) {
-    __shared__ uint32_t cnt[2048];
+    __shared__ uint32_t cnt[kBuckets];
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t s_total;
     __shared__ uint32_t s_prefix;
-    __shared__ long long s_cnt_gt;
-    __shared__ int s_bad;
+    __shared__ long long s_cnt_gt, s_dummy;
+    __shared__ int s_bad, s_chosen;
     const int head = blockIdx.x;
     const int l = head / Hkv;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const float *c = scores + (int64_t)head * T;
     int32_t *out = idx + (int64_t)head * k_max;
     long long B = budget[l];
@@ -346,45 +410,36 @@ __global__ void __launch_bounds__(kSelThreads)
         s_cnt_gt = 0;
         s_bad = 0;
     }
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = 0; pass < kPasses; ++pass) {
         const int nb = 1 << digit_bits(pass);
-        for (int d = tid; d < nb; d += kSelThreads) cnt[d] = 0;
+        for (int i = tid; i < nb; i += kSelThreads) cnt[i] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        for (int j = tid; j < P; j += kSelThreads) {
-            const float v = c[j];
+        const int lane = tid & 31;
+        for (int base = 0; base < P; base += kSelThreads) {
+            const int j = base + tid;
+            const float v = j < P ? c[j] : 0.f;
             const uint32_t key = __float_as_uint(v);
-            if (pass == 0 && !(v >= 0.f)) s_bad = 1;
-            if (in_prefix(key, pass, prefix)) atomicAdd(&cnt[digit_of(key, pass)], 1u);
+            if (pass == 0 && j < P && !(v >= 0.f)) s_bad = 1;
+            const bool valid = j < P && in_prefix(key, pass, prefix);
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            if (vmask == 0) continue;
+            const int d = digit_of(key, pass);
+            const int leader = __ffs(vmask) - 1;
+            const int dl = __shfl_sync(0xffffffffu, d, leader);
+            const bool same = valid && d == dl;
+            const unsigned smask = __ballot_sync(0xffffffffu, same);
+            if (lane == leader) atomicAdd(&cnt[dl], (uint32_t)__popc(smask));
+            if (valid && !same) atomicAdd(&cnt[d], 1u);
         }
         __syncthreads();
-        if (tid < 32) {
-            const int per = nb / 32;
-            const int lo = nb - (tid + 1) * per;
-            long long lc = 0;
-            for (int d = lo; d < lo + per; ++d) lc += cnt[d];
-            long long incl = lc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long a = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += a;
-            }
-            const long long base = s_cnt_gt;
-            const unsigned mask = __ballot_sync(0xffffffffu, base + incl >= B);
-            const int L = __ffs(mask) - 1;
-            if (tid == L) {
-                long long run = base + incl - lc;
-                int chosen = lo;
-                for (int d = lo + per - 1; d >= lo; --d) {
-                    if (run + cnt[d] >= B) {
-                        chosen = d;
-                        break;
-                    }
-                    run += cnt[d];
-                }
-                s_cnt_gt = run;
-                s_prefix = (prefix << digit_bits(pass)) | (uint32_t)chosen;
-            }
+        if (warp == 0) {
+            // counts stand in for the values: walk until B elements are reached
+            find_bucket<long long>(
+                cnt, cnt, nb, s_cnt_gt, 0, [&](long long x) { return x >= B; }, &s_chosen,
+                &s_cnt_gt, &s_dummy);
+            __syncwarp();
+            if (tid == 0) s_prefix = (prefix << digit_bits(pass)) | (uint32_t)s_chosen;
         }
         __syncthreads();
     }
@@ -432,7 +487,13 @@ __global__ void __launch_bounds__(kSelThreads)
 int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
                uint32_t *status, cudaStream_t st) {
     const int heads = s.n_layers * s.n_kv_heads;
-    mba_kernel<<<heads, kSelThreads, 0, st>>>(scores, s.seq_len, num, den, mba, status);
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(mba_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(MbaSmem));
+        attr = true;
+    }
+    mba_kernel<<<heads, kSelThreads, sizeof(MbaSmem), st>>>(scores, s.seq_len, num, den, mba, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_mba_budget: MBA launch failed: %s", cudaGetErrorString(e));
