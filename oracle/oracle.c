@@ -381,6 +381,57 @@ int ora_topk_all_f32(const ora_shape *s, const float *scores, const int32_t *bud
 }
 
 /* ---------------------------------------------------------------------------
+ * Optional: pooling of the prefix scores before top-K              [SNAP]
+ *
+ * The post pools each head's scores in 1D ("like a Gaussian blur") so that
+ * the neighbours of an important token are kept with it; it names neither
+ * the kernel's size nor its type.  Reading: an odd kernel k, "same" length
+ * over the prefix j in [0,P): mode 0 averages the in-range entries
+ * j-k/2 .. j+k/2 (dividing by how many lie inside [0,P)), mode 1 takes
+ * their maximum.  Window positions j >= P are copied unchanged (they are
+ * always kept and take no part in the ranking).  Output fp64 [L][H_kv][T].
+ * ------------------------------------------------------------------------- */
+int ora_pool(const ora_shape *s, const double *scores, int32_t kernel, int32_t mode,
+             double *pooled)
+{
+    if (!ora_shape_ok(s) || kernel < 1 || kernel % 2 == 0 || (mode != 0 && mode != 1))
+        return -1;
+    const int64_t T = s->seq_len, P = T - s->window;
+    const int64_t units = (int64_t)s->n_layers * s->n_kv_heads, half = kernel / 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t u = 0; u < units; ++u) {
+        const double *c = scores + u * T;
+        double *o = pooled + u * T;
+        for (int64_t j = 0; j < T; ++j) {
+            if (j >= P) {
+                o[j] = c[j];
+                continue;
+            }
+            const int64_t lo = j - half < 0 ? 0 : j - half;
+            const int64_t hi = j + half > P - 1 ? P - 1 : j + half;
+            double acc = c[lo];
+            for (int64_t t = lo + 1; t <= hi; ++t)
+                acc = mode == 0 ? acc + c[t] : (c[t] > acc ? c[t] : acc);
+            o[j] = mode == 0 ? acc / (double)(hi - lo + 1) : acc;
+        }
+    }
+    return 0;
+}
+
+int ora_pool_f32(const ora_shape *s, const float *scores, int32_t kernel, int32_t mode,
+                 double *pooled)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t n = (int64_t)s->n_layers * s->n_kv_heads * s->seq_len;
+    double *c = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!c) return -2;
+    for (int64_t i = 0; i < n; ++i) c[i] = (double)scores[i];
+    int r = ora_pool(s, c, kernel, mode, pooled);
+    free(c);
+    return r;
+}
+
+/* ---------------------------------------------------------------------------
  * a5. Compaction                                             [SNAP]
  *
  * Layer l of the output holds [H_kv][n_l + W][D] with n_l = min(B_l, P): the

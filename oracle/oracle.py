@@ -63,6 +63,8 @@ def lib():
                 "ora_topk": (i64, [i64, p, i64, p]),
                 "ora_topk_all": (C.c_int, [sp, p, p, i64, p]),
                 "ora_topk_all_f32": (C.c_int, [sp, p, p, i64, p]),
+                "ora_pool": (C.c_int, [sp, p, i32, i32, p]),
+                "ora_pool_f32": (C.c_int, [sp, p, i32, i32, p]),
                 "ora_compact_rows": (i64, [sp, p]),
                 "ora_compact": (i64, [sp, p, p, p, i64, p]),
                 "ora_keep_channels": (i32, [d, i32]),
@@ -172,6 +174,19 @@ def topk_all(s: Shape, scores, budget_l, k_max: int) -> np.ndarray:
         sc = np.ascontiguousarray(scores, dtype=np.float64)
         _check(lib().ora_topk_all(C.byref(s), _ptr(sc), _ptr(b), k_max, _ptr(idx)), "topk")
     return idx
+
+
+def pool(s: Shape, scores, kernel: int, mode: int = 0) -> np.ndarray:
+    """SnapKV pooling of the prefix scores (mode 0 average, 1 max); fp64
+    [L][H_kv][T], window positions copied unchanged."""
+    out = np.empty((s.n_layers, s.n_kv_heads, s.seq_len), dtype=np.float64)
+    if scores.dtype == np.float32:
+        sc = np.ascontiguousarray(scores)
+        _check(lib().ora_pool_f32(C.byref(s), _ptr(sc), kernel, mode, _ptr(out)), "pool")
+    else:
+        sc = np.ascontiguousarray(scores, dtype=np.float64)
+        _check(lib().ora_pool(C.byref(s), _ptr(sc), kernel, mode, _ptr(out)), "pool")
+    return out
 
 
 def compact_rows(s: Shape, budget_l) -> int:

@@ -260,6 +260,71 @@ def test_topk_special_cases():
     assert np.all(np.diff(got) > 0)
 
 
+# ------------------------------------------------------------- optional pooling
+def _pool_shape(L, H, T, W):
+    return O.shape_of(L, H, H, 16, T, W, "f32")
+
+
+@pytest.mark.parametrize("kernel", [1, 3, 5, 7, 31])
+def test_pool_average_equals_normalised_convolution(kernel):
+    # average of the in-range neighbours == box convolution of the prefix
+    # divided by the box convolution of the prefix's indicator ("same" mode)
+    L, H, T, W = 2, 3, 257, 17
+    P = T - W
+    c = np.random.default_rng(kernel).random((L, H, T)) ** 3
+    got = O.pool(_pool_shape(L, H, T, W), c, kernel, 0)
+    box = np.ones(kernel)
+    count = np.convolve(np.ones(P), box, mode="same")
+    for l in range(L):
+        for h in range(H):
+            want = np.convolve(c[l, h, :P], box, mode="same") / count
+            np.testing.assert_allclose(got[l, h, :P], want, rtol=1e-13, atol=0)
+            np.testing.assert_array_equal(got[l, h, P:], c[l, h, P:])
+
+
+@pytest.mark.parametrize("kernel", [1, 3, 9, 63])
+def test_pool_max_equals_maximum_filter(kernel):
+    from scipy.ndimage import maximum_filter1d
+    L, H, T, W = 1, 4, 300, 40
+    P = T - W
+    c = np.random.default_rng(50 + kernel).random((L, H, T))
+    got = O.pool(_pool_shape(L, H, T, W), c, kernel, 1)
+    for h in range(H):
+        want = maximum_filter1d(c[0, h, :P], size=kernel, mode="constant", cval=-np.inf)
+        np.testing.assert_array_equal(got[0, h, :P], want)
+        np.testing.assert_array_equal(got[0, h, P:], c[0, h, P:])
+
+
+def test_pool_special_cases():
+    L, H, T, W = 1, 2, 64, 8
+    s = _pool_shape(L, H, T, W)
+    c = np.random.default_rng(3).random((L, H, T))
+    np.testing.assert_array_equal(O.pool(s, c, 1, 0), c)           # kernel 1: identity
+    np.testing.assert_array_equal(O.pool(s, c, 1, 1), c)
+    flat = np.full((L, H, T), 0.125)
+    np.testing.assert_allclose(O.pool(s, flat, 15, 0), flat, rtol=1e-15)   # edges stay flat
+    # a kernel wider than the prefix averages the whole prefix everywhere
+    s2 = _pool_shape(1, 1, 20, 15)
+    c2 = np.random.default_rng(4).random((1, 1, 20))
+    np.testing.assert_allclose(O.pool(s2, c2, 31, 0)[0, 0, :5], np.full(5, c2[0, 0, :5].mean()),
+                               rtol=1e-14)
+    assert (O.pool(s2, c2, 31, 1)[0, 0, :5] == c2[0, 0, :5].max()).all()
+    for kernel, mode in [(2, 0), (0, 0), (3, 2)]:
+        with pytest.raises(ValueError):
+            O.pool(s, c, kernel, mode)
+
+
+def test_pool_keeps_the_neighbours_of_a_spike():
+    # the point of pooling before top-K: a one-hot spike pulls its neighbours
+    # into the kept set (average ties resolved to the lower index)
+    L, H, T, W = 1, 1, 200, 10
+    c = np.full((L, H, T), 1e-6)
+    c[0, 0, 80] = 1.0
+    pooled = O.pool(_pool_shape(L, H, T, W), c, 5, 0)
+    assert O.topk(pooled[0, 0], T - W, 5).tolist() == [78, 79, 80, 81, 82]
+    assert O.topk(c[0, 0], T - W, 5).tolist() == [0, 1, 2, 3, 80]
+
+
 # --------------------------------------------------------------------------- a5
 def test_compact_equals_fancy_indexing():
     L, H, D, T, W = 3, 2, 8, 40, 5
