@@ -227,6 +227,21 @@ int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *
     return launch_topk(*shape, scores, budget, k_max, idx, status_word(ws), stream);
 }
 
+int kvc_pool_scores(const kvc_shape *shape, const float *scores, int32_t kernel, int32_t mode,
+                    float *pooled, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_pool_scores")) return KVC_ERR_INVALID_ARG;
+    if (!scores || !pooled) return fail(KVC_ERR_INVALID_ARG, "kvc_pool_scores: NULL tensor");
+    if (scores == pooled)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_pool_scores: pooled must not alias scores");
+    if (kernel < 1 || (kernel & 1) == 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_pool_scores: kernel must be odd and >= 1");
+    if (mode != 0 && mode != 1)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_pool_scores: mode must be 0 (average) or 1 (max)");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_pool_scores")) return KVC_ERR_WORKSPACE;
+    return launch_pool(*shape, scores, kernel, mode, pooled, stream);
+}
+
 int kvc_compact(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
                 const int32_t *budget, int32_t k_max, void *k_out, void *v_out, int64_t out_rows,
                 void *ws, size_t ws_bytes, cudaStream_t stream) {

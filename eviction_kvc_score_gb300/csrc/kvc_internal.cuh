@@ -308,6 +308,8 @@ int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t
                   int32_t *budget, cudaStream_t st);
 int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int32_t k_max,
                 int32_t *idx, uint32_t *status, cudaStream_t st);
+int launch_pool(const kvc_shape &s, const float *scores, int32_t kernel, int32_t mode, float *pooled,
+                cudaStream_t st);
 int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
                    const int32_t *budget, int32_t k_max, void *k_out, void *v_out,
                    int64_t out_rows, uint32_t *status, cudaStream_t st);

@@ -54,6 +54,7 @@ _SIGS = {
     "kvc_score_noalloc": (C.c_int, [_sp, _p, _p, _p, _p, _p]),
     "kvc_mba_budget": (C.c_int, [_sp, _p, _u32, _u32, _i64, _i32, _p, _p, _p, _sz, _p]),
     "kvc_topk_select": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
+    "kvc_pool_scores": (C.c_int, [_sp, _p, _i32, _i32, _p, _p, _sz, _p]),
     "kvc_compact": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune": (C.c_int, [_sp, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
     "kvc_keep_channels": (_i32, [_d, _i32]),
@@ -144,6 +145,13 @@ def kvc_mba_budget(s: KvcShape, scores, mass_num: int, mass_den: int, total_budg
 def kvc_topk_select(s: KvcShape, scores, budget, k_max: int, idx, ws, stream=None) -> None:
     _check("kvc_topk_select", _lib.kvc_topk_select(
         C.byref(s), _ptr(scores), _ptr(budget), int(k_max), _ptr(idx), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def kvc_pool_scores(s: KvcShape, scores, kernel: int, mode: int, pooled, ws, stream=None) -> None:
+    """SnapKV 1D pooling of the prefix scores (mode 0 average, 1 max)."""
+    _check("kvc_pool_scores", _lib.kvc_pool_scores(
+        C.byref(s), _ptr(scores), int(kernel), int(mode), _ptr(pooled), _ptr(ws), ws.numel(),
         _stream(stream)))
 
 

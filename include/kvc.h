@@ -170,6 +170,22 @@ int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *
                     int32_t k_max, int32_t *idx, void *ws, size_t ws_bytes,
                     cudaStream_t stream);
 
+/* Optional step before a4 -- SnapKV pooling of the prefix scores (blog post
+ * "ZigZagKV, KVCache 80% compression near-lossless", section "SnapKV": the
+ * scores are pooled in 1D so that a kept token's neighbours are kept with
+ * it; the post gives neither the kernel's size nor its type).  For every
+ * head and prefix position j < T-W, over the in-range positions
+ * t in [max(0, j-kernel/2), min(T-W-1, j+kernel/2)]:
+ *   mode 0: pooled[j] = their mean (sum / their count, not / kernel);
+ *   mode 1: pooled[j] = their maximum.
+ * Window positions are copied unchanged.  kernel must be odd, 1..255
+ * (above 255: KVC_ERR_UNSUPPORTED); each mean is summed left to right in
+ * fp32.  pooled has the layout of scores and must not alias it; pass it to
+ * kvc_topk_select in place of scores (MBA stays on the raw scores).  The
+ * workspace is only validated (header size), not used. */
+int kvc_pool_scores(const kvc_shape *shape, const float *scores, int32_t kernel, int32_t mode,
+                    float *pooled, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* a5 -- compaction.  Gathers, for every head, rows idx[l][k][0..n_l) and then
  * the W window rows T-W..T-1 of k and v into k_out / v_out (packed layout
  * above).  out_rows is the capacity of each output in rows of D elements;
