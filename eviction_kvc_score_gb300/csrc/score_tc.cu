@@ -16,7 +16,7 @@
 //           epilogue thread owns one TMEM lane = one query row and keeps an
 //           online (max, sum) over its CTA's keys -> per-CTA partials;
 //   merge   (score_simt.cu) combines the partials into nb_r = -(m_r + log2 l_r);
-//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 128 query rows): each
+//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 256 query rows): each
 //           epilogue thread owns one key and sums 2^(x_rj + nb_r) over the
 //           query rows in registers -- the column sum needs no cross-lane
 //           reduction in this orientation.
@@ -25,13 +25,16 @@
 // tile) pairs, keeps the unit's Q block resident in shared memory and streams
 // K tiles with TMA through an mbarrier ring.  Warp roles: warp 0 TMA
 // producer, warp 1 MMA issuer (and TMEM owner), warps 2-9 epilogue in two
-// warpgroups.  TMEM holds four 128-column accumulator slots; each MMA job
-// fills one 128 x 128 slot and the warpgroups take alternate jobs, so one
-// computes while the other waits for its TMEM load or its next MMA.  A job is
-// read from TMEM in two 64-column halves; each thread keeps eight independent
-// max / sum chains, and the epilogue has one copy of its inner loop (the
-// window's causal mask is applied by setting invisible logits to -inf first)
-// so that it fits the instruction cache.
+// warpgroups.  Pass 1 splits TMEM into four 128-column accumulator slots
+// (one 128 x 128 job each); pass 2 into two 256-column slots (one
+// 128 x 256 job each: with both operands in shared memory the wider MMA
+// reads fewer operand bytes per flop and runs closer to the tensor peak).
+// The warpgroups take alternate jobs, so one computes while the other waits
+// for its TMEM load or its next MMA.  A job is read from TMEM in 64-column
+// pieces; each thread keeps eight independent max / sum chains, and the
+// epilogue has one copy of its inner loop (the window's causal mask is
+// applied by setting invisible logits to -inf first) so that it fits the
+// instruction cache.
 // Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
@@ -197,9 +200,10 @@ __device__ __forceinline__ void mma_drain(const Smem &s) {
     mbar_drain(s.drain, 0);
 }
 
-// MMA issuer (one thread).  For every K tile: njob jobs of 128 x 128 fp32
-// accumulators into TMEM slot (job % 4).  Pass 1 (KEYS_AS_B): A = Q row block
-// jb, B = the K tile.  Pass 2: A = the K tile, B = Q rows 128 jb ...
+// MMA issuer (one thread).  For every K tile: njob jobs of fp32 accumulators
+// into TMEM.  Pass 1 (KEYS_AS_B): 128 x 128 jobs into slot job % 4, A = Q
+// row block jb, B = the K tile.  Pass 2: 128 x n jobs (n <= 256) into slot
+// job % 2, A = the K tile, B = Q rows 256 jb ...
 template <int KH, bool KEYS_AS_B>
 __device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int64_t t0, int64_t t1,
                            int njob) {
@@ -216,20 +220,22 @@ __device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int6
         if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
         tc_fence_after();
         for (int jb = 0; jb < njob; ++jb, ++job) {
-            const uint32_t slot = job & 3, use = job >> 2;
+            constexpr uint32_t kSlots = KEYS_AS_B ? 4 : 2;
+            constexpr int kCols = KEYS_AS_B ? 128 : 256;   // TMEM columns per slot
+            const uint32_t slot = job % kSlots, use = job / kSlots;
             if (!mbar_wait(&s.t_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int n = KEYS_AS_B ? kTileKeys : min(128, p.n_pad - jb * 128);
+            const int n = KEYS_AS_B ? kTileKeys : min(kCols, p.n_pad - jb * kCols);
             const uint32_t idesc = idesc_bf16_f32(128, n);
-            const uint32_t d = tmem + slot * 128;
+            const uint32_t d = tmem + slot * kCols;
 #pragma unroll
             for (int ks = 0; ks < KH * 4; ++ks) {
                 const int kh = ks >> 2, off = (ks & 3) * 32;
                 const uint32_t qa =
-                    smem_u32(s.q + ((size_t)kh * p.rows_pad + jb * 128) * 128) + off;
+                    smem_u32(s.q + ((size_t)kh * p.rows_pad + jb * kCols) * 128) + off;
                 const uint32_t ka = smem_u32(s.k + ((size_t)stage * KH + kh) * kBoxBytes) + off;
                 const uint64_t a = sw128_kmajor_desc(KEYS_AS_B ? qa : ka);
                 const uint64_t b = sw128_kmajor_desc(KEYS_AS_B ? ka : qa);
@@ -422,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c = blockIdx.x;
     const int64_t t0 = split_begin(p.n_tiles, p.grid, c), t1 = split_begin(p.n_tiles, p.grid, c + 1);
-    const int nch = (p.n_pad + 127) / 128;   // 128-row query chunks (MMA N)
+    const int nch = (p.n_pad + 255) / 256;   // query-row chunks of up to 256 (MMA N)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int nc = 0; nc < nch; ++nc) {
                 const uint32_t jj = job + nc;
-                const uint32_t slot = jj & 3, use = jj >> 2;
+                const uint32_t slot = jj & 1, use = jj >> 1;
                 const int owner = nch >= 2 ? (nc & 1) : (int)(tl & 1);
                 if (owner != ewg) continue;
                 if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
@@ -480,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int n = min(128, p.n_pad - nc * 128);
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 128;
+                const int n = min(256, p.n_pad - nc * 256);
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 256;
                 const int nh = (n + 63) / 64;
 #pragma unroll 1
                 for (int h = 0; h < nh; ++h) {
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 64; ++i)
                             if (i >= valid) v[i >> 5][i & 31] = -INFINITY;
                     }
-                    const int r0 = nc * 128 + h * 64;
+                    const int r0 = nc * 256 + h * 64;
                     if (masked) {
                         int w = r0 % p.W;
                         mask_cols(v[0], w, dj, p.W);
