@@ -31,10 +31,13 @@
 // reads fewer operand bytes per flop and runs closer to the tensor peak).
 // The warpgroups take alternate jobs, so one computes while the other waits
 // for its TMEM load or its next MMA.  A job is read from TMEM in 64-column
-// pieces; each thread keeps eight independent max / sum chains, and the
-// epilogue has one copy of its inner loop (the window's causal mask is
+// pieces; each thread keeps independent sum chains on packed fp32 pairs, and
+// the epilogue has one copy of its inner loop (the window's causal mask is
 // applied by setting invisible logits to -inf first) so that it fits the
-// instruction cache.
+// instruction cache.  The epilogue competes with the MMA stream for the SM
+// (shared memory and issue), so every instruction per logit counts: pass 1
+// keeps a running reference that is raised only when a piece would overflow
+// instead of taking every piece's maximum.
 // Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
@@ -293,20 +296,70 @@ __device__ __forceinline__ void row_stats64(const float (&v)[2][32], float cs, f
     m_run = mnew;
 }
 
-// Add 2^(x * cs + nb[i]) for 64 query-row columns into eight partial sums.
+// The same fold with a running reference that is raised only when needed:
+// the piece's exponentials are taken against m_run, and if their sum stays
+// below 2^60 (no logit more than ~60 above m_run, so nothing overflowed) it is
+// added to l_run as it is; otherwise the piece is redone against its exact
+// maximum.  Either way l_run * 2^m_run is the sum of 2^(x*cs) over the keys
+// seen, which is all the merge needs; skipping the per-piece maximum removes
+// one instruction per logit.  The logit arithmetic runs on packed fp32 pairs.
+__device__ __forceinline__ void row_stats64_lazy(const float (&v)[2][32], float cs, float &m_run,
+                                                 float &l_run) {
+    if (m_run == -INFINITY) {
+        row_stats64(v, cs, m_run, l_run);
+        return;
+    }
+    unsigned long long s4[4] = {0ull, 0ull, 0ull, 0ull};
+    const unsigned long long cs2 = f2_pack(cs, cs), nm2 = f2_pack(-m_run, -m_run);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+        const unsigned long long y =
+            f2_fma(f2_pack(v[i >> 5][i & 31], v[i >> 5][(i & 31) + 1]), cs2, nm2);
+        float y0, y1;
+        f2_unpack(y, y0, y1);
+        s4[(i >> 1) & 3] = f2_add(s4[(i >> 1) & 3], f2_pack(ex2(y0), ex2(y1)));
+    }
+    float s8[8];
+    f2_unpack(s4[0], s8[0], s8[1]);
+    f2_unpack(s4[1], s8[2], s8[3]);
+    f2_unpack(s4[2], s8[4], s8[5]);
+    f2_unpack(s4[3], s8[6], s8[7]);
+    const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+    if (sum < 0x1p60f) {
+        l_run += sum;
+        return;
+    }
+    row_stats64(v, cs, m_run, l_run);
+}
+
+// Add 2^(x * cs + nb[i]) for 64 query-row columns into eight partial sums
+// (packed fp32 pairs for the logit scaling and the accumulation).
 __device__ __forceinline__ void col_sums64(const float (&v)[2][32], const float *nb, float cs,
                                            float (&a8)[8]) {
     const float4 *nb4 = reinterpret_cast<const float4 *>(nb);
+    unsigned long long a4[4] = {0ull, 0ull, 0ull, 0ull};
+    const unsigned long long cs2 = f2_pack(cs, cs);
 #pragma unroll
     for (int i4 = 0; i4 < 16; ++i4) {
         const float4 b4 = nb4[i4];
-        const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = i4 * 4 + e;
-            a8[i & 7] += ex2(fmaf(v[i >> 5][i & 31], cs, bb[e]));
-        }
+        const int i = i4 * 4;
+        const unsigned long long y01 =
+            f2_fma(f2_pack(v[i >> 5][i & 31], v[i >> 5][(i & 31) + 1]), cs2, f2_pack(b4.x, b4.y));
+        const unsigned long long y23 = f2_fma(
+            f2_pack(v[i >> 5][(i & 31) + 2], v[i >> 5][(i & 31) + 3]), cs2, f2_pack(b4.z, b4.w));
+        float y0, y1, y2, y3;
+        f2_unpack(y01, y0, y1);
+        f2_unpack(y23, y2, y3);
+        a4[(2 * i4) & 3] = f2_add(a4[(2 * i4) & 3], f2_pack(ex2(y0), ex2(y1)));
+        a4[(2 * i4 + 1) & 3] = f2_add(a4[(2 * i4 + 1) & 3], f2_pack(ex2(y2), ex2(y3)));
     }
+    float t[8];
+    f2_unpack(a4[0], t[0], t[1]);
+    f2_unpack(a4[1], t[2], t[3]);
+    f2_unpack(a4[2], t[4], t[5]);
+    f2_unpack(a4[3], t[6], t[7]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a8[i] += t[i];
 }
 
 // Causal mask inside the window for pass 2: row r = g*W + w sees the key iff
@@ -386,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 64; ++i)
                             if (h * 64 + i > lim) v[i >> 5][i & 31] = -INFINITY;
                     }
-                    row_stats64(v, p.cs, m, l);
+                    row_stats64_lazy(v, p.cs, m, l);
                 }
                 if (rb >> 1) {
                     m1 = m;
