@@ -30,6 +30,8 @@
  *               keep floor((1-lambda) D) channels per head, Top_T of M.
  *  [THINK-IMPL] same page, "Implementation of THINK": recent tokens are not
  *               pruned.
+ *  [THINK-QD]   same page, "Greedy algorithm" and "Observation window":
+ *               channel score = Frobenius norm of Q[-S_obs:, j] K[:, j]^T.
  *
  * Readings where the pages are silent or garbled:
  *  - GQA: query head h belongs to KV head h / G (G = H_q / H_kv); the score
@@ -536,6 +538,87 @@ int ora_channel_prune(const ora_shape *s, const void *k_out, const int32_t *budg
             ch[d].m = m;
             ch[d].d = (int32_t)d;
             if (norms) norms[u * D + d] = m;
+        }
+        qsort(ch, (size_t)D, sizeof(ora_chan), ora_cmp_chan);
+        int32_t *sel = chan + u * keep;
+        for (int32_t i = 0; i < keep; ++i) sel[i] = ch[i].d;
+        qsort(sel, (size_t)keep, sizeof(int32_t), ora_cmp_i32);
+        if (k_pruned) {
+            const unsigned char *src = (const unsigned char *)k_out;
+            unsigned char *dst = (unsigned char *)k_pruned;
+            const int64_t o0 = out_el[l] + h * n * keep;
+            for (int64_t r = 0; r < n; ++r)
+                for (int32_t i = 0; i < keep; ++i)
+                    memcpy(dst + (size_t)(o0 + r * keep + i) * es,
+                           src + (size_t)((row0 + r) * D + sel[i]) * es, es);
+        }
+        free(ch);
+    }
+    free(in_row);
+    free(out_el);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Optional: ThinK query-driven key-channel pruning        [THINK-QD]
+ *
+ * "ThinK: Thinner Key Cache by Query-Driven Pruning", section "Greedy
+ * algorithm" and "Observation window": channel j of a head scores the
+ * Frobenius norm of the outer product of its query column (the last S_obs
+ * window queries) and its key column, Q[-S_obs:, j] K[:, j]^T; the T
+ * channels with the largest scores are kept.  The Frobenius norm of an outer
+ * product is the product of the two column norms, so ranking by
+ *   score_d = (sum over window query rows of q[d]^2) * (sum over kept key
+ *              rows of k[d]^2)
+ * (the squared norm, monotone in the norm) gives the same channels.
+ * Readings: with grouped-query attention a KV head's query column stacks
+ * the W window rows of each of its G query heads (all of them see this key
+ * cache); the key column is the n_l kept prefix rows, as for the magnitude
+ * criterion (window rows stay full width).  Ties go to the lower channel.
+ * q is [L][H_q][W][D]; the other arguments and outputs are those of
+ * ora_channel_prune, with `scores` receiving score_d.
+ * ------------------------------------------------------------------------- */
+int ora_channel_prune_query(const ora_shape *s, const void *q, const void *k_out,
+                            const int32_t *budget, double lambda, int32_t *chan,
+                            double *scores, void *k_pruned)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t D = s->head_dim, W = s->window, P = (int64_t)s->seq_len - W;
+    const int64_t Hkv = s->n_kv_heads, Hq = s->n_q_heads, L = s->n_layers, G = Hq / Hkv;
+    const int32_t keep = ora_keep_channels(lambda, (int32_t)D);
+    if (keep < 1 || keep > D) return -1;
+    const size_t es = s->dtype == 0 ? 4 : 2;
+    int64_t *in_row = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    int64_t *out_el = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    int64_t ir = 0, oe = 0;
+    for (int64_t l = 0; l < L; ++l) {
+        in_row[l] = ir;
+        out_el[l] = oe;
+        const int64_t n = ora_kept(budget[l], P);
+        ir += Hkv * (n + W);
+        oe += Hkv * n * keep;
+    }
+    const int64_t units = L * Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < units; ++u) {
+        const int64_t l = u / Hkv, h = u % Hkv;
+        const int64_t n = ora_kept(budget[l], P);
+        const int64_t row0 = in_row[l] + h * (n + W);
+        const int64_t qrow0 = (l * Hq + h * G) * W;   /* G*W consecutive window rows */
+        ora_chan *ch = (ora_chan *)malloc(sizeof(ora_chan) * (size_t)D);
+        for (int64_t d = 0; d < D; ++d) {
+            double kk = 0.0, qq = 0.0;
+            for (int64_t r = 0; r < n; ++r) {
+                const double x = ora_elem(k_out, (row0 + r) * D + d, s->dtype);
+                kk += x * x;
+            }
+            for (int64_t r = 0; r < G * W; ++r) {
+                const double x = ora_elem(q, (qrow0 + r) * D + d, s->dtype);
+                qq += x * x;
+            }
+            ch[d].m = qq * kk;
+            ch[d].d = (int32_t)d;
+            if (scores) scores[u * D + d] = qq * kk;
         }
         qsort(ch, (size_t)D, sizeof(ora_chan), ora_cmp_chan);
         int32_t *sel = chan + u * keep;

@@ -69,6 +69,7 @@ def lib():
                 "ora_compact": (i64, [sp, p, p, p, i64, p]),
                 "ora_keep_channels": (i32, [d, i32]),
                 "ora_channel_prune": (C.c_int, [sp, p, p, d, p, p, p]),
+                "ora_channel_prune_query": (C.c_int, [sp, p, p, p, d, p, p, p]),
                 "ora_compress": (C.c_int, [sp, p, p, p, u32, u32, i64, i64, d, i64,
                                            p, p, p, p, p, p, p, p]),
             }
@@ -222,6 +223,22 @@ def channel_prune(s: Shape, k_out, budget_l, lam: float):
     _check(lib().ora_channel_prune(C.byref(s), _ptr(ka), _ptr(b), float(lam), _ptr(chan),
                                    _ptr(norms), _ptr(kp)), "channel_prune")
     return chan, norms, kp
+
+
+def channel_prune_query(s: Shape, q, k_out, budget_l, lam: float):
+    """ThinK query-driven criterion.  Returns (chan [L][H_kv][keep],
+    scores [L][H_kv][D] fp64, k_pruned raw)."""
+    qa, ka = raw(q), raw(k_out)
+    b = np.ascontiguousarray(budget_l, dtype=np.int32)
+    keep = keep_channels(lam, s.head_dim)
+    P = s.seq_len - s.window
+    n = np.clip(b, 0, P).astype(np.int64)
+    chan = np.empty((s.n_layers, s.n_kv_heads, max(keep, 1)), dtype=np.int32)
+    sc = np.empty((s.n_layers, s.n_kv_heads, s.head_dim), dtype=np.float64)
+    kp = np.empty(int(s.n_kv_heads * n.sum() * max(keep, 1)), dtype=ka.dtype)
+    _check(lib().ora_channel_prune_query(C.byref(s), _ptr(qa), _ptr(ka), _ptr(b), float(lam),
+                                         _ptr(chan), _ptr(sc), _ptr(kp)), "channel_prune_query")
+    return chan, sc, kp
 
 
 def compress(s: Shape, q, k, v, total: int, floor: int, k_max: int,

@@ -410,6 +410,71 @@ def test_channel_prune_keeps_outlier_channels():
             assert set(outl) <= set(chan[l, h].tolist())
 
 
+# ------------------------------------------------- optional query-driven ThinK
+@pytest.mark.parametrize("seed", range(6))
+def test_channel_prune_query_bruteforce(seed):
+    """Scores equal the squared Frobenius norm of the explicit outer product of
+    the stacked window-query column and the kept-key column (numpy, no product
+    of norms); for D <= 8 the kept channels are the keep-subset with the
+    largest total score, lowest channel indices winning ties; pruned rows are
+    the kept rows' chosen columns."""
+    rng = np.random.default_rng(700 + seed)
+    L, Hq, H, D, T, W = 2, 4, 2, 6, 12, 3
+    G = Hq // H
+    P = T - W
+    lam = [0.3, 0.5, 0.17][seed % 3]
+    keep = O.keep_channels(lam, D)
+    bud = np.array([int(rng.integers(0, P + 1)) for _ in range(L)], dtype=np.int32)
+    rows = H * int((bud + W).sum())
+    k_out = (rng.integers(-3, 4, size=(rows, D)) / 2.0).astype(np.float32)
+    q = (rng.integers(-3, 4, size=(L, Hq, W, D)) / 4.0).astype(np.float32)
+    s = O.shape_of(L, Hq, H, D, T, W, "f32")
+    chan, sc, kp = O.channel_prune_query(s, q, k_out, bud, lam)
+    r0, o0 = 0, 0
+    for l in range(L):
+        n = int(bud[l])
+        for h in range(H):
+            blk = k_out[r0: r0 + n].astype(np.float64)
+            qcol = q[l, h * G:(h + 1) * G].reshape(G * W, D).astype(np.float64)
+            for d in range(D):
+                outer = np.outer(qcol[:, d], blk[:, d])
+                assert sc[l, h, d] == pytest.approx(np.linalg.norm(outer, "fro") ** 2, rel=1e-12,
+                                                    abs=1e-300)
+            fr = [Fraction(float(x)) for x in sc[l, h]]
+            best = max(itertools.combinations(range(D), keep),
+                       key=lambda sub: (sum((fr[d] for d in sub), Fraction(0)), tuple(-d for d in sub)))
+            assert chan[l, h].tolist() == list(best)
+            got = kp[o0: o0 + n * keep].reshape(n, keep)
+            assert np.array_equal(got, k_out[r0: r0 + n][:, list(best)])
+            r0 += n + W
+            o0 += n * keep
+
+
+def test_channel_prune_query_special_cases():
+    """Equal query energy in every channel reduces the criterion to the
+    magnitude one; a channel the window queries never use (all-zero query
+    column) loses to every channel with a positive score."""
+    rng = np.random.default_rng(11)
+    L, Hq, H, D, T, W = 1, 2, 1, 16, 40, 4
+    P = T - W
+    bud = np.array([25], dtype=np.int32)
+    k_out = rng.standard_normal((H * (25 + W), D)).astype(np.float32)
+    s = O.shape_of(L, Hq, H, D, T, W, "f32")
+    signs = np.where(rng.random((L, Hq, W, D)) < 0.5, -1.0, 1.0).astype(np.float32)
+    q_flat = 0.5 * signs                       # |q| = 0.5 everywhere
+    chan_q, _, kp_q = O.channel_prune_query(s, q_flat, k_out, bud, 0.25)
+    chan_m, _, kp_m = O.channel_prune(s, k_out, bud, 0.25)
+    assert chan_q.tolist() == chan_m.tolist() and np.array_equal(kp_q, kp_m)
+    q = rng.standard_normal((L, Hq, W, D)).astype(np.float32)
+    k_big = k_out.copy()
+    k_big[:, 5] *= 100.0                       # by far the largest key magnitude ...
+    q[..., 5] = 0.0                            # ... but no query weight on it
+    chan, sc, _ = O.channel_prune_query(s, q, k_big, bud, 0.25)
+    assert sc[0, 0, 5] == 0.0 and 5 not in chan[0, 0].tolist()
+    chan_mag, _, _ = O.channel_prune(s, k_big, bud, 0.25)
+    assert 5 in chan_mag[0, 0].tolist()
+
+
 # --------------------------------------------------------------------- end to end
 def test_tiny_planted_keys_are_selected():
     """The tiny MHA workload plants 4 keys per head equal to 3x the head's mean
