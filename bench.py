@@ -38,7 +38,7 @@ METRIC = "prompt tokens compressed/sec (score+budget+select+gather); % of HBM ro
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # kernels each C-ABI call launches
 LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
-            "kvc_channel_prune": 1}
+            "kvc_channel_prune": 1, "kvc_pool_scores": 1}
 
 
 def parse():
@@ -53,6 +53,11 @@ def parse():
                     help="profiling only: run the workload with this many layers")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool", type=int, default=0,
+                    help="optional SnapKV pooling: odd kernel size of an average pool applied "
+                         "to the scores before top-K (0 = off)")
+    ap.add_argument("--think-criterion", default="magnitude", choices=["magnitude", "query"],
+                    help="ThinK key-channel criterion on workloads that prune channels")
     return ap.parse_args()
 
 
@@ -222,24 +227,48 @@ def run_kvc(args):
         x = wk.make_inputs(wl, wk.seed_for(2, 100 * rank + i), device=dev)
         total, floor = wl.budget_args()
         b = kvc.alloc_buffers(kvc.shape_of(wl), total, wl.k_max, lam=wl.think_lambda)
+        if args.pool > 1:
+            b.pooled = torch.empty_like(b.scores)
         jobs.append((wl, x, b, total, floor))
     torch.cuda.synchronize()
 
-    def step(score_ev=None):
+    def step(score_ev=None, stage_ev=None):
+        def mark(name):
+            if stage_ev is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                stage_ev.append((name, e))
+
         for wl, x, b, total, floor in jobs:
+            mark("start")
             if score_ev is not None:
                 score_ev[0].record(stream)
             kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
             if score_ev is not None:
                 score_ev[1].record(stream)
+            mark("kvc_score")
             kvc.kvc_mba_budget(b.shape, b.scores, wl.mass_num, wl.mass_den, total, floor,
                                b.mba, b.budget, b.ws)
-            kvc.kvc_topk_select(b.shape, b.scores, b.budget, b.k_max, b.idx, b.ws)
+            mark("kvc_mba_budget")
+            sel = b.scores
+            if args.pool > 1:
+                kvc.kvc_pool_scores(b.shape, b.scores, args.pool, 0, b.pooled, b.ws)
+                sel = b.pooled
+                mark("kvc_pool_scores")
+            kvc.kvc_topk_select(b.shape, sel, b.budget, b.k_max, b.idx, b.ws)
+            mark("kvc_topk_select")
             kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
                             b.v_out, b.ws)
+            mark("kvc_compact")
             if wl.think_lambda is not None:
-                kvc.kvc_channel_prune(b.shape, b.k_out, b.budget, wl.think_lambda, b.chan,
-                                      b.k_pruned, b.ws)
+                if args.think_criterion == "query":
+                    kvc.kvc_channel_prune_query(b.shape, x["q"], b.k_out, b.budget,
+                                                wl.think_lambda, b.chan, b.k_pruned, b.ws)
+                    mark("kvc_channel_prune_query")
+                else:
+                    kvc.kvc_channel_prune(b.shape, b.k_out, b.budget, wl.think_lambda, b.chan,
+                                          b.k_pruned, b.ws)
+                    mark("kvc_channel_prune")
 
     for _ in range(args.warmup):
         step()
@@ -267,6 +296,17 @@ def run_kvc(args):
         t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
+    # per-stage device times, on separate steps after the timed region (events
+    # between the stages would otherwise sit inside it)
+    stages = {}
+    n_stage = min(20, args.steps)
+    for _ in range(n_stage):
+        evs = []
+        step(stage_ev=evs)
+        torch.cuda.synchronize()
+        for (_, a), (name, e) in zip(evs[:-1], evs[1:]):
+            if name != "start":
+                stages[name] = stages.get(name, 0.0) + a.elapsed_time(e) / n_stage
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     ms_local = sum(step_ms) / len(step_ms)
     tokens_local = float(sum(wl.seq_len for wl in wls))
@@ -302,6 +342,9 @@ def run_kvc(args):
                    "head_dim": jobs[0][0].head_dim,
                    "seq_len": [wl.seq_len for wl in wls] if not single else wls[0].seq_len,
                    "window": jobs[0][0].window, "think_lambda": jobs[0][0].think_lambda,
+                   "think_criterion": (args.think_criterion if jobs[0][0].think_lambda is not None
+                                       else None),
+                   "pool_kernel": args.pool if args.pool > 1 else None,
                    "l2": "inputs larger than the 129 MB L2 (K and V resident in HBM); no flush",
                    "parallelism": f"replica x{world} (one prompt per GPU)"},
         "hbm_roofline": {"algorithmic_bytes_per_step": alg_bytes,
@@ -310,9 +353,12 @@ def run_kvc(args):
                          "peak_source": pk_src},
         "roofline": roof,
         "clocks": clk.summary(),
-        "gpu_launches": args.steps * sum(LAUNCHES[k] for k in LAUNCHES
-                                         if k != "kvc_channel_prune" or wls[0].think_lambda
-                                         is not None) * len(jobs),
+        "gpu_launches": args.steps * len(jobs) * (
+            sum(LAUNCHES[k] for k in ("kvc_score", "kvc_mba_budget", "kvc_topk_select",
+                                      "kvc_compact"))
+            + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)
+            + (LAUNCHES["kvc_pool_scores"] if args.pool > 1 else 0)),
+        "stages_ms": {k: round(v / len(jobs), 4) for k, v in stages.items()},
         "wall_s_timed": round(t_wall, 3),
     }
     out["e2e"] = run_e2e(args, jobs, stream) if args.e2e_steps > 0 else None
@@ -347,7 +393,7 @@ def run_e2e(args, jobs, stream):
             for kname in ("q", "k", "v"):
                 x[kname].copy_(hin[kname], non_blocking=True)
             kvc.compress(b, x["q"], x["k"], x["v"], total, floor, wl.mass_num, wl.mass_den,
-                         lam=wl.think_lambda)
+                         lam=wl.think_lambda, pool_kernel=args.pool, think=args.think_criterion)
             hout["budget"].copy_(b.budget, non_blocking=True)
             hout["idx"].copy_(b.idx, non_blocking=True)
             hout["k_out"].copy_(b.k_out, non_blocking=True)

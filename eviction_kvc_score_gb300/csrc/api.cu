@@ -273,7 +273,23 @@ int kvc_channel_prune(const kvc_shape *shape, const void *k_out, const int32_t *
     if (keep < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: lambda keeps no channel");
     if (pruned_elems < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: bad pruned_elems");
     if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_channel_prune")) return KVC_ERR_WORKSPACE;
-    return launch_channel_prune(*shape, k_out, budget, keep, chan, k_pruned, pruned_elems,
+    return launch_channel_prune(*shape, nullptr, k_out, budget, keep, chan, k_pruned, pruned_elems,
+                                status_word(ws), stream);
+}
+
+int kvc_channel_prune_query(const kvc_shape *shape, const void *q_obs, const void *k_out,
+                            const int32_t *budget, double lambda, int32_t *chan, void *k_pruned,
+                            int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_channel_prune_query")) return KVC_ERR_INVALID_ARG;
+    if (!q_obs || !k_out || !budget || !chan || !k_pruned)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_query: NULL tensor");
+    const int32_t keep = kvc_keep_channels(lambda, shape->head_dim);
+    if (keep < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_query: lambda keeps no channel");
+    if (pruned_elems < 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_query: bad pruned_elems");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_channel_prune_query")) return KVC_ERR_WORKSPACE;
+    return launch_channel_prune(*shape, q_obs, k_out, budget, keep, chan, k_pruned, pruned_elems,
                                 status_word(ws), stream);
 }
 

@@ -126,9 +126,10 @@ constexpr int kPruneThreads = 256;
 
 template <typename T>
 __global__ void __launch_bounds__(kPruneThreads)
-    channel_prune_kernel(const T *__restrict__ k_out, const int32_t *__restrict__ budget, int T_len,
-                         int W, int Hkv, int D, int keep, int32_t *__restrict__ chan,
-                         T *__restrict__ k_pruned, int64_t pruned_elems, uint32_t *status) {
+    channel_prune_kernel(const T *__restrict__ k_out, const T *__restrict__ q, int Hq,
+                         const int32_t *__restrict__ budget, int T_len, int W, int Hkv, int D,
+                         int keep, int32_t *__restrict__ chan, T *__restrict__ k_pruned,
+                         int64_t pruned_elems, uint32_t *status) {
     __shared__ FF part[kPruneThreads];
     __shared__ double m[256];
     __shared__ int sel[256];
@@ -164,6 +165,24 @@ __global__ void __launch_bounds__(kPruneThreads)
         m[tid] = (double)tot.hi + (double)tot.lo;
     }
     __syncthreads();
+    // 1b. query-driven criterion: times the squared norm of the channel's
+    // window-query column (the W rows of each of the KV head's G query heads)
+    if (q != nullptr) {
+        const int G = Hq / Hkv;
+        const int64_t qrow0 = ((int64_t)l * Hq + (int64_t)h * G) * W;
+        const int qrows = G * W;
+        FF qa = {0.f, 0.f};
+        if (g < groups)
+            for (int r = g; r < qrows; r += groups) qa = ff_add_sq(qa, ld_f(q, (qrow0 + r) * D + d));
+        part[tid] = qa;
+        __syncthreads();
+        if (tid < D) {
+            FF tot = part[tid];
+            for (int gg = 1; gg < groups; ++gg) tot = ff_add(tot, part[gg * D + tid]);
+            m[tid] *= (double)tot.hi + (double)tot.lo;
+        }
+        __syncthreads();
+    }
     // 2. rank channels by (M desc, d asc); keep the first `keep`, ascending
     if (tid < D) {
         const double mine = m[tid];
@@ -226,18 +245,19 @@ int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32
     return KVC_OK;
 }
 
-int launch_channel_prune(const kvc_shape &s, const void *k_out, const int32_t *budget, int32_t keep,
-                         int32_t *chan, void *k_pruned, int64_t pruned_elems, uint32_t *status,
-                         cudaStream_t st) {
+int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, const int32_t *budget,
+                         int32_t keep, int32_t *chan, void *k_pruned, int64_t pruned_elems,
+                         uint32_t *status, cudaStream_t st) {
     const int heads = s.n_layers * s.n_kv_heads;
     if (s.dtype == KVC_F32) {
         channel_prune_kernel<float><<<heads, kPruneThreads, 0, st>>>(
-            (const float *)k_out, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim, keep, chan,
-            (float *)k_pruned, pruned_elems, status);
+            (const float *)k_out, (const float *)q, s.n_q_heads, budget, s.seq_len, s.window,
+            s.n_kv_heads, s.head_dim, keep, chan, (float *)k_pruned, pruned_elems, status);
     } else {
         channel_prune_kernel<__nv_bfloat16><<<heads, kPruneThreads, 0, st>>>(
-            (const __nv_bfloat16 *)k_out, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim,
-            keep, chan, (__nv_bfloat16 *)k_pruned, pruned_elems, status);
+            (const __nv_bfloat16 *)k_out, (const __nv_bfloat16 *)q, s.n_q_heads, budget,
+            s.seq_len, s.window, s.n_kv_heads, s.head_dim, keep, chan,
+            (__nv_bfloat16 *)k_pruned, pruned_elems, status);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -313,9 +313,10 @@ int launch_pool(const kvc_shape &s, const float *scores, int32_t kernel, int32_t
 int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
                    const int32_t *budget, int32_t k_max, void *k_out, void *v_out,
                    int64_t out_rows, uint32_t *status, cudaStream_t st);
-int launch_channel_prune(const kvc_shape &s, const void *k_out, const int32_t *budget, int32_t keep,
-                         int32_t *chan, void *k_pruned, int64_t pruned_elems, uint32_t *status,
-                         cudaStream_t st);
+// q == nullptr: magnitude criterion; otherwise the query-driven one.
+int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, const int32_t *budget,
+                         int32_t keep, int32_t *chan, void *k_pruned, int64_t pruned_elems,
+                         uint32_t *status, cudaStream_t st);
 
 void set_error(const char *fmt, ...);
 

@@ -57,6 +57,7 @@ _SIGS = {
     "kvc_pool_scores": (C.c_int, [_sp, _p, _i32, _i32, _p, _p, _sz, _p]),
     "kvc_compact": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune": (C.c_int, [_sp, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
+    "kvc_channel_prune_query": (C.c_int, [_sp, _p, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
     "kvc_keep_channels": (_i32, [_d, _i32]),
     "kvc_status_string": (C.c_char_p, [C.c_int]),
     "kvc_last_error": (C.c_char_p, []),
@@ -168,6 +169,14 @@ def kvc_channel_prune(s: KvcShape, k_out, budget, lam: float, chan, k_pruned, ws
         k_pruned.numel(), _ptr(ws), ws.numel(), _stream(stream)))
 
 
+def kvc_channel_prune_query(s: KvcShape, q_obs, k_out, budget, lam: float, chan, k_pruned, ws,
+                            stream=None) -> None:
+    """ThinK query-driven key-channel criterion (window-query x kept-key norms)."""
+    _check("kvc_channel_prune_query", _lib.kvc_channel_prune_query(
+        C.byref(s), _ptr(q_obs), _ptr(k_out), _ptr(budget), float(lam), _ptr(chan),
+        _ptr(k_pruned), k_pruned.numel(), _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def kvc_keep_channels(lam: float, head_dim: int) -> int:
     return int(_lib.kvc_keep_channels(float(lam), int(head_dim)))
 
@@ -199,6 +208,7 @@ class Buffers:
     chan: Optional[torch.Tensor] = None
     k_pruned: Optional[torch.Tensor] = None
     keep: int = 0
+    pooled: Optional[torch.Tensor] = None
 
 
 def alloc_buffers(s: KvcShape, total_budget: int, k_max: int, lam: Optional[float] = None,
@@ -227,14 +237,30 @@ def alloc_buffers(s: KvcShape, total_budget: int, k_max: int, lam: Optional[floa
 
 
 def compress(b: Buffers, q_obs, k, v, total_budget: int, layer_floor: int, mass_num: int = 9,
-             mass_den: int = 10, lam: Optional[float] = None, stream=None) -> None:
-    """Enqueue the whole path: score -> MBA/budget -> top-K -> compact
-    (-> channel prune when lam is given).  Asynchronous on `stream`."""
+             mass_den: int = 10, lam: Optional[float] = None, stream=None,
+             pool_kernel: int = 0, pool_mode: int = 0, think: str = "magnitude") -> None:
+    """Enqueue the whole path: score -> MBA/budget -> (pool ->) top-K -> compact
+    (-> channel prune when lam is given, by key magnitude or, with
+    think="query", by the query-driven criterion).  pool_kernel > 1 pools the
+    scores before top-K (MBA stays on the raw scores).  Asynchronous on
+    `stream`."""
     s = b.shape
     kvc_score(s, q_obs, k, b.scores, b.ws, stream)
     kvc_mba_budget(s, b.scores, mass_num, mass_den, total_budget, layer_floor, b.mba, b.budget,
                    b.ws, stream)
-    kvc_topk_select(s, b.scores, b.budget, b.k_max, b.idx, b.ws, stream)
+    sel = b.scores
+    if pool_kernel > 1:
+        if getattr(b, "pooled", None) is None:
+            b.pooled = torch.empty_like(b.scores)
+        kvc_pool_scores(s, b.scores, pool_kernel, pool_mode, b.pooled, b.ws, stream)
+        sel = b.pooled
+    kvc_topk_select(s, sel, b.budget, b.k_max, b.idx, b.ws, stream)
     kvc_compact(s, k, v, b.idx, b.budget, b.k_max, b.k_out, b.v_out, b.ws, stream)
     if lam is not None:
-        kvc_channel_prune(s, b.k_out, b.budget, lam, b.chan, b.k_pruned, b.ws, stream)
+        if think == "query":
+            kvc_channel_prune_query(s, q_obs, b.k_out, b.budget, lam, b.chan, b.k_pruned, b.ws,
+                                    stream)
+        elif think == "magnitude":
+            kvc_channel_prune(s, b.k_out, b.budget, lam, b.chan, b.k_pruned, b.ws, stream)
+        else:
+            raise ValueError(f"unknown ThinK criterion {think!r}")

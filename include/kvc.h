@@ -206,6 +206,20 @@ int kvc_channel_prune(const kvc_shape *shape, const void *k_out, const int32_t *
                       double lambda, int32_t *chan, void *k_pruned, int64_t pruned_elems,
                       void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Optional variant of a6 -- ThinK's query-driven key-channel criterion
+ * ("ThinK: Thinner Key Cache by Query-Driven Pruning", sections "Greedy
+ * algorithm" and "Observation window": channel j scores the Frobenius norm of
+ * Q[-S_obs:, j] K[:, j]^T).  Same outputs and layouts as kvc_channel_prune;
+ * channels are ranked by (sum over the window query rows of q[d]^2) *
+ * (sum over the n_l kept prefix rows of k_out[r][d]^2) -- the square of that
+ * norm -- instead of the key magnitude alone.  With grouped-query attention
+ * the query column of KV head k stacks the W window rows of its G query heads
+ * (q_obs [L][H_q][W][D], dtype of the shape).  Both sums are float-float
+ * (about 44 significant bits); ties go to the lower channel. */
+int kvc_channel_prune_query(const kvc_shape *shape, const void *q_obs, const void *k_out,
+                            const int32_t *budget, double lambda, int32_t *chan, void *k_pruned,
+                            int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* floor((1 - lambda) * head_dim) computed in double; 0 if lambda is outside
  * [0,1). */
 int32_t kvc_keep_channels(double lambda, int32_t head_dim);
