@@ -32,6 +32,12 @@
  *               pruned.
  *  [THINK-QD]   same page, "Greedy algorithm" and "Observation window":
  *               channel score = Frobenius norm of Q[-S_obs:, j] K[:, j]^T.
+ *  [ZZ-HEAD]    ZigZagKV post: memory per attention head should follow the
+ *               tokens that head needs; each head's K follows its quota.
+ *  [THRESH]     ZigZagKV post, "SnapKV": scores above a threshold mark the
+ *               important tokens; "NVIDIA AI presents KVzap" (kiadev.net):
+ *               low-score entries are dropped, a sliding window of recent
+ *               tokens is kept.
  *
  * Readings where the pages are silent or garbled:
  *  - GQA: query head h belongs to KV head h / G (G = H_q / H_kv); the score
@@ -638,6 +644,131 @@ int ora_channel_prune_query(const ora_shape *s, const void *q, const void *k_out
     free(in_row);
     free(out_el);
     return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Optional: per-head budgets inside a layer                   [ZZ-HEAD]
+ *
+ * Blog post "ZigZagKV, KVCache 80% compression near-lossless", opening of
+ * the ZigZagKV part (memory should follow how many tokens each attention
+ * head needs to keep most of its information, not be equal per head) and
+ * "ZigZagKV token selection" (each head's K follows its quota).  Reading:
+ * the layer's H_kv * B_l prefix tokens are split over its heads in
+ * proportion to MBA_{l,k} with the same largest-remainder rule as the layer
+ * split (ties to the lower head, equal shares when every MBA is zero), no
+ * per-head minimum, each head capped at P with the excess re-split over the
+ * uncapped heads until none exceeds P.  head_budget: [L][H_kv].
+ * ------------------------------------------------------------------------- */
+int ora_head_budget(int L, int Hkv, const int32_t *mba, const int32_t *budget, int64_t prefix,
+                    int32_t *head_budget)
+{
+    if (L < 1 || Hkv < 1 || prefix < 1) return -1;
+    int64_t *w = (int64_t *)malloc(sizeof(int64_t) * (size_t)Hkv);
+    int64_t *B = (int64_t *)malloc(sizeof(int64_t) * (size_t)Hkv);
+    int64_t *add = (int64_t *)malloc(sizeof(int64_t) * (size_t)Hkv);
+    unsigned char *elig = (unsigned char *)malloc((size_t)Hkv);
+    for (int l = 0; l < L; ++l) {
+        const int64_t Bl = budget[l] < 0 ? 0 : (budget[l] > prefix ? prefix : budget[l]);
+        for (int k = 0; k < Hkv; ++k) {
+            w[k] = mba[(int64_t)l * Hkv + k];
+            elig[k] = 1;
+        }
+        ora_split(Hkv, w, elig, (int64_t)Hkv * Bl, add);
+        for (int k = 0; k < Hkv; ++k) B[k] = add[k];
+        for (;;) {
+            int64_t excess = 0;
+            for (int k = 0; k < Hkv; ++k)
+                if (B[k] > prefix) { excess += B[k] - prefix; B[k] = prefix; }
+            if (excess == 0) break;
+            for (int k = 0; k < Hkv; ++k) elig[k] = (unsigned char)(B[k] < prefix);
+            ora_split(Hkv, w, elig, excess, add);
+            for (int k = 0; k < Hkv; ++k) B[k] += add[k];
+        }
+        for (int k = 0; k < Hkv; ++k) head_budget[(int64_t)l * Hkv + k] = (int32_t)B[k];
+    }
+    free(w); free(B); free(add); free(elig);
+    return 0;
+}
+
+/* Top-K with per-head budgets: head (l,k) keeps min(max(hb,0), P) prefix
+ * positions by (score desc, index asc), written ascending.  idx:
+ * [L][H_kv][k_max]; returns -1 if a head needs more than k_max. */
+int ora_topk_heads(const ora_shape *s, const double *scores, const int32_t *head_budget,
+                   int64_t k_max, int32_t *idx)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t T = s->seq_len, P = T - s->window;
+    const int64_t units = (int64_t)s->n_layers * s->n_kv_heads;
+    for (int64_t u = 0; u < units; ++u)
+        if (ora_kept(head_budget[u], P) > k_max) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t u = 0; u < units; ++u)
+        if (ora_topk(P, scores + u * T, head_budget[u], idx + u * k_max) < 0) bad = 1;
+    return bad ? -2 : 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Optional: threshold selection with the recent window           [THRESH]
+ *
+ * Blog post above, section "SnapKV" (a token counts as important when its
+ * attention score exceeds a set threshold) and "NVIDIA AI presents KVzap"
+ * (entries with low scores are dropped while a sliding window of the most
+ * recent tokens is always kept, so each head keeps as many tokens as its
+ * context needs).  Reading: per head, keep every prefix position j < P with
+ * c_j >= tau (fp32 scores compared as stored), ascending, plus the W window
+ * rows; counts[l][k] is the number of prefix positions kept.  A head with
+ * more than k_max such positions keeps the first k_max and the call
+ * returns 1 (the counts still report the full number).
+ * ------------------------------------------------------------------------- */
+int ora_threshold_select(const ora_shape *s, const float *scores, float tau, int64_t k_max,
+                         int32_t *idx, int32_t *counts)
+{
+    if (!ora_shape_ok(s) || k_max < 1) return -1;
+    const int64_t T = s->seq_len, P = T - s->window;
+    const int64_t units = (int64_t)s->n_layers * s->n_kv_heads;
+    int over = 0;
+    for (int64_t u = 0; u < units; ++u) {
+        int64_t n = 0;
+        for (int64_t j = 0; j < P; ++j) {
+            if (scores[u * T + j] >= tau) {
+                if (n < k_max) idx[u * k_max + n] = (int32_t)j;
+                ++n;
+            }
+        }
+        counts[u] = (int32_t)n;
+        if (n > k_max) over = 1;
+    }
+    return over;
+}
+
+/* ---------------------------------------------------------------------------
+ * Compaction with per-head counts                                  [SNAP]
+ *
+ * Head (l,k) contributes its n_{l,k} = min(max(counts,0), P, k_max) kept
+ * rows idx[l][k][0..n) and then the W window rows; heads follow each other
+ * in (l, k) order.  Returns the rows written, or -1.
+ * ------------------------------------------------------------------------- */
+int64_t ora_compact_heads(const ora_shape *s, const void *src, const int32_t *idx,
+                          const int32_t *counts, int64_t k_max, void *out)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t D = s->head_dim, T = s->seq_len, W = s->window, P = T - W;
+    const size_t es = s->dtype == 0 ? 4 : 2;
+    const int64_t units = (int64_t)s->n_layers * s->n_kv_heads;
+    const unsigned char *in = (const unsigned char *)src;
+    unsigned char *o = (unsigned char *)out;
+    int64_t row = 0;
+    for (int64_t u = 0; u < units; ++u) {
+        int64_t n = ora_kept(counts[u], P);
+        if (n > k_max) n = k_max;
+        for (int64_t r = 0; r < n; ++r, ++row)
+            memcpy(o + (size_t)row * D * es, in + (size_t)(u * T + idx[u * k_max + r]) * D * es,
+                   (size_t)D * es);
+        for (int64_t w = 0; w < W; ++w, ++row)
+            memcpy(o + (size_t)row * D * es, in + (size_t)(u * T + P + w) * D * es, (size_t)D * es);
+    }
+    return row;
 }
 
 /* ---------------------------------------------------------------------------

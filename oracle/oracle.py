@@ -66,6 +66,10 @@ def lib():
                 "ora_pool": (C.c_int, [sp, p, i32, i32, p]),
                 "ora_pool_f32": (C.c_int, [sp, p, i32, i32, p]),
                 "ora_compact_rows": (i64, [sp, p]),
+                "ora_head_budget": (C.c_int, [C.c_int, C.c_int, p, p, i64, p]),
+                "ora_topk_heads": (C.c_int, [sp, p, p, i64, p]),
+                "ora_threshold_select": (C.c_int, [sp, p, C.c_float, i64, p, p]),
+                "ora_compact_heads": (i64, [sp, p, p, p, i64, p]),
                 "ora_compact": (i64, [sp, p, p, p, i64, p]),
                 "ora_keep_channels": (i32, [d, i32]),
                 "ora_channel_prune": (C.c_int, [sp, p, p, d, p, p, p]),
@@ -187,6 +191,49 @@ def pool(s: Shape, scores, kernel: int, mode: int = 0) -> np.ndarray:
     else:
         sc = np.ascontiguousarray(scores, dtype=np.float64)
         _check(lib().ora_pool(C.byref(s), _ptr(sc), kernel, mode, _ptr(out)), "pool")
+    return out
+
+
+def head_budget(mba_lk, budget_l, prefix: int) -> np.ndarray:
+    """Per-head split of each layer's H_kv * B_l tokens by MBA: [L][H_kv]."""
+    m = np.ascontiguousarray(mba_lk, dtype=np.int32)
+    b = np.ascontiguousarray(budget_l, dtype=np.int32)
+    L, H = m.shape
+    out = np.empty((L, H), dtype=np.int32)
+    _check(lib().ora_head_budget(L, H, _ptr(m), _ptr(b), prefix, _ptr(out)), "head_budget")
+    return out
+
+
+def topk_heads(s: Shape, scores, head_budget_lk, k_max: int) -> np.ndarray:
+    hb = np.ascontiguousarray(head_budget_lk, dtype=np.int32)
+    idx = np.full((s.n_layers, s.n_kv_heads, max(k_max, 1)), -1, dtype=np.int32)
+    sc = np.ascontiguousarray(scores, dtype=np.float64)
+    _check(lib().ora_topk_heads(C.byref(s), _ptr(sc), _ptr(hb), k_max, _ptr(idx)), "topk_heads")
+    return idx
+
+
+def threshold_select(s: Shape, scores_f32, tau: float, k_max: int):
+    """Returns (idx [L][H_kv][k_max] (-1 past the count), counts [L][H_kv],
+    overflowed)."""
+    sc = np.ascontiguousarray(scores_f32, dtype=np.float32)
+    idx = np.full((s.n_layers, s.n_kv_heads, max(k_max, 1)), -1, dtype=np.int32)
+    cnt = np.empty((s.n_layers, s.n_kv_heads), dtype=np.int32)
+    rc = _check(lib().ora_threshold_select(C.byref(s), _ptr(sc), float(tau), k_max, _ptr(idx),
+                                           _ptr(cnt)), "threshold_select")
+    return idx, cnt, bool(rc)
+
+
+def compact_heads(s: Shape, x, idx, counts, k_max: int) -> np.ndarray:
+    xa = raw(x)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    P = s.seq_len - s.window
+    n = np.minimum(np.clip(c, 0, P), k_max).astype(np.int64)
+    rows = int((n + s.window).sum())
+    out = np.empty((rows, s.head_dim), dtype=xa.dtype)
+    got = _check(lib().ora_compact_heads(C.byref(s), _ptr(xa), _ptr(ix), _ptr(c), k_max, _ptr(out)),
+                 "compact_heads")
+    assert got == rows
     return out
 
 

@@ -475,6 +475,97 @@ def test_channel_prune_query_special_cases():
     assert 5 in chan_mag[0, 0].tolist()
 
 
+# ------------------------------------------- optional per-head and threshold
+@pytest.mark.parametrize("seed", range(8))
+def test_head_budget_bruteforce_largest_remainder(seed):
+    """Each layer's H_kv * B_l tokens are apportioned over its heads by MBA
+    with the largest-remainder rule (checked by enumeration), remainder ties
+    to the lower head; no cap binds here."""
+    rng = np.random.default_rng(900 + seed)
+    L = int(rng.integers(1, 4))
+    H = int(rng.integers(1, 4))
+    mba = rng.integers(0, 7, size=(L, H)).astype(np.int32)
+    bud = rng.integers(0, 4, size=L).astype(np.int32)
+    hb = O.head_budget(mba, bud, 10_000)
+    for l in range(L):
+        R = H * int(bud[l])
+        ok, lex_max = _hamilton_ok([int(x) for x in mba[l]], R, [int(x) for x in hb[l]])
+        assert ok, (mba[l], R, hb[l])
+        assert tuple(int(x) for x in hb[l]) == lex_max
+
+
+def test_head_budget_invariants_and_caps():
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        L = int(rng.integers(1, 12))
+        H = int(rng.integers(1, 9))
+        P = int(rng.integers(1, 300))
+        bud = rng.integers(0, P + 1, size=L).astype(np.int32)
+        mba = rng.integers(0, 3 * P, size=(L, H)).astype(np.int32)
+        hb = O.head_budget(mba, bud, P)
+        assert hb.min() >= 0 and hb.max() <= P
+        assert np.array_equal(hb.sum(axis=1), H * bud.astype(np.int64))
+    # equal MBAs: every head gets the layer budget; all-zero MBAs: equal split
+    assert O.head_budget(np.full((2, 4), 5, np.int32), np.array([7, 9], np.int32), 50).tolist() \
+        == [[7] * 4, [9] * 4]
+    assert O.head_budget(np.zeros((1, 3), np.int32), np.array([4], np.int32), 50).tolist() == [[4, 4, 4]]
+    # one dominant head is capped at P and the excess is water-filled
+    hb = O.head_budget(np.array([[1000, 1, 1, 2]], np.int32), np.array([10], np.int32), 16)
+    assert hb[0, 0] == 16 and hb.sum() == 40 and hb[0, 1:].tolist() == [6, 6, 12]
+
+
+def test_topk_heads_equals_stable_sort():
+    rng = np.random.default_rng(5)
+    L, H, T, W = 2, 3, 60, 7
+    P = T - W
+    sc = (rng.integers(0, 5, size=(L, H, T)) / 7.0)
+    hb = rng.integers(0, P + 1, size=(L, H)).astype(np.int32)
+    s = O.shape_of(L, H, H, 8, T, W, "f32")
+    idx = O.topk_heads(s, sc, hb, P)
+    for l in range(L):
+        for h in range(H):
+            order = np.lexsort((np.arange(P), -sc[l, h, :P]))   # score desc, index asc
+            want = np.sort(order[: hb[l, h]])
+            assert idx[l, h, : hb[l, h]].tolist() == want.tolist()
+
+
+def test_threshold_select_equals_nonzero():
+    rng = np.random.default_rng(6)
+    L, H, T, W = 2, 2, 300, 20
+    P = T - W
+    sc = rng.random((L, H, T)).astype(np.float32) / 100
+    s = O.shape_of(L, H, H, 8, T, W, "f32")
+    for tau in [0.0, 0.002, 0.005, 0.0099, 1.0]:
+        idx, cnt, over = O.threshold_select(s, sc, tau, P)
+        assert not over
+        for l in range(L):
+            for h in range(H):
+                want = np.nonzero(sc[l, h, :P] >= np.float32(tau))[0]
+                assert cnt[l, h] == want.size and idx[l, h, : want.size].tolist() == want.tolist()
+    idx, cnt, _ = O.threshold_select(s, sc, 0.0, P)
+    assert (cnt == P).all()                              # tau = 0 keeps the whole prefix
+    idx, cnt, over = O.threshold_select(s, sc, 0.0, 50)   # more than k_max: first k_max kept
+    assert over and (cnt == P).all() and idx[0, 0].tolist() == list(range(50))
+
+
+def test_compact_heads_equals_fancy_indexing():
+    rng = np.random.default_rng(8)
+    L, H, T, W, D = 2, 3, 40, 5, 4
+    P = T - W
+    x = rng.standard_normal((L, H, T, D)).astype(np.float32)
+    cnt = rng.integers(0, P + 1, size=(L, H)).astype(np.int32)
+    k_max = P
+    idx = np.full((L, H, k_max), -1, np.int32)
+    for l in range(L):
+        for h in range(H):
+            idx[l, h, : cnt[l, h]] = np.sort(rng.choice(P, cnt[l, h], replace=False))
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    got = O.compact_heads(s, x, idx, cnt, k_max)
+    want = np.concatenate([np.concatenate([x[l, h, idx[l, h, : cnt[l, h]]], x[l, h, P:]])
+                           for l in range(L) for h in range(H)])
+    assert np.array_equal(got, want)
+
+
 # --------------------------------------------------------------------- end to end
 def test_tiny_planted_keys_are_selected():
     """The tiny MHA workload plants 4 keys per head equal to 3x the head's mean
