@@ -38,7 +38,8 @@ METRIC = "prompt tokens compressed/sec (score+budget+select+gather); % of HBM ro
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # kernels each C-ABI call launches
 LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
-            "kvc_channel_prune": 1, "kvc_pool_scores": 1}
+            "kvc_channel_prune": 1, "kvc_pool_scores": 1, "kvc_head_budget": 1,
+            "kvc_threshold_select": 1}
 
 
 def parse():
@@ -58,6 +59,11 @@ def parse():
                          "to the scores before top-K (0 = off)")
     ap.add_argument("--think-criterion", default="magnitude", choices=["magnitude", "query"],
                     help="ThinK key-channel criterion on workloads that prune channels")
+    ap.add_argument("--select", default="layer", choices=["layer", "head", "threshold"],
+                    help="token selection: per-layer budgets (default), per-head budgets split "
+                         "by MBA inside each layer, or every prefix token scoring >= tau")
+    ap.add_argument("--tau-mult", type=float, default=4.0,
+                    help="threshold selection: tau = tau_mult / seq_len (mean score x tau_mult)")
     return ap.parse_args()
 
 
@@ -86,10 +92,12 @@ def workload_list(name, rank, layers=0):
     return wls
 
 
-def algorithmic_bytes(wl, budget):
+def algorithmic_bytes(wl, budget, head_counts=None):
     """Each input read once, each output written once (scores count as an
     output): K, Q_obs, scores, indices, kept K/V rows read, compacted V
-    written, compacted (or pruned) K written."""
+    written, compacted (or pruned) K written.  budget: kept prefix tokens per
+    layer; head_counts ([L][H_kv]) replaces it when heads keep different
+    numbers of tokens."""
     s = wl.elt_size
     L, Hq, H, T, W, D = (wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.seq_len, wl.window,
                          wl.head_dim)
@@ -99,11 +107,14 @@ def algorithmic_bytes(wl, budget):
         import math
         keep = int(math.floor((1.0 - wl.think_lambda) * D))
     total = 0
-    for b in budget:
-        n = max(0, min(int(b), P))
-        total += H * T * D * s + Hq * W * D * s + 4 * H * T + 4 * H * n
-        total += 2 * H * (n + W) * D * s + H * (n + W) * D * s
-        total += H * (n * keep + W * D) * s if keep else H * (n + W) * D * s
+    for l in range(L):
+        total += H * T * D * s + Hq * W * D * s + 4 * H * T
+        ns = ([head_counts[l][k] for k in range(H)] if head_counts is not None
+              else [budget[l]] * H)
+        for b in ns:
+            n = max(0, min(int(b), P))
+            total += 4 * n + 2 * (n + W) * D * s + (n + W) * D * s
+            total += (n * keep + W * D) * s if keep else (n + W) * D * s
     return total
 
 
@@ -221,6 +232,9 @@ def run_kvc(args):
     rank, world, dist = dist_setup(args.gpus)
     dev = torch.device("cuda", torch.cuda.current_device())
     wls = workload_list(args.workload, rank, args.layers)
+    if args.select != "layer" and any(wl.think_lambda is not None for wl in wls):
+        raise SystemExit("--select head/threshold packs heads individually; ThinK pruning "
+                         "works on the per-layer packing, so use a workload without ThinK")
     stream = torch.cuda.current_stream()
     jobs = []
     for i, wl in enumerate(wls):
@@ -229,6 +243,19 @@ def run_kvc(args):
         b = kvc.alloc_buffers(kvc.shape_of(wl), total, wl.k_max, lam=wl.think_lambda)
         if args.pool > 1:
             b.pooled = torch.empty_like(b.scores)
+        if args.select != "layer":
+            L, H, P = wl.n_layers, wl.n_kv_heads, wl.seq_len - wl.window
+            b.head_counts = torch.empty((L, H), dtype=torch.int32, device=dev)
+            if args.select == "threshold":
+                # any head may keep its whole prefix
+                b.k_max = P
+                b.idx = torch.empty((L, H, P), dtype=torch.int32, device=dev)
+                rows = L * H * wl.seq_len
+                b.k_out = torch.empty((rows, wl.head_dim), dtype=b.k_out.dtype, device=dev)
+                b.v_out = torch.empty((rows, wl.head_dim), dtype=b.v_out.dtype, device=dev)
+                b.ws = torch.empty(kvc.kvc_workspace_size(b.shape, P), dtype=torch.uint8,
+                                   device=dev)
+                kvc.kvc_workspace_init(b.ws)
         jobs.append((wl, x, b, total, floor))
     torch.cuda.synchronize()
 
@@ -247,6 +274,14 @@ def run_kvc(args):
             if score_ev is not None:
                 score_ev[1].record(stream)
             mark("kvc_score")
+            if args.select == "threshold":
+                kvc.kvc_threshold_select(b.shape, b.scores, args.tau_mult / wl.seq_len, b.k_max,
+                                         b.idx, b.head_counts, b.ws)
+                mark("kvc_threshold_select")
+                kvc.kvc_compact_heads(b.shape, x["k"], x["v"], b.idx, b.head_counts, b.k_max,
+                                      b.k_out, b.v_out, b.ws)
+                mark("kvc_compact_heads")
+                continue
             kvc.kvc_mba_budget(b.shape, b.scores, wl.mass_num, wl.mass_den, total, floor,
                                b.mba, b.budget, b.ws)
             mark("kvc_mba_budget")
@@ -255,11 +290,20 @@ def run_kvc(args):
                 kvc.kvc_pool_scores(b.shape, b.scores, args.pool, 0, b.pooled, b.ws)
                 sel = b.pooled
                 mark("kvc_pool_scores")
-            kvc.kvc_topk_select(b.shape, sel, b.budget, b.k_max, b.idx, b.ws)
-            mark("kvc_topk_select")
-            kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
-                            b.v_out, b.ws)
-            mark("kvc_compact")
+            if args.select == "head":
+                kvc.kvc_head_budget(b.shape, b.mba, b.budget, b.head_counts, b.ws)
+                mark("kvc_head_budget")
+                kvc.kvc_topk_select_heads(b.shape, sel, b.head_counts, b.k_max, b.idx, b.ws)
+                mark("kvc_topk_select_heads")
+                kvc.kvc_compact_heads(b.shape, x["k"], x["v"], b.idx, b.head_counts, b.k_max,
+                                      b.k_out, b.v_out, b.ws)
+                mark("kvc_compact_heads")
+            else:
+                kvc.kvc_topk_select(b.shape, sel, b.budget, b.k_max, b.idx, b.ws)
+                mark("kvc_topk_select")
+                kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
+                                b.v_out, b.ws)
+                mark("kvc_compact")
             if wl.think_lambda is not None:
                 if args.think_criterion == "query":
                     kvc.kvc_channel_prune_query(b.shape, x["q"], b.k_out, b.budget,
@@ -315,7 +359,10 @@ def run_kvc(args):
 
     pk, pk_src = peaks()
     budgets = [b.budget.cpu().tolist() for _, _, b, _, _ in jobs]
-    alg_bytes = sum(algorithmic_bytes(wl, bud) for (wl, *_), bud in zip(jobs, budgets))
+    heads = ([b.head_counts.cpu().tolist() for _, _, b, _, _ in jobs] if args.select != "layer"
+             else [None] * len(jobs))
+    alg_bytes = sum(algorithmic_bytes(wl, bud, hc)
+                    for (wl, *_), bud, hc in zip(jobs, budgets, heads))
     hbm_frac = alg_bytes / (ms_local / 1e3) / (pk["hbm_gbs"] * 1e9)
     roof = None
     if single:
@@ -345,6 +392,11 @@ def run_kvc(args):
                    "think_criterion": (args.think_criterion if jobs[0][0].think_lambda is not None
                                        else None),
                    "pool_kernel": args.pool if args.pool > 1 else None,
+                   "select": args.select,
+                   "tau": (args.tau_mult / wls[0].seq_len if args.select == "threshold" else None),
+                   "mean_kept_per_head": (round(statistics.mean(
+                       v for hc in heads for row in hc for v in row), 1)
+                       if args.select != "layer" else None),
                    "l2": "inputs larger than the 129 MB L2 (K and V resident in HBM); no flush",
                    "parallelism": f"replica x{world} (one prompt per GPU)"},
         "hbm_roofline": {"algorithmic_bytes_per_step": alg_bytes,
@@ -354,14 +406,19 @@ def run_kvc(args):
         "roofline": roof,
         "clocks": clk.summary(),
         "gpu_launches": args.steps * len(jobs) * (
-            sum(LAUNCHES[k] for k in ("kvc_score", "kvc_mba_budget", "kvc_topk_select",
-                                      "kvc_compact"))
-            + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)
-            + (LAUNCHES["kvc_pool_scores"] if args.pool > 1 else 0)),
+            (LAUNCHES["kvc_score"] + LAUNCHES["kvc_threshold_select"] + LAUNCHES["kvc_compact"]
+             if args.select == "threshold" else
+             sum(LAUNCHES[k] for k in ("kvc_score", "kvc_mba_budget", "kvc_topk_select",
+                                       "kvc_compact"))
+             + (LAUNCHES["kvc_head_budget"] if args.select == "head" else 0)
+             + (LAUNCHES["kvc_pool_scores"] if args.pool > 1 else 0))
+            + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)),
         "stages_ms": {k: round(v / len(jobs), 4) for k, v in stages.items()},
         "wall_s_timed": round(t_wall, 3),
     }
-    out["e2e"] = run_e2e(args, jobs, stream) if args.e2e_steps > 0 else None
+    # the end-to-end leg runs the public compress() call, i.e. the default selection
+    out["e2e"] = (run_e2e(args, jobs, stream) if args.e2e_steps > 0 and args.select == "layer"
+                  else None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(jobs[0][0], jobs[0][1])
     if dist:

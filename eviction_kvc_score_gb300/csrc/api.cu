@@ -224,7 +224,57 @@ int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *
     if (!scores || !budget || !idx) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: NULL tensor");
     if (k_max < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: k_max must be >= 1");
     if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_topk_select")) return KVC_ERR_WORKSPACE;
-    return launch_topk(*shape, scores, budget, k_max, idx, status_word(ws), stream);
+    return launch_topk(*shape, scores, budget, 0, k_max, idx, status_word(ws), stream);
+}
+
+int kvc_head_budget(const kvc_shape *shape, const int32_t *mba, const int32_t *budget,
+                    int32_t *head_budget, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_head_budget")) return KVC_ERR_INVALID_ARG;
+    if (!mba || !budget || !head_budget) return fail(KVC_ERR_INVALID_ARG, "kvc_head_budget: NULL tensor");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_head_budget")) return KVC_ERR_WORKSPACE;
+    return launch_head_budget(*shape, mba, budget, head_budget, stream);
+}
+
+int kvc_topk_select_heads(const kvc_shape *shape, const float *scores, const int32_t *head_budget,
+                          int32_t k_max, int32_t *idx, void *ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_topk_select_heads")) return KVC_ERR_INVALID_ARG;
+    if (!scores || !head_budget || !idx)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select_heads: NULL tensor");
+    if (k_max < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select_heads: k_max must be >= 1");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_topk_select_heads")) return KVC_ERR_WORKSPACE;
+    return launch_topk(*shape, scores, head_budget, 1, k_max, idx, status_word(ws), stream);
+}
+
+int kvc_threshold_select(const kvc_shape *shape, const float *scores, float tau, int32_t k_max,
+                         int32_t *idx, int32_t *counts, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_threshold_select")) return KVC_ERR_INVALID_ARG;
+    if (!scores || !idx || !counts)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_threshold_select: NULL tensor");
+    if (k_max < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_threshold_select: k_max must be >= 1");
+    if (!(tau == tau)) return fail(KVC_ERR_INVALID_ARG, "kvc_threshold_select: tau is NaN");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_threshold_select")) return KVC_ERR_WORKSPACE;
+    return launch_threshold(*shape, scores, tau, k_max, idx, counts, status_word(ws), stream);
+}
+
+int kvc_compact_heads(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
+                      const int32_t *counts, int32_t k_max, void *k_out, void *v_out,
+                      int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_compact_heads")) return KVC_ERR_INVALID_ARG;
+    if (!k || !v || !idx || !counts || !k_out || !v_out)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact_heads: NULL tensor");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact_heads: tensors must be 16-byte aligned");
+    if (k_max < 1 || out_rows < 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compact_heads: bad k_max/out_rows");
+    if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_compact_heads")) return KVC_ERR_WORKSPACE;
+    return launch_compact(*shape, k, v, idx, counts, 1, k_max, k_out, v_out, out_rows,
+                          status_word(ws), stream);
 }
 
 int kvc_pool_scores(const kvc_shape *shape, const float *scores, int32_t kernel, int32_t mode,
@@ -253,7 +303,7 @@ int kvc_compact(const kvc_shape *shape, const void *k, const void *v, const int3
         return fail(KVC_ERR_INVALID_ARG, "kvc_compact: tensors must be 16-byte aligned");
     if (k_max < 1 || out_rows < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_compact: bad k_max/out_rows");
     if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_compact")) return KVC_ERR_WORKSPACE;
-    return launch_compact(*shape, k, v, idx, budget, k_max, k_out, v_out, out_rows, status_word(ws),
+    return launch_compact(*shape, k, v, idx, budget, 0, k_max, k_out, v_out, out_rows, status_word(ws),
                           stream);
 }
 

@@ -1,11 +1,13 @@
-// gather.cu -- K/V compaction and ThinK magnitude channel pruning.
+// gather.cu -- K/V compaction and ThinK key-channel pruning.
 //
 // Compaction (blog post "ZigZagKV, KVCache 80% compression near-lossless",
 // section "SnapKV": the kept tokens are the top-K plus every token of the
 // last window): for head (l,k) the output block holds the n_l kept prefix
 // rows in ascending position order, then the W window rows.  The copy is
 // pure data movement: each thread moves 16-byte vectors, consecutive threads
-// write consecutive addresses, reads are whole rows gathered by index.
+// write consecutive addresses, reads are whole rows gathered by index.  With
+// per-head counts (per-head budgets or threshold selection) head (l,k) keeps
+// its own n_{l,k} rows and the heads follow each other in (l, k) order.
 //
 // ThinK ("ThinK: Thinner Key Cache by Query-Driven Pruning", "Magnitude-based
 // pruning", "Implementation of THINK"): per head, M_d = ||K[:, d]||_2^2 over
@@ -39,19 +41,27 @@ __device__ __forceinline__ int64_t layer_row_offset(const int32_t *budget, int l
 template <typename V>
 __global__ void __launch_bounds__(kCopyThreads)
     compact_kernel(const V *__restrict__ k, const V *__restrict__ v, const int32_t *__restrict__ idx,
-                   const int32_t *__restrict__ budget, int T, int W, int Hkv, int k_max,
-                   int vec_per_row, V *__restrict__ k_out, V *__restrict__ v_out, int64_t out_rows,
-                   uint32_t *status) {
+                   const int32_t *__restrict__ budget, int per_head, int T, int W, int Hkv,
+                   int k_max, int vec_per_row, V *__restrict__ k_out, V *__restrict__ v_out,
+                   int64_t out_rows, uint32_t *status) {
     __shared__ int64_t s_row0;
     __shared__ int s_n;
     const int head = blockIdx.x;
     const int l = head / Hkv, h = head % Hkv;
     const int P = T - W;
     if (threadIdx.x == 0) {
-        int64_t n = kept(budget[l], P);
-        if (n > k_max) n = k_max;   // reported by the top-K step
-        s_n = (int)n;
-        s_row0 = layer_row_offset(budget, l, Hkv, P, W) + (int64_t)h * (kept(budget[l], P) + W);
+        if (per_head) {
+            // budget holds one count per head; heads follow each other
+            int64_t off = 0;
+            for (int u = 0; u < head; ++u) off += min(kept(budget[u], P), (int64_t)k_max) + W;
+            s_n = (int)min(kept(budget[head], P), (int64_t)k_max);
+            s_row0 = off;
+        } else {
+            int64_t n = kept(budget[l], P);
+            if (n > k_max) n = k_max;   // reported by the top-K step
+            s_n = (int)n;
+            s_row0 = layer_row_offset(budget, l, Hkv, P, W) + (int64_t)h * (kept(budget[l], P) + W);
+        }
     }
     __syncthreads();
     const int n = s_n;
@@ -215,8 +225,8 @@ __global__ void __launch_bounds__(kPruneThreads)
 }  // namespace
 
 int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
-                   const int32_t *budget, int32_t k_max, void *k_out, void *v_out, int64_t out_rows,
-                   uint32_t *status, cudaStream_t st) {
+                   const int32_t *budget, int per_head, int32_t k_max, void *k_out, void *v_out,
+                   int64_t out_rows, uint32_t *status, cudaStream_t st) {
     const size_t es = s.dtype == KVC_F32 ? 4 : 2;
     const size_t row_bytes = es * (size_t)s.head_dim;
     const int heads = s.n_layers * s.n_kv_heads;
@@ -224,16 +234,17 @@ int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32
     dim3 grid(heads, (unsigned)min(32, (max_rows + kRowsPerBlock - 1) / kRowsPerBlock));
     if (row_bytes % 16 == 0) {
         compact_kernel<uint4><<<grid, kCopyThreads, 0, st>>>(
-            (const uint4 *)k, (const uint4 *)v, idx, budget, s.seq_len, s.window, s.n_kv_heads,
-            k_max, (int)(row_bytes / 16), (uint4 *)k_out, (uint4 *)v_out, out_rows, status);
+            (const uint4 *)k, (const uint4 *)v, idx, budget, per_head, s.seq_len, s.window,
+            s.n_kv_heads, k_max, (int)(row_bytes / 16), (uint4 *)k_out, (uint4 *)v_out, out_rows,
+            status);
     } else if (row_bytes % 4 == 0) {
         compact_kernel<uint32_t><<<grid, kCopyThreads, 0, st>>>(
-            (const uint32_t *)k, (const uint32_t *)v, idx, budget, s.seq_len, s.window,
+            (const uint32_t *)k, (const uint32_t *)v, idx, budget, per_head, s.seq_len, s.window,
             s.n_kv_heads, k_max, (int)(row_bytes / 4), (uint32_t *)k_out, (uint32_t *)v_out,
             out_rows, status);
     } else {
         compact_kernel<uint16_t><<<grid, kCopyThreads, 0, st>>>(
-            (const uint16_t *)k, (const uint16_t *)v, idx, budget, s.seq_len, s.window,
+            (const uint16_t *)k, (const uint16_t *)v, idx, budget, per_head, s.seq_len, s.window,
             s.n_kv_heads, k_max, (int)(row_bytes / 2), (uint16_t *)k_out, (uint16_t *)v_out,
             out_rows, status);
     }

@@ -306,12 +306,17 @@ int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t d
                uint32_t *status, cudaStream_t st);
 int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,
                   int32_t *budget, cudaStream_t st);
-int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int32_t k_max,
-                int32_t *idx, uint32_t *status, cudaStream_t st);
+// per_head == 0: budget[L] per layer; 1: budget[L][H_kv] per head.
+int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int per_head,
+                int32_t k_max, int32_t *idx, uint32_t *status, cudaStream_t st);
+int launch_head_budget(const kvc_shape &s, const int32_t *mba, const int32_t *budget,
+                       int32_t *head_budget, cudaStream_t st);
+int launch_threshold(const kvc_shape &s, const float *scores, float tau, int32_t k_max,
+                     int32_t *idx, int32_t *counts, uint32_t *status, cudaStream_t st);
 int launch_pool(const kvc_shape &s, const float *scores, int32_t kernel, int32_t mode, float *pooled,
                 cudaStream_t st);
 int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
-                   const int32_t *budget, int32_t k_max, void *k_out, void *v_out,
+                   const int32_t *budget, int per_head, int32_t k_max, void *k_out, void *v_out,
                    int64_t out_rows, uint32_t *status, cudaStream_t st);
 // q == nullptr: magnitude criterion; otherwise the query-driven one.
 int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, const int32_t *budget,

@@ -346,6 +346,44 @@ __global__ void __launch_bounds__(kMaxLayers)
     if (act) budget[l] = (int32_t)B;
 }
 
+// Per-head budgets: block l splits the layer's H_kv * B_l tokens over its
+// heads by MBA (the same largest-remainder split, no per-head minimum), caps
+// each head at P and re-splits the excess over the uncapped heads.  One
+// thread per head (H_kv <= 1024).
+__global__ void __launch_bounds__(kMaxLayers)
+    head_budget_kernel(const int32_t *__restrict__ mba, const int32_t *__restrict__ budget, int Hkv,
+                       long long P, int32_t *__restrict__ head_budget) {
+    __shared__ long long S[kMaxLayers], rem[kMaxLayers];
+    __shared__ unsigned char elig[kMaxLayers];
+    __shared__ unsigned long long red[3];
+    const int l = blockIdx.x, k = threadIdx.x;
+    const bool act = k < Hkv;
+    long long Bl = budget[l];
+    Bl = Bl < 0 ? 0 : (Bl > P ? P : Bl);
+    if (act) {
+        S[k] = mba[(int64_t)l * Hkv + k];
+        elig[k] = 1;
+    }
+    __syncthreads();
+    long long B = lr_split(Hkv, S, elig, (long long)Hkv * Bl, rem, red);
+    while (true) {
+        if (k == 0) red[0] = 0;
+        __syncthreads();
+        if (act && B > P) {
+            atomicAdd(&red[0], (unsigned long long)(B - P));
+            B = P;
+        }
+        __syncthreads();
+        const unsigned long long excess = red[0];
+        __syncthreads();
+        if (excess == 0) break;
+        if (act) elig[k] = B < P;
+        __syncthreads();
+        B += lr_split(Hkv, S, elig, (long long)excess, rem, red);
+    }
+    if (act) head_budget[(int64_t)l * Hkv + k] = (int32_t)B;
+}
+
 // ------------------------------------------------------------------ top-K
 // Block-wide exclusive scan of one uint32 per thread.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tot, uint32_t *total) {
@@ -377,8 +415,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
 
 __global__ void __launch_bounds__(kSelThreads)
     topk_kernel(const float *__restrict__ scores, int T, int P, int Hkv,
-                const int32_t *__restrict__ budget, int k_max, int32_t *__restrict__ idx,
-                uint32_t *status) {
+                const int32_t *__restrict__ budget, int per_head, int k_max,
+                int32_t *__restrict__ idx, uint32_t *status) {
     __shared__ uint32_t cnt[kBuckets];
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t s_total;
@@ -390,7 +428,7 @@ __global__ void __launch_bounds__(kSelThreads)
     const int tid = threadIdx.x, warp = tid >> 5;
     const float *c = scores + (int64_t)head * T;
     int32_t *out = idx + (int64_t)head * k_max;
-    long long B = budget[l];
+    long long B = per_head ? budget[head] : budget[l];
     if (B < 0) {
         if (tid == 0) set_status(status, KVC_DEV_BAD_BUDGET);
         B = 0;
@@ -482,7 +520,75 @@ __global__ void __launch_bounds__(kSelThreads)
     }
 }
 
+// Threshold selection: per head, every prefix position with score >= tau,
+// ascending (ordered block compaction), at most k_max written; counts[head]
+// is the full number (more than k_max sets KVC_DEV_BAD_BUDGET).
+__global__ void __launch_bounds__(kSelThreads)
+    threshold_kernel(const float *__restrict__ scores, int T, int P, float tau, int k_max,
+                     int32_t *__restrict__ idx, int32_t *__restrict__ counts, uint32_t *status) {
+    __shared__ uint32_t warp_tot[32];
+    __shared__ uint32_t s_total;
+    const int head = blockIdx.x;
+    const int tid = threadIdx.x;
+    const float *c = scores + (int64_t)head * T;
+    int32_t *out = idx + (int64_t)head * k_max;
+    long long before = 0;
+    for (int base = 0; base < P; base += 4 * kSelThreads) {
+        const int j0 = base + 4 * tid;
+        uint32_t keep[4], nk = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = j0 + i;
+            keep[i] = (j < P) && c[j] >= tau;
+            nk += keep[i];
+        }
+        long long pos = before + block_excl_scan(nk, warp_tot, &s_total);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (keep[i]) {
+                if (pos < k_max) out[pos] = j0 + i;
+                ++pos;
+            }
+        }
+        before += s_total;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        counts[head] = (int32_t)min(before, (long long)INT32_MAX);
+        if (before > k_max) set_status(status, KVC_DEV_BAD_BUDGET);
+    }
+}
+
 }  // namespace
+
+int launch_head_budget(const kvc_shape &s, const int32_t *mba, const int32_t *budget,
+                       int32_t *head_budget, cudaStream_t st) {
+    if (s.n_kv_heads > kMaxLayers) {
+        set_error("kvc_head_budget: at most %d KV heads", kMaxLayers);
+        return KVC_ERR_UNSUPPORTED;
+    }
+    head_budget_kernel<<<s.n_layers, (s.n_kv_heads + 31) / 32 * 32, 0, st>>>(
+        mba, budget, s.n_kv_heads, (long long)s.seq_len - s.window, head_budget);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_head_budget: launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
+
+int launch_threshold(const kvc_shape &s, const float *scores, float tau, int32_t k_max,
+                     int32_t *idx, int32_t *counts, uint32_t *status, cudaStream_t st) {
+    const int heads = s.n_layers * s.n_kv_heads;
+    threshold_kernel<<<heads, kSelThreads, 0, st>>>(scores, s.seq_len, s.seq_len - s.window, tau,
+                                                    k_max, idx, counts, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_threshold_select: launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    return KVC_OK;
+}
 
 int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
                uint32_t *status, cudaStream_t st) {
@@ -519,11 +625,11 @@ int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t
     return KVC_OK;
 }
 
-int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int32_t k_max,
-                int32_t *idx, uint32_t *status, cudaStream_t st) {
+int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int per_head,
+                int32_t k_max, int32_t *idx, uint32_t *status, cudaStream_t st) {
     const int heads = s.n_layers * s.n_kv_heads;
     topk_kernel<<<heads, kSelThreads, 0, st>>>(scores, s.seq_len, s.seq_len - s.window,
-                                                s.n_kv_heads, budget, k_max, idx, status);
+                                                s.n_kv_heads, budget, per_head, k_max, idx, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_topk_select: launch failed: %s", cudaGetErrorString(e));

@@ -55,6 +55,10 @@ _SIGS = {
     "kvc_mba_budget": (C.c_int, [_sp, _p, _u32, _u32, _i64, _i32, _p, _p, _p, _sz, _p]),
     "kvc_topk_select": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
     "kvc_pool_scores": (C.c_int, [_sp, _p, _i32, _i32, _p, _p, _sz, _p]),
+    "kvc_head_budget": (C.c_int, [_sp, _p, _p, _p, _p, _sz, _p]),
+    "kvc_topk_select_heads": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
+    "kvc_threshold_select": (C.c_int, [_sp, _p, C.c_float, _i32, _p, _p, _p, _sz, _p]),
+    "kvc_compact_heads": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
     "kvc_compact": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune": (C.c_int, [_sp, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune_query": (C.c_int, [_sp, _p, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
@@ -154,6 +158,35 @@ def kvc_pool_scores(s: KvcShape, scores, kernel: int, mode: int, pooled, ws, str
     _check("kvc_pool_scores", _lib.kvc_pool_scores(
         C.byref(s), _ptr(scores), int(kernel), int(mode), _ptr(pooled), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def kvc_head_budget(s: KvcShape, mba, budget, head_budget, ws, stream=None) -> None:
+    """Per-head split of each layer's budget by MBA (head_budget [L][H_kv])."""
+    _check("kvc_head_budget", _lib.kvc_head_budget(
+        C.byref(s), _ptr(mba), _ptr(budget), _ptr(head_budget), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def kvc_topk_select_heads(s: KvcShape, scores, head_budget, k_max: int, idx, ws,
+                          stream=None) -> None:
+    _check("kvc_topk_select_heads", _lib.kvc_topk_select_heads(
+        C.byref(s), _ptr(scores), _ptr(head_budget), int(k_max), _ptr(idx), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def kvc_threshold_select(s: KvcShape, scores, tau: float, k_max: int, idx, counts, ws,
+                         stream=None) -> None:
+    """Keep every prefix position whose score is >= tau (plus the window)."""
+    _check("kvc_threshold_select", _lib.kvc_threshold_select(
+        C.byref(s), _ptr(scores), float(tau), int(k_max), _ptr(idx), _ptr(counts), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def kvc_compact_heads(s: KvcShape, k, v, idx, counts, k_max: int, k_out, v_out, ws,
+                      stream=None) -> None:
+    _check("kvc_compact_heads", _lib.kvc_compact_heads(
+        C.byref(s), _ptr(k), _ptr(v), _ptr(idx), _ptr(counts), int(k_max), _ptr(k_out),
+        _ptr(v_out), k_out.shape[0], _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def kvc_compact(s: KvcShape, k, v, idx, budget, k_max: int, k_out, v_out, ws, stream=None) -> None:

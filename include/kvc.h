@@ -170,6 +170,47 @@ int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *
                     int32_t k_max, int32_t *idx, void *ws, size_t ws_bytes,
                     cudaStream_t stream);
 
+/* Optional variant of a3/a4 -- per-head budgets inside a layer (blog post
+ * "ZigZagKV, KVCache 80% compression near-lossless": memory should follow
+ * how many tokens each attention head needs, and in "ZigZagKV token
+ * selection" each head's K follows its quota).  For every layer l the
+ * H_kv * min(max(budget[l],0), T-W) prefix tokens are split over its heads in
+ * proportion to mba[l][k] by the largest-remainder rule (ties to the lower
+ * head, equal shares if the layer's MBAs are all zero, no per-head minimum),
+ * each head capped at T-W with the excess re-split over the uncapped heads.
+ * mba [L][H_kv] and budget [L] are DEVICE arrays (kvc_mba_budget's
+ * outputs); head_budget [L][H_kv] int32 is written.  H_kv <= 1024. */
+int kvc_head_budget(const kvc_shape *shape, const int32_t *mba, const int32_t *budget,
+                    int32_t *head_budget, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* kvc_topk_select with one budget per head: head (l,k) keeps
+ * min(max(head_budget[l][k],0), T-W) positions (device array [L][H_kv]). */
+int kvc_topk_select_heads(const kvc_shape *shape, const float *scores, const int32_t *head_budget,
+                          int32_t k_max, int32_t *idx, void *ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* Optional variant of a4 -- threshold selection with the recent window (the
+ * ZigZagKV post, section "SnapKV": scores above a threshold mark the
+ * important tokens; "NVIDIA AI presents KVzap": low-score entries are dropped
+ * and a sliding window of recent tokens is kept, so every head keeps as many
+ * tokens as its context needs).  Per head, every prefix position j < T-W
+ * with scores[l][k][j] >= tau (fp32 compare) is written ascending to
+ * idx[l][k][0..); counts[l][k] (int32, device) receives how many there are.
+ * At most k_max are written; a head with more sets KVC_DEV_BAD_BUDGET.
+ * tau must not be NaN.  Pass idx/counts to kvc_compact_heads. */
+int kvc_threshold_select(const kvc_shape *shape, const float *scores, float tau, int32_t k_max,
+                         int32_t *idx, int32_t *counts, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* kvc_compact with one count per head: head (l,k) contributes
+ * n = min(max(counts[l][k],0), T-W, k_max) rows idx[l][k][0..n), then its W
+ * window rows; heads follow each other in (l, k) order, so head (l,k) starts
+ * at row sum over earlier heads of (n + W).  counts is a DEVICE array
+ * [L][H_kv] (kvc_head_budget's or kvc_threshold_select's output). */
+int kvc_compact_heads(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
+                      const int32_t *counts, int32_t k_max, void *k_out, void *v_out,
+                      int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Optional step before a4 -- SnapKV pooling of the prefix scores (blog post
  * "ZigZagKV, KVCache 80% compression near-lossless", section "SnapKV": the
  * scores are pooled in 1D so that a kept token's neighbours are kept with
