@@ -16,6 +16,8 @@
 // Sums of squares run in a float-float pair (error-free products via FMA and
 // TwoSum additions), about 44 significant bits, so the channel order matches
 // an fp64 sum except for channels equal to within ~1e-13.
+#include <cooperative_groups.h>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -132,21 +134,34 @@ __device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16 *p, int
     return __bfloat162float(p[i]);
 }
 
-constexpr int kPruneThreads = 256;
+constexpr int kPruneThreads = 512;
+constexpr int kPruneCluster = 8;   // CTAs per head, one cluster
 
+// One cluster of kPruneCluster CTAs per head: CTA `rank` owns a contiguous
+// slice of the head's kept prefix rows (and of its window-query rows for the
+// query-driven criterion).  Each CTA forms float-float per-channel sums of
+// squares over its slice (thread = channel x row group, two interleaved
+// accumulators per thread); after a cluster barrier every CTA adds the
+// slices' sums in rank order from distributed shared memory -- the same
+// fixed order in every CTA, so all of them rank the channels identically --
+// and copies the chosen channels of its own rows.
 template <typename T>
 __global__ void __launch_bounds__(kPruneThreads)
     channel_prune_kernel(const T *__restrict__ k_out, const T *__restrict__ q, int Hq,
                          const int32_t *__restrict__ budget, int T_len, int W, int Hkv, int D,
                          int keep, int32_t *__restrict__ chan, T *__restrict__ k_pruned,
                          int64_t pruned_elems, uint32_t *status) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
     __shared__ FF part[kPruneThreads];
+    __shared__ FF slice_k[256], slice_q[256];
     __shared__ double m[256];
     __shared__ int sel[256];
     __shared__ int flag[256];
     __shared__ int64_t s_row0, s_o0;
     __shared__ int s_n;
-    const int head = blockIdx.x;
+    const int rank = (int)cluster.block_rank();
+    const int head = blockIdx.x / kPruneCluster;
     const int l = head / Hkv, h = head % Hkv;
     const int P = T_len - W;
     const int tid = threadIdx.x;
@@ -161,65 +176,104 @@ __global__ void __launch_bounds__(kPruneThreads)
     __syncthreads();
     const int n = s_n;
     const int64_t row0 = s_row0;
-    // 1. per-channel sums of squares: thread = (channel, row group)
+    const int r_lo = (int)((int64_t)n * rank / kPruneCluster);
+    const int r_hi = (int)((int64_t)n * (rank + 1) / kPruneCluster);
     const int groups = kPruneThreads / D;
     const int d = tid % D, g = tid / D;
-    FF acc = {0.f, 0.f};
-    if (g < groups)
-        for (int r = g; r < n; r += groups) acc = ff_add_sq(acc, ld_f(k_out, (row0 + r) * D + d));
-    part[tid] = acc;
-    __syncthreads();
-    if (tid < D) {
-        FF tot = part[tid];
-        for (int gg = 1; gg < groups; ++gg) tot = ff_add(tot, part[gg * D + tid]);
-        m[tid] = (double)tot.hi + (double)tot.lo;
-    }
-    __syncthreads();
-    // 1b. query-driven criterion: times the squared norm of the channel's
-    // window-query column (the W rows of each of the KV head's G query heads)
-    if (q != nullptr) {
-        const int G = Hq / Hkv;
-        const int64_t qrow0 = ((int64_t)l * Hq + (int64_t)h * G) * W;
-        const int qrows = G * W;
-        FF qa = {0.f, 0.f};
-        if (g < groups)
-            for (int r = g; r < qrows; r += groups) qa = ff_add_sq(qa, ld_f(q, (qrow0 + r) * D + d));
-        part[tid] = qa;
+
+    // 1. this CTA's slice: per-channel sums of squares of its rows
+    auto slice_sum = [&](const T *base, int64_t first_row, int lo, int hi, FF *out) {
+        FF a0 = {0.f, 0.f}, a1 = {0.f, 0.f};
+        if (g < groups) {
+            int r = lo + g;
+            for (; r + groups < hi; r += 2 * groups) {
+                a0 = ff_add_sq(a0, ld_f(base, (first_row + r) * D + d));
+                a1 = ff_add_sq(a1, ld_f(base, (first_row + r + groups) * D + d));
+            }
+            if (r < hi) a0 = ff_add_sq(a0, ld_f(base, (first_row + r) * D + d));
+        }
+        part[tid] = ff_add(a0, a1);
         __syncthreads();
         if (tid < D) {
             FF tot = part[tid];
             for (int gg = 1; gg < groups; ++gg) tot = ff_add(tot, part[gg * D + tid]);
-            m[tid] *= (double)tot.hi + (double)tot.lo;
+            out[tid] = tot;
         }
         __syncthreads();
+    };
+    slice_sum(k_out, row0, r_lo, r_hi, slice_k);
+    if (q != nullptr) {
+        // query-driven criterion: the W window rows of each of the head's G
+        // query heads, split over the cluster like the key rows
+        const int G = Hq / Hkv;
+        const int qrows = G * W;
+        slice_sum(q, ((int64_t)l * Hq + (int64_t)h * G) * W,
+                  (int)((int64_t)qrows * rank / kPruneCluster),
+                  (int)((int64_t)qrows * (rank + 1) / kPruneCluster), slice_q);
     }
-    // 2. rank channels by (M desc, d asc); keep the first `keep`, ascending
+    cluster.sync();
+
+    // 2. whole-head sums in rank order, then rank by (score desc, d asc)
+    if (tid < D) {
+        FF tk = {0.f, 0.f}, tq = {0.f, 0.f};
+        for (int rr = 0; rr < kPruneCluster; ++rr) {
+            tk = ff_add(tk, cluster.map_shared_rank(slice_k, rr)[tid]);
+            if (q != nullptr) tq = ff_add(tq, cluster.map_shared_rank(slice_q, rr)[tid]);
+        }
+        double mk = (double)tk.hi + (double)tk.lo;
+        if (q != nullptr) mk *= (double)tq.hi + (double)tq.lo;
+        m[tid] = mk;
+    }
+    __syncthreads();
     if (tid < D) {
         const double mine = m[tid];
-        int rank = 0;
-        for (int o = 0; o < D; ++o) rank += (m[o] > mine) || (m[o] == mine && o < tid);
-        flag[tid] = rank < keep;
+        int rk = 0;
+        for (int o = 0; o < D; ++o) rk += (m[o] > mine) || (m[o] == mine && o < tid);
+        flag[tid] = rk < keep;
     }
     __syncthreads();
     if (tid < D && flag[tid]) {
         int pos = 0;
         for (int o = 0; o < tid; ++o) pos += flag[o];
         sel[pos] = tid;
-        chan[(int64_t)head * keep + pos] = tid;
+        if (rank == 0) chan[(int64_t)head * keep + pos] = tid;
     }
-    __syncthreads();
-    // 3. copy the kept channels of the prefix rows
-    const int64_t o0 = s_o0;
-    const int64_t total = (int64_t)n * keep;
-    for (int64_t i = tid; i < total; i += kPruneThreads) {
-        const int64_t r = i / keep;
-        const int c = (int)(i % keep);
+    // no CTA may leave while another still reads its slice sums
+    cluster.sync();
+
+    // 3. copy the kept channels of this CTA's rows
+    const int64_t o0 = s_o0 + (int64_t)r_lo * keep;
+    const int total = (r_hi - r_lo) * keep;
+    for (int i = tid; i < total; i += kPruneThreads) {
+        const int r = i / keep;
+        const int c = i - r * keep;
         if (o0 + i >= pruned_elems) {
             set_status(status, KVC_DEV_OUT_CAPACITY);
             break;
         }
-        k_pruned[o0 + i] = k_out[(row0 + r) * D + sel[c]];
+        k_pruned[o0 + i] = k_out[(row0 + r_lo + r) * D + sel[c]];
     }
+}
+
+template <typename T>
+cudaError_t launch_prune_t(const kvc_shape &s, const void *q, const void *k_out,
+                           const int32_t *budget, int32_t keep, int32_t *chan, void *k_pruned,
+                           int64_t pruned_elems, uint32_t *status, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(s.n_layers * s.n_kv_heads * kPruneCluster));
+    cfg.blockDim = dim3(kPruneThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPruneCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, channel_prune_kernel<T>, (const T *)k_out, (const T *)q,
+                              s.n_q_heads, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim,
+                              (int)keep, chan, (T *)k_pruned, pruned_elems, status);
 }
 
 }  // namespace
@@ -259,16 +313,18 @@ int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32
 int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, const int32_t *budget,
                          int32_t keep, int32_t *chan, void *k_pruned, int64_t pruned_elems,
                          uint32_t *status, cudaStream_t st) {
-    const int heads = s.n_layers * s.n_kv_heads;
-    if (s.dtype == KVC_F32) {
-        channel_prune_kernel<float><<<heads, kPruneThreads, 0, st>>>(
-            (const float *)k_out, (const float *)q, s.n_q_heads, budget, s.seq_len, s.window,
-            s.n_kv_heads, s.head_dim, keep, chan, (float *)k_pruned, pruned_elems, status);
-    } else {
-        channel_prune_kernel<__nv_bfloat16><<<heads, kPruneThreads, 0, st>>>(
-            (const __nv_bfloat16 *)k_out, (const __nv_bfloat16 *)q, s.n_q_heads, budget,
-            s.seq_len, s.window, s.n_kv_heads, s.head_dim, keep, chan,
-            (__nv_bfloat16 *)k_pruned, pruned_elems, status);
+    if (s.head_dim > 256) {
+        set_error("kvc_channel_prune: head_dim above 256 is not supported");
+        return KVC_ERR_UNSUPPORTED;
+    }
+    cudaError_t e0 = s.dtype == KVC_F32
+                         ? launch_prune_t<float>(s, q, k_out, budget, keep, chan, k_pruned,
+                                                 pruned_elems, status, st)
+                         : launch_prune_t<__nv_bfloat16>(s, q, k_out, budget, keep, chan, k_pruned,
+                                                         pruned_elems, status, st);
+    if (e0 != cudaSuccess) {
+        set_error("kvc_channel_prune: launch failed: %s", cudaGetErrorString(e0));
+        return KVC_ERR_CUDA;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
