@@ -34,6 +34,9 @@
  *               channel score = Frobenius norm of Q[-S_obs:, j] K[:, j]^T.
  *  [ZZ-HEAD]    ZigZagKV post: memory per attention head should follow the
  *               tokens that head needs; each head's K follows its quota.
+ *  [KEYF]       "Keyformer: KV Cache reduction through key tokens selection"
+ *               (moyutianzun.com): Gumbel noise on the logits, temperature
+ *               softmax, recent w tokens plus the top k - w older ones.
  *  [THRESH]     ZigZagKV post, "SnapKV": scores above a threshold mark the
  *               important tokens; "NVIDIA AI presents KVzap" (kiadev.net):
  *               low-score entries are dropped, a sliding window of recent
@@ -769,6 +772,107 @@ int64_t ora_compact_heads(const ora_shape *s, const void *src, const int32_t *id
             memcpy(o + (size_t)row * D * es, in + (size_t)(u * T + P + w) * D * es, (size_t)D * es);
     }
     return row;
+}
+
+/* ---------------------------------------------------------------------------
+ * Optional: Keyformer scoring with Gumbel noise                 [KEYF]
+ *
+ * "Keyformer: KV Cache reduction through key tokens selection" (notes on
+ * moyutianzun.com): the logits x_i = q.k_i / sqrt(d) get Gumbel noise,
+ * y_i = x_i + zeta_i, and a temperature, f(y_i) = softmax(y / tau); in the
+ * prompt phase the w most recent tokens are kept and the other k - w are the
+ * highest-scoring older tokens.  Readings: the page's prompt-phase tau is
+ * "infinite", which would make every score equal, so tau is a parameter; the
+ * queries are the W window rows (as for SnapKV) and the score of a key is the
+ * mean of f over them, causal inside the window, GQA rows averaged; the
+ * recent tokens are the window, and the older tokens are chosen by the same
+ * top-K step.  zeta = -ln(-ln u) with u uniform on (0,1) from the
+ * counter-based generator below, one draw per (unit, row, key).
+ *
+ * Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011): a 4 x 32-bit counter and a 2 x 32-bit key;
+ * each of ten rounds multiplies counter words 0 and 2 by two constants into
+ * 64-bit products, and the new counter is (hi(c2*M1) ^ c1 ^ k0, lo(c2*M1),
+ * hi(c0*M0) ^ c3 ^ k1, lo(c0*M0)); the key gains the Weyl increments after
+ * every round but the last.
+ * ------------------------------------------------------------------------- */
+void ora_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)M0 * c0, p1 = (uint64_t)M1 * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        if (round < 9) { k0 += W0; k1 += W1; }
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The uniform draw for (unit u, row r, key j): word 0 of Philox4x32-10 at
+ * counter (j, r, u, 0) with key (seed low, seed high); its top 24 bits b give
+ * u = (b + 1/2) * 2^-24, exactly representable and strictly inside (0,1). */
+double ora_keyformer_uniform(uint64_t seed, int64_t unit, int64_t row, int64_t key)
+{
+    const uint32_t ctr[4] = {(uint32_t)key, (uint32_t)row, (uint32_t)unit, 0u};
+    const uint32_t k[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    ora_philox4x32_10(ctr, k, o);
+    return ((double)(o[0] >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+
+int ora_score_keyformer(const ora_shape *s, const void *q, const void *k, uint64_t seed,
+                        double tau, double *scores)
+{
+    if (!ora_shape_ok(s) || !(tau > 0.0)) return -1;
+    const int64_t D = s->head_dim, T = s->seq_len, W = s->window;
+    const int64_t Hq = s->n_q_heads, Hkv = s->n_kv_heads, G = Hq / Hkv, L = s->n_layers;
+    const int64_t P = T - W;
+    const double rows = (double)(G * W);
+    const double root_d = sqrt((double)D);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t u = 0; u < L * Hkv; ++u) {
+        const int64_t layer = u / Hkv, kv_head = u % Hkv;
+        double *c = scores + u * T;
+        const int64_t k_base = u * T * D;
+        double *y = (double *)malloc(sizeof(double) * (size_t)T);
+        double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!y || !qr) { free(y); free(qr); bad = 1; continue; }
+        for (int64_t j = 0; j < T; ++j) c[j] = 0.0;
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t h = kv_head * G + g;
+            for (int64_t i = 0; i < W; ++i) {
+                const int64_t r = g * W + i;
+                const int64_t q_base = ((layer * Hq + h) * W + i) * D;
+                for (int64_t d = 0; d < D; ++d) qr[d] = ora_elem(q, q_base + d, s->dtype);
+                const int64_t t = P + i;
+                double mu = -INFINITY;
+                for (int64_t j = 0; j <= t; ++j) {
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += qr[d] * ora_elem(k, k_base + j * D + d, s->dtype);
+                    const double zeta = -log(-log(ora_keyformer_uniform(seed, u, r, j)));
+                    y[j] = (dot / root_d + zeta) / tau;
+                    if (y[j] > mu) mu = y[j];
+                }
+                double z = 0.0;
+                for (int64_t j = 0; j <= t; ++j) {
+                    y[j] = exp(y[j] - mu);
+                    z += y[j];
+                }
+                for (int64_t j = 0; j <= t; ++j) c[j] += y[j] / z / rows;
+            }
+        }
+        free(y);
+        free(qr);
+    }
+    return bad ? -2 : 0;
 }
 
 /* ---------------------------------------------------------------------------

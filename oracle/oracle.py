@@ -66,6 +66,9 @@ def lib():
                 "ora_pool": (C.c_int, [sp, p, i32, i32, p]),
                 "ora_pool_f32": (C.c_int, [sp, p, i32, i32, p]),
                 "ora_compact_rows": (i64, [sp, p]),
+                "ora_philox4x32_10": (None, [p, p, p]),
+                "ora_keyformer_uniform": (d, [C.c_uint64, i64, i64, i64]),
+                "ora_score_keyformer": (C.c_int, [sp, p, p, C.c_uint64, d, p]),
                 "ora_head_budget": (C.c_int, [C.c_int, C.c_int, p, p, i64, p]),
                 "ora_topk_heads": (C.c_int, [sp, p, p, i64, p]),
                 "ora_threshold_select": (C.c_int, [sp, p, C.c_float, i64, p, p]),
@@ -235,6 +238,28 @@ def compact_heads(s: Shape, x, idx, counts, k_max: int) -> np.ndarray:
                  "compact_heads")
     assert got == rows
     return out
+
+
+def philox4x32_10(counter, key) -> list:
+    c = (C.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in counter])
+    k = (C.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    o = (C.c_uint32 * 4)()
+    lib().ora_philox4x32_10(c, k, o)
+    return list(o)
+
+
+def keyformer_uniform(seed: int, unit: int, row: int, key: int) -> float:
+    return lib().ora_keyformer_uniform(int(seed), int(unit), int(row), int(key))
+
+
+def score_keyformer(s: Shape, q, k, seed: int, tau: float) -> np.ndarray:
+    """Keyformer window scores with Gumbel noise and temperature: fp64
+    [L][H_kv][T]."""
+    qa, ka = raw(q), raw(k)
+    c = np.empty((s.n_layers, s.n_kv_heads, s.seq_len), dtype=np.float64)
+    _check(lib().ora_score_keyformer(C.byref(s), _ptr(qa), _ptr(ka), int(seed), float(tau),
+                                     _ptr(c)), "score_keyformer")
+    return c
 
 
 def compact_rows(s: Shape, budget_l) -> int:

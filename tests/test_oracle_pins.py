@@ -566,6 +566,68 @@ def test_compact_heads_equals_fancy_indexing():
     assert np.array_equal(got, want)
 
 
+# ----------------------------------------------------------- optional Keyformer
+def test_philox4x32_10_known_answers():
+    """Known-answer vectors published with the Philox4x32-10 generator
+    (zero counter and key, all-ones counter and key, and the pi-digits
+    counter and key)."""
+    cases = [((0, 0, 0, 0), (0, 0), (0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8)),
+             ((0xffffffff,) * 4, (0xffffffff,) * 2, (0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd)),
+             ((0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344), (0xa4093822, 0x299f31d0),
+              (0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1))]
+    for ctr, key, want in cases:
+        assert O.philox4x32_10(ctr, key) == list(want)
+
+
+def test_keyformer_uniforms_and_gumbel_moments():
+    """The draws are strictly inside (0,1) with the right mean, and
+    -ln(-ln u) has the Gumbel mean (Euler's gamma) and variance (pi^2/6)."""
+    u = np.array([O.keyformer_uniform(7, unit, row, key)
+                  for unit in range(4) for row in range(50) for key in range(500)])
+    assert u.min() > 0.0 and u.max() < 1.0
+    assert abs(u.mean() - 0.5) < 0.01
+    z = -np.log(-np.log(u))
+    assert abs(z.mean() - np.euler_gamma) < 0.02
+    assert abs(z.var() - np.pi ** 2 / 6) < 0.05
+    assert O.keyformer_uniform(7, 1, 2, 3) != O.keyformer_uniform(8, 1, 2, 3)
+
+
+@pytest.mark.parametrize("tau", [0.5, 1.0, 3.0])
+def test_keyformer_single_row_is_noisy_softmax(tau):
+    """W = 1, G = 1: the score is one softmax of (q.k/sqrt(D) + zeta)/tau over
+    the visible keys, zeta the Gumbel inverse CDF (scipy) of the uniforms."""
+    from scipy.stats import gumbel_r
+    L, H, D, T, W = 1, 2, 16, 50, 1
+    q, k = _rand_inputs(L, H, H, D, T, W, 3)
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    c = O.score_keyformer(s, q, k, 99, tau)
+    for h in range(H):
+        x = k[0, h].double().numpy() @ q[0, h, 0].double().numpy() / np.sqrt(D)
+        zeta = gumbel_r.ppf([O.keyformer_uniform(99, h, 0, j) for j in range(T)])
+        want = scipy.special.softmax((x + zeta) / tau)
+        np.testing.assert_allclose(c[0, h], want, rtol=1e-9, atol=1e-300)
+
+
+def test_keyformer_rows_sum_to_one_and_hot_temperature_is_uniform():
+    L, Hq, H, D, T, W = 2, 4, 2, 8, 40, 5
+    q, k = _rand_inputs(L, Hq, H, D, T, W, 4)
+    s = O.shape_of(L, Hq, H, D, T, W, "f32")
+    c = O.score_keyformer(s, q, k, 5, 1.0)
+    np.testing.assert_allclose(c.sum(-1), 1.0, rtol=1e-12)
+    # a very hot temperature flattens every row to 1/(visible keys)
+    hot = O.score_keyformer(s, q, k, 5, 1e12)
+    P = T - W
+    want = np.zeros(T)
+    for i in range(W):
+        want[: P + i + 1] += 1.0 / (P + i + 1) / W
+    for l in range(L):
+        for h in range(H):
+            np.testing.assert_allclose(hot[l, h], want, rtol=1e-9)
+    # different seeds give different scores; the same seed the same scores
+    assert not np.array_equal(c, O.score_keyformer(s, q, k, 6, 1.0))
+    assert np.array_equal(c, O.score_keyformer(s, q, k, 5, 1.0))
+
+
 # --------------------------------------------------------------------- end to end
 def test_tiny_planted_keys_are_selected():
     """The tiny MHA workload plants 4 keys per head equal to 3x the head's mean
