@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--select", default="layer", choices=["layer", "head", "threshold"],
                     help="token selection: per-layer budgets (default), per-head budgets split "
                          "by MBA inside each layer, or every prefix token scoring >= tau")
+    ap.add_argument("--score", default="snapkv", choices=["snapkv", "keyformer"],
+                    help="window scores: SnapKV (default) or Keyformer's Gumbel-noised, "
+                         "temperature-softened scores (CUDA-core fp32 kernels)")
+    ap.add_argument("--keyformer-tau", type=float, default=1.0)
     ap.add_argument("--tau-mult", type=float, default=4.0,
                     help="threshold selection: tau = tau_mult / seq_len (mean score x tau_mult)")
     return ap.parse_args()
@@ -180,9 +184,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_for(kernel_src):
+def traffic_for(kernel_src, workload):
     """DRAM bytes per launch recorded by an ncu capture of this exact kernel
-    source (profiles/score_traffic.txt); None if absent or stale."""
+    source on this workload (profiles/score_traffic.txt); None if absent,
+    stale or recorded for another workload."""
     p = os.path.join(ROOT, "profiles", "score_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -192,7 +197,7 @@ def traffic_for(kernel_src):
         if "=" in ln and not ln.lstrip().startswith("#"):
             k, v = ln.split("=", 1)
             rec[k.strip()] = v.strip()
-    if rec.get("kernel_src_sha256_16") != h:
+    if rec.get("kernel_src_sha256_16") != h or rec.get("workload") != workload:
         return None
     try:
         return float(rec["traffic_bytes_per_step_score"])
@@ -270,10 +275,14 @@ def run_kvc(args):
             mark("start")
             if score_ev is not None:
                 score_ev[0].record(stream)
-            kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
+            if args.score == "keyformer":
+                kvc.kvc_score_keyformer(b.shape, x["q"], x["k"], 0x5EED, args.keyformer_tau,
+                                        b.scores, b.ws)
+            else:
+                kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
             if score_ev is not None:
                 score_ev[1].record(stream)
-            mark("kvc_score")
+            mark("kvc_score_keyformer" if args.score == "keyformer" else "kvc_score")
             if args.select == "threshold":
                 kvc.kvc_threshold_select(b.shape, b.scores, args.tau_mult / wl.seq_len, b.k_max,
                                          b.idx, b.head_counts, b.ws)
@@ -371,12 +380,23 @@ def run_kvc(args):
         flops = score_flops(wl)
         achieved = flops / (score_ms / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-        traffic = traffic_for(os.path.join(ROOT, "eviction_kvc_score_gb300", "csrc", "score_tc.cu"))
+        traffic = traffic_for(os.path.join(ROOT, "eviction_kvc_score_gb300", "csrc", "score_tc.cu"),
+                              args.workload if not args.layers else None)
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": "kvc_score (stats + merge + column-mean launches)",
                 "ms_per_launch": round(score_ms, 4), "flops_per_launch": flops,
                 "peak_source": f"{pk_src} bf16_tflops_sustained"}
+        if args.score == "keyformer":
+            # CUDA-core fp32 kernels: FFMA peak = SMs x 128 lanes x 2 flop x max SM clock
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            peak = sms * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": "kvc_score_keyformer (stats + merge + column-mean launches, fp32 "
+                              "FFMA, Philox + Gumbel per logit not counted)",
+                    "ms_per_launch": round(score_ms, 4), "flops_per_launch": flops,
+                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -393,6 +413,8 @@ def run_kvc(args):
                                        else None),
                    "pool_kernel": args.pool if args.pool > 1 else None,
                    "select": args.select,
+                   "score": args.score,
+                   "keyformer_tau": args.keyformer_tau if args.score == "keyformer" else None,
                    "tau": (args.tau_mult / wls[0].seq_len if args.select == "threshold" else None),
                    "mean_kept_per_head": (round(statistics.mean(
                        v for hc in heads for row in hc for v in row), 1)
@@ -417,7 +439,8 @@ def run_kvc(args):
         "wall_s_timed": round(t_wall, 3),
     }
     # the end-to-end leg runs the public compress() call, i.e. the default selection
-    out["e2e"] = (run_e2e(args, jobs, stream) if args.e2e_steps > 0 and args.select == "layer"
+    out["e2e"] = (run_e2e(args, jobs, stream)
+                  if args.e2e_steps > 0 and args.select == "layer" and args.score == "snapkv"
                   else None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(jobs[0][0], jobs[0][1])

@@ -197,6 +197,27 @@ int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *s
     return tc ? launch_score_tc(s, sp, a, device_info().sms, stream) : launch_score_simt(s, sp, a, stream);
 }
 
+int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,
+                        double tau, float *scores, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_score_keyformer")) return KVC_ERR_INVALID_ARG;
+    if (!q_obs || !k || !scores) return fail(KVC_ERR_INVALID_ARG, "kvc_score_keyformer: NULL tensor");
+    if (!(tau > 0.0) || tau > 1e30)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_score_keyformer: tau must be in (0, 1e30]");
+    const kvc_shape &s = *shape;
+    const WsLayout w = ws_layout(s);
+    if (!ws_ok(ws, ws_bytes, w.total, "kvc_score_keyformer")) return KVC_ERR_WORKSPACE;
+    const ScoreSplit sp = make_split(s, false);
+    ScoreArgs a;
+    a.q = q_obs;
+    a.k = k;
+    a.scores = scores;
+    a.partial = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.partial_off);
+    a.neg_bias = reinterpret_cast<float *>(static_cast<char *>(ws) + w.bias_off);
+    a.status = status_word(ws);
+    return launch_score_keyformer(s, sp, a, seed, tau, stream);
+}
+
 int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_num, uint32_t mass_den,
                    int64_t total_budget, int32_t layer_floor, int32_t *mba, int32_t *budget, void *ws,
                    size_t ws_bytes, cudaStream_t stream) {

@@ -302,6 +302,8 @@ int launch_score_simt(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs 
                       cudaStream_t st);
 int launch_score_merge(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
                        cudaStream_t st);
+int launch_score_keyformer(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
+                           uint64_t seed, double tau, cudaStream_t st);
 int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
                uint32_t *status, cudaStream_t st);
 int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,

@@ -1,7 +1,10 @@
 // score_simt.cu -- observation-window scores on the CUDA cores (fp32 FFMA),
 // for fp32 inputs and for bf16 shapes outside the tensor-core kernel's range
 // (head_dim other than 64/128, or more than 512 window rows per KV head);
-// also the merge of pass-1 partial row statistics used by both paths.
+// the merge of pass-1 partial row statistics used by both paths; and the
+// optional Keyformer scores ("Keyformer: KV Cache reduction through key
+// tokens selection": Gumbel noise on the logits, temperature softmax), the
+// same two passes with a counter-based Gumbel draw per (unit, row, key).
 //
 // Same two-pass definition as score_tc.cu (SnapKV window scoring with
 // softmax(q.k / sqrt(D)), causal inside the window, GQA rows averaged), same
@@ -31,11 +34,51 @@ struct SimtParams {
     float2 *partial;
     const float *neg_bias;
     float *scores;
+    // Keyformer noise (NOISE kernels only): Philox key, log2(e) / tau
+    uint32_t key0, key1;
+    float noise_scale;
 };
+
+// Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2,
+// 3", SC 2011), word 0 of the output block for counter (c0, c1, c2, 0).
+__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                 uint32_t k0, uint32_t k1) {
+    uint32_t c3 = 0;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c0;
+}
+
+// Gumbel draw for (unit, row, key): u = (b + 1/2) 2^-24 from the top 24 bits
+// b, zeta = -ln(-ln u).  -ln u is formed from whichever of u and 1 - u is
+// exact in fp32 (log1p near 1), so the rare draws close to 1 -- the large
+// zeta that dominate a row -- come out accurately.
+__device__ __forceinline__ float gumbel(uint32_t unit, uint32_t row, uint32_t key, uint32_t k0,
+                                        uint32_t k1) {
+    const uint32_t b = philox_word0(key, row, unit, k0, k1) >> 8;
+    float nlu;
+    if (b >= (1u << 23)) {
+        const float v = ((float)((1u << 24) - 1u - b) + 0.5f) * 0x1p-24f;   // 1 - u, exact
+        nlu = -log1pf(-v);
+    } else {
+        const float u = ((float)b + 0.5f) * 0x1p-24f;                       // exact
+        nlu = -logf(u);
+    }
+    return -logf(nlu);
+}
 
 // Pass 1: thread = query row; for each 32-key sub-tile held in shared memory
 // the thread forms its 32 logits and folds them into an online (max, sum).
-template <typename T>
+template <typename T, bool NOISE>
 __global__ void __launch_bounds__(kSimtThreads)
     score_stats_simt(const T *__restrict__ q, const T *__restrict__ k, SimtParams p) {
     extern __shared__ float ks[];                   // [kSub][D]
@@ -73,6 +116,30 @@ __global__ void __launch_bounds__(kSimtThreads)
                     for (int i = 0; i < kSub; ++i) s[i] = fmaf(qd, ks[i * D + d], s[i]);
                 }
                 const int lim = p.P + w - j0;   // largest visible sub-tile column
+                if (NOISE) {
+                    // base-2 noisy logits (x / sqrt(D) + zeta) / tau, logits
+                    // beyond the causal limit stay out of the max and sum
+#pragma unroll
+                    for (int i = 0; i < kSub; ++i)
+                        if (i <= lim && j0 + i < p.T)
+                            s[i] = fmaf(gumbel((uint32_t)u, (uint32_t)r, (uint32_t)(j0 + i),
+                                               p.key0, p.key1),
+                                        p.noise_scale, s[i] * p.cs);
+                        else
+                            s[i] = -INFINITY;
+                    float mxn = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < kSub; ++i) mxn = fmaxf(mxn, s[i]);
+                    if (mxn > -INFINITY) {
+                        const float mnew = fmaxf(m_run, mxn);
+                        float sum = 0.f;
+#pragma unroll
+                        for (int i = 0; i < kSub; ++i) sum += ex2(s[i] - mnew);
+                        l_run = l_run * ex2(m_run - mnew) + sum;
+                        m_run = mnew;
+                    }
+                    continue;
+                }
                 float mx = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < kSub; ++i)
@@ -98,7 +165,7 @@ __global__ void __launch_bounds__(kSimtThreads)
 
 // Pass 2: thread = key; the unit's query rows stream through shared memory
 // 32 at a time; each thread sums 2^(x + nb_r) over the rows that see it.
-template <typename T>
+template <typename T, bool NOISE>
 __global__ void __launch_bounds__(kSimtThreads)
     score_colmean_simt(const T *__restrict__ q, const T *__restrict__ k, SimtParams p) {
     extern __shared__ float qs[];                   // [kSub][D] then nb[kSub]
@@ -135,8 +202,12 @@ __global__ void __launch_bounds__(kSimtThreads)
 #pragma unroll
             for (int i = 0; i < kSub; ++i) {
                 const int rr = rbase + i;
-                const bool vis = rr < p.rows && (rr % p.W) >= dj;
-                const float e = ex2(fmaf(s[i], p.cs, nbs[i]));
+                const bool vis = rr < p.rows && (rr % p.W) >= dj && j < p.T;
+                float arg = fmaf(s[i], p.cs, nbs[i]);
+                if (NOISE && vis)
+                    arg = fmaf(gumbel((uint32_t)u, (uint32_t)rr, (uint32_t)j, p.key0, p.key1),
+                               p.noise_scale, arg);
+                const float e = ex2(arg);
                 acc += vis ? e : 0.f;
             }
         }
@@ -173,8 +244,9 @@ __global__ void score_merge(const float2 *__restrict__ partial, float *__restric
     neg_bias[i] = -(m + log2f(l));
 }
 
-template <typename T>
-int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st) {
+template <typename T, bool NOISE>
+int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st,
+                  uint64_t seed = 0, double tau = 1.0) {
     SimtParams p;
     p.n_tiles = sp.n_tiles;
     p.tiles_per_unit = sp.tiles_per_unit;
@@ -186,7 +258,12 @@ int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, 
     p.D = s.head_dim;
     p.rows = sp.rows;
     p.rows_pad = sp.rows_pad;
-    p.cs = (float)(kLog2e / sqrt((double)s.head_dim));
+    // Keyformer divides the noisy logits by tau: both the logit scale and
+    // the noise scale carry 1/tau (plain scores: tau = 1, no noise)
+    p.cs = (float)(kLog2e / sqrt((double)s.head_dim) / tau);
+    p.key0 = (uint32_t)seed;
+    p.key1 = (uint32_t)(seed >> 32);
+    p.noise_scale = (float)(kLog2e / tau);
     p.partial = a.partial;
     p.neg_bias = a.neg_bias;
     p.scores = a.scores;
@@ -194,9 +271,11 @@ int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, 
     const T *k = static_cast<const T *>(a.k);
     const size_t sm1 = (size_t)kSub * s.head_dim * sizeof(float);
     const size_t sm2 = sm1 + kSub * sizeof(float);
-    cudaFuncSetAttribute(score_stats_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
-    cudaFuncSetAttribute(score_colmean_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
-    score_stats_simt<T><<<sp.grid, kSimtThreads, sm1, st>>>(q, k, p);
+    cudaFuncSetAttribute(score_stats_simt<T, NOISE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm1);
+    cudaFuncSetAttribute(score_colmean_simt<T, NOISE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm2);
+    score_stats_simt<T, NOISE><<<sp.grid, kSimtThreads, sm1, st>>>(q, k, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_score: SIMT pass-1 launch failed: %s", cudaGetErrorString(e));
@@ -204,7 +283,7 @@ int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, 
     }
     int rc = launch_score_merge(s, sp, a, st);
     if (rc) return rc;
-    score_colmean_simt<T><<<sp.grid, kSimtThreads, sm2, st>>>(q, k, p);
+    score_colmean_simt<T, NOISE><<<sp.grid, kSimtThreads, sm2, st>>>(q, k, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_score: SIMT pass-2 launch failed: %s", cudaGetErrorString(e));
@@ -233,8 +312,14 @@ int launch_score_merge(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs
 
 int launch_score_simt(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
                       cudaStream_t st) {
-    if (s.dtype == KVC_F32) return launch_simt_t<float>(s, sp, a, st);
-    return launch_simt_t<__nv_bfloat16>(s, sp, a, st);
+    if (s.dtype == KVC_F32) return launch_simt_t<float, false>(s, sp, a, st);
+    return launch_simt_t<__nv_bfloat16, false>(s, sp, a, st);
+}
+
+int launch_score_keyformer(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
+                           uint64_t seed, double tau, cudaStream_t st) {
+    if (s.dtype == KVC_F32) return launch_simt_t<float, true>(s, sp, a, st, seed, tau);
+    return launch_simt_t<__nv_bfloat16, true>(s, sp, a, st, seed, tau);
 }
 
 }  // namespace kvc

@@ -52,6 +52,7 @@ _SIGS = {
     "kvc_workspace_status": (C.c_int, [_p, _sz, C.POINTER(_u32), _p]),
     "kvc_score": (C.c_int, [_sp, _p, _p, _p, _p, _sz, _p]),
     "kvc_score_noalloc": (C.c_int, [_sp, _p, _p, _p, _p, _p]),
+    "kvc_score_keyformer": (C.c_int, [_sp, _p, _p, C.c_uint64, _d, _p, _p, _sz, _p]),
     "kvc_mba_budget": (C.c_int, [_sp, _p, _u32, _u32, _i64, _i32, _p, _p, _p, _sz, _p]),
     "kvc_topk_select": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
     "kvc_pool_scores": (C.c_int, [_sp, _p, _i32, _i32, _p, _p, _sz, _p]),
@@ -138,6 +139,14 @@ def kvc_score_noalloc(s: KvcShape, q_obs, k, scores, dev_status=None, stream=Non
     stream."""
     _check("kvc_score_noalloc", _lib.kvc_score_noalloc(
         C.byref(s), _ptr(q_obs), _ptr(k), _ptr(scores), _ptr(dev_status), _stream(stream)))
+
+
+def kvc_score_keyformer(s: KvcShape, q_obs, k, seed: int, tau: float, scores, ws,
+                        stream=None) -> None:
+    """Keyformer window scores: Gumbel-noised logits, temperature tau."""
+    _check("kvc_score_keyformer", _lib.kvc_score_keyformer(
+        C.byref(s), _ptr(q_obs), _ptr(k), int(seed) & 0xFFFFFFFFFFFFFFFF, float(tau),
+        _ptr(scores), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def kvc_mba_budget(s: KvcShape, scores, mass_num: int, mass_den: int, total_budget: int,

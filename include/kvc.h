@@ -142,6 +142,25 @@ int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *s
 int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, const void *k, float *scores,
                       uint32_t *dev_status, cudaStream_t stream);
 
+/* Optional variant of a1 -- Keyformer scores ("Keyformer: KV Cache reduction
+ * through key tokens selection": Gumbel noise zeta is added to the logits
+ * x = q.k / sqrt(D) and a temperature tau softens the softmax,
+ * f = softmax((x + zeta) / tau); the most recent tokens are kept and the
+ * remaining budget goes to the highest-scoring older tokens).  Same layouts,
+ * workspace and two-pass structure as kvc_score, with
+ *   scores[l][k][j] = 1/(G W) sum over window rows r that see j of
+ *                     softmax_j((x_rj + zeta_rj) / tau),
+ * zeta_rj = -ln(-ln u), u = (b + 1/2) 2^-24 where b is the top 24 bits of
+ * word 0 of Philox4x32-10 at counter (j, r, l*H_kv + k, 0) and key
+ * (seed & 0xffffffff, seed >> 32); r = g*W + w is the row within the unit.
+ * The page sets tau to infinity in the prompt phase, which would make every
+ * score equal; here tau is a parameter in (0, 1e30].  The window is the
+ * recent part that compaction always keeps; pass the scores to
+ * kvc_mba_budget / kvc_topk_select for the older part.  Runs on the CUDA
+ * cores in fp32 (every dtype and head_dim up to 256). */
+int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,
+                        double tau, float *scores, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* a2 + a3 -- ZigZagKV budgets.
  * mba[l][k] = smallest m with mass_den * (sum of the m largest u) >=
  *             mass_num * (sum of all u), u_j = floor(scores[l][k][j] * 2^56),
