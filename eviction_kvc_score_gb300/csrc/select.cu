@@ -1,14 +1,16 @@
-// select.cu -- ZigZagKV MBA, layer budgets and per-head top-K.
+// select.cu -- ZigZagKV MBA, layer budgets and per-head top-K (and the
+// optional per-head budgets and threshold selection).
 //
 // MBA (blog post "ZigZagKV, KVCache 80% compression near-lossless", section
 // "ZigZagKV's new observations"): the fewest tokens whose scores reach 90%
 // of a head's attention mass.  Mass is exact fixed point u = floor(c*2^56),
 // so the count does not depend on summation order.  Instead of sorting, an
 // MSB radix select over the fp32 bit patterns (non-negative floats order like
-// their bit patterns) keeps, per digit bucket, the count and the u-mass, and
-// descends into the bucket where the running mass from the top first reaches
-// the threshold.  The exact crossing value v* and the mass above it then give
-// the count in closed form.
+// their bit patterns) finds the crossing value v* -- the score at which the
+// running mass from the top first reaches the threshold -- and the exact
+// mass above it gives the count in closed form.  The first digit's bucket is
+// found from truncated bucket masses and confirmed with one exact pass; the two
+// remaining digits use exact 64-bit bucket masses.
 //
 // Budgets (same post, "ZigZagKV space allocation"): integer proportional
 // split with a floor and largest remainders, capped at the prefix length.
@@ -18,12 +20,11 @@
 // keeps everything above it and the lowest-index ties, writing positions in
 // ascending order.
 //
-// Histograms: one shared histogram per block with a 12-bit first digit
-// (exponent plus four mantissa bits, so a head's scores spread over many
-// buckets).  Within a warp the lanes that share the first active lane's digit
-// are added as one group (ballot + warp reductions), the rest one by one.
-// Only native 32-bit shared atomics are used: the exact 64-bit mass of a
-// bucket is a (hi, lo) word pair, lo's carry folded into hi.
+// One 1024-thread block per head; the head's scores are read from global
+// memory once and kept in shared memory for the later passes (when they fit,
+// T <= 36,864); every bucket search is a block-wide scan with one to four
+// buckets per thread.  Only native 32-bit shared atomics are used: a 64-bit
+// bucket mass is a (hi, lo) word pair, lo's carry folded into hi.
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -32,215 +33,319 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kBuckets = 4096;
-constexpr int kPasses = 3;
-
-// A valid score is a non-negative float, so its sign bit is zero and its
-// 31-bit pattern orders like its value.  Three radix digits, most significant
-// first: bits 30..19 (exponent and top mantissa bits), 18..9, 8..0.
-__device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 19 : pass == 1 ? 9 : 0; }
-__device__ __forceinline__ int digit_bits(int pass) { return pass == 0 ? 12 : pass == 1 ? 10 : 9; }
-
-__device__ __forceinline__ int digit_of(uint32_t key, int pass) {
-    return (int)((key >> digit_shift(pass)) & ((1u << digit_bits(pass)) - 1u));
-}
-
-// Does key lie inside the bucket chosen by the earlier passes?
-__device__ __forceinline__ bool in_prefix(uint32_t key, int pass, uint32_t prefix) {
-    return pass == 0 || (key >> digit_shift(pass - 1)) == prefix;
-}
-
-// floor(c * 2^56) for a float 0 <= c <= 1, from its bits with integer
-// operations only (exact): c = m * 2^(e-150) with the 24-bit significand m,
-// so c * 2^56 = m * 2^(e-94).
-__device__ __forceinline__ unsigned long long fixed56(uint32_t key) {
-    const int e = (int)(key >> 23);
-    if (e == 0) return 0;   // zero and subnormals: below 2^-126
-    const unsigned long long m = (key & 0x7FFFFFu) | 0x800000u;
-    const int sh = e - 94;
-    if (sh >= 0) return m << sh;   // sh <= 33 for c <= 1
-    if (sh <= -24) return 0;
-    return m >> (-sh);
-}
-
-// Called by all 32 lanes of one warp.  Walks the nb buckets from the largest
-// digit down and finds the first one at which the running total (base plus
-// everything above) reaches the target, as decided by reach(total).  Lane L
-// owns the buckets [nb-(L+1)per, nb-L*per); the lanes scan their range sums
-// and the first lane whose range reaches walks its own buckets.  That lane
-// stores the bucket, the total strictly above it and the count strictly above
-// it to *chosen, *above, *cabove (shared memory).
-template <typename V, typename VA, typename Reach>
-__device__ __forceinline__ void find_bucket(const VA *val, const uint32_t *cnt, int nb, V base,
-                                            long long cbase, Reach reach, int *chosen, V *above,
-                                            long long *cabove) {
-    const int lane = threadIdx.x & 31;
-    const int per = nb / 32;
-    const int lo = nb - (lane + 1) * per;
-    V ls = 0;
-    long long lc = 0;
-    for (int k = 0; k < per; ++k) {   // staggered order: no bank conflicts
-        const int d = lo + ((k + lane) & (per - 1));
-        ls += (V)val[d];
-        lc += cnt[d];
-    }
-    V incl = ls;
-    long long incl_c = lc;
+// ------------------------------------------------------------------ scans
+// Block-wide exclusive scan of one value per thread (1024 threads); *total
+// receives the block sum.  warp_tot must hold 32 values.
+template <typename V>
+__device__ __forceinline__ V block_scan_excl(V v, V *warp_tot, V *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    V incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const V a = __shfl_up_sync(0xffffffffu, incl, o);
-        const long long b = __shfl_up_sync(0xffffffffu, incl_c, o);
-        if (lane >= o) {
-            incl += a;
-            incl_c += b;
+        if (lane >= o) incl += a;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const V w = warp_tot[lane];
+        V wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const V a = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += a;
+        }
+        warp_tot[lane] = wi - w;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const V r = warp_tot[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// Block sum; total must point to shared memory (the scan's last lane writes
+// it, every thread reads it after the scan's barriers).
+template <typename V>
+__device__ __forceinline__ V block_sum(V v, V *warp_tot, V *total) {
+    (void)block_scan_excl(v, warp_tot, total);
+    return *total;
+}
+
+// floor(c * 2^56) for 0 <= c <= 1: the product is exact in fp32 (a power of
+// two, subnormal inputs flush to 0 like their fixed-point value) and the
+// truncating conversion is the floor.
+__device__ __forceinline__ unsigned long long fixed56f(float c) {
+    return __float2ull_rz(c * 0x1p56f);
+}
+
+// Copy n floats of one head from global to shared memory with many loads in
+// flight per thread (16-byte vectors when the row is 16-byte aligned), so
+// the later passes never wait on global-memory latency.
+__device__ __forceinline__ void stage_scores(const float *__restrict__ g, float *sm, int n) {
+    const int tid = threadIdx.x;
+    if ((reinterpret_cast<uintptr_t>(g) & 15) == 0) {
+        const int n4 = n >> 2;
+        const float4 *g4 = reinterpret_cast<const float4 *>(g);
+        float4 *s4 = reinterpret_cast<float4 *>(sm);
+        for (int base = 0; base < n4; base += 8 * kSelThreads) {
+            float4 r[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = base + i * kSelThreads + tid;
+                if (k < n4) r[i] = g4[k];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = base + i * kSelThreads + tid;
+                if (k < n4) s4[k] = r[i];
+            }
+        }
+        for (int j = (n4 << 2) + tid; j < n; j += kSelThreads) sm[j] = g[j];
+    } else {
+        for (int base = 0; base < n; base += 8 * kSelThreads) {
+            float r[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = base + i * kSelThreads + tid;
+                if (k < n) r[i] = g[k];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = base + i * kSelThreads + tid;
+                if (k < n) sm[k] = r[i];
+            }
         }
     }
-    const unsigned mask = __ballot_sync(0xffffffffu, reach(base + incl));
-    const int finder = mask ? __ffs(mask) - 1 : 31;   // no lane: corrupt input
-    if (lane == finder) {
-        V run = base + incl - ls;
-        long long runc = cbase + incl_c - lc;
-        int pick = lo;
-        for (int d = lo + per - 1; d >= lo; --d) {
-            if (reach(run + (V)val[d])) {
-                pick = d;
-                break;
-            }
-            run += (V)val[d];
-            runc += cnt[d];
+}
+
+// Visit scores 0..n-1 of one head: thread tid gets k = base + i*1024 + tid,
+// eight loads issued before any is used (latency hidden when the scores come
+// from global memory).  f(k, v, in) is called for every lane, with in false
+// past the end, so warp-wide votes inside f stay uniform.
+template <typename F>
+__device__ __forceinline__ void for_scores(const float *__restrict__ src, int n, F f) {
+    const int tid = threadIdx.x;
+    for (int base = 0; base < n; base += 8 * kSelThreads) {
+        float r[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = base + i * kSelThreads + tid;
+            r[i] = k < n ? src[k] : 0.f;
         }
-        *chosen = pick;
-        *above = run;
-        *cabove = runc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = base + i * kSelThreads + tid;
+            f(k, r[i], k < n);
+        }
     }
 }
 
 // ------------------------------------------------------------------ MBA
-struct MbaSmem {
-    uint32_t cnt[kBuckets];
-    uint32_t lo[kBuckets];
-    uint32_t hi[kBuckets];
-    unsigned long long msum[kBuckets];
-};
+// Per head (one 1024-thread block): the scores are read once from global
+// memory into shared memory (when they fit), then
+//  1. a 4096-bucket histogram of the top 12 key bits with counts and
+//     truncated 32-bit masses (native shared atomics; the lanes of a warp
+//     that share a bucket add as one group), and the exact total
+//     U = sum u_j in per-thread 64-bit sums;
+//  2. the truncated masses point to the bucket d1 where the running mass
+//     from the top reaches num/den of the total; one exact pass (64-bit per-thread
+//     sums) checks it -- den * A < num * U <= den * (A + M_d1), A the exact
+//     mass above d1 -- and steps to the neighbouring non-empty bucket in the
+//     rare case rounding picked the wrong one;
+//  3. two exact radix passes (10 and 9 bits, 64-bit masses as (hi, lo) word
+//     pairs) inside that bucket find the crossing value v*;
+// each bucket search is a block-wide scan, one bucket per thread.  The count
+// then follows in closed form from the exact mass above v*.
+constexpr int kCacheFloats = 36864;   // scores per head kept in shared memory (144 KiB)
+constexpr int kB0 = 4096;
 
-__device__ __forceinline__ void add_mass(MbaSmem &sm, int d, unsigned long long x) {
-    const uint32_t lo = (uint32_t)x;
-    const uint32_t old = atomicAdd(&sm.lo[d], lo);
-    atomicAdd(&sm.hi[d], (uint32_t)(x >> 32) + (old + lo < old ? 1u : 0u));
+__device__ __forceinline__ void add_mass64(uint32_t *lo, uint32_t *hi, int d, unsigned long long x) {
+    const uint32_t l = (uint32_t)x;
+    const uint32_t old = atomicAdd(&lo[d], l);
+    atomicAdd(&hi[d], (uint32_t)(x >> 32) + (old + l < old ? 1u : 0u));
 }
 
 __global__ void __launch_bounds__(kSelThreads)
-    mba_kernel(const float *__restrict__ scores, int T, uint32_t num, uint32_t den,
+    mba_kernel(const float *__restrict__ scores, int T, uint32_t num, uint32_t den, int cached,
                int32_t *__restrict__ mba, uint32_t *status) {
     extern __shared__ __align__(16) uint8_t sel_smem[];
-    MbaSmem &sm = *reinterpret_cast<MbaSmem *>(sel_smem);
-    __shared__ unsigned long long s_total, s_sum_gt;
-    __shared__ long long s_cnt_gt;
-    __shared__ uint32_t s_prefix;
-    __shared__ int s_bad, s_done, s_chosen;
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(sel_smem);   // [4096]
+    uint32_t *fm = cnt + kB0;                                   // [4096] floor(c * 2^27) sums
+    uint32_t *lo = fm + kB0;                                    // [1024]
+    uint32_t *hi = lo + 1024;                                   // [1024]
+    float *cache = reinterpret_cast<float *>(hi + 1024);        // [T] when cached
+    __shared__ unsigned long long wt64[32], s_tot64;
+    __shared__ uint32_t wt32[32], s_tot32;
+    __shared__ int s_d, s_step;
+    __shared__ unsigned long long s_add;
+    __shared__ long long s_cadd;
+    const int tid = threadIdx.x;
     const float *c = scores + (int64_t)blockIdx.x * T;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    if (tid == 0) {
-        s_sum_gt = 0;
-        s_cnt_gt = 0;
-        s_prefix = 0;
-        s_bad = 0;
-        s_done = 0;
+    const float *src = cached ? cache : c;
+
+    // 1. histogram, exact total
+    for (int i = tid; i < kB0; i += kSelThreads) {
+        cnt[i] = 0;
+        fm[i] = 0u;
     }
-    for (int pass = 0; pass < kPasses; ++pass) {
-        const int nb = 1 << digit_bits(pass);
-        for (int i = tid; i < nb; i += kSelThreads) {
-            sm.cnt[i] = 0;
-            sm.lo[i] = 0;
-            sm.hi[i] = 0;
+    if (cached) stage_scores(c, cache, T);
+    __syncthreads();
+    unsigned long long my_u = 0;
+    int bad = 0;
+    const int lane = tid & 31;
+    for_scores(src, T, [&](int j, float v, bool in) {
+        const bool valid = in && v >= 0.f && v <= 1.f;
+        if (in && !valid) bad = 1;
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        if (vmask == 0) return;
+        const int d = (int)(__float_as_uint(v) >> 19);
+        const uint32_t f = valid ? (uint32_t)(v * 0x1p27f) : 0u;   // guide mass, truncated
+        if (valid) my_u += fixed56f(v);
+        // lanes sharing the first valid lane's bucket add as one group
+        const int leader = __ffs(vmask) - 1;
+        const int dl = __shfl_sync(0xffffffffu, d, leader);
+        const bool same = valid && d == dl;
+        const unsigned smask = __ballot_sync(0xffffffffu, same);
+        const uint32_t fs = __reduce_add_sync(0xffffffffu, same ? f : 0u);
+        if (lane == leader) {
+            atomicAdd(&cnt[dl], (uint32_t)__popc(smask));
+            atomicAdd(&fm[dl], fs);
         }
-        __syncthreads();
-        const uint32_t prefix = s_prefix;
-        const int lane = tid & 31;
-        for (int base = 0; base < T; base += kSelThreads) {   // uniform trip count
-            const int j = base + tid;
-            const float v = j < T ? c[j] : 0.f;
-            const uint32_t key = __float_as_uint(v);
-            if (pass == 0 && j < T && !(v >= 0.f && v <= 1.f)) s_bad = 1;
-            const bool valid = j < T && key <= 0x3F800000u && in_prefix(key, pass, prefix);
-            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-            if (vmask == 0) continue;
-            // peel the first valid lane's digit: its lanes add as one group
-            const int d = digit_of(key, pass);
-            const int leader = __ffs(vmask) - 1;
-            const int dl = __shfl_sync(0xffffffffu, d, leader);
-            const bool same = valid && d == dl;
-            const unsigned smask = __ballot_sync(0xffffffffu, same);
-            const unsigned long long u = valid ? fixed56(key) : 0ull;
-            const unsigned long long us = same ? u : 0ull;
-            const unsigned s0 = __reduce_add_sync(0xffffffffu, (unsigned)(us & 0x7FFFu));
-            const unsigned s1 = __reduce_add_sync(0xffffffffu, (unsigned)((us >> 15) & 0x7FFFu));
-            const unsigned s2 = __reduce_add_sync(0xffffffffu, (unsigned)((us >> 30) & 0x7FFFu));
-            const unsigned s3 = __reduce_add_sync(0xffffffffu, (unsigned)(us >> 45));
-            if (lane == leader) {
-                atomicAdd(&sm.cnt[dl], (uint32_t)__popc(smask));
-                add_mass(sm, dl, (unsigned long long)s0 + ((unsigned long long)s1 << 15) +
-                                     ((unsigned long long)s2 << 30) + ((unsigned long long)s3 << 45));
-            }
-            if (valid && !same) {
-                atomicAdd(&sm.cnt[d], 1u);
-                add_mass(sm, d, u);
-            }
+        if (valid && !same) {
+            atomicAdd(&cnt[d], 1u);
+            atomicAdd(&fm[d], f);
         }
-        __syncthreads();
-        for (int d = tid; d < nb; d += kSelThreads)
-            sm.msum[d] = ((unsigned long long)sm.hi[d] << 32) + sm.lo[d];
-        __syncthreads();
-        if (warp == 0) {
-            if (pass == 0) {
-                unsigned long long tot = 0;
-                for (int d = tid; d < nb; d += 32) tot += sm.msum[d];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-                if (tid == 0) {
-                    s_total = tot;
-                    // a head whose scores sum above 16 (or hold invalid values)
-                    // would overflow the exact comparisons below
-                    if (s_bad || tot > (1ull << 60)) s_bad = 1;
-                    if (s_bad || (unsigned __int128)num * tot == 0) s_done = 1;
-                }
-                __syncwarp();
-            }
-            if (!s_done) {
-                const unsigned __int128 need = (unsigned __int128)num * s_total;
-                find_bucket<unsigned long long>(
-                    sm.msum, sm.cnt, nb, s_sum_gt, s_cnt_gt,
-                    [&](unsigned long long x) { return (unsigned __int128)den * x >= need; },
-                    &s_chosen, &s_sum_gt, &s_cnt_gt);
-                __syncwarp();
-                if (tid == 0) s_prefix = (prefix << digit_bits(pass)) | (uint32_t)s_chosen;
-            }
-        }
-        __syncthreads();
-        if (s_done) break;
-    }
-    if (tid == 0) {
-        if (s_bad) {
+    });
+    bad = __syncthreads_or(bad);
+    const unsigned long long U = block_sum(my_u, wt64, &s_tot64);
+    if (bad || U > (1ull << 60)) {   // invalid scores, or a head summing above 16
+        if (tid == 0) {
             set_status(status, KVC_DEV_BAD_SCORE);
             mba[blockIdx.x] = 0;
-        } else if (s_done) {
-            mba[blockIdx.x] = 0;
-        } else {
-            // s_prefix is now the exact crossing value v*; every element above
-            // it is counted in s_cnt_gt / s_sum_gt; ties at v* each carry u*.
-            const unsigned long long ustar = fixed56(s_prefix);
-            const unsigned __int128 need = (unsigned __int128)num * s_total;
-            const unsigned __int128 have = (unsigned __int128)den * s_sum_gt;
-            const unsigned __int128 step = (unsigned __int128)den * ustar;
-            if (step == 0 || have >= need) {
-                // unreachable for valid scores (the crossing bucket always
-                // carries mass); never divide by zero on corrupt input
-                set_status(status, KVC_DEV_BAD_SCORE);
-                mba[blockIdx.x] = (int32_t)s_cnt_gt;
-            } else {
-                const long long k = (long long)((need - have + step - 1) / step);
-                mba[blockIdx.x] = (int32_t)(s_cnt_gt + k);
+        }
+        return;
+    }
+    if (U == 0 || num == 0) {
+        if (tid == 0) mba[blockIdx.x] = 0;
+        return;
+    }
+    const unsigned __int128 need = (unsigned __int128)num * U;
+
+    // 2. guide from the truncated masses (floor(c 2^27) per element, at most
+    // T units below the exact mass): thread t holds buckets 4095-4t ..
+    // 4092-4t (descending)
+    uint32_t f4[4], fl = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f4[i] = fm[kB0 - 1 - 4 * tid - i];
+        fl += f4[i];
+    }
+    const uint32_t fpre = block_scan_excl(fl, wt32, &s_tot32);
+    const unsigned long long target = ((unsigned long long)s_tot32 * num + den - 1) / den;
+    if (tid == 0) s_d = -1;
+    __syncthreads();
+    {
+        unsigned long long run = fpre;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (f4[i] > 0 && run < target && run + f4[i] >= target)
+                atomicMax(&s_d, kB0 - 1 - 4 * tid - i);
+            run += f4[i];
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && s_d < 0) {   // rounding left the target unreached: lowest non-empty bucket
+        int d = 0;
+        while (d < kB0 - 1 && cnt[d] == 0) ++d;
+        s_d = d;
+    }
+    __syncthreads();
+    // exact check of the bucket, moving one non-empty bucket at a time
+    unsigned long long A = 0;
+    long long C = 0;
+    for (int iter = 0; iter < kB0; ++iter) {
+        const int d1 = s_d;
+        unsigned long long a = 0, m = 0;
+        uint32_t cg = 0;
+        for_scores(src, T, [&](int, float v, bool in) {
+            const int d = (int)(__float_as_uint(v) >> 19);
+            const unsigned long long u = in ? fixed56f(v) : 0ull;
+            if (d > d1) {
+                a += u;
+                cg += in;
+            } else if (d == d1) {
+                m += u;
             }
+        });
+        A = block_sum(a, wt64, &s_tot64);
+        const unsigned long long M = block_sum(m, wt64, &s_tot64);
+        C = (long long)block_sum(cg, wt32, &s_tot32);
+        if (tid == 0) {
+            s_step = 0;
+            if ((unsigned __int128)den * A >= need) {
+                int d = d1 + 1;
+                while (d < kB0 - 1 && cnt[d] == 0) ++d;
+                s_d = d;
+                s_step = 1;
+            } else if ((unsigned __int128)den * (A + M) < need) {
+                int d = d1 - 1;
+                while (d > 0 && cnt[d] == 0) --d;
+                s_d = d;
+                s_step = 1;
+            }
+        }
+        __syncthreads();
+        if (!s_step) break;
+    }
+    // 3. exact radix passes inside the bucket
+    uint32_t prefix = (uint32_t)s_d;
+    for (int pass = 1; pass < 3; ++pass) {
+        const int bits = pass == 1 ? 10 : 9, shift = pass == 1 ? 9 : 0, nb = 1 << bits;
+        for (int i = tid; i < nb; i += kSelThreads) {
+            cnt[i] = 0;
+            lo[i] = 0;
+            hi[i] = 0;
+        }
+        __syncthreads();
+        for_scores(src, T, [&](int, float v, bool in) {
+            const uint32_t key = __float_as_uint(v);
+            if (!in || (key >> (shift + bits)) != prefix) return;
+            const int dd = (int)((key >> shift) & (uint32_t)(nb - 1));
+            atomicAdd(&cnt[dd], 1u);
+            add_mass64(lo, hi, dd, fixed56f(v));
+        });
+        __syncthreads();
+        // thread t holds bucket nb-1-t (descending); threads past nb hold 0
+        const int b = nb - 1 - tid;
+        const unsigned long long mb = b >= 0 ? ((unsigned long long)hi[b] << 32) | lo[b] : 0ull;
+        const uint32_t cb = b >= 0 ? cnt[b] : 0u;
+        const unsigned long long mpre = block_scan_excl(mb, wt64, &s_tot64);
+        const uint32_t cpre = block_scan_excl(cb, wt32, &s_tot32);
+        if (mb > 0 && (unsigned __int128)den * (A + mpre) < need &&
+            (unsigned __int128)den * (A + mpre + mb) >= need) {
+            s_d = b;
+            s_add = mpre;
+            s_cadd = cpre;
+        }
+        __syncthreads();
+        A += s_add;
+        C += s_cadd;
+        prefix = (prefix << bits) | (uint32_t)s_d;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        // prefix is the crossing value v*; the elements above it carry A and
+        // number C; each tie at v* adds u*
+        const unsigned long long ustar = fixed56f(__uint_as_float(prefix));
+        const unsigned __int128 have = (unsigned __int128)den * A;
+        const unsigned __int128 step = (unsigned __int128)den * ustar;
+        if (step == 0 || have >= need) {
+            set_status(status, KVC_DEV_BAD_SCORE);   // unreachable for valid scores
+            mba[blockIdx.x] = (int32_t)C;
+        } else {
+            const long long k = (long long)((need - have + step - 1) / step);
+            mba[blockIdx.x] = (int32_t)(C + k);
         }
     }
 }
@@ -415,18 +520,20 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
 
 __global__ void __launch_bounds__(kSelThreads)
     topk_kernel(const float *__restrict__ scores, int T, int P, int Hkv,
-                const int32_t *__restrict__ budget, int per_head, int k_max,
+                const int32_t *__restrict__ budget, int per_head, int k_max, int cached,
                 int32_t *__restrict__ idx, uint32_t *status) {
-    __shared__ uint32_t cnt[kBuckets];
+    extern __shared__ __align__(16) uint8_t sel_smem[];
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(sel_smem);   // [4096]
+    float *cache = reinterpret_cast<float *>(cnt + kB0);        // [P] when cached
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t s_total;
-    __shared__ uint32_t s_prefix;
-    __shared__ long long s_cnt_gt, s_dummy;
-    __shared__ int s_bad, s_chosen;
+    __shared__ int s_d;
+    __shared__ uint32_t s_cadd;
     const int head = blockIdx.x;
     const int l = head / Hkv;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const float *c = scores + (int64_t)head * T;
+    const float *src = cached ? cache : c;
     int32_t *out = idx + (int64_t)head * k_max;
     long long B = per_head ? budget[head] : budget[l];
     if (B < 0) {
@@ -443,50 +550,71 @@ __global__ void __launch_bounds__(kSelThreads)
         for (int j = tid; j < P; j += kSelThreads) out[j] = j;
         return;
     }
-    if (tid == 0) {
-        s_prefix = 0;
-        s_cnt_gt = 0;
-        s_bad = 0;
+    // radix select of the B-th largest key: 12 bits (4096 buckets), then 10
+    // and 9 bits inside the chosen bucket; each bucket search is a block-wide
+    // scan, one or four buckets per thread
+    for (int i = tid; i < kB0; i += kSelThreads) cnt[i] = 0;
+    if (cached) stage_scores(c, cache, P);
+    __syncthreads();
+    int bad = 0;
+    for_scores(src, P, [&](int, float v, bool in) {
+        if (!in) return;
+        if (!(v >= 0.f)) bad = 1;
+        atomicAdd(&cnt[(__float_as_uint(v) >> 19) & (kB0 - 1)], 1u);
+    });
+    bad = __syncthreads_or(bad);
+    if (tid == 0 && bad) set_status(status, KVC_DEV_BAD_SCORE);
+    long long C = 0;   // elements strictly above the current bucket
+    {
+        uint32_t c4[4], cl = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c4[i] = cnt[kB0 - 1 - 4 * tid - i];
+            cl += c4[i];
+        }
+        uint32_t run = block_scan_excl(cl, warp_tot, &s_total);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (c4[i] > 0 && run < B && run + c4[i] >= B) {
+                s_d = kB0 - 1 - 4 * tid - i;
+                s_cadd = run;
+            }
+            run += c4[i];
+        }
+        __syncthreads();
+        C = s_cadd;
     }
-    for (int pass = 0; pass < kPasses; ++pass) {
-        const int nb = 1 << digit_bits(pass);
+    uint32_t prefix = (uint32_t)s_d;
+    for (int pass = 1; pass < 3; ++pass) {
+        const int bits = pass == 1 ? 10 : 9, shift = pass == 1 ? 9 : 0, nb = 1 << bits;
+        __syncthreads();
         for (int i = tid; i < nb; i += kSelThreads) cnt[i] = 0;
         __syncthreads();
-        const uint32_t prefix = s_prefix;
-        const int lane = tid & 31;
-        for (int base = 0; base < P; base += kSelThreads) {
-            const int j = base + tid;
-            const float v = j < P ? c[j] : 0.f;
+        for_scores(src, P, [&](int, float v, bool in) {
             const uint32_t key = __float_as_uint(v);
-            if (pass == 0 && j < P && !(v >= 0.f)) s_bad = 1;
-            const bool valid = j < P && in_prefix(key, pass, prefix);
-            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-            if (vmask == 0) continue;
-            const int d = digit_of(key, pass);
-            const int leader = __ffs(vmask) - 1;
-            const int dl = __shfl_sync(0xffffffffu, d, leader);
-            const bool same = valid && d == dl;
-            const unsigned smask = __ballot_sync(0xffffffffu, same);
-            if (lane == leader) atomicAdd(&cnt[dl], (uint32_t)__popc(smask));
-            if (valid && !same) atomicAdd(&cnt[d], 1u);
+            if (in && (key >> (shift + bits)) == prefix)
+                atomicAdd(&cnt[(key >> shift) & (uint32_t)(nb - 1)], 1u);
+        });
+        __syncthreads();
+        const int b = nb - 1 - tid;
+        const uint32_t cb = b >= 0 ? cnt[b] : 0u;
+        const uint32_t cpre = block_scan_excl(cb, warp_tot, &s_total);
+        if (cb > 0 && C + cpre < B && C + cpre + cb >= B) {
+            s_d = b;
+            s_cadd = cpre;
         }
         __syncthreads();
-        if (warp == 0) {
-            // counts stand in for the values: walk until B elements are reached
-            find_bucket<long long>(
-                cnt, cnt, nb, s_cnt_gt, 0, [&](long long x) { return x >= B; }, &s_chosen,
-                &s_cnt_gt, &s_dummy);
-            __syncwarp();
-            if (tid == 0) s_prefix = (prefix << digit_bits(pass)) | (uint32_t)s_chosen;
-        }
-        __syncthreads();
+        C += s_cadd;
+        prefix = (prefix << bits) | (uint32_t)s_d;
     }
-    if (tid == 0 && s_bad) set_status(status, KVC_DEV_BAD_SCORE);
-    const uint32_t vstar = s_prefix;
-    const long long need_eq = B - s_cnt_gt;   // >= 1
+    const uint32_t vstar = prefix;
+    const long long need_eq = B - C;   // >= 1
     // Ordered compaction: position of a kept j is G(j) + min(E(j), need_eq)
     // with G/E the numbers of elements above / equal to v* before j.
     long long g_before = 0, e_before = 0;
+    uint32_t nxt[4];   // next chunk's keys, loaded before this chunk's scan
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nxt[i] = 4 * tid + i < P ? __float_as_uint(src[4 * tid + i]) : 0u;
     for (int base = 0; base < P; base += 4 * kSelThreads) {
         const int j0 = base + 4 * tid;
         uint32_t gt[4], eq[4];
@@ -494,11 +622,16 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int j = j0 + i;
-            const uint32_t key = j < P ? __float_as_uint(c[j]) : 0u;
+            const uint32_t key = nxt[i];
             gt[i] = (j < P) && key > vstar;
             eq[i] = (j < P) && key == vstar;
             ng += gt[i];
             ne += eq[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int jn = j0 + 4 * kSelThreads + i;
+            nxt[i] = jn < P ? __float_as_uint(src[jn]) : 0u;
         }
         const uint32_t packed = block_excl_scan(ng | (ne << 16), warp_tot, &s_total);
         long long G = g_before + (packed & 0xFFFFu);
@@ -593,13 +726,15 @@ int launch_threshold(const kvc_shape &s, const float *scores, float tau, int32_t
 int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
                uint32_t *status, cudaStream_t st) {
     const int heads = s.n_layers * s.n_kv_heads;
+    const int cached = s.seq_len <= kCacheFloats;
+    const size_t smem = (size_t)(2 * kB0 + 2 * 1024) * 4 + (cached ? (size_t)s.seq_len * 4 : 0);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(mba_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(MbaSmem));
+                             (2 * kB0 + 2 * 1024 + kCacheFloats) * 4);
         attr = true;
     }
-    mba_kernel<<<heads, kSelThreads, sizeof(MbaSmem), st>>>(scores, s.seq_len, num, den, mba, status);
+    mba_kernel<<<heads, kSelThreads, smem, st>>>(scores, s.seq_len, num, den, cached, mba, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_mba_budget: MBA launch failed: %s", cudaGetErrorString(e));
@@ -628,8 +763,17 @@ int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t
 int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int per_head,
                 int32_t k_max, int32_t *idx, uint32_t *status, cudaStream_t st) {
     const int heads = s.n_layers * s.n_kv_heads;
-    topk_kernel<<<heads, kSelThreads, 0, st>>>(scores, s.seq_len, s.seq_len - s.window,
-                                                s.n_kv_heads, budget, per_head, k_max, idx, status);
+    const int P = s.seq_len - s.window;
+    const int cached = P <= kCacheFloats;
+    const size_t smem = (size_t)kB0 * 4 + (cached ? (size_t)P * 4 : 0);
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (kB0 + kCacheFloats) * 4);
+        attr = true;
+    }
+    topk_kernel<<<heads, kSelThreads, smem, st>>>(scores, s.seq_len, P, s.n_kv_heads, budget,
+                                                   per_head, k_max, cached, idx, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_topk_select: launch failed: %s", cudaGetErrorString(e));
