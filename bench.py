@@ -451,10 +451,13 @@ def run_kvc(args):
 
 
 def run_e2e(args, jobs, stream):
-    """Same metric through the public API with HOST buffers: every step copies
-    the prompt's Q_obs, K, V from pinned host memory, runs the path and reads
-    the compacted K/V, indices and budgets back."""
+    """Same metric through the public API with HOST buffers: every step runs
+    kvc_compress_host on the prompt's Q_obs, K, V in pinned host memory (Q
+    and K are copied, K layer by layer on a second stream while earlier layers
+    are scored; the kept V rows are read in place through the device mapping)
+    and reads the compacted K/V, indices and budgets back."""
     from eviction_kvc_score_gb300 import kvc
+    copy_stream = torch.cuda.Stream()
     host = []
     for wl, x, b, total, floor in jobs:
         hin = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v")}
@@ -465,15 +468,21 @@ def run_e2e(args, jobs, stream):
         if wl.think_lambda is not None:
             hout["k_pruned"] = torch.empty_like(b.k_pruned, device="cpu").pin_memory()
         host.append((hin, hout))
-    h2d = sum(t.numel() * t.element_size() for hin, _ in host for t in hin.values())
+    h2d = sum(hin[k].numel() * hin[k].element_size() for hin, _ in host for k in ("q", "k"))
     d2h = sum(t.numel() * t.element_size() for _, hout in host for t in hout.values())
 
     def e2e_step():
         for (wl, x, b, total, floor), (hin, hout) in zip(jobs, host):
-            for kname in ("q", "k", "v"):
-                x[kname].copy_(hin[kname], non_blocking=True)
-            kvc.compress(b, x["q"], x["k"], x["v"], total, floor, wl.mass_num, wl.mass_den,
-                         lam=wl.think_lambda, pool_kernel=args.pool, think=args.think_criterion)
+            kvc.kvc_compress_host(b.shape, hin["q"], hin["k"], hin["v"], x["q"], x["k"],
+                                  wl.mass_num, wl.mass_den, total, floor, b.k_max, b.scores, b.mba,
+                                  b.budget, b.idx, b.k_out, b.v_out, b.ws, stream, copy_stream)
+            if wl.think_lambda is not None:
+                if args.think_criterion == "query":
+                    kvc.kvc_channel_prune_query(b.shape, x["q"], b.k_out, b.budget,
+                                                wl.think_lambda, b.chan, b.k_pruned, b.ws, stream)
+                else:
+                    kvc.kvc_channel_prune(b.shape, b.k_out, b.budget, wl.think_lambda, b.chan,
+                                          b.k_pruned, b.ws, stream)
             hout["budget"].copy_(b.budget, non_blocking=True)
             hout["idx"].copy_(b.idx, non_blocking=True)
             hout["k_out"].copy_(b.k_out, non_blocking=True)
@@ -483,6 +492,15 @@ def run_e2e(args, jobs, stream):
 
     e2e_step()
     torch.cuda.synchronize()
+    for _, _, b, _, _ in jobs:
+        st = kvc.kvc_workspace_status(b.ws)
+        if st:
+            raise RuntimeError(f"device status {st:#x} in the end-to-end leg")
+    # the kept V rows cross the host link by reading, not by a copy
+    P_of = {id(wl): wl.seq_len - wl.window for wl, *_ in jobs}
+    v_read = sum(wl.n_kv_heads * sum(min(max(int(n), 0), P_of[id(wl)]) + wl.window
+                                     for n in b.budget.cpu().tolist())
+                 * wl.head_dim * wl.elt_size for wl, _, b, _, _ in jobs)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -493,7 +511,9 @@ def run_e2e(args, jobs, stream):
     ms = e0.elapsed_time(e1) / args.e2e_steps
     tokens = sum(wl.seq_len for wl, *_ in jobs)
     return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "v_rows_read_in_place_bytes_per_step": v_read, "steps": args.e2e_steps,
+            "api": "kvc_compress_host"}
 
 
 # ----------------------------------------------------------------- oracle arm

@@ -197,6 +197,92 @@ int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *s
     return tc ? launch_score_tc(s, sp, a, device_info().sms, stream) : launch_score_simt(s, sp, a, stream);
 }
 
+// Host-resident prompt, whole default path (see kvc.h).
+int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_host,
+                      const void *v_host, void *q_dev, void *k_dev, uint32_t mass_num,
+                      uint32_t mass_den, int64_t total_budget, int32_t layer_floor, int32_t k_max,
+                      float *scores, int32_t *mba, int32_t *budget, int32_t *idx, void *k_out,
+                      void *v_out, int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream,
+                      cudaStream_t copy_stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_compress_host")) return KVC_ERR_INVALID_ARG;
+    const kvc_shape &s = *shape;
+    if (!q_host || !k_host || !v_host || !q_dev || !k_dev || !scores || !mba || !budget || !idx ||
+        !k_out || !v_out)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: NULL pointer");
+    if (stream == copy_stream)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: copies need a stream of their own");
+    if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(k_out) || !aligned16(v_out))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: device buffers must be 16-byte aligned");
+    if (k_max < 1 || out_rows < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: bad k_max/out_rows");
+    const WsLayout w = ws_layout(s);
+    if (!ws_ok(ws, ws_bytes, w.total, "kvc_compress_host")) return KVC_ERR_WORKSPACE;
+    // V is never copied: the compaction reads the kept rows through the
+    // device's mapping of the (pinned) host buffer
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, v_host) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
+        pa.devicePointer == nullptr) {
+        cudaGetLastError();
+        return fail(KVC_ERR_INVALID_ARG,
+                    "kvc_compress_host: v_host must be pinned host memory mapped for the device");
+    }
+    const void *v_dev = pa.devicePointer;
+    if (!aligned16(v_dev)) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: v_host must be 16-byte aligned");
+    // one event per layer (plus one for Q), created once per device
+    constexpr int kMaxEv = 1026;
+    static cudaEvent_t events[16][kMaxEv];
+    static int n_events[16] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 16 || s.n_layers + 2 > kMaxEv)
+        return fail(KVC_ERR_UNSUPPORTED, "kvc_compress_host: at most 1024 layers on devices 0..15");
+    while (n_events[dev] < s.n_layers + 2) {
+        if (cudaEventCreateWithFlags(&events[dev][n_events[dev]], cudaEventDisableTiming) != cudaSuccess)
+            return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
+        ++n_events[dev];
+    }
+    const size_t es = s.dtype == KVC_F32 ? 4 : 2;
+    const size_t q_layer = (size_t)s.n_q_heads * s.window * s.head_dim * es;
+    const size_t k_layer = (size_t)s.n_kv_heads * s.seq_len * s.head_dim * es;
+    // 0. the staging buffers may still be read by work already on `stream`
+    // (a previous call's compaction): the copies start after it
+    cudaEvent_t ev_prev = events[dev][s.n_layers + 1];
+    cudaError_t e = cudaEventRecord(ev_prev, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(copy_stream, ev_prev, 0);
+    // 1. the copy stream moves Q, then K layer by layer, marking each layer
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(q_dev, q_host, q_layer * s.n_layers, cudaMemcpyHostToDevice,
+                            copy_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(events[dev][0], copy_stream);
+    for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
+        e = cudaMemcpyAsync(static_cast<char *>(k_dev) + l * k_layer,
+                            static_cast<const char *>(k_host) + l * k_layer, k_layer,
+                            cudaMemcpyHostToDevice, copy_stream);
+        if (e == cudaSuccess) e = cudaEventRecord(events[dev][l + 1], copy_stream);
+    }
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_compress_host: copy: %s", cudaGetErrorString(e));
+    // 2. each layer is scored as soon as its keys have landed
+    kvc_shape s1 = s;
+    s1.n_layers = 1;
+    e = cudaStreamWaitEvent(stream, events[dev][0], 0);
+    for (int l = 0; l < s.n_layers; ++l) {
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, events[dev][l + 1], 0);
+        if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_compress_host: %s", cudaGetErrorString(e));
+        const int rc = kvc_score(&s1, static_cast<const char *>(q_dev) + l * q_layer,
+                                 static_cast<const char *>(k_dev) + l * k_layer,
+                                 scores + (size_t)l * s.n_kv_heads * s.seq_len, ws, ws_bytes, stream);
+        if (rc) return rc;
+    }
+    // 3. budgets, selection and compaction over all layers
+    int rc = kvc_mba_budget(&s, scores, mass_num, mass_den, total_budget, layer_floor, mba, budget,
+                            ws, ws_bytes, stream);
+    if (rc) return rc;
+    rc = kvc_topk_select(&s, scores, budget, k_max, idx, ws, ws_bytes, stream);
+    if (rc) return rc;
+    return kvc_compact(&s, k_dev, v_dev, idx, budget, k_max, k_out, v_out, out_rows, ws, ws_bytes,
+                       stream);
+}
+
 int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,
                         double tau, float *scores, void *ws, size_t ws_bytes, cudaStream_t stream) {
     g_err[0] = 0;

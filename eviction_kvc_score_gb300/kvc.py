@@ -53,6 +53,8 @@ _SIGS = {
     "kvc_score": (C.c_int, [_sp, _p, _p, _p, _p, _sz, _p]),
     "kvc_score_noalloc": (C.c_int, [_sp, _p, _p, _p, _p, _p]),
     "kvc_score_keyformer": (C.c_int, [_sp, _p, _p, C.c_uint64, _d, _p, _p, _sz, _p]),
+    "kvc_compress_host": (C.c_int, [_sp, _p, _p, _p, _p, _p, _u32, _u32, _i64, _i32, _i32, _p, _p, _p,
+                                    _p, _p, _p, _i64, _p, _sz, _p, _p]),
     "kvc_mba_budget": (C.c_int, [_sp, _p, _u32, _u32, _i64, _i32, _p, _p, _p, _sz, _p]),
     "kvc_topk_select": (C.c_int, [_sp, _p, _p, _i32, _p, _p, _sz, _p]),
     "kvc_pool_scores": (C.c_int, [_sp, _p, _i32, _i32, _p, _p, _sz, _p]),
@@ -139,6 +141,27 @@ def kvc_score_noalloc(s: KvcShape, q_obs, k, scores, dev_status=None, stream=Non
     stream."""
     _check("kvc_score_noalloc", _lib.kvc_score_noalloc(
         C.byref(s), _ptr(q_obs), _ptr(k), _ptr(scores), _ptr(dev_status), _stream(stream)))
+
+
+def _hptr(t: torch.Tensor):
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("kvc_compress_host takes pinned host tensors for q/k/v")
+    return C.c_void_p(t.data_ptr())
+
+
+def kvc_compress_host(s: KvcShape, q_host, k_host, v_host, q_dev, k_dev, mass_num: int,
+                      mass_den: int, total_budget: int, layer_floor: int, k_max: int, scores, mba,
+                      budget, idx, k_out, v_out, ws, stream=None, copy_stream=None) -> None:
+    """Whole default path from pinned host Q/K/V: K copied layer by layer on
+    copy_stream while earlier layers are scored on stream; V rows read in
+    place through the device mapping."""
+    if copy_stream is None:
+        raise ValueError("kvc_compress_host needs a copy stream")
+    _check("kvc_compress_host", _lib.kvc_compress_host(
+        C.byref(s), _hptr(q_host), _hptr(k_host), _hptr(v_host), _ptr(q_dev), _ptr(k_dev),
+        int(mass_num), int(mass_den), int(total_budget), int(layer_floor), int(k_max),
+        _ptr(scores), _ptr(mba), _ptr(budget), _ptr(idx), _ptr(k_out), _ptr(v_out),
+        k_out.shape[0], _ptr(ws), ws.numel(), _stream(stream), _stream(copy_stream)))
 
 
 def kvc_score_keyformer(s: KvcShape, q_obs, k, seed: int, tau: float, scores, ws,

@@ -161,6 +161,28 @@ int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, const void *k, 
 int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,
                         double tau, float *scores, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The default path (kvc_score -> kvc_mba_budget -> kvc_topk_select ->
+ * kvc_compact) for a prompt whose Q_obs, K and V live in HOST memory, the
+ * pages have no counterpart (it is how the path is fed from a host).  The
+ * copy of K is pipelined against the scoring: copy_stream moves Q_obs, then
+ * K one layer at a time into the caller's device staging buffers q_dev / k_dev
+ * (layouts as for kvc_score), and every layer is scored on `stream` as soon
+ * as its keys have landed; V is never copied -- kvc_compact reads only the
+ * kept rows through the device's mapping of v_host.  q_host and k_host must
+ * be pinned (page-locked) for the copies to be asynchronous; v_host must be
+ * pinned and mapped for the device (cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped), else KVC_ERR_INVALID_ARG.  copy_stream must differ
+ * from stream.  Outputs, capacities and the workspace are those of the four
+ * calls it makes (see them); the call is asynchronous on both streams, and
+ * the host buffers must stay valid until `stream` has finished.  At most 1024
+ * layers; one event per layer is created once per device and kept. */
+int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_host,
+                      const void *v_host, void *q_dev, void *k_dev, uint32_t mass_num,
+                      uint32_t mass_den, int64_t total_budget, int32_t layer_floor, int32_t k_max,
+                      float *scores, int32_t *mba, int32_t *budget, int32_t *idx, void *k_out,
+                      void *v_out, int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream,
+                      cudaStream_t copy_stream);
+
 /* a2 + a3 -- ZigZagKV budgets.
  * mba[l][k] = smallest m with mass_den * (sum of the m largest u) >=
  *             mass_num * (sum of all u), u_j = floor(scores[l][k][j] * 2^56),
