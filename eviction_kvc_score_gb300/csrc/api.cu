@@ -246,9 +246,17 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     const size_t k_layer = (size_t)s.n_kv_heads * s.seq_len * s.head_dim * es;
     // 0. the staging buffers may still be read by work already on `stream`
     // (a previous call's compaction): the copies start after it
-    cudaEvent_t ev_prev = events[dev][s.n_layers + 1];
-    cudaError_t e = cudaEventRecord(ev_prev, stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(copy_stream, ev_prev, 0);
+    // ev_done marks the end of the previous call's last read of the staging
+    // buffers (its compaction); this call's copies start after it -- and only
+    // after it, so whatever the caller enqueued since (reading the outputs
+    // back) overlaps with the next prompt's copies.  Waiting on an event that
+    // was never recorded returns at once.
+    cudaEvent_t ev_done = events[dev][s.n_layers + 1];
+    static cudaEvent_t last_done[16] = {};
+    if (!last_done[dev] && cudaEventCreateWithFlags(&last_done[dev], cudaEventDisableTiming) != cudaSuccess)
+        return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
+    (void)ev_done;
+    cudaError_t e = cudaStreamWaitEvent(copy_stream, last_done[dev], 0);
     // 1. the copy stream moves Q, then K layer by layer, marking each layer
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(q_dev, q_host, q_layer * s.n_layers, cudaMemcpyHostToDevice,
@@ -279,8 +287,12 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     if (rc) return rc;
     rc = kvc_topk_select(&s, scores, budget, k_max, idx, ws, ws_bytes, stream);
     if (rc) return rc;
-    return kvc_compact(&s, k_dev, v_dev, idx, budget, k_max, k_out, v_out, out_rows, ws, ws_bytes,
-                       stream);
+    rc = kvc_compact(&s, k_dev, v_dev, idx, budget, k_max, k_out, v_out, out_rows, ws, ws_bytes,
+                     stream);
+    if (rc) return rc;
+    e = cudaEventRecord(last_done[dev], stream);
+    if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_compress_host: %s", cudaGetErrorString(e));
+    return KVC_OK;
 }
 
 int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,

@@ -174,8 +174,11 @@ int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k
  * cudaHostRegisterMapped), else KVC_ERR_INVALID_ARG.  copy_stream must differ
  * from stream.  Outputs, capacities and the workspace are those of the four
  * calls it makes (see them); the call is asynchronous on both streams, and
- * the host buffers must stay valid until `stream` has finished.  At most 1024
- * layers; one event per layer is created once per device and kept. */
+ * the host buffers must stay valid until `stream` has finished.  A call's
+ * copies wait only for the previous call's compaction on this device (the
+ * last read of the staging buffers), so reading the outputs back overlaps
+ * with the next prompt's copies.  At most 1024 layers; one event per layer
+ * is created once per device and kept. */
 int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_host,
                       const void *v_host, void *q_dev, void *k_dev, uint32_t mass_num,
                       uint32_t mass_den, int64_t total_budget, int32_t layer_floor, int32_t k_max,
