@@ -185,12 +185,20 @@ __global__ void __launch_bounds__(kPruneThreads)
     auto slice_sum = [&](const T *base, int64_t first_row, int lo, int hi, FF *out) {
         FF a0 = {0.f, 0.f}, a1 = {0.f, 0.f};
         if (g < groups) {
+            // eight rows' loads in flight before their sums (the rows come
+            // from global memory; the sums are a dependent chain)
             int r = lo + g;
-            for (; r + groups < hi; r += 2 * groups) {
-                a0 = ff_add_sq(a0, ld_f(base, (first_row + r) * D + d));
-                a1 = ff_add_sq(a1, ld_f(base, (first_row + r + groups) * D + d));
+            for (; r + 7 * groups < hi; r += 8 * groups) {
+                float x[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[k] = ld_f(base, (first_row + r + k * groups) * D + d);
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    a0 = ff_add_sq(a0, x[k]);
+                    a1 = ff_add_sq(a1, x[k + 1]);
+                }
             }
-            if (r < hi) a0 = ff_add_sq(a0, ld_f(base, (first_row + r) * D + d));
+            for (; r < hi; r += groups) a0 = ff_add_sq(a0, ld_f(base, (first_row + r) * D + d));
         }
         part[tid] = ff_add(a0, a1);
         __syncthreads();
@@ -243,15 +251,17 @@ __global__ void __launch_bounds__(kPruneThreads)
 
     // 3. copy the kept channels of this CTA's rows
     const int64_t o0 = s_o0 + (int64_t)r_lo * keep;
-    const int total = (r_hi - r_lo) * keep;
+    int total = (r_hi - r_lo) * keep;
+    if (o0 + total > pruned_elems) {   // output too small: copy what fits, report it
+        if (tid == 0) set_status(status, KVC_DEV_OUT_CAPACITY);
+        total = (int)max((int64_t)0, pruned_elems - o0);
+    }
+    const T *src = k_out + (row0 + r_lo) * D;
+    T *dst = k_pruned + o0;
+#pragma unroll 4
     for (int i = tid; i < total; i += kPruneThreads) {
         const int r = i / keep;
-        const int c = i - r * keep;
-        if (o0 + i >= pruned_elems) {
-            set_status(status, KVC_DEV_OUT_CAPACITY);
-            break;
-        }
-        k_pruned[o0 + i] = k_out[(row0 + r_lo + r) * D + sel[c]];
+        dst[i] = src[(int64_t)r * D + sel[i - r * keep]];
     }
 }
 

@@ -120,21 +120,22 @@ __device__ __forceinline__ void stage_scores(const float *__restrict__ g, float 
 }
 
 // Visit scores 0..n-1 of one head: thread tid gets k = base + i*1024 + tid,
-// eight loads issued before any is used (latency hidden when the scores come
+// sixteen loads issued before any is used (latency hidden when the scores come
 // from global memory).  f(k, v, in) is called for every lane, with in false
 // past the end, so warp-wide votes inside f stay uniform.
 template <typename F>
 __device__ __forceinline__ void for_scores(const float *__restrict__ src, int n, F f) {
+    constexpr int kBatch = 16;
     const int tid = threadIdx.x;
-    for (int base = 0; base < n; base += 8 * kSelThreads) {
-        float r[8];
+    for (int base = 0; base < n; base += kBatch * kSelThreads) {
+        float r[kBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kBatch; ++i) {
             const int k = base + i * kSelThreads + tid;
             r[i] = k < n ? src[k] : 0.f;
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kBatch; ++i) {
             const int k = base + i * kSelThreads + tid;
             f(k, r[i], k < n);
         }
