@@ -16,28 +16,33 @@
 //           epilogue thread owns one TMEM lane = one query row and keeps an
 //           online (max, sum) over its CTA's keys -> per-CTA partials;
 //   merge   (score_simt.cu) combines the partials into nb_r = -(m_r + log2 l_r);
-//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 256 query rows): each
-//           epilogue thread owns one key and sums 2^(x_rj + nb_r) over the
-//           query rows in registers -- the column sum needs no cross-lane
-//           reduction in this orientation.
+//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 256 query rows) plus one
+//           extra K-step that adds nb_r / (log2(e)/sqrt(D)) to every column r
+//           (ones against the row biases split into three bf16 terms): each
+//           epilogue thread owns one key and sums 2^(x'_rj) over the query
+//           rows in registers -- no cross-lane reduction in this orientation,
+//           and no per-logit bias load.
 //
 // Both passes are persistent: CTA c owns a contiguous run of (unit, key
 // tile) pairs, keeps the unit's Q block resident in shared memory and streams
 // K tiles with TMA through an mbarrier ring.  Warp roles: warp 0 TMA
 // producer, warp 1 MMA issuer (and TMEM owner), warps 2-9 epilogue in two
 // warpgroups.  Pass 1 splits TMEM into four 128-column accumulator slots
-// (one 128 x 128 job each); pass 2 into two 256-column slots (one
-// 128 x 256 job each: with both operands in shared memory the wider MMA
-// reads fewer operand bytes per flop and runs closer to the tensor peak).
-// The warpgroups take alternate jobs, so one computes while the other waits
-// for its TMEM load or its next MMA.  A job is read from TMEM in 64-column
+// (one 128 x 128 job each; the warpgroups take alternate jobs); pass 2 into
+// two 256-column slots (one 128 x 256 job each: with both operands in shared
+// memory the wider MMA reads fewer operand bytes per flop), each job's
+// columns split between the two warpgroups so that a slot is free again
+// after two TMEM loads per warp.  A job is read from TMEM in 64-column
 // pieces; each thread keeps independent sum chains on packed fp32 pairs, and
 // the epilogue has one copy of its inner loop (the window's causal mask is
 // applied by setting invisible logits to -inf first) so that it fits the
-// instruction cache.  The epilogue competes with the MMA stream for the SM
-// (shared memory and issue), so every instruction per logit counts: pass 1
-// keeps a running reference that is raised only when a piece would overflow
-// instead of taking every piece's maximum.
+// instruction cache.  Measured on this GPU, shared-memory loads in the
+// epilogue compete with the MMAs' shared-memory operand reads (an exp loop
+// with them runs at half speed beside the MMA stream, without them at full
+// speed), which is why pass 2 takes the row biases through the MMA; and
+// every instruction per logit counts, which is why pass 1 keeps a running
+// reference that is raised only when a piece would overflow instead of
+// taking every piece's maximum.
 // Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
@@ -79,10 +84,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 struct Smem {
     uint8_t *q;        // [KH][rows_pad][128 B], 128-byte swizzled (TMA)
     uint8_t *k;        // [stages][KH][128 keys][128 B]
+    uint8_t *aug_k;    // [128 keys][32 B] pass-2 extra K-step operand: ones
+    uint8_t *aug_q;    // [rows_pad][32 B] pass-2 extra K-step operand: row biases
     float *red;        // [2][128] pass-2 partial column sums handed WG1 -> WG0
-    float *nb;         // [rows_pad] pass-2 row biases of the current unit
     uint64_t *full, *empty, *q_full, *q_empty, *t_full, *t_empty, *c_full, *c_empty;
-    uint64_t *nb_ready, *nb_done, *drain;
+    uint64_t *aug_full, *aug_empty, *drain;
     uint32_t *tmem_base;
     volatile int *abort_flag;
 };
@@ -95,10 +101,12 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
     b += (size_t)KH * p.rows_pad * 128;
     s.k = b;
     b += (size_t)p.stages * KH * kBoxBytes;
+    s.aug_k = b;
+    b += 128 * 32;
+    s.aug_q = b;
+    b += (size_t)p.rows_pad * 32;
     s.red = reinterpret_cast<float *>(b);
     b += 2 * 128 * sizeof(float);
-    s.nb = reinterpret_cast<float *>(b);
-    b += (size_t)p.rows_pad * sizeof(float);
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
     s.full = bars;
     s.empty = bars + p.stages;
@@ -108,9 +116,9 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
     s.t_empty = s.t_full + 4;   // 4
     s.c_full = s.t_empty + 4;   // 2
     s.c_empty = s.c_full + 2;   // 2
-    s.nb_ready = s.c_empty + 2;
-    s.nb_done = s.nb_ready + 1;
-    s.drain = s.nb_done + 1;
+    s.aug_full = s.c_empty + 2;
+    s.aug_empty = s.aug_full + 1;
+    s.drain = s.aug_empty + 1;
     s.tmem_base = reinterpret_cast<uint32_t *>(s.drain + 1);
     s.abort_flag = reinterpret_cast<volatile int *>(s.tmem_base + 1);
     return s;
@@ -118,12 +126,12 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
 
 template <int KH>
 size_t smem_bytes(int rows_pad, int stages) {
-    return 1024 + (size_t)KH * rows_pad * 128 + (size_t)stages * KH * kBoxBytes + 2 * 128 * 4 +
-           (size_t)rows_pad * 4 + (size_t)(2 * stages + 17) * 8 + 16;
+    return 1024 + (size_t)KH * rows_pad * 128 + (size_t)stages * KH * kBoxBytes + 128 * 32 +
+           (size_t)rows_pad * 32 + 2 * 128 * 4 + (size_t)(2 * stages + 17) * 8 + 16;
 }
 
 // Barrier set-up, TMEM allocation; returns the TMEM base column address.
-__device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p) {
+__device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p, int t_empty_count) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -134,14 +142,14 @@ __device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p) {
         mbar_init(s.q_empty, 1);
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s.t_full[i], 1);
-            mbar_init(&s.t_empty[i], 4);  // one arrive per warp of the owning warpgroup
+            mbar_init(&s.t_empty[i], t_empty_count);  // one arrive per warp reading the slot
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.c_full[i], 128);
             mbar_init(&s.c_empty[i], 128);
         }
-        mbar_init(s.nb_ready, kEpi);
-        mbar_init(s.nb_done, kEpi);
+        mbar_init(s.aug_full, kEpi);
+        mbar_init(s.aug_empty, 1);
         mbar_init(s.drain, 1);
         *s.abort_flag = 0;
         fence_barrier_init();
@@ -203,6 +211,19 @@ __device__ __forceinline__ void mma_drain(const Smem &s) {
     mbar_drain(s.drain, 0);
 }
 
+// K-major operand in the 32-byte swizzled layout: rows of 32 bytes (16
+// bf16, one MMA K-step), 8-row groups 256 bytes apart (stride offset 256),
+// layout code 6 in bits [61,64).
+__device__ __forceinline__ uint64_t sw32_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(256 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(6) << 61;
+    return d;
+}
+
 // MMA issuer (one thread).  For every K tile: njob jobs of fp32 accumulators
 // into TMEM.  Pass 1 (KEYS_AS_B): 128 x 128 jobs into slot job % 4, A = Q
 // row block jb, B = the K tile.  Pass 2: 128 x n jobs (n <= 256) into slot
@@ -218,6 +239,8 @@ __device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int6
         const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
         if (t == t0 || jt == 0) {
             if (!mbar_wait(s.q_full, q_loads & 1, s.abort_flag, p.status)) break;
+            // pass 2 also needs the unit's row-bias operand
+            if (!KEYS_AS_B && !mbar_wait(s.aug_full, q_loads & 1, s.abort_flag, p.status)) break;
             ++q_loads;
         }
         if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
@@ -244,11 +267,18 @@ __device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int6
                 const uint64_t b = sw128_kmajor_desc(KEYS_AS_B ? ka : qa);
                 tc_mma_bf16(d, a, b, idesc, ks > 0);
             }
+            if (!KEYS_AS_B) {
+                // one more K-step adds each query row's bias to its column:
+                // ones (keys) x the row's bias / cs split into bf16 terms
+                tc_mma_bf16(d, sw32_kmajor_desc(smem_u32(s.aug_k)),
+                            sw32_kmajor_desc(smem_u32(s.aug_q + (size_t)jb * kCols * 32)), idesc, 1u);
+            }
             tc_commit(&s.t_full[slot]);
         }
         if (!ok) break;
         tc_commit(&s.empty[stage]);
         if (last) tc_commit(s.q_empty);
+        if (last && !KEYS_AS_B) tc_commit(s.aug_empty);
         if (++stage == p.stages) {
             stage = 0;
             phase ^= 1;
@@ -332,26 +362,18 @@ __device__ __forceinline__ void row_stats64_lazy(const float (&v)[2][32], float 
     row_stats64(v, cs, m_run, l_run);
 }
 
-// Add 2^(x * cs + nb[i]) for 64 query-row columns into eight partial sums
-// (packed fp32 pairs for the logit scaling and the accumulation).
-__device__ __forceinline__ void col_sums64(const float (&v)[2][32], const float *nb, float cs,
-                                           float (&a8)[8]) {
-    const float4 *nb4 = reinterpret_cast<const float4 *>(nb);
+// Add 2^(x * cs) for 64 query-row columns into eight partial sums; the
+// accumulators already carry each row's bias nb_r / cs (packed fp32 pairs for
+// the scaling and the accumulation).
+__device__ __forceinline__ void col_sums64(const float (&v)[2][32], float cs, float (&a8)[8]) {
     unsigned long long a4[4] = {0ull, 0ull, 0ull, 0ull};
     const unsigned long long cs2 = f2_pack(cs, cs);
 #pragma unroll
-    for (int i4 = 0; i4 < 16; ++i4) {
-        const float4 b4 = nb4[i4];
-        const int i = i4 * 4;
-        const unsigned long long y01 =
-            f2_fma(f2_pack(v[i >> 5][i & 31], v[i >> 5][(i & 31) + 1]), cs2, f2_pack(b4.x, b4.y));
-        const unsigned long long y23 = f2_fma(
-            f2_pack(v[i >> 5][(i & 31) + 2], v[i >> 5][(i & 31) + 3]), cs2, f2_pack(b4.z, b4.w));
-        float y0, y1, y2, y3;
-        f2_unpack(y01, y0, y1);
-        f2_unpack(y23, y2, y3);
-        a4[(2 * i4) & 3] = f2_add(a4[(2 * i4) & 3], f2_pack(ex2(y0), ex2(y1)));
-        a4[(2 * i4 + 1) & 3] = f2_add(a4[(2 * i4 + 1) & 3], f2_pack(ex2(y2), ex2(y3)));
+    for (int i = 0; i < 64; i += 2) {
+        const unsigned long long y = f2_mul(f2_pack(v[i >> 5][i & 31], v[i >> 5][(i & 31) + 1]), cs2);
+        float y0, y1;
+        f2_unpack(y, y0, y1);
+        a4[(i >> 1) & 3] = f2_add(a4[(i >> 1) & 3], f2_pack(ex2(y0), ex2(y1)));
     }
     float t[8];
     f2_unpack(a4[0], t[0], t[1]);
@@ -380,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve<KH>(smem_raw, p);
-    const uint32_t tmem = setup(s, p);
+    const uint32_t tmem = setup(s, p, 4);   // a slot is read by one warpgroup
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c = blockIdx.x;
     const int64_t t0 = split_begin(p.n_tiles, p.grid, c), t1 = split_begin(p.n_tiles, p.grid, c + 1);
@@ -477,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve<KH>(smem_raw, p);
-    const uint32_t tmem = setup(s, p);
+    const uint32_t tmem = setup(s, p, 8);   // both warpgroups read every slot
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c = blockIdx.x;
     const int64_t t0 = split_begin(p.n_tiles, p.grid, c), t1 = split_begin(p.n_tiles, p.grid, c + 1);
@@ -493,10 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mma_issuer<KH, false>(s, p, tmem, t0, t1, nch);
     } else {
         // Epilogue.  Each thread owns one key (its TMEM lane) and sums
-        // 2^(x + nb_r) over the query rows r of the chunks its warpgroup owns:
-        // chunk nc goes to warpgroup nc % 2 when a tile has several chunks
-        // (warpgroup 1 then hands its partial sum to warpgroup 0 through
-        // shared memory), otherwise whole tiles alternate between the two.
+        // 2^(x' * cs) over query rows, x' = q.k + nb_r / cs already in the
+        // accumulator.  Every job (up to 256 rows) is split by columns:
+        // warpgroup e reads columns [128 e, 128 e + 128), so a slot is free
+        // again after two 64-column loads per warp; warpgroup 1 hands its
+        // partial sum to warpgroup 0 through shared memory once per tile.
         const int quarter = warp & 3;
         const int ewg = (warp - 2) >> 2;
         const int etid = threadIdx.x - 64;
@@ -510,16 +533,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j0 = jt * kTileKeys;
             const uint32_t tl = (uint32_t)(t - t0);
             if (t == t0 || jt == 0) {
-                // stage the unit's row biases in shared memory: everyone is
-                // done with the previous unit's, then everyone sees the new
-                if (unit_changes > 0) {
-                    mbar_arrive(s.nb_done);
-                    if (!mbar_wait(s.nb_done, (unit_changes - 1) & 1, s.abort_flag, p.status)) break;
+                // The unit's row biases become one more MMA K-step: row r of
+                // aug_q holds nb_r / cs split into three bf16 terms (about 24
+                // significant bits) in its first 16 bytes, zeros in the other
+                // 16; every row of aug_k holds ones at the same three places in
+                // both halves, so the product picks the terms up whatever the
+                // 32-byte swizzle does to the two halves of a row.  Pad rows
+                // get a bias that sends their exponentials to zero.
+                if (unit_changes == 0) {
+                    const __nv_bfloat16 one = __float2bfloat16(1.f), z = __float2bfloat16(0.f);
+                    __align__(16) __nv_bfloat16 h8[8] = {one, one, one, z, z, z, z, z};
+                    for (int i = etid; i < 128 * 2; i += kEpi)
+                        *reinterpret_cast<uint4 *>(s.aug_k + i * 16) = *reinterpret_cast<const uint4 *>(h8);
+                } else if (!mbar_wait(s.aug_empty, (unit_changes - 1) & 1, s.abort_flag, p.status)) {
+                    break;   // the previous unit's MMAs still read aug_q
                 }
-                for (int r = etid; r < p.rows_pad; r += kEpi)
-                    s.nb[r] = p.neg_bias_in[(int64_t)u * p.rows_pad + r];
-                mbar_arrive(s.nb_ready);
-                if (!mbar_wait(s.nb_ready, unit_changes & 1, s.abort_flag, p.status)) break;
+                for (int r = etid; r < p.rows_pad; r += kEpi) {
+                    const float nb = p.neg_bias_in[(int64_t)u * p.rows_pad + r];
+                    const float v = (r < p.rows && nb > -3.0e4f * p.cs) ? nb / p.cs : -3.0e4f;
+                    const __nv_bfloat16 hi = __float2bfloat16(v);
+                    const float r1 = v - __bfloat162float(hi);
+                    const __nv_bfloat16 mid = __float2bfloat16(r1);
+                    const __nv_bfloat16 lo = __float2bfloat16(r1 - __bfloat162float(mid));
+                    const __nv_bfloat16 z = __float2bfloat16(0.f);
+                    __align__(16) __nv_bfloat16 h8[8] = {hi, mid, lo, z, z, z, z, z};
+                    uint4 *dst = reinterpret_cast<uint4 *>(s.aug_q + (size_t)r * 32);
+                    dst[0] = *reinterpret_cast<const uint4 *>(h8);
+                    dst[1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMA
+                mbar_arrive(s.aug_full);
                 ++unit_changes;
             }
             const int j = j0 + key_in_tile;
@@ -532,53 +575,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int nc = 0; nc < nch; ++nc) {
                 const uint32_t jj = job + nc;
                 const uint32_t slot = jj & 1, use = jj >> 1;
-                const int owner = nch >= 2 ? (nc & 1) : (int)(tl & 1);
-                if (owner != ewg) continue;
                 if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int n = min(256, p.n_pad - nc * 256);
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 256;
-                const int nh = (n + 63) / 64;
+                const int c0 = ewg * 128;
+                const int cn = min(128, n - c0);   // this warpgroup's columns (may be none)
+                if (cn <= 0) {
+                    release_slot(&s.t_empty[slot], lane);
+                    continue;
+                }
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 256 + c0;
+                const int nh = (cn + 63) / 64;
 #pragma unroll 1
                 for (int h = 0; h < nh; ++h) {
                     float v[2][32];
                     load_row64(taddr + h * 64, v);
                     if (h == nh - 1) release_slot(&s.t_empty[slot], lane);
-                    const int valid = n - h * 64;   // narrow last chunk: 16..48 columns
+                    const int valid = cn - h * 64;   // narrow last chunk: 16..48 columns
                     if (valid < 64) {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
                             if (i >= valid) v[i >> 5][i & 31] = -INFINITY;
                     }
-                    const int r0 = nc * 256 + h * 64;
                     if (masked) {
-                        int w = r0 % p.W;
+                        int w = (nc * 256 + c0 + h * 64) % p.W;
                         mask_cols(v[0], w, dj, p.W);
                         mask_cols(v[1], w, dj, p.W);
                     }
-                    col_sums64(v, s.nb + r0, p.cs, a8);
+                    col_sums64(v, p.cs, a8);
                 }
             }
             job += nch;
             if (!ok) break;
             float acc = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
-            if (nch >= 2) {
-                const uint32_t b = tl & 1, ub = tl >> 1;
-                float *red = s.red + b * 128;
-                if (ewg == 1) {
-                    if (!mbar_wait(&s.c_empty[b], (ub & 1) ^ 1, s.abort_flag, p.status)) break;
-                    red[key_in_tile] = acc;
-                    mbar_arrive(&s.c_full[b]);
-                } else {
-                    if (!mbar_wait(&s.c_full[b], ub & 1, s.abort_flag, p.status)) break;
-                    acc += red[key_in_tile];
-                    mbar_arrive(&s.c_empty[b]);
-                    if (j < p.T) p.scores[(int64_t)u * p.T + j] = acc / rows_f;
-                }
-            } else if ((int)(tl & 1) == ewg) {
+            const uint32_t b = tl & 1, ub = tl >> 1;
+            float *red = s.red + b * 128;
+            if (ewg == 1) {
+                if (!mbar_wait(&s.c_empty[b], (ub & 1) ^ 1, s.abort_flag, p.status)) break;
+                red[key_in_tile] = acc;
+                mbar_arrive(&s.c_full[b]);
+            } else {
+                if (!mbar_wait(&s.c_full[b], ub & 1, s.abort_flag, p.status)) break;
+                acc += red[key_in_tile];
+                mbar_arrive(&s.c_empty[b]);
                 if (j < p.T) p.scores[(int64_t)u * p.T + j] = acc / rows_f;
             }
         }
