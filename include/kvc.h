@@ -26,10 +26,11 @@
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer owned by the caller,
- *    contiguous in the layout stated below.  No call allocates device
- *    memory; scratch lives in a caller-provided workspace of
- *    kvc_workspace_size() bytes, zeroed once with kvc_workspace_init()
- *    (kvc_score_noalloc alone uses a fixed array inside the library).
+ *    contiguous in the layout stated below (kvc_compress_host alone takes
+ *    its prompt in pinned host memory).  No call allocates device memory;
+ *    scratch lives in a caller-provided workspace of kvc_workspace_size()
+ *    bytes, zeroed once with kvc_workspace_init() (kvc_score_noalloc alone
+ *    uses a fixed array inside the library).
  *  - Work is enqueued on `stream` and is asynchronous.  Argument errors are
  *    detected on the host before anything is launched and returned as a
  *    negative kvc_status; kvc_last_error() then holds a message.
