@@ -229,14 +229,14 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     const void *v_dev = pa.devicePointer;
     if (!aligned16(v_dev)) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: v_host must be 16-byte aligned");
     // one event per layer (plus one for Q), created once per device
-    constexpr int kMaxEv = 1026;
+    constexpr int kMaxEv = 1025;
     static cudaEvent_t events[16][kMaxEv];
     static int n_events[16] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 16 || s.n_layers + 2 > kMaxEv)
+    if (dev >= 16 || s.n_layers + 1 > kMaxEv)
         return fail(KVC_ERR_UNSUPPORTED, "kvc_compress_host: at most 1024 layers on devices 0..15");
-    while (n_events[dev] < s.n_layers + 2) {
+    while (n_events[dev] < s.n_layers + 1) {
         if (cudaEventCreateWithFlags(&events[dev][n_events[dev]], cudaEventDisableTiming) != cudaSuccess)
             return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
         ++n_events[dev];
@@ -244,18 +244,14 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     const size_t es = s.dtype == KVC_F32 ? 4 : 2;
     const size_t q_layer = (size_t)s.n_q_heads * s.window * s.head_dim * es;
     const size_t k_layer = (size_t)s.n_kv_heads * s.seq_len * s.head_dim * es;
-    // 0. the staging buffers may still be read by work already on `stream`
-    // (a previous call's compaction): the copies start after it
-    // ev_done marks the end of the previous call's last read of the staging
-    // buffers (its compaction); this call's copies start after it -- and only
-    // after it, so whatever the caller enqueued since (reading the outputs
-    // back) overlaps with the next prompt's copies.  Waiting on an event that
-    // was never recorded returns at once.
-    cudaEvent_t ev_done = events[dev][s.n_layers + 1];
+    // 0. last_done marks the end of the previous call's last read of the
+    // staging buffers (its compaction); this call's copies start after it --
+    // and only after it, so whatever the caller enqueued since (reading the
+    // outputs back) overlaps with the next prompt's copies.  Waiting on an
+    // event that was never recorded returns at once.
     static cudaEvent_t last_done[16] = {};
     if (!last_done[dev] && cudaEventCreateWithFlags(&last_done[dev], cudaEventDisableTiming) != cudaSuccess)
         return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
-    (void)ev_done;
     cudaError_t e = cudaStreamWaitEvent(copy_stream, last_done[dev], 0);
     // 1. the copy stream moves Q, then K layer by layer, marking each layer
     if (e == cudaSuccess)

@@ -146,8 +146,7 @@ __device__ __forceinline__ void for_scores(const float *__restrict__ src, int n,
 // Per head (one 1024-thread block): the scores are read once from global
 // memory into shared memory (when they fit), then
 //  1. a 4096-bucket histogram of the top 12 key bits with counts and
-//     truncated 32-bit masses (native shared atomics; the lanes of a warp
-//     that share a bucket add as one group), and the exact total
+//     truncated 32-bit masses (native shared atomics), and the exact total
 //     U = sum u_j in per-thread 64-bit sums;
 //  2. the truncated masses point to the bucket d1 where the running mass
 //     from the top reaches num/den of the total; one exact pass (64-bit per-thread
@@ -194,29 +193,14 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
     unsigned long long my_u = 0;
     int bad = 0;
-    const int lane = tid & 31;
-    for_scores(src, T, [&](int j, float v, bool in) {
+    for_scores(src, T, [&](int, float v, bool in) {
         const bool valid = in && v >= 0.f && v <= 1.f;
         if (in && !valid) bad = 1;
-        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        if (vmask == 0) return;
+        if (!valid) return;
         const int d = (int)(__float_as_uint(v) >> 19);
-        const uint32_t f = valid ? (uint32_t)(v * 0x1p27f) : 0u;   // guide mass, truncated
-        if (valid) my_u += fixed56f(v);
-        // lanes sharing the first valid lane's bucket add as one group
-        const int leader = __ffs(vmask) - 1;
-        const int dl = __shfl_sync(0xffffffffu, d, leader);
-        const bool same = valid && d == dl;
-        const unsigned smask = __ballot_sync(0xffffffffu, same);
-        const uint32_t fs = __reduce_add_sync(0xffffffffu, same ? f : 0u);
-        if (lane == leader) {
-            atomicAdd(&cnt[dl], (uint32_t)__popc(smask));
-            atomicAdd(&fm[dl], fs);
-        }
-        if (valid && !same) {
-            atomicAdd(&cnt[d], 1u);
-            atomicAdd(&fm[d], f);
-        }
+        my_u += fixed56f(v);
+        atomicAdd(&cnt[d], 1u);
+        atomicAdd(&fm[d], (uint32_t)(v * 0x1p27f));   // guide mass, truncated
     });
     bad = __syncthreads_or(bad);
     const unsigned long long U = block_sum(my_u, wt64, &s_tot64);
