@@ -76,24 +76,8 @@ int score_impl_choice() {
 }
 
 ScoreSplit make_split(const kvc_shape &s, bool tc) {
-    ScoreSplit sp;
-    const int G = s.n_q_heads / s.n_kv_heads;
-    sp.n_units = (int64_t)s.n_layers * s.n_kv_heads;
-    sp.tiles_per_unit = (s.seq_len + kTileKeys - 1) / kTileKeys;
-    sp.n_tiles = sp.n_units * sp.tiles_per_unit;
-    const int sms = device_info().sms > 0 ? device_info().sms : 148;
-    const int64_t want = tc ? sms : 4LL * sms;
-    sp.grid = (int)(sp.n_tiles < want ? sp.n_tiles : want);
-    sp.rows = G * s.window;
-    sp.rows_pad = (sp.rows + 127) / 128 * 128;
-    int mx = 1;
-    for (int64_t u = 0; u < sp.n_units; ++u) {
-        const int64_t a = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit);
-        const int64_t b = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit + sp.tiles_per_unit - 1);
-        if (b - a + 1 > mx) mx = (int)(b - a + 1);
-    }
-    sp.max_slots = mx;
-    return sp;
+    const int sms = device_info().sms;
+    return make_score_split(s, tc, sms, tc ? score_tc_pairs(sms) : 0);
 }
 
 struct WsLayout {
@@ -194,7 +178,7 @@ int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *s
     a.partial = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.partial_off);
     a.neg_bias = reinterpret_cast<float *>(static_cast<char *>(ws) + w.bias_off);
     a.status = status_word(ws);
-    return tc ? launch_score_tc(s, sp, a, device_info().sms, stream) : launch_score_simt(s, sp, a, stream);
+    return tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
 }
 
 // Host-resident prompt, whole default path (see kvc.h).

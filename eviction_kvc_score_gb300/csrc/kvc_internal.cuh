@@ -13,7 +13,8 @@
 namespace kvc {
 
 // ---------------------------------------------------------------- constants
-constexpr int kTileKeys = 128;          // keys per score tile (MMA M or N)
+constexpr int kTileKeys = 128;          // keys per score tile of the CUDA-core path
+constexpr int kPairKeys = 256;          // keys per SM-pair tile of the tensor-core path
 constexpr int kMaxRowsTC = 512;         // G*W handled by the tensor-core path
 constexpr size_t kWsHeader = 256;       // status word + padding
 constexpr double kLog2e = 1.4426950408889634;
@@ -21,20 +22,25 @@ constexpr double kLog2e = 1.4426950408889634;
 // Every pipeline wait gives up after this many nanoseconds of %globaltimer,
 // sets KVC_DEV_TIMEOUT and lets the kernel unwind.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// A waiting thread is suspended in hardware until the barrier's phase
+// completes or this many nanoseconds pass (then the limit above is checked):
+// far fewer polling instructions than a spin.
+#define KVC_SUSPEND_HINT_NS "10000000"
 
 // ---------------------------------------------------------------- score split
 // The score passes walk the flat sequence of (unit, key-tile) pairs, unit =
-// (layer, KV head), in unit-major order.  CTA c of a grid of g owns tiles
-// [floor(N c / g), floor(N (c+1) / g)).  Pass 1 leaves one partial (max, sum)
-// per row for every (unit, CTA touching it) in slot c - first_cta(unit).
+// (layer, KV head), in unit-major order.  Worker c of g (a CTA on the CUDA
+// cores, a 2-CTA cluster on the tensor cores) owns tiles [floor(N c / g),
+// floor(N (c+1) / g)).  Pass 1 leaves one partial (max, sum) per row for
+// every (unit, worker touching it) in slot c - first_worker(unit).
 struct ScoreSplit {
     int64_t n_units;       // L * H_kv
     int64_t tiles_per_unit;
     int64_t n_tiles;       // n_units * tiles_per_unit
-    int grid;              // CTAs
+    int grid;              // workers: CTAs, or CTA pairs on the tensor-core path
     int max_slots;         // partial slots per unit
     int rows;              // G * W
-    int rows_pad;          // rows rounded up to 128
+    int rows_pad;          // rows rounded up to 128 (CUDA cores) or 256 (tensor cores)
 };
 
 __host__ __device__ inline int64_t split_begin(int64_t n, int g, int64_t c) {
@@ -42,6 +48,30 @@ __host__ __device__ inline int64_t split_begin(int64_t n, int g, int64_t c) {
 }
 __host__ __device__ inline int64_t split_cta_of(int64_t n, int g, int64_t t) {
     return ((int64_t)g * (t + 1) - 1) / n;
+}
+
+// tc: 256-key tiles over `pairs` CTA pairs; otherwise 128-key tiles over
+// four CTAs per SM.
+inline ScoreSplit make_score_split(const kvc_shape &s, bool tc, int sms, int pairs) {
+    ScoreSplit sp;
+    const int G = s.n_q_heads / s.n_kv_heads;
+    const int tile = tc ? kPairKeys : kTileKeys;
+    sp.n_units = (int64_t)s.n_layers * s.n_kv_heads;
+    sp.tiles_per_unit = (s.seq_len + tile - 1) / tile;
+    sp.n_tiles = sp.n_units * sp.tiles_per_unit;
+    const int64_t want = tc ? (pairs > 0 ? pairs : 1) : 4LL * (sms > 0 ? sms : 148);
+    sp.grid = (int)(sp.n_tiles < want ? sp.n_tiles : want);
+    sp.rows = G * s.window;
+    const int rb = tc ? 256 : 128;
+    sp.rows_pad = (sp.rows + rb - 1) / rb * rb;
+    int mx = 1;
+    for (int64_t u = 0; u < sp.n_units; ++u) {
+        const int64_t a = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit);
+        const int64_t b = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit + sp.tiles_per_unit - 1);
+        if (b - a + 1 > mx) mx = (int)(b - a + 1);
+    }
+    sp.max_slots = mx;
+    return sp;
 }
 
 // ---------------------------------------------------------------- status word
@@ -83,7 +113,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, " KVC_SUSPEND_HINT_NS ";\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -109,12 +139,76 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// The same bounded wait with acquire at cluster scope, for barriers that
+// other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, " KVC_SUSPEND_HINT_NS ";\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                             uint32_t *status) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait_cl(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_status(status, KVC_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Wait used only while unwinding: bounded, ignores the abort flag.
 __device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
         if (globaltimer() - t0 > kWaitLimitNs) return false;
     return true;
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address, in the cluster's shared window, of the object at shared-memory
+// address `saddr` of CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier given by its cluster address.  The plain form
+// releases at CTA scope, enough when the arriving thread's own work is
+// already complete (a finished TMEM load, an observed TMA completion) and
+// cheap; the _cluster form orders the thread's earlier shared-memory writes
+// for readers in the other CTA and costs a cluster-scope fence.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -185,6 +279,43 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// SM-pair forms (cta_group::2): TMEM is allocated in both CTAs of a 2-CTA
+// cluster by one warp of each; one thread of the even CTA issues M = 256
+// MMAs whose A rows 0-127 and B rows 0..N/2-1 come from the even CTA's
+// shared memory and the rest from the odd CTA's at the same offsets, each
+// CTA's TMEM receiving its own 128 rows of D; a commit arrives on the
+// barrier at the same offset in every CTA of the mask.  A kernel uses
+// either these forms or the single-CTA ones, never both.
+__device__ __forceinline__ void tmem_alloc2(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit2(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 
@@ -301,8 +432,10 @@ struct ScoreArgs {
     uint32_t *status;
 };
 
-int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, int num_sms,
-                    cudaStream_t st);
+// CTA pairs of the tensor-core score kernels that the current device runs at
+// once (cached per device; half the SM count if the query fails).
+int score_tc_pairs(int sms);
+int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st);
 int launch_score_simt(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
                       cudaStream_t st);
 int launch_score_merge(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,

@@ -120,22 +120,7 @@ extern "C" int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, cons
     const int sms = sm_count() > 0 ? sm_count() : 148;
 
     // Same work split as kvc_score.
-    ScoreSplit sp;
-    sp.n_units = (int64_t)s.n_layers * s.n_kv_heads;
-    sp.tiles_per_unit = (s.seq_len + kTileKeys - 1) / kTileKeys;
-    sp.n_tiles = sp.n_units * sp.tiles_per_unit;
-    const int64_t want = tc ? sms : 4LL * sms;
-    sp.grid = (int)(sp.n_tiles < want ? sp.n_tiles : want);
-    sp.rows = G * s.window;
-    sp.rows_pad = (sp.rows + 127) / 128 * 128;
-    int mx = 1;
-    for (int64_t u = 0; u < sp.n_units; ++u) {
-        const int64_t a = split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit);
-        const int64_t b =
-            split_cta_of(sp.n_tiles, sp.grid, u * sp.tiles_per_unit + sp.tiles_per_unit - 1);
-        if (b - a + 1 > mx) mx = (int)(b - a + 1);
-    }
-    sp.max_slots = mx;
+    const ScoreSplit sp = make_score_split(s, tc, sms, tc ? score_tc_pairs(sms) : 0);
 
     const size_t partial_bytes = round256((size_t)sp.n_units * sp.max_slots * sp.rows_pad * sizeof(float2));
     const size_t bias_bytes = round256((size_t)sp.n_units * sp.rows_pad * sizeof(float));
@@ -164,5 +149,5 @@ extern "C" int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, cons
     a.partial = reinterpret_cast<float2 *>(scratch + kWsHeader);
     a.neg_bias = reinterpret_cast<float *>(scratch + kWsHeader + partial_bytes);
     a.status = status;
-    return tc ? launch_score_tc(s, sp, a, sms, stream) : launch_score_simt(s, sp, a, stream);
+    return tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
 }

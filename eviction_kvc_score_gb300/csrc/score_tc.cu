@@ -12,37 +12,40 @@
 // The exact column mean needs each row's final normaliser before any column
 // can be summed, so the contraction runs twice and the R x T matrix is never
 // stored:
-//   pass 1  D = Q K^T (M = 128 query rows per MMA, N = 128 keys): each
-//           epilogue thread owns one TMEM lane = one query row and keeps an
-//           online (max, sum) over its CTA's keys -> per-CTA partials;
+//   pass 1  D = Q K^T: each epilogue thread owns one TMEM lane = one query
+//           row and keeps an online (max, sum) -> per-worker partials;
 //   merge   (score_simt.cu) combines the partials into nb_r = -(m_r + log2 l_r);
-//   pass 2  D = K Q^T (M = 128 keys per MMA, N <= 256 query rows) plus one
-//           extra K-step that adds nb_r / (log2(e)/sqrt(D)) to every column r
-//           (ones against the row biases split into three bf16 terms): each
-//           epilogue thread owns one key and sums 2^(x'_rj) over the query
-//           rows in registers -- no cross-lane reduction in this orientation,
-//           and no per-logit bias load.
+//   pass 2  D = K Q^T plus one extra K-step that adds nb_r / (log2(e)/sqrt(D))
+//           to every column r (ones against the row biases split into three
+//           bf16 terms): each epilogue thread owns one key and sums
+//           2^(x'_rj) over the query rows in registers -- no cross-lane
+//           reduction in this orientation, and no per-logit bias load.
 //
-// Both passes are persistent: CTA c owns a contiguous run of (unit, key
-// tile) pairs, keeps the unit's Q block resident in shared memory and streams
-// K tiles with TMA through an mbarrier ring.  Warp roles: warp 0 TMA
-// producer, warp 1 MMA issuer (and TMEM owner), warps 2-9 epilogue in two
-// warpgroups.  Pass 1 splits TMEM into four 128-column accumulator slots
-// (one 128 x 128 job each; the warpgroups take alternate jobs); pass 2 into
-// two 256-column slots (one 128 x 256 job each: with both operands in shared
-// memory the wider MMA reads fewer operand bytes per flop), each job's
-// columns split between the two warpgroups so that a slot is free again
-// after two TMEM loads per warp.  A job is read from TMEM in 64-column
-// pieces; each thread keeps independent sum chains on packed fp32 pairs, and
-// the epilogue has one copy of its inner loop (the window's causal mask is
-// applied by setting invisible logits to -inf first) so that it fits the
-// instruction cache.  Measured on this GPU, shared-memory loads in the
-// epilogue compete with the MMAs' shared-memory operand reads (an exp loop
-// with them runs at half speed beside the MMA stream, without them at full
-// speed), which is why pass 2 takes the row biases through the MMA; and
-// every instruction per logit counts, which is why pass 1 keeps a running
-// reference that is raised only when a piece would overflow instead of
-// taking every piece's maximum.
+// Both passes run on SM pairs: a 2-CTA cluster issues cta_group::2 MMAs of
+// M = 256 and N = 256 (measured on this GPU: 128 clk per 256x256x16 bf16
+// MMA, the full rate of both SMs' tensor cores, against 166 clk for a
+// single SM's 128x256x16 with both operands in shared memory).  The pair
+// walks a contiguous run of (unit, 256-key tile) steps; CTA r of the pair
+// holds keys [128 r, 128 r + 128) of each tile and the query row blocks
+// [256 b + 128 r, +128) of the unit's Q block, which is exactly its share of
+// the A and B operands in both orientations:
+//   pass 1  A = Q rows (M = 256 over the pair), B = the tile's 256 keys;
+//           CTA r's TMEM gets its 128 query rows x 256 keys;
+//   pass 2  A = the tile's keys (M = 256), B = 256 query rows;
+//           CTA r's TMEM gets its own 128 keys x 256 query rows.
+// TMEM holds two 256-column accumulator slots (job b of a tile -> slot
+// b mod 2).  Warp roles in each CTA: warp 0 TMA producer (its own K half and
+// Q rows), warp 1 MMA issuer in the even CTA and, in the odd CTA, a relay
+// that forwards each completed load to the even CTA's barriers; the other
+// warps are the epilogue, in EWG warpgroups (four in pass 1, two in pass 2),
+// each reading 256 / EWG columns of every job.  A warp loads its columns at
+// once and frees the slot before any arithmetic, so the next job's MMAs do
+// not wait on the exponentials.  Each thread keeps independent sum chains on
+// packed fp32 pairs; the window's causal mask sets invisible logits to -inf.  Measured on this GPU, shared-memory loads in the
+// epilogue compete with the MMAs' shared-memory operand reads, which is why
+// pass 2 takes the row biases through the MMA; and every instruction per
+// logit counts, which is why pass 1 keeps a running reference that is raised
+// only when a piece would overflow instead of taking every piece's maximum.
 // Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
@@ -54,20 +57,35 @@ namespace kvc {
 
 namespace {
 
-constexpr int kThreads = 320;     // 10 warps: producer, MMA, 2 x 4 epilogue
-constexpr int kEpi = 256;         // epilogue threads
+// Epilogue warpgroups per pass.  More warps hide more of the exponentials'
+// latency, fewer carry less per-job overhead: pass 1 (a fold per row with a
+// compare per piece) gains from four, pass 2 (a plain sum) runs best on two.
+constexpr int kEWG1 = 4, kEWG2 = 2;
+constexpr int kMaxEWG = 4;
+__host__ __device__ constexpr int wg_cols(int ewg) { return 256 / ewg; }   // columns per warpgroup
+__host__ __device__ constexpr int epi_threads(int ewg) { return 128 * ewg; }
+__host__ __device__ constexpr int cta_threads(int ewg) { return 64 + epi_threads(ewg); }
+// Registers per thread: each of the SM's four schedulers has a quarter of
+// the register file for the warps it holds (warps are dealt round-robin), in
+// steps of 8 per thread.
+__host__ __device__ constexpr int max_regs(int ewg) {
+    return (16384 / (((cta_threads(ewg) / 32 + 3) / 4) * 32)) / 8 * 8;
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+constexpr int kSlotCols = 256;        // TMEM columns per accumulator slot
+constexpr int kMinSmem = 120 * 1024;  // > half an SM's shared memory: one CTA per SM
+constexpr int kRedBytes = (kMaxEWG - 1) * 2 * 128 * 8;   // epilogue hand-over buffer
 
 struct TcParams {
-    int64_t n_tiles;
+    int64_t n_tiles;          // (unit, 256-key tile) steps
     int64_t tiles_per_unit;
-    int grid;
+    int pairs;
     int max_slots;
     int T, P, W;
     int rows;       // G*W
-    int rows_pad;   // multiple of 128
-    int n_pad;      // rows rounded up to 16 (pass-2 MMA N extent)
+    int rows_pad;   // multiple of 256
+    int rows_half;  // rows_pad / 2: query rows held by one CTA
     int stages;
     float cs;       // log2(e) / sqrt(D)
     float2 *partial;
@@ -80,14 +98,18 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Shared-memory carve-up common to both passes.
+// Shared-memory carve-up, identical in both CTAs of a pair (the MMA reads
+// the odd CTA's operands at the even CTA's offsets).
 struct Smem {
-    uint8_t *q;        // [KH][rows_pad][128 B], 128-byte swizzled (TMA)
+    uint8_t *q;        // [KH][rows_half][128 B], 128-byte swizzled (TMA)
     uint8_t *k;        // [stages][KH][128 keys][128 B]
     uint8_t *aug_k;    // [128 keys][32 B] pass-2 extra K-step operand: ones
-    uint8_t *aug_q;    // [rows_pad][32 B] pass-2 extra K-step operand: row biases
-    float *red;        // [2][128] pass-2 partial column sums handed WG1 -> WG0
-    uint64_t *full, *empty, *q_full, *q_empty, *t_full, *t_empty, *c_full, *c_empty;
+    uint8_t *aug_q;    // [rows_half][32 B] pass-2 extra K-step operand: row biases
+    float2 *red;       // epilogue hand-over warpgroups 1.. -> 0 (kRedBytes)
+    uint64_t *full, *empty, *pfull;   // K ring: own loads, MMA done, peer's loads (even CTA)
+    uint64_t *q_full, *q_empty, *q_pfull;
+    uint64_t *t_full, *t_empty;       // [2] TMEM slots (t_empty counts both CTAs' warps)
+    uint64_t *c_full, *c_empty;       // [2]
     uint64_t *aug_full, *aug_empty, *drain;
     uint32_t *tmem_base;
     volatile int *abort_flag;
@@ -98,23 +120,25 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
     Smem s;
     uint8_t *b = align1024(raw);
     s.q = b;
-    b += (size_t)KH * p.rows_pad * 128;
+    b += (size_t)KH * p.rows_half * 128;
     s.k = b;
     b += (size_t)p.stages * KH * kBoxBytes;
     s.aug_k = b;
     b += 128 * 32;
     s.aug_q = b;
-    b += (size_t)p.rows_pad * 32;
-    s.red = reinterpret_cast<float *>(b);
-    b += 2 * 128 * sizeof(float);
+    b += (size_t)p.rows_half * 32;
+    s.red = reinterpret_cast<float2 *>(b);
+    b += kRedBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
     s.full = bars;
     s.empty = bars + p.stages;
-    s.q_full = bars + 2 * p.stages;
+    s.pfull = bars + 2 * p.stages;
+    s.q_full = bars + 3 * p.stages;
     s.q_empty = s.q_full + 1;
-    s.t_full = s.q_empty + 1;   // 4
-    s.t_empty = s.t_full + 4;   // 4
-    s.c_full = s.t_empty + 4;   // 2
+    s.q_pfull = s.q_empty + 1;
+    s.t_full = s.q_pfull + 1;   // 2
+    s.t_empty = s.t_full + 2;   // 2
+    s.c_full = s.t_empty + 2;   // 2
     s.c_empty = s.c_full + 2;   // 2
     s.aug_full = s.c_empty + 2;
     s.aug_empty = s.aug_full + 1;
@@ -126,71 +150,100 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, const TcParams &p) {
 
 template <int KH>
 size_t smem_bytes(int rows_pad, int stages) {
-    return 1024 + (size_t)KH * rows_pad * 128 + (size_t)stages * KH * kBoxBytes + 128 * 32 +
-           (size_t)rows_pad * 32 + 2 * 128 * 4 + (size_t)(2 * stages + 17) * 8 + 16;
+    const size_t need = 1024 + (size_t)KH * (rows_pad / 2) * 128 + (size_t)stages * KH * kBoxBytes +
+                        128 * 32 + (size_t)(rows_pad / 2) * 32 + kRedBytes +
+                        (size_t)(3 * stages + 14) * 8 + 16;
+    return need < (size_t)kMinSmem ? (size_t)kMinSmem : need;
 }
 
-// Barrier set-up, TMEM allocation; returns the TMEM base column address.
-__device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p, int t_empty_count) {
+// (unit, tile) of step t, kept incrementally: no 64-bit division per step.
+struct Step {
+    int u, jt, tpu;
+    __device__ Step(int64_t t, int64_t tiles_per_unit)
+        : u((int)(t / tiles_per_unit)), jt((int)(t % tiles_per_unit)), tpu((int)tiles_per_unit) {}
+    __device__ void next() {
+        if (++jt == tpu) {
+            jt = 0;
+            ++u;
+        }
+    }
+};
+
+// Barrier set-up and TMEM allocation in both CTAs; returns the TMEM base.
+template <int EWG>
+__device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], 1);
+            mbar_init(&s.pfull[i], 1);
         }
         mbar_init(s.q_full, 1);
         mbar_init(s.q_empty, 1);
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&s.t_full[i], 1);
-            mbar_init(&s.t_empty[i], t_empty_count);  // one arrive per warp reading the slot
-        }
+        mbar_init(s.q_pfull, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.c_full[i], 128);
+            mbar_init(&s.t_full[i], 1);
+            mbar_init(&s.t_empty[i], 2 * 4 * EWG);   // epilogue warps of both CTAs
+            mbar_init(&s.c_full[i], (EWG - 1) * 128);
             mbar_init(&s.c_empty[i], 128);
         }
-        mbar_init(s.aug_full, kEpi);
+        mbar_init(s.aug_full, 2 * epi_threads(EWG));
         mbar_init(s.aug_empty, 1);
         mbar_init(s.drain, 1);
         *s.abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(s.tmem_base, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc2(s.tmem_base, kTmemCols);
+        tmem_relinquish2();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();   // the peer's barriers exist before any remote arrive
     tc_fence_after();
     return *s.tmem_base;
 }
 
-// TMA producer (one thread): the unit's Q block whenever the unit changes,
-// then one K tile per stage.  Returns after draining its own copies.
+__device__ __forceinline__ void teardown(uint32_t tmem) {
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // no MMA, load or remote arrive of the pair is left
+    if ((threadIdx.x >> 5) == 1) {
+        tc_fence_after();
+        tmem_dealloc2(tmem, kTmemCols);
+    }
+    cluster_sync_all();
+}
+
+// TMA producer (one thread per CTA): the CTA's Q rows whenever the unit
+// changes, then its 128-key half of each tile.  Returns after draining its
+// own copies.
 template <int KH>
 __device__ void producer(const Smem &s, const TcParams &p, const CUtensorMap *tq,
-                         const CUtensorMap *tk, int64_t t0, int64_t t1) {
+                         const CUtensorMap *tk, int64_t t0, int64_t t1, int rank) {
     int stage = 0;
     uint32_t phase = 0;
     uint32_t q_loads = 0;
     int64_t issued = 0;
-    for (int64_t t = t0; t < t1; ++t) {
-        const int u = (int)(t / p.tiles_per_unit);
-        const int jt = (int)(t % p.tiles_per_unit);
+    Step st(t0, p.tiles_per_unit);
+    for (int64_t t = t0; t < t1; ++t, st.next()) {
+        const int u = st.u, jt = st.jt;
         if (t == t0 || jt == 0) {
             if (q_loads > 0 && !mbar_wait(s.q_empty, (q_loads - 1) & 1, s.abort_flag, p.status))
                 break;
-            mbar_arrive_expect_tx(s.q_full, (uint32_t)(KH * p.rows_pad * 128));
+            mbar_arrive_expect_tx(s.q_full, (uint32_t)(KH * p.rows_half * 128));
             for (int kh = 0; kh < KH; ++kh)
-                for (int rb = 0; rb < p.rows_pad / 128; ++rb)
-                    tma_load_3d(tq, s.q_full, s.q + ((size_t)kh * p.rows_pad + rb * 128) * 128,
-                                kh * 64, rb * 128, u);
+                for (int b = 0; b < p.rows_half / 128; ++b)
+                    tma_load_3d(tq, s.q_full, s.q + ((size_t)kh * p.rows_half + b * 128) * 128,
+                                kh * 64, b * 256 + rank * 128, u);
             ++q_loads;
         }
         if (!mbar_wait(&s.empty[stage], phase ^ 1, s.abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&s.full[stage], (uint32_t)(KH * kBoxBytes));
         for (int kh = 0; kh < KH; ++kh)
             tma_load_3d(tk, &s.full[stage], s.k + ((size_t)stage * KH + kh) * kBoxBytes, kh * 64,
-                        jt * kTileKeys, u);
+                        jt * kPairKeys + rank * 128, u);
         ++issued;
         if (++stage == p.stages) {
             stage = 0;
@@ -198,7 +251,6 @@ __device__ void producer(const Smem &s, const TcParams &p, const CUtensorMap *tq
         }
     }
     // Unwind: every copy this thread started must land before the CTA exits.
-    // In the normal case the consumer already saw them all complete.
     if (*s.abort_flag) {
         for (int64_t i = issued > p.stages ? issued - p.stages : 0; i < issued; ++i)
             mbar_drain(&s.full[i % p.stages], (uint32_t)((i / p.stages) & 1));
@@ -206,8 +258,32 @@ __device__ void producer(const Smem &s, const TcParams &p, const CUtensorMap *tq
     }
 }
 
+// Odd CTA (one thread): forward the completion of each of its own loads to
+// the even CTA, whose MMAs read them.
+__device__ void relay(const Smem &s, const TcParams &p, int64_t t0, int64_t t1) {
+    const uint32_t r_pfull = mapa_shared(smem_u32(s.pfull), 0);
+    const uint32_t r_qpfull = mapa_shared(smem_u32(s.q_pfull), 0);
+    int stage = 0;
+    uint32_t phase = 0, q_loads = 0;
+    Step st(t0, p.tiles_per_unit);
+    for (int64_t t = t0; t < t1; ++t, st.next()) {
+        const int jt = st.jt;
+        if (t == t0 || jt == 0) {
+            if (!mbar_wait(s.q_full, q_loads & 1, s.abort_flag, p.status)) break;
+            mbar_arrive_remote(r_qpfull);
+            ++q_loads;
+        }
+        if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
+        mbar_arrive_remote(r_pfull + (uint32_t)stage * 8u);
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1;
+        }
+    }
+}
+
 __device__ __forceinline__ void mma_drain(const Smem &s) {
-    tc_commit(s.drain);
+    tc_commit2(s.drain, 1);
     mbar_drain(s.drain, 0);
 }
 
@@ -224,61 +300,63 @@ __device__ __forceinline__ uint64_t sw32_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
-// MMA issuer (one thread).  For every K tile: njob jobs of fp32 accumulators
-// into TMEM.  Pass 1 (KEYS_AS_B): 128 x 128 jobs into slot job % 4, A = Q
-// row block jb, B = the K tile.  Pass 2: 128 x n jobs (n <= 256) into slot
-// job % 2, A = the K tile, B = Q rows 256 jb ...
+// MMA issuer (one thread of the even CTA).  For every tile: njob jobs of
+// 256 x 256 fp32 accumulators into slot job % 2 of both CTAs' TMEM.
+// Pass 1 (KEYS_AS_B): A = Q rows of job b (each CTA's local block b), B = the
+// tile's keys.  Pass 2: A = the tile's keys, B = Q rows of job b, then the
+// bias K-step.
 template <int KH, bool KEYS_AS_B>
 __device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int64_t t0, int64_t t1,
                            int njob) {
+    constexpr uint16_t kBoth = 3;
+    const uint32_t idesc = idesc_bf16_f32(256, 256);
     int stage = 0;
     uint32_t phase = 0, q_loads = 0, job = 0;
     bool ok = true;
-    for (int64_t t = t0; t < t1 && ok; ++t) {
-        const int jt = (int)(t % p.tiles_per_unit);
+    Step st(t0, p.tiles_per_unit);
+    for (int64_t t = t0; t < t1 && ok; ++t, st.next()) {
+        const int jt = st.jt;
         const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
         if (t == t0 || jt == 0) {
             if (!mbar_wait(s.q_full, q_loads & 1, s.abort_flag, p.status)) break;
-            // pass 2 also needs the unit's row-bias operand
-            if (!KEYS_AS_B && !mbar_wait(s.aug_full, q_loads & 1, s.abort_flag, p.status)) break;
+            if (!mbar_wait(s.q_pfull, q_loads & 1, s.abort_flag, p.status)) break;
+            // pass 2 also needs both CTAs' row-bias operands for the unit
+            if (!KEYS_AS_B && !mbar_wait_cl(s.aug_full, q_loads & 1, s.abort_flag, p.status)) break;
             ++q_loads;
         }
         if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
+        if (!mbar_wait(&s.pfull[stage], phase, s.abort_flag, p.status)) break;
         tc_fence_after();
         for (int jb = 0; jb < njob; ++jb, ++job) {
-            constexpr uint32_t kSlots = KEYS_AS_B ? 4 : 2;
-            constexpr int kCols = KEYS_AS_B ? 128 : 256;   // TMEM columns per slot
-            const uint32_t slot = job % kSlots, use = job / kSlots;
+            const uint32_t slot = job & 1, use = job >> 1;
             if (!mbar_wait(&s.t_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int n = KEYS_AS_B ? kTileKeys : min(kCols, p.n_pad - jb * kCols);
-            const uint32_t idesc = idesc_bf16_f32(128, n);
-            const uint32_t d = tmem + slot * kCols;
+            const uint32_t d = tmem + slot * kSlotCols;
 #pragma unroll
             for (int ks = 0; ks < KH * 4; ++ks) {
                 const int kh = ks >> 2, off = (ks & 3) * 32;
                 const uint32_t qa =
-                    smem_u32(s.q + ((size_t)kh * p.rows_pad + jb * kCols) * 128) + off;
+                    smem_u32(s.q + ((size_t)kh * p.rows_half + jb * 128) * 128) + off;
                 const uint32_t ka = smem_u32(s.k + ((size_t)stage * KH + kh) * kBoxBytes) + off;
                 const uint64_t a = sw128_kmajor_desc(KEYS_AS_B ? qa : ka);
                 const uint64_t b = sw128_kmajor_desc(KEYS_AS_B ? ka : qa);
-                tc_mma_bf16(d, a, b, idesc, ks > 0);
+                tc_mma2_bf16(d, a, b, idesc, ks > 0);
             }
             if (!KEYS_AS_B) {
                 // one more K-step adds each query row's bias to its column:
                 // ones (keys) x the row's bias / cs split into bf16 terms
-                tc_mma_bf16(d, sw32_kmajor_desc(smem_u32(s.aug_k)),
-                            sw32_kmajor_desc(smem_u32(s.aug_q + (size_t)jb * kCols * 32)), idesc, 1u);
+                tc_mma2_bf16(d, sw32_kmajor_desc(smem_u32(s.aug_k)),
+                             sw32_kmajor_desc(smem_u32(s.aug_q + (size_t)jb * 128 * 32)), idesc, 1u);
             }
-            tc_commit(&s.t_full[slot]);
+            tc_commit2(&s.t_full[slot], kBoth);
         }
         if (!ok) break;
-        tc_commit(&s.empty[stage]);
-        if (last) tc_commit(s.q_empty);
-        if (last && !KEYS_AS_B) tc_commit(s.aug_empty);
+        tc_commit2(&s.empty[stage], kBoth);
+        if (last) tc_commit2(s.q_empty, kBoth);
+        if (last && !KEYS_AS_B) tc_commit2(s.aug_empty, kBoth);
         if (++stage == p.stages) {
             stage = 0;
             phase ^= 1;
@@ -287,22 +365,30 @@ __device__ void mma_issuer(const Smem &s, const TcParams &p, uint32_t tmem, int6
     mma_drain(s);
 }
 
-// Release a TMEM slot once this warp's loads from it have completed.
-__device__ __forceinline__ void release_slot(uint64_t *bar, int lane) {
+// Release a TMEM slot (on the even CTA's barrier) once this warp's loads
+// from it have completed.
+__device__ __forceinline__ void release_slot(uint32_t r_bar, int lane) {
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
+    if (lane == 0) mbar_arrive_remote(r_bar);
 }
 
-// 64 consecutive fp32 columns of this thread's TMEM lane -> v, completed.
-__device__ __forceinline__ void load_row64(uint32_t taddr, float (&v)[2][32]) {
-    tmem_ld32(taddr + 0, v[0]);
-    tmem_ld32(taddr + 32, v[1]);
+// 32 NC consecutive fp32 columns of this thread's TMEM lane -> v, completed
+// (all loads in flight, one wait): the warp's whole share of a slot, so the
+// slot can be released before any arithmetic.
+template <int NC>
+__device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[NC][32]) {
+#pragma unroll
+    for (int i = 0; i < NC; ++i) tmem_ld32(taddr + 32 * i, v[i]);
     tmem_ld_wait();
-    reg_fence(v[0]);
-    reg_fence(v[1]);
+#pragma unroll
+    for (int i = 0; i < NC; ++i) reg_fence(v[i]);
 }
-
+// The 64-column piece h of a row.
+template <int NC>
+__device__ __forceinline__ float (&piece64(float (&v)[NC][32], int h))[2][32] {
+    return *reinterpret_cast<float(*)[2][32]>(&v[2 * h]);
+}
 // Fold 64 logits (-inf = not visible) into a row's online (max, sum) in base
 // 2, with eight independent max and sum chains.
 __device__ __forceinline__ void row_stats64(const float (&v)[2][32], float cs, float &m_run,
@@ -395,75 +481,103 @@ __device__ __forceinline__ void mask_cols(float (&v)[32], int &w, int dj, int W)
     }
 }
 
+// Combine two (max, sum) folds of the same row: l * 2^m is the sum either way.
+__device__ __forceinline__ void fold_pair(float &m, float &l, float2 o) {
+    if (o.x == -INFINITY) return;
+    if (m == -INFINITY) {
+        m = o.x;
+        l = o.y;
+        return;
+    }
+    const float mn = fmaxf(m, o.x);
+    l = l * ex2(m - mn) + o.y * ex2(o.x - mn);
+    m = mn;
+}
+
 // --------------------------------------------------------------- pass 1
-template <int KH>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KH, int EWG>
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
     score_stats_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve<KH>(smem_raw, p);
-    const uint32_t tmem = setup(s, p, 4);   // a slot is read by one warpgroup
+    const uint32_t tmem = setup<EWG>(s, p);
+    constexpr int kCols = wg_cols(EWG);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c = blockIdx.x;
-    const int64_t t0 = split_begin(p.n_tiles, p.grid, c), t1 = split_begin(p.n_tiles, p.grid, c + 1);
-    const int nrb = p.rows_pad / 128;
+    const int rank = (int)cluster_ctarank();
+    const int64_t c = cluster_id_x();
+    const int64_t t0 = split_begin(p.n_tiles, p.pairs, c), t1 = split_begin(p.n_tiles, p.pairs, c + 1);
+    const int njob = p.rows_pad / 256;
 
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
-            producer<KH>(s, p, &tq, &tk, t0, t1);
+            producer<KH>(s, p, &tq, &tk, t0, t1, rank);
         }
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer<KH, true>(s, p, tmem, t0, t1, nrb);
+        if (lane == 0) {
+            if (rank == 0)
+                mma_issuer<KH, true>(s, p, tmem, t0, t1, njob);
+            else
+                relay(s, p, t0, t1);
+        }
     } else {
-        // Epilogue.  Warpgroup ewg owns the row blocks rb with rb % 2 == ewg;
-        // a warp's TMEM lane quarter is fixed by its id % 4, so each thread
-        // owns one query row per row block (two at most: m0/l0, m1/l1).
+        // Epilogue.  Warpgroup ewg reads key columns [kCols ewg, +kCols)
+        // of every job; a warp's TMEM lane quarter is fixed by its id % 4, so
+        // each thread owns query row 256 b + 128 rank + 32 quarter + lane of
+        // job b (two at most: m0/l0, m1/l1) over its share of the tile's
+        // keys.  The warpgroups' folds of a row are combined when the unit
+        // ends, in warpgroup order.
         const int quarter = warp & 3;
         const int ewg = (warp - 2) >> 2;
         const int row_in_blk = quarter * 32 + lane;
+        const uint32_t r_tempty = mapa_shared(smem_u32(s.t_empty), 0);
         float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-        uint32_t job = 0;
+        // window positions w = r % W of this thread's two rows
+        const int w0 = (rank * 128 + row_in_blk) % p.W, w1 = (256 + rank * 128 + row_in_blk) % p.W;
+        uint32_t job = 0, unit_ends = 0;
         bool ok = true;
-        for (int64_t t = t0; t < t1 && ok; ++t) {
-            const int u = (int)(t / p.tiles_per_unit);
-            const int jt = (int)(t % p.tiles_per_unit);
-            const int j0 = jt * kTileKeys;
+        Step st(t0, p.tiles_per_unit);
+        for (int64_t t = t0; t < t1 && ok; ++t, st.next()) {
+            const int u = st.u, jt = st.jt;
+            const int j0 = jt * kPairKeys + ewg * kCols;   // this warpgroup's first key
             const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
             if (t == t0 || jt == 0) {
                 m0 = m1 = -INFINITY;
                 l0 = l1 = 0.f;
             }
-            const bool masked = j0 + kTileKeys - 1 > p.P;
+            const bool masked = j0 + kCols - 1 > p.P;
 #pragma unroll 1
-            for (int rb = ewg; rb < nrb; rb += 2) {
-                const uint32_t jj = job + rb;
-                const uint32_t slot = jj & 3, use = jj >> 2;
+            for (int b = 0; b < njob; ++b) {
+                const uint32_t jj = job + b;
+                const uint32_t slot = jj & 1, use = jj >> 1;
                 if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 128;
-                const int r = rb * 128 + row_in_blk;
-                // Largest column of this tile that row r may see.
-                const int lim = masked ? p.P + (r % p.W) - j0 : kTileKeys - 1;
-                float m = (rb >> 1) ? m1 : m0;
-                float l = (rb >> 1) ? l1 : l0;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[2][32];
-                    load_row64(taddr + h * 64, v);
-                    if (h == 1) release_slot(&s.t_empty[slot], lane);   // values are in registers
-                    if (masked) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (h * 64 + i > lim) v[i >> 5][i & 31] = -INFINITY;
-                    }
-                    row_stats64_lazy(v, p.cs, m, l);
+                if (b * 256 + rank * 128 >= p.rows) {   // this CTA's rows of the job are padding
+                    release_slot(r_tempty + slot * 8u, lane);
+                    continue;
                 }
-                if (rb >> 1) {
+                const uint32_t taddr =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + ewg * kCols;
+                // Largest column of this warpgroup's share that row r may see.
+                const int lim = masked ? p.P + (b ? w1 : w0) - j0 : kCols - 1;
+                float m = b ? m1 : m0;
+                float l = b ? l1 : l0;
+                float v[kCols / 32][32];
+                load_cols(taddr, v);
+                release_slot(r_tempty + slot * 8u, lane);   // values are in registers
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i)
+                        if (i > lim) v[i >> 5][i & 31] = -INFINITY;
+                }
+#pragma unroll
+                for (int h = 0; h < kCols / 64; ++h) row_stats64_lazy(piece64(v, h), p.cs, m, l);
+                if (b) {
                     m1 = m;
                     l1 = l;
                 } else {
@@ -471,70 +585,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l0 = l;
                 }
             }
-            job += nrb;
+            job += njob;
             if (!ok) break;
             if (last) {
-                const int64_t slot_u = c - split_cta_of(p.n_tiles, p.grid, (int64_t)u * p.tiles_per_unit);
-                float2 *dst = p.partial + ((int64_t)u * p.max_slots + slot_u) * p.rows_pad;
-                for (int rb = ewg; rb < nrb; rb += 2) {
-                    const int r = rb * 128 + row_in_blk;
-                    if (r < p.rows) dst[r] = (rb >> 1) ? make_float2(m1, l1) : make_float2(m0, l0);
+                const uint32_t ue = unit_ends++;
+                if (ewg > 0) {
+                    if (!mbar_wait(&s.c_empty[0], (ue & 1) ^ 1, s.abort_flag, p.status)) break;
+                    float2 *dst = s.red + (ewg - 1) * 256;
+                    dst[row_in_blk] = make_float2(m0, l0);
+                    dst[128 + row_in_blk] = make_float2(m1, l1);
+                    mbar_arrive(&s.c_full[0]);
+                } else {
+                    if (!mbar_wait(&s.c_full[0], ue & 1, s.abort_flag, p.status)) break;
+#pragma unroll
+                    for (int e = 0; e < EWG - 1; ++e) {
+                        fold_pair(m0, l0, s.red[e * 256 + row_in_blk]);
+                        fold_pair(m1, l1, s.red[e * 256 + 128 + row_in_blk]);
+                    }
+                    mbar_arrive(&s.c_empty[0]);
+                    const int64_t slot_u =
+                        c - split_cta_of(p.n_tiles, p.pairs, (int64_t)u * p.tiles_per_unit);
+                    float2 *dst = p.partial + ((int64_t)u * p.max_slots + slot_u) * p.rows_pad;
+                    for (int b = 0; b < njob; ++b) {
+                        const int r = b * 256 + rank * 128 + row_in_blk;
+                        if (r < p.rows) dst[r] = b ? make_float2(m1, l1) : make_float2(m0, l0);
+                    }
                 }
             }
         }
     }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
+    teardown(tmem);
 }
 
 // --------------------------------------------------------------- pass 2
-template <int KH>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KH, int EWG>
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
     score_colmean_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve<KH>(smem_raw, p);
-    const uint32_t tmem = setup(s, p, 8);   // both warpgroups read every slot
+    const uint32_t tmem = setup<EWG>(s, p);
+    constexpr int kCols = wg_cols(EWG);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c = blockIdx.x;
-    const int64_t t0 = split_begin(p.n_tiles, p.grid, c), t1 = split_begin(p.n_tiles, p.grid, c + 1);
-    const int nch = (p.n_pad + 255) / 256;   // query-row chunks of up to 256 (MMA N)
+    const int rank = (int)cluster_ctarank();
+    const int64_t c = cluster_id_x();
+    const int64_t t0 = split_begin(p.n_tiles, p.pairs, c), t1 = split_begin(p.n_tiles, p.pairs, c + 1);
+    const int njob = p.rows_pad / 256;
 
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
-            producer<KH>(s, p, &tq, &tk, t0, t1);
+            producer<KH>(s, p, &tq, &tk, t0, t1, rank);
         }
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer<KH, false>(s, p, tmem, t0, t1, nch);
+        if (lane == 0) {
+            if (rank == 0)
+                mma_issuer<KH, false>(s, p, tmem, t0, t1, njob);
+            else
+                relay(s, p, t0, t1);
+        }
     } else {
-        // Epilogue.  Each thread owns one key (its TMEM lane) and sums
-        // 2^(x' * cs) over query rows, x' = q.k + nb_r / cs already in the
-        // accumulator.  Every job (up to 256 rows) is split by columns:
-        // warpgroup e reads columns [128 e, 128 e + 128), so a slot is free
-        // again after two 64-column loads per warp; warpgroup 1 hands its
-        // partial sum to warpgroup 0 through shared memory once per tile.
+        // Epilogue.  Each thread owns one of the CTA's keys (its TMEM lane)
+        // and sums 2^(x' * cs) over query rows, x' = q.k + nb_r / cs already
+        // in the accumulator.  Warpgroup e reads columns [kCols e, +kCols)
+        // of every job (query rows 256 b + kCols e + i); warpgroups 1.. hand
+        // their partial sums to warpgroup 0 through shared memory once per
+        // tile, added in warpgroup order.
         const int quarter = warp & 3;
         const int ewg = (warp - 2) >> 2;
         const int etid = threadIdx.x - 64;
         const int key_in_tile = quarter * 32 + lane;
         const float rows_f = (float)p.rows;
+        const uint32_t r_tempty = mapa_shared(smem_u32(s.t_empty), 0);
+        const uint32_t r_augfull = mapa_shared(smem_u32(s.aug_full), 0);
+        float *red = reinterpret_cast<float *>(s.red);
         uint32_t job = 0, unit_changes = 0;
         bool ok = true;
-        for (int64_t t = t0; t < t1 && ok; ++t) {
-            const int u = (int)(t / p.tiles_per_unit);
-            const int jt = (int)(t % p.tiles_per_unit);
-            const int j0 = jt * kTileKeys;
+        Step st(t0, p.tiles_per_unit);
+        for (int64_t t = t0; t < t1 && ok; ++t, st.next()) {
+            const int u = st.u, jt = st.jt;
+            const int j0 = jt * kPairKeys + rank * 128;   // this CTA's first key
             const uint32_t tl = (uint32_t)(t - t0);
             if (t == t0 || jt == 0) {
-                // The unit's row biases become one more MMA K-step: row r of
-                // aug_q holds nb_r / cs split into three bf16 terms (about 24
+                // The unit's row biases become one more MMA K-step: local row
+                // i of aug_q (query row 256 (i / 128) + 128 rank + i % 128)
+                // holds nb_r / cs split into three bf16 terms (about 24
                 // significant bits) in its first 16 bytes, zeros in the other
                 // 16; every row of aug_k holds ones at the same three places in
                 // both halves, so the product picks the terms up whatever the
@@ -543,12 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (unit_changes == 0) {
                     const __nv_bfloat16 one = __float2bfloat16(1.f), z = __float2bfloat16(0.f);
                     __align__(16) __nv_bfloat16 h8[8] = {one, one, one, z, z, z, z, z};
-                    for (int i = etid; i < 128 * 2; i += kEpi)
+                    for (int i = etid; i < 128 * 2; i += epi_threads(EWG))
                         *reinterpret_cast<uint4 *>(s.aug_k + i * 16) = *reinterpret_cast<const uint4 *>(h8);
                 } else if (!mbar_wait(s.aug_empty, (unit_changes - 1) & 1, s.abort_flag, p.status)) {
                     break;   // the previous unit's MMAs still read aug_q
                 }
-                for (int r = etid; r < p.rows_pad; r += kEpi) {
+                for (int i = etid; i < p.rows_half; i += epi_threads(EWG)) {
+                    const int r = (i >> 7) * 256 + rank * 128 + (i & 127);
                     const float nb = p.neg_bias_in[(int64_t)u * p.rows_pad + r];
                     const float v = (r < p.rows && nb > -3.0e4f * p.cs) ? nb / p.cs : -3.0e4f;
                     const __nv_bfloat16 hi = __float2bfloat16(v);
@@ -557,22 +694,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __nv_bfloat16 lo = __float2bfloat16(r1 - __bfloat162float(mid));
                     const __nv_bfloat16 z = __float2bfloat16(0.f);
                     __align__(16) __nv_bfloat16 h8[8] = {hi, mid, lo, z, z, z, z, z};
-                    uint4 *dst = reinterpret_cast<uint4 *>(s.aug_q + (size_t)r * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(s.aug_q + (size_t)i * 32);
                     dst[0] = *reinterpret_cast<const uint4 *>(h8);
                     dst[1] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMA
-                mbar_arrive(s.aug_full);
+                mbar_arrive_remote_cluster(r_augfull);
                 ++unit_changes;
             }
             const int j = j0 + key_in_tile;
             const int dj = j - p.P;   // row r = g*W + w sees key j iff w >= dj
-            const bool masked = j0 + kTileKeys - 1 > p.P;
+            const bool masked = j0 + 127 > p.P;   // this CTA's 128 keys reach the window
             float a8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) a8[i] = 0.f;
 #pragma unroll 1
-            for (int nc = 0; nc < nch; ++nc) {
+            for (int nc = 0; nc < njob; ++nc) {
                 const uint32_t jj = job + nc;
                 const uint32_t slot = jj & 1, use = jj >> 1;
                 if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
@@ -580,58 +717,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int n = min(256, p.n_pad - nc * 256);
-                const int c0 = ewg * 128;
-                const int cn = min(128, n - c0);   // this warpgroup's columns (may be none)
+                const int n = min(256, p.rows - nc * 256);   // real query rows of this job
+                const int c0 = ewg * kCols;
+                const int cn = min(kCols, n - c0);   // this warpgroup's columns (may be none)
                 if (cn <= 0) {
-                    release_slot(&s.t_empty[slot], lane);
+                    release_slot(r_tempty + slot * 8u, lane);
                     continue;
                 }
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + slot * 256 + c0;
-                const int nh = (cn + 63) / 64;
-#pragma unroll 1
-                for (int h = 0; h < nh; ++h) {
-                    float v[2][32];
-                    load_row64(taddr + h * 64, v);
-                    if (h == nh - 1) release_slot(&s.t_empty[slot], lane);
-                    const int valid = cn - h * 64;   // narrow last chunk: 16..48 columns
-                    if (valid < 64) {
+                const uint32_t taddr =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + c0;
+                float v[kCols / 32][32];
+                load_cols(taddr, v);
+                release_slot(r_tempty + slot * 8u, lane);   // values are in registers
+                if (cn < kCols) {   // narrow last job: columns past the real rows
 #pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (i >= valid) v[i >> 5][i & 31] = -INFINITY;
-                    }
-                    if (masked) {
-                        int w = (nc * 256 + c0 + h * 64) % p.W;
-                        mask_cols(v[0], w, dj, p.W);
-                        mask_cols(v[1], w, dj, p.W);
-                    }
-                    col_sums64(v, p.cs, a8);
+                    for (int i = 0; i < kCols; ++i)
+                        if (i >= cn) v[i >> 5][i & 31] = -INFINITY;
                 }
+                if (masked) {
+                    int w = (nc * 256 + c0) % p.W;
+#pragma unroll
+                    for (int q = 0; q < kCols / 32; ++q) mask_cols(v[q], w, dj, p.W);
+                }
+#pragma unroll
+                for (int h = 0; h < kCols / 64; ++h)
+                    if (cn > 64 * h) col_sums64(piece64(v, h), p.cs, a8);
             }
-            job += nch;
+            job += njob;
             if (!ok) break;
             float acc = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
             const uint32_t b = tl & 1, ub = tl >> 1;
-            float *red = s.red + b * 128;
-            if (ewg == 1) {
+            float *rb = red + b * (EWG - 1) * 128;
+            if (ewg > 0) {
                 if (!mbar_wait(&s.c_empty[b], (ub & 1) ^ 1, s.abort_flag, p.status)) break;
-                red[key_in_tile] = acc;
+                rb[(ewg - 1) * 128 + key_in_tile] = acc;
                 mbar_arrive(&s.c_full[b]);
             } else {
                 if (!mbar_wait(&s.c_full[b], ub & 1, s.abort_flag, p.status)) break;
-                acc += red[key_in_tile];
+#pragma unroll
+                for (int e = 0; e < EWG - 1; ++e) acc += rb[e * 128 + key_in_tile];
                 mbar_arrive(&s.c_empty[b]);
                 if (j < p.T) p.scores[(int64_t)u * p.T + j] = acc / rows_f;
             }
         }
     }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
+    teardown(tmem);
 }
 
 // --------------------------------------------------------------- host side
@@ -649,6 +779,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 3-D bf16 view [outer][mid][inner] with a (64, 128, 1) box, 128-byte swizzle.
+// Rows past `mid` read as zeros.
 bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer) {
     auto enc = get_encode();
     if (!enc) return false;
@@ -662,6 +793,28 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, ui
     return r == CUDA_SUCCESS;
 }
 
+constexpr size_t kSmemLimit = 232448;   // 227 KiB per CTA
+
+template <int KH>
+int pick_stages(int rows_pad) {
+    // Deepest K ring that fits next to the resident Q rows.
+    int stages = 4;
+    while (stages > 2 && smem_bytes<KH>(rows_pad, stages) > kSmemLimit) --stages;
+    return stages;
+}
+
+template <int KH>
+void set_smem_attr() {
+    static bool done = false;
+    if (!done) {
+        cudaFuncSetAttribute(score_stats_tc<KH, kEWG1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemLimit);
+        cudaFuncSetAttribute(score_colmean_tc<KH, kEWG2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemLimit);
+        done = true;
+    }
+}
+
 template <int KH>
 int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st) {
     const int G = s.n_q_heads / s.n_kv_heads;
@@ -671,35 +824,31 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
         set_error("kvc_score: cuTensorMapEncodeTiled failed (alignment or driver)");
         return KVC_ERR_CUDA;
     }
+    if (sp.rows_pad % 256 || sp.rows_pad > kMaxRowsTC) {
+        set_error("kvc_score: tensor-core split needs rows padded to 256 (got %d)", sp.rows_pad);
+        return KVC_ERR_UNSUPPORTED;
+    }
     TcParams p;
     p.n_tiles = sp.n_tiles;
     p.tiles_per_unit = sp.tiles_per_unit;
-    p.grid = sp.grid;
+    p.pairs = sp.grid;
     p.max_slots = sp.max_slots;
     p.T = s.seq_len;
     p.W = s.window;
     p.P = s.seq_len - s.window;
     p.rows = sp.rows;
     p.rows_pad = sp.rows_pad;
-    p.n_pad = (sp.rows + 15) / 16 * 16;
+    p.rows_half = sp.rows_pad / 2;
     p.cs = (float)(kLog2e / sqrt((double)s.head_dim));
     p.partial = a.partial;
     p.neg_bias_in = a.neg_bias;
     p.scores = a.scores;
     p.status = a.status;
-    // Deepest K ring that fits next to the resident Q block.
-    int stages = 4;
-    while (stages > 2 && smem_bytes<KH>(sp.rows_pad, stages) > 232448) --stages;
-    p.stages = stages;
-    const size_t smem = smem_bytes<KH>(sp.rows_pad, stages);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(score_stats_tc<KH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        cudaFuncSetAttribute(score_colmean_tc<KH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             232448);
-        attr_set = true;
-    }
-    score_stats_tc<KH><<<sp.grid, kThreads, smem, st>>>(tq, tk, p);
+    p.stages = pick_stages<KH>(sp.rows_pad);
+    const size_t smem = smem_bytes<KH>(sp.rows_pad, p.stages);
+    set_smem_attr<KH>();
+    const int ctas = 2 * sp.grid;   // one 2-CTA cluster per pair
+    score_stats_tc<KH, kEWG1><<<ctas, cta_threads(kEWG1), smem, st>>>(tq, tk, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_score: pass-1 launch failed: %s", cudaGetErrorString(e));
@@ -707,7 +856,7 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
     }
     int rc = launch_score_merge(s, sp, a, st);
     if (rc) return rc;
-    score_colmean_tc<KH><<<sp.grid, kThreads, smem, st>>>(tq, tk, p);
+    score_colmean_tc<KH, kEWG2><<<ctas, cta_threads(kEWG2), smem, st>>>(tq, tk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_score: pass-2 launch failed: %s", cudaGetErrorString(e));
@@ -718,9 +867,37 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
 
 }  // namespace
 
-int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, int num_sms,
-                    cudaStream_t st) {
-    (void)num_sms;
+int score_tc_pairs(int sms) {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev] = {0};
+    int dev = 0;
+    const int fallback = (sms > 0 ? sms : 148) / 2;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        cudaGetLastError();
+        return fallback;
+    }
+    if (cached[dev]) return cached[dev];
+    // Clusters of the largest configuration (head_dim 128, 512 rows) that
+    // the device keeps resident at once: a persistent grid larger than that
+    // would run its last pairs in a second wave.
+    int n = fallback;
+    set_smem_attr<2>();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * fallback, 1, 1);
+    cfg.blockDim = dim3(cta_threads(kEWG1), 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<2>(kMaxRowsTC, pick_stages<2>(kMaxRowsTC));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, score_stats_tc<2, kEWG1>, &cfg) == cudaSuccess &&
+        clusters > 0) {
+        if (clusters < n) n = clusters;
+    } else {
+        cudaGetLastError();
+    }
+    cached[dev] = n;
+    return n;
+}
+
+int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st) {
     if (s.head_dim == 128) return launch_kh<2>(s, sp, a, st);
     if (s.head_dim == 64) return launch_kh<1>(s, sp, a, st);
     set_error("kvc_score: tensor-core path needs head_dim 64 or 128");
