@@ -37,10 +37,12 @@
 // b mod 2).  Warp roles in each CTA: warp 0 TMA producer (its own K half and
 // Q rows), warp 1 MMA issuer in the even CTA and, in the odd CTA, a relay
 // that forwards each completed load to the even CTA's barriers; the other
-// warps are the epilogue, in EWG warpgroups (four in pass 1, two in pass 2),
-// each reading 256 / EWG columns of every job.  A warp loads its columns at
-// once and frees the slot before any arithmetic, so the next job's MMAs do
-// not wait on the exponentials.  Each thread keeps independent sum chains on
+// warps are the epilogue.  Pass 1 has four warpgroups, two per job of a tile,
+// each folding 128 of the job's 256 key columns in two 64-column pieces (one
+// job per warp and tile: the per-job waits, loads and bookkeeping are paid
+// half as often as with every warpgroup reading every job).  Pass 2 has two
+// warpgroups, each reading 128 columns of every job at once and freeing the
+// slot before any arithmetic.  Each thread keeps independent sum chains on
 // packed fp32 pairs; the window's causal mask sets invisible logits to -inf.  Measured on this GPU, shared-memory loads in the
 // epilogue compete with the MMAs' shared-memory operand reads, which is why
 // pass 2 takes the row biases through the MMA; and every instruction per
@@ -59,7 +61,8 @@ namespace {
 
 // Epilogue warpgroups per pass.  More warps hide more of the exponentials'
 // latency, fewer carry less per-job overhead: pass 1 (a fold per row with a
-// compare per piece) gains from four, pass 2 (a plain sum) runs best on two.
+// compare per piece) gains from four, pass 2 (a plain sum) runs best on two
+// (measured on the 32K workload: four warpgroups there cost 4%).
 constexpr int kEWG1 = 4, kEWG2 = 2;
 constexpr int kMaxEWG = 4;
 __host__ __device__ constexpr int wg_cols(int ewg) { return 256 / ewg; }   // columns per warpgroup
@@ -171,7 +174,8 @@ struct Step {
 
 // Barrier set-up and TMEM allocation in both CTAs; returns the TMEM base.
 template <int EWG>
-__device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p) {
+__device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p, uint32_t t_empty_count,
+                                          uint32_t c_full_count) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -184,8 +188,8 @@ __device__ __forceinline__ uint32_t setup(const Smem &s, const TcParams &p) {
         mbar_init(s.q_pfull, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.t_full[i], 1);
-            mbar_init(&s.t_empty[i], 2 * 4 * EWG);   // epilogue warps of both CTAs
-            mbar_init(&s.c_full[i], (EWG - 1) * 128);
+            mbar_init(&s.t_empty[i], t_empty_count);   // epilogue warps of both CTAs
+            mbar_init(&s.c_full[i], c_full_count);
             mbar_init(&s.c_empty[i], 128);
         }
         mbar_init(s.aug_full, 2 * epi_threads(EWG));
@@ -501,13 +505,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                    TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve<KH>(smem_raw, p);
-    const uint32_t tmem = setup<EWG>(s, p);
-    constexpr int kCols = wg_cols(EWG);
+    const int njob = p.rows_pad / 256;
+    const int wpj = EWG / njob;   // epilogue warpgroups per job
+    // a slot is read by the job's warpgroups in both CTAs; the other
+    // warpgroups of a job hand their folds to its first one
+    const uint32_t tmem = setup<EWG>(s, p, 2u * 4u * wpj, (uint32_t)(wpj - 1) * 128u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)cluster_ctarank();
     const int64_t c = cluster_id_x();
     const int64_t t0 = split_begin(p.n_tiles, p.pairs, c), t1 = split_begin(p.n_tiles, p.pairs, c + 1);
-    const int njob = p.rows_pad / 256;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -523,93 +529,78 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                 relay(s, p, t0, t1);
         }
     } else {
-        // Epilogue.  Warpgroup ewg reads key columns [kCols ewg, +kCols)
-        // of every job; a warp's TMEM lane quarter is fixed by its id % 4, so
-        // each thread owns query row 256 b + 128 rank + 32 quarter + lane of
-        // job b (two at most: m0/l0, m1/l1) over its share of the tile's
-        // keys.  The warpgroups' folds of a row are combined when the unit
-        // ends, in warpgroup order.
+        // Epilogue.  The warpgroups are split between the tile's jobs: wpj =
+        // EWG / njob of them read job my_job, warpgroup sub of those the key
+        // columns [cols sub, +cols) in 64-column pieces.  A warp's TMEM lane
+        // quarter is fixed by its id % 4, so each thread owns query row
+        // 256 my_job + 128 rank + 32 quarter + lane over its share of the
+        // tile's keys; the shares of a row are combined when the unit ends,
+        // in warpgroup order.
         const int quarter = warp & 3;
         const int ewg = (warp - 2) >> 2;
         const int row_in_blk = quarter * 32 + lane;
+        const int my_job = ewg / wpj, sub = ewg % wpj;
+        const int cols = kPairKeys / wpj, npc = cols / 64;
+        const int r = my_job * 256 + rank * 128 + row_in_blk;
+        const bool pad = my_job * 256 + rank * 128 >= p.rows;   // this CTA's rows of the job
+        const int w_r = r % p.W;                                 // window position of row r
         const uint32_t r_tempty = mapa_shared(smem_u32(s.t_empty), 0);
-        float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-        // window positions w = r % W of this thread's two rows
-        const int w0 = (rank * 128 + row_in_blk) % p.W, w1 = (256 + rank * 128 + row_in_blk) % p.W;
+        float m = -INFINITY, l = 0.f;
         uint32_t job = 0, unit_ends = 0;
         bool ok = true;
         Step st(t0, p.tiles_per_unit);
         for (int64_t t = t0; t < t1 && ok; ++t, st.next()) {
             const int u = st.u, jt = st.jt;
-            const int j0 = jt * kPairKeys + ewg * kCols;   // this warpgroup's first key
+            const int j0 = jt * kPairKeys + sub * cols;   // this warpgroup's first key
             const bool last = (t == t1 - 1) || (jt == p.tiles_per_unit - 1);
             if (t == t0 || jt == 0) {
-                m0 = m1 = -INFINITY;
-                l0 = l1 = 0.f;
+                m = -INFINITY;
+                l = 0.f;
             }
-            const bool masked = j0 + kCols - 1 > p.P;
-#pragma unroll 1
-            for (int b = 0; b < njob; ++b) {
-                const uint32_t jj = job + b;
-                const uint32_t slot = jj & 1, use = jj >> 1;
-                if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (b * 256 + rank * 128 >= p.rows) {   // this CTA's rows of the job are padding
-                    release_slot(r_tempty + slot * 8u, lane);
-                    continue;
-                }
-                const uint32_t taddr =
-                    tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + ewg * kCols;
-                // Largest column of this warpgroup's share that row r may see.
-                const int lim = masked ? p.P + (b ? w1 : w0) - j0 : kCols - 1;
-                float m = b ? m1 : m0;
-                float l = b ? l1 : l0;
-                float v[kCols / 32][32];
-                load_cols(taddr, v);
-                release_slot(r_tempty + slot * 8u, lane);   // values are in registers
-                if (masked) {
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i)
-                        if (i > lim) v[i >> 5][i & 31] = -INFINITY;
-                }
-#pragma unroll
-                for (int h = 0; h < kCols / 64; ++h) row_stats64_lazy(piece64(v, h), p.cs, m, l);
-                if (b) {
-                    m1 = m;
-                    l1 = l;
-                } else {
-                    m0 = m;
-                    l0 = l;
-                }
-            }
+            const bool masked = j0 + cols - 1 > p.P;
+            const uint32_t jj = job + my_job;
+            const uint32_t slot = jj & 1, use = jj >> 1;
             job += njob;
-            if (!ok) break;
+            if (!mbar_wait(&s.t_full[slot], use & 1, s.abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + sub * cols;
+            if (pad) {
+                release_slot(r_tempty + slot * 8u, lane);
+            } else {
+                // Largest column of this warpgroup's share that row r may see.
+                const int lim = masked ? p.P + w_r - j0 : cols - 1;
+#pragma unroll 1
+                for (int h = 0; h < npc; ++h) {
+                    float v[2][32];
+                    load_cols(taddr + h * 64, v);
+                    if (h == npc - 1) release_slot(r_tempty + slot * 8u, lane);
+                    if (masked) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (h * 64 + i > lim) v[i >> 5][i & 31] = -INFINITY;
+                    }
+                    row_stats64_lazy(v, p.cs, m, l);
+                }
+            }
             if (last) {
                 const uint32_t ue = unit_ends++;
-                if (ewg > 0) {
-                    if (!mbar_wait(&s.c_empty[0], (ue & 1) ^ 1, s.abort_flag, p.status)) break;
-                    float2 *dst = s.red + (ewg - 1) * 256;
-                    dst[row_in_blk] = make_float2(m0, l0);
-                    dst[128 + row_in_blk] = make_float2(m1, l1);
-                    mbar_arrive(&s.c_full[0]);
+                float2 *red = s.red + my_job * (kMaxEWG - 1) * 128;
+                if (sub > 0) {
+                    if (!mbar_wait(&s.c_empty[my_job], (ue & 1) ^ 1, s.abort_flag, p.status)) break;
+                    red[(sub - 1) * 128 + row_in_blk] = make_float2(m, l);
+                    mbar_arrive(&s.c_full[my_job]);
                 } else {
-                    if (!mbar_wait(&s.c_full[0], ue & 1, s.abort_flag, p.status)) break;
-#pragma unroll
-                    for (int e = 0; e < EWG - 1; ++e) {
-                        fold_pair(m0, l0, s.red[e * 256 + row_in_blk]);
-                        fold_pair(m1, l1, s.red[e * 256 + 128 + row_in_blk]);
-                    }
-                    mbar_arrive(&s.c_empty[0]);
+                    if (!mbar_wait(&s.c_full[my_job], ue & 1, s.abort_flag, p.status)) break;
+                    for (int e = 1; e < wpj; ++e) fold_pair(m, l, red[(e - 1) * 128 + row_in_blk]);
+                    mbar_arrive(&s.c_empty[my_job]);
                     const int64_t slot_u =
                         c - split_cta_of(p.n_tiles, p.pairs, (int64_t)u * p.tiles_per_unit);
                     float2 *dst = p.partial + ((int64_t)u * p.max_slots + slot_u) * p.rows_pad;
-                    for (int b = 0; b < njob; ++b) {
-                        const int r = b * 256 + rank * 128 + row_in_blk;
-                        if (r < p.rows) dst[r] = b ? make_float2(m1, l1) : make_float2(m0, l0);
-                    }
+                    if (r < p.rows) dst[r] = make_float2(m, l);
                 }
             }
         }
@@ -624,7 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                      TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve<KH>(smem_raw, p);
-    const uint32_t tmem = setup<EWG>(s, p);
+    const uint32_t tmem = setup<EWG>(s, p, 2u * 4u * EWG, (uint32_t)(EWG - 1) * 128u);
     constexpr int kCols = wg_cols(EWG);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)cluster_ctarank();
