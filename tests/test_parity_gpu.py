@@ -130,6 +130,12 @@ SMALL = {
     "tc_rows256_think": (wk.ZIGZAG_32K.scaled(
         n_layers=2, n_kv_heads=2, n_q_heads=8, seq_len=4100, window=64,
         total_budget=2 * 820, layer_floor=102, temperature=None), 0.4, 34),
+    # 384 window rows: the second 256-row job of a tile is half padding (the
+    # odd CTA's rows), so pass 1 skips that CTA's share and pass 2 has a
+    # warpgroup with no real columns; T = 2000 leaves a ragged last tile
+    "tc_rows384_pad_job": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=2, n_q_heads=8, seq_len=2000, window=96,
+        total_budget=2 * 380, layer_floor=30, temperature=(0.5, 2.0)), None, 37),
     "tiny_mha_f32": (wk.TINY, None, wk.seed_for(0)),
     "simt_odd_dim": (wk.ZIGZAG_32K.scaled(
         n_layers=2, n_kv_heads=2, n_q_heads=4, head_dim=80, seq_len=333, window=8,
