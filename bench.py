@@ -184,6 +184,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# Lane operations of one Keyformer draw: Philox4x32-10 is 10 rounds of two
+# 32x32 -> 64-bit multiplies (high and low halves: 4 operations), 4 XORs and
+# 2 key additions (100); the 24-bit uniform, two logarithms and the scaling
+# add about 10.
+KEYFORMER_OPS_PER_DRAW = 110
+
+
+def keyformer_draws(wl):
+    """Visible logits of one pass: window row w sees keys 0 .. T-W+w."""
+    G = wl.n_q_heads // wl.n_kv_heads
+    P = wl.seq_len - wl.window
+    per_unit = G * (wl.window * (P + 1) + wl.window * (wl.window - 1) // 2)
+    return wl.n_layers * wl.n_kv_heads * per_unit
+
+
 def traffic_for(kernel_src, workload):
     """DRAM bytes per launch recorded by an ncu capture of this exact kernel
     source on this workload (profiles/score_traffic.txt); None if absent,
@@ -388,15 +403,21 @@ def run_kvc(args):
                 "ms_per_launch": round(score_ms, 4), "flops_per_launch": flops,
                 "peak_source": f"{pk_src} bf16_tflops_sustained"}
         if args.score == "keyformer":
-            # CUDA-core fp32 kernels: FFMA peak = SMs x 128 lanes x 2 flop x max SM clock
+            # The contraction runs on the tensor cores; the bound is the noise:
+            # one Philox4x32-10 draw and two logarithms per visible logit and
+            # pass, KEYFORMER_OPS_PER_DRAW 32-bit lane operations, against one
+            # lane operation per FP32/INT32 lane and clock.
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            peak = sms * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-            roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                    "kernel": "kvc_score_keyformer (stats + merge + column-mean launches, fp32 "
-                              "FFMA, Philox + Gumbel per logit not counted)",
-                    "ms_per_launch": round(score_ms, 4), "flops_per_launch": flops,
-                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+            peak = sms * 128 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            ops = 2 * keyformer_draws(wl) * KEYFORMER_OPS_PER_DRAW
+            ach_ops = ops / (score_ms / 1e3) / 1e12
+            roof = {"bound": "alu", "achieved": round(ach_ops, 2), "peak": round(peak, 1),
+                    "unit": "Tops/s", "frac": round(ach_ops / peak, 4), "traffic": None,
+                    "kernel": "kvc_score_keyformer (stats + merge + column-mean launches; "
+                              f"{KEYFORMER_OPS_PER_DRAW} lane ops per Gumbel draw, two passes)",
+                    "ms_per_launch": round(score_ms, 4), "ops_per_launch": ops,
+                    "tensor_tflops": round(achieved, 1),
+                    "peak_source": "derived: SMs x 128 lanes x max SM clock"}
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,

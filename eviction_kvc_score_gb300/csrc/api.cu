@@ -285,7 +285,17 @@ int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k
     const kvc_shape &s = *shape;
     const WsLayout w = ws_layout(s);
     if (!ws_ok(ws, ws_bytes, w.total, "kvc_score_keyformer")) return KVC_ERR_WORKSPACE;
-    const ScoreSplit sp = make_split(s, false);
+    const int choice = score_impl_choice();
+    if (choice < 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_score_keyformer: KVC_SCORE_IMPL must be auto, simt or tc");
+    const bool can_tc = tc_eligible(s);
+    if (choice == 2 && !can_tc)
+        return fail(KVC_ERR_UNSUPPORTED, "kvc_score_keyformer: tensor-core path needs bf16, head_dim "
+                                         "64/128, G*W <= 512 and an sm_100-family device");
+    const bool tc = can_tc && choice != 1;
+    if (tc && !aligned16(q_obs)) return fail(KVC_ERR_INVALID_ARG, "kvc_score_keyformer: q_obs must be 16-byte aligned");
+    if (tc && !aligned16(k)) return fail(KVC_ERR_INVALID_ARG, "kvc_score_keyformer: k must be 16-byte aligned");
+    const ScoreSplit sp = make_split(s, tc);
     ScoreArgs a;
     a.q = q_obs;
     a.k = k;
@@ -293,7 +303,8 @@ int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k
     a.partial = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.partial_off);
     a.neg_bias = reinterpret_cast<float *>(static_cast<char *>(ws) + w.bias_off);
     a.status = status_word(ws);
-    return launch_score_keyformer(s, sp, a, seed, tau, stream);
+    return tc ? launch_score_tc_keyformer(s, sp, a, seed, tau, stream)
+              : launch_score_keyformer(s, sp, a, seed, tau, stream);
 }
 
 int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_num, uint32_t mass_den,

@@ -39,43 +39,6 @@ struct SimtParams {
     float noise_scale;
 };
 
-// Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2,
-// 3", SC 2011), word 0 of the output block for counter (c0, c1, c2, 0).
-__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2,
-                                                 uint32_t k0, uint32_t k1) {
-    uint32_t c3 = 0;
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-        c0 = hi1 ^ c1 ^ k0;
-        c1 = lo1;
-        c2 = hi0 ^ c3 ^ k1;
-        c3 = lo0;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-    }
-    return c0;
-}
-
-// Gumbel draw for (unit, row, key): u = (b + 1/2) 2^-24 from the top 24 bits
-// b, zeta = -ln(-ln u).  -ln u is formed from whichever of u and 1 - u is
-// exact in fp32 (log1p near 1), so the rare draws close to 1 -- the large
-// zeta that dominate a row -- come out accurately.
-__device__ __forceinline__ float gumbel(uint32_t unit, uint32_t row, uint32_t key, uint32_t k0,
-                                        uint32_t k1) {
-    const uint32_t b = philox_word0(key, row, unit, k0, k1) >> 8;
-    float nlu;
-    if (b >= (1u << 23)) {
-        const float v = ((float)((1u << 24) - 1u - b) + 0.5f) * 0x1p-24f;   // 1 - u, exact
-        nlu = -log1pf(-v);
-    } else {
-        const float u = ((float)b + 0.5f) * 0x1p-24f;                       // exact
-        nlu = -logf(u);
-    }
-    return -logf(nlu);
-}
-
 // Pass 1: thread = query row; for each 32-key sub-tile held in shared memory
 // the thread forms its 32 logits and folds them into an online (max, sum).
 template <typename T, bool NOISE>

@@ -90,7 +90,9 @@ struct TcParams {
     int rows_pad;   // multiple of 256
     int rows_half;  // rows_pad / 2: query rows held by one CTA
     int stages;
-    float cs;       // log2(e) / sqrt(D)
+    float cs;       // log2(e) / (sqrt(D) tau); tau = 1 without noise
+    float noise_scale;      // log2(e) / tau (Keyformer noise)
+    uint32_t key0, key1;    // Philox key (Keyformer noise)
     float2 *partial;
     const float *neg_bias_in;
     float *scores;
@@ -388,6 +390,21 @@ __device__ __forceinline__ void load_cols(uint32_t taddr, float (&v)[NC][32]) {
 #pragma unroll
     for (int i = 0; i < NC; ++i) reg_fence(v[i]);
 }
+// 8 consecutive fp32 columns -> v, completed.
+__device__ __forceinline__ void load_cols8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+    tmem_ld_wait();
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // The 64-column piece h of a row.
 template <int NC>
 __device__ __forceinline__ float (&piece64(float (&v)[NC][32], int h))[2][32] {
@@ -499,7 +516,7 @@ __device__ __forceinline__ void fold_pair(float &m, float &l, float2 o) {
 }
 
 // --------------------------------------------------------------- pass 1
-template <int KH, int EWG>
+template <int KH, int EWG, bool NOISE>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
     score_stats_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    TcParams p) {
@@ -509,7 +526,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
     const int wpj = EWG / njob;   // epilogue warpgroups per job
     // a slot is read by the job's warpgroups in both CTAs; the other
     // warpgroups of a job hand their folds to its first one
-    const uint32_t tmem = setup<EWG>(s, p, 2u * 4u * wpj, (uint32_t)(wpj - 1) * 128u);
+    const uint32_t tmem =
+        setup<EWG>(s, p, 2u * 4u * wpj, wpj > 1 ? (uint32_t)(wpj - 1) * 128u : 1u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)cluster_ctarank();
     const int64_t c = cluster_id_x();
@@ -570,6 +588,35 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                 tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + sub * cols;
             if (pad) {
                 release_slot(r_tempty + slot * 8u, lane);
+            } else if constexpr (NOISE) {
+                // Keyformer: base-2 noisy logits x cs + zeta log2(e)/tau (the
+                // Gumbel draw of (unit, row, key)), drawn only where the row
+                // sees the key, folded exactly 8 columns at a time
+                const int lim = masked ? p.P + w_r - j0 : cols - 1;
+#pragma unroll 1
+                for (int ch = 0; ch < cols / 8; ++ch) {
+                    float v8[8];
+                    load_cols8(taddr + ch * 8, v8);
+                    if (ch == cols / 8 - 1) release_slot(r_tempty + slot * 8u, lane);
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int col = ch * 8 + i;
+                        v8[i] = col <= lim ? fmaf(gumbel((uint32_t)u, (uint32_t)r, (uint32_t)(j0 + col),
+                                                         p.key0, p.key1),
+                                                  p.noise_scale, v8[i] * p.cs)
+                                           : -INFINITY;
+                        mx = fmaxf(mx, v8[i]);
+                    }
+                    if (mx > -INFINITY) {
+                        const float mnew = fmaxf(m, mx);
+                        float sum = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) sum += ex2(v8[i] - mnew);
+                        l = l * ex2(m - mnew) + sum;
+                        m = mnew;
+                    }
+                }
             } else {
                 // Largest column of this warpgroup's share that row r may see.
                 const int lim = masked ? p.P + w_r - j0 : cols - 1;
@@ -594,9 +641,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                     red[(sub - 1) * 128 + row_in_blk] = make_float2(m, l);
                     mbar_arrive(&s.c_full[my_job]);
                 } else {
-                    if (!mbar_wait(&s.c_full[my_job], ue & 1, s.abort_flag, p.status)) break;
-                    for (int e = 1; e < wpj; ++e) fold_pair(m, l, red[(e - 1) * 128 + row_in_blk]);
-                    mbar_arrive(&s.c_empty[my_job]);
+                    if (wpj > 1) {   // a job with one warpgroup has nothing to combine
+                        if (!mbar_wait(&s.c_full[my_job], ue & 1, s.abort_flag, p.status)) break;
+                        for (int e = 1; e < wpj; ++e)
+                            fold_pair(m, l, red[(e - 1) * 128 + row_in_blk]);
+                        mbar_arrive(&s.c_empty[my_job]);
+                    }
                     const int64_t slot_u =
                         c - split_cta_of(p.n_tiles, p.pairs, (int64_t)u * p.tiles_per_unit);
                     float2 *dst = p.partial + ((int64_t)u * p.max_slots + slot_u) * p.rows_pad;
@@ -609,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
 }
 
 // --------------------------------------------------------------- pass 2
-template <int KH, int EWG>
+template <int KH, int EWG, bool NOISE>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
     score_colmean_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      TcParams p) {
@@ -715,6 +765,30 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                     release_slot(r_tempty + slot * 8u, lane);
                     continue;
                 }
+                if constexpr (NOISE) {
+                    // Keyformer: 2^(x' cs + zeta log2(e)/tau) over the rows
+                    // that see this key, 8 columns at a time
+                    const uint32_t taddr8 =
+                        tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + c0;
+                    const int nch = (cn + 7) / 8;
+#pragma unroll 1
+                    for (int ch = 0; ch < nch; ++ch) {
+                        float v8[8];
+                        load_cols8(taddr8 + ch * 8, v8);
+                        if (ch == nch - 1) release_slot(r_tempty + slot * 8u, lane);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int col = ch * 8 + i;
+                            const int row = nc * 256 + c0 + col;
+                            const bool vis = col < cn && (!masked || row % p.W >= dj);
+                            if (vis)
+                                a8[i] += ex2(fmaf(gumbel((uint32_t)u, (uint32_t)row, (uint32_t)j,
+                                                         p.key0, p.key1),
+                                                  p.noise_scale, v8[i] * p.cs));
+                        }
+                    }
+                    continue;
+                }
                 const uint32_t taddr =
                     tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + c0;
                 float v[kCols / 32][32];
@@ -794,20 +868,31 @@ int pick_stages(int rows_pad) {
     return stages;
 }
 
+// Keyformer's noise makes the epilogue ALU-bound (a Philox draw and two
+// logarithms per logit): four warpgroups in both passes hide the draws'
+// dependency chains better than two (measured 0.77 vs 1.20 ms on one 16K
+// Llama-3-8B-shaped layer).
+constexpr int kEWGNoise = 4;
+
 template <int KH>
 void set_smem_attr() {
     static bool done = false;
     if (!done) {
-        cudaFuncSetAttribute(score_stats_tc<KH, kEWG1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemLimit);
-        cudaFuncSetAttribute(score_colmean_tc<KH, kEWG2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemLimit);
+        cudaFuncSetAttribute(score_stats_tc<KH, kEWG1, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+        cudaFuncSetAttribute(score_colmean_tc<KH, kEWG2, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+        cudaFuncSetAttribute(score_stats_tc<KH, kEWGNoise, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+        cudaFuncSetAttribute(score_colmean_tc<KH, kEWGNoise, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
         done = true;
     }
 }
 
 template <int KH>
-int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st) {
+int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st,
+              bool noise, uint64_t seed, double tau) {
     const int G = s.n_q_heads / s.n_kv_heads;
     CUtensorMap tq, tk;
     if (!make_map(&tq, a.q, (uint64_t)s.head_dim, (uint64_t)G * s.window, (uint64_t)sp.n_units) ||
@@ -830,7 +915,12 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
     p.rows = sp.rows;
     p.rows_pad = sp.rows_pad;
     p.rows_half = sp.rows_pad / 2;
-    p.cs = (float)(kLog2e / sqrt((double)s.head_dim));
+    // Keyformer divides the noisy logits by tau: both the logit scale and
+    // the noise scale carry 1/tau (plain scores: tau = 1, no noise)
+    p.cs = (float)(kLog2e / sqrt((double)s.head_dim) / tau);
+    p.noise_scale = (float)(kLog2e / tau);
+    p.key0 = (uint32_t)seed;
+    p.key1 = (uint32_t)(seed >> 32);
     p.partial = a.partial;
     p.neg_bias_in = a.neg_bias;
     p.scores = a.scores;
@@ -839,7 +929,10 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
     const size_t smem = smem_bytes<KH>(sp.rows_pad, p.stages);
     set_smem_attr<KH>();
     const int ctas = 2 * sp.grid;   // one 2-CTA cluster per pair
-    score_stats_tc<KH, kEWG1><<<ctas, cta_threads(kEWG1), smem, st>>>(tq, tk, p);
+    if (noise)
+        score_stats_tc<KH, kEWGNoise, true><<<ctas, cta_threads(kEWGNoise), smem, st>>>(tq, tk, p);
+    else
+        score_stats_tc<KH, kEWG1, false><<<ctas, cta_threads(kEWG1), smem, st>>>(tq, tk, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_score: pass-1 launch failed: %s", cudaGetErrorString(e));
@@ -847,7 +940,10 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
     }
     int rc = launch_score_merge(s, sp, a, st);
     if (rc) return rc;
-    score_colmean_tc<KH, kEWG2><<<ctas, cta_threads(kEWG2), smem, st>>>(tq, tk, p);
+    if (noise)
+        score_colmean_tc<KH, kEWGNoise, true><<<ctas, cta_threads(kEWGNoise), smem, st>>>(tq, tk, p);
+    else
+        score_colmean_tc<KH, kEWG2, false><<<ctas, cta_threads(kEWG2), smem, st>>>(tq, tk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_score: pass-2 launch failed: %s", cudaGetErrorString(e));
@@ -878,7 +974,8 @@ int score_tc_pairs(int sms) {
     cfg.blockDim = dim3(cta_threads(kEWG1), 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<2>(kMaxRowsTC, pick_stages<2>(kMaxRowsTC));
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, score_stats_tc<2, kEWG1>, &cfg) == cudaSuccess &&
+    if (cudaOccupancyMaxActiveClusters(&clusters, score_stats_tc<2, kEWG1, false>, &cfg) ==
+            cudaSuccess &&
         clusters > 0) {
         if (clusters < n) n = clusters;
     } else {
@@ -889,9 +986,17 @@ int score_tc_pairs(int sms) {
 }
 
 int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st) {
-    if (s.head_dim == 128) return launch_kh<2>(s, sp, a, st);
-    if (s.head_dim == 64) return launch_kh<1>(s, sp, a, st);
+    if (s.head_dim == 128) return launch_kh<2>(s, sp, a, st, false, 0, 1.0);
+    if (s.head_dim == 64) return launch_kh<1>(s, sp, a, st, false, 0, 1.0);
     set_error("kvc_score: tensor-core path needs head_dim 64 or 128");
+    return KVC_ERR_UNSUPPORTED;
+}
+
+int launch_score_tc_keyformer(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
+                              uint64_t seed, double tau, cudaStream_t st) {
+    if (s.head_dim == 128) return launch_kh<2>(s, sp, a, st, true, seed, tau);
+    if (s.head_dim == 64) return launch_kh<1>(s, sp, a, st, true, seed, tau);
+    set_error("kvc_score_keyformer: tensor-core path needs head_dim 64 or 128");
     return KVC_ERR_UNSUPPORTED;
 }
 

@@ -52,6 +52,11 @@ CASES = {
     "f32_mha": (wk.TINY.scaled(n_layers=2, seq_len=600, window=16), 101),
     "bf16_gqa_rows512": (wk.ZIGZAG_32K.scaled(
         n_layers=1, n_kv_heads=2, n_q_heads=8, seq_len=1200, temperature=None), 102),
+    # tensor-core path with one 256-row job per tile (two warpgroups per job
+    # in pass 1), D = 64, ragged last tile
+    "bf16_d64_rows256": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=2, n_q_heads=4, head_dim=64, seq_len=900, window=64,
+        total_budget=2 * 100, layer_floor=20, temperature=None), 104),
     "bf16_odd_dim": (wk.ZIGZAG_32K.scaled(
         n_layers=2, n_kv_heads=2, n_q_heads=4, head_dim=80, seq_len=333, window=8,
         total_budget=2 * 60, layer_floor=10, temperature=None), 103),
@@ -100,6 +105,19 @@ def test_keyformer_full_llama3_layer_16k():
     want = O().score_keyformer(oshape(wl), x["q"], x["k"], 11, 1.0)
     got = sc.cpu().numpy().astype(np.float64)
     assert (np.abs(got - want) <= 1e-3 * want + 1e-30).all()
+
+
+def test_keyformer_tensor_core_and_cuda_core_paths_agree(monkeypatch):
+    """The same draws through both implementations: scores within 1e-3 of
+    each other element by element (both are within 1e-3 of the oracle)."""
+    wl, seed = CASES["bf16_gqa_rows512"]
+    x = wk.make_inputs(wl, seed, device="cuda")
+    monkeypatch.setenv("KVC_SCORE_IMPL", "tc")
+    a, _ = _gpu_scores(wl, x, 5, 2.0)
+    monkeypatch.setenv("KVC_SCORE_IMPL", "simt")
+    b, _ = _gpu_scores(wl, x, 5, 2.0)
+    a, b = a.double(), b.double()
+    assert ((a - b).abs() <= 2e-3 * b + 1e-30).all()
 
 
 def test_keyformer_rejects_bad_tau():
