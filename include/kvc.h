@@ -157,8 +157,10 @@ int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, const void *k, 
  * The page sets tau to infinity in the prompt phase, which would make every
  * score equal; here tau is a parameter in (0, 1e30].  The window is the
  * recent part that compaction always keeps; pass the scores to
- * kvc_mba_budget / kvc_topk_select for the older part.  Runs on the CUDA
- * cores in fp32 (every dtype and head_dim up to 256). */
+ * kvc_mba_budget / kvc_topk_select for the older part.  bf16 inputs with D in
+ * {64,128} and G*W <= 512 run on the tcgen05 tensor cores (the noise drawn in
+ * the epilogue), everything else on a CUDA-core fp32 path; both draw the same
+ * numbers.  On the tensor-core path q_obs and k must be 16-byte aligned. */
 int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,
                         double tau, float *scores, void *ws, size_t ws_bytes, cudaStream_t stream);
 
