@@ -43,11 +43,20 @@
 // half as often as with every warpgroup reading every job).  Pass 2 has two
 // warpgroups, each reading 128 columns of every job at once and freeing the
 // slot before any arithmetic.  Each thread keeps independent sum chains on
-// packed fp32 pairs; the window's causal mask sets invisible logits to -inf.  Measured on this GPU, shared-memory loads in the
-// epilogue compete with the MMAs' shared-memory operand reads, which is why
-// pass 2 takes the row biases through the MMA; and every instruction per
-// logit counts, which is why pass 1 keeps a running reference that is raised
-// only when a piece would overflow instead of taking every piece's maximum.
+// packed fp32 pairs; the window's causal mask sets invisible logits to -inf.
+// Measured on this GPU, shared-memory loads in the epilogue compete with the
+// MMAs' shared-memory operand reads, which is why pass 2 takes the row
+// biases through the MMA; and every instruction per logit counts, which is
+// why pass 1 keeps a running reference that is raised only when a piece
+// would overflow instead of taking every piece's maximum.
+//
+// Keyformer (the NOISE instantiations; "Keyformer: KV Cache reduction
+// through key tokens selection"): the same passes with logits
+// (x_rj + zeta_rj) / tau, zeta the Gumbel draw of (unit, row, key) from
+// Philox4x32-10 (kvc_internal.cuh, shared with the CUDA-core path), drawn in
+// the epilogue for the visible logits only, 8 TMEM columns at a time; four
+// epilogue warpgroups in both passes.
+//
 // Every wait is bounded (kvc_internal.cuh); there are no named barriers.
 #include "kvc_internal.cuh"
 
