@@ -120,7 +120,10 @@ int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status,
  * row cannot see are zero for that row.  Computed with fp32 accumulation;
  * bf16 inputs with D in {64,128} and G*W <= 512 run on the tcgen05 tensor
  * cores, everything else on a CUDA-core fp32 path.  q_obs and k must be
- * 16-byte aligned.  Uses the workspace for per-row softmax statistics. */
+ * 16-byte aligned.  Uses the workspace for per-row softmax statistics.
+ * The tensor-core kernels are persistent: one 2-CTA cluster per SM pair,
+ * ~216 KB of shared memory and all 512 TMEM columns of every SM they run on;
+ * other work on the device shares the SMs only between their launches. */
 int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *scores,
               void *ws, size_t ws_bytes, cudaStream_t stream);
 
