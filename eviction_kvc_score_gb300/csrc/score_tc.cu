@@ -449,32 +449,34 @@ __device__ __forceinline__ void row_stats64(const float (&v)[2][32], float cs, f
 // maximum.  Either way l_run * 2^m_run is the sum of 2^(x*cs) over the keys
 // seen, which is all the merge needs; skipping the per-piece maximum removes
 // one instruction per logit.  The logit arithmetic runs on packed fp32 pairs.
+// The exact fold (a row's first piece, or a piece that would overflow) is
+// one shared code path: a second inlined copy cost registers and ~1% of
+// pass 1.
 __device__ __forceinline__ void row_stats64_lazy(const float (&v)[2][32], float cs, float &m_run,
                                                  float &l_run) {
-    if (m_run == -INFINITY) {
-        row_stats64(v, cs, m_run, l_run);
-        return;
-    }
-    unsigned long long s4[4] = {0ull, 0ull, 0ull, 0ull};
-    const unsigned long long cs2 = f2_pack(cs, cs), nm2 = f2_pack(-m_run, -m_run);
+    if (m_run != -INFINITY) {
+        unsigned long long s4[4] = {0ull, 0ull, 0ull, 0ull};
+        const unsigned long long cs2 = f2_pack(cs, cs), nm2 = f2_pack(-m_run, -m_run);
 #pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-        const unsigned long long y =
-            f2_fma(f2_pack(v[i >> 5][i & 31], v[i >> 5][(i & 31) + 1]), cs2, nm2);
-        float y0, y1;
-        f2_unpack(y, y0, y1);
-        s4[(i >> 1) & 3] = f2_add(s4[(i >> 1) & 3], f2_pack(ex2(y0), ex2(y1)));
+        for (int i = 0; i < 64; i += 2) {
+            const unsigned long long y =
+                f2_fma(f2_pack(v[i >> 5][i & 31], v[i >> 5][(i & 31) + 1]), cs2, nm2);
+            float y0, y1;
+            f2_unpack(y, y0, y1);
+            s4[(i >> 1) & 3] = f2_add(s4[(i >> 1) & 3], f2_pack(ex2(y0), ex2(y1)));
+        }
+        float s8[8];
+        f2_unpack(s4[0], s8[0], s8[1]);
+        f2_unpack(s4[1], s8[2], s8[3]);
+        f2_unpack(s4[2], s8[4], s8[5]);
+        f2_unpack(s4[3], s8[6], s8[7]);
+        const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        if (sum < 0x1p60f) {
+            l_run += sum;
+            return;
+        }
     }
-    float s8[8];
-    f2_unpack(s4[0], s8[0], s8[1]);
-    f2_unpack(s4[1], s8[2], s8[3]);
-    f2_unpack(s4[2], s8[4], s8[5]);
-    f2_unpack(s4[3], s8[6], s8[7]);
-    const float sum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-    if (sum < 0x1p60f) {
-        l_run += sum;
-        return;
-    }
+    // first piece of a row, or one that would overflow: fold exactly
     row_stats64(v, cs, m_run, l_run);
 }
 
