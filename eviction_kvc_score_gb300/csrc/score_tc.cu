@@ -61,6 +61,7 @@
 #include "kvc_internal.cuh"
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <cudaTypedefs.h>
 
@@ -102,6 +103,7 @@ struct TcParams {
     float cs;       // log2(e) / (sqrt(D) tau); tau = 1 without noise
     float noise_scale;      // log2(e) / tau (Keyformer noise)
     uint32_t key0, key1;    // Philox key (Keyformer noise)
+    int skip_first_relay;   // test knob: the odd CTA withholds its first load's arrival
     float2 *partial;
     const float *neg_bias_in;
     float *scores;
@@ -289,7 +291,10 @@ __device__ void relay(const Smem &s, const TcParams &p, int64_t t0, int64_t t1) 
             ++q_loads;
         }
         if (!mbar_wait(&s.full[stage], phase, s.abort_flag, p.status)) break;
-        mbar_arrive_remote(r_pfull + (uint32_t)stage * 8u);
+        // (the test knob leaves the even CTA waiting for this arrival: its
+        // bounded wait runs out, it records KVC_DEV_TIMEOUT and the pair
+        // unwinds)
+        if (!(p.skip_first_relay && t == t0)) mbar_arrive_remote(r_pfull + (uint32_t)stage * 8u);
         if (++stage == p.stages) {
             stage = 0;
             phase ^= 1;
@@ -936,6 +941,11 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
     p.neg_bias_in = a.neg_bias;
     p.scores = a.scores;
     p.status = a.status;
+    // Test knob (KVC_TEST_SKIP_ARRIVE=1): pass 1 runs with one arrival
+    // withheld, so every pair's bounded waits run out; used only to check
+    // that the timeout is reported and the context stays usable.
+    const char *skip = getenv("KVC_TEST_SKIP_ARRIVE");
+    p.skip_first_relay = (skip && skip[0] == '1') ? 1 : 0;
     p.stages = pick_stages<KH>(sp.rows_pad);
     const size_t smem = smem_bytes<KH>(sp.rows_pad, p.stages);
     set_smem_attr<KH>();
@@ -951,6 +961,7 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
     }
     int rc = launch_score_merge(s, sp, a, st);
     if (rc) return rc;
+    p.skip_first_relay = 0;
     if (noise)
         score_colmean_tc<KH, kEWGNoise, true><<<ctas, cta_threads(kEWGNoise), smem, st>>>(tq, tk, p);
     else

@@ -123,7 +123,11 @@ int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status,
  * 16-byte aligned.  Uses the workspace for per-row softmax statistics.
  * The tensor-core kernels are persistent: one 2-CTA cluster per SM pair,
  * ~216 KB of shared memory and all 512 TMEM columns of every SM they run on;
- * other work on the device shares the SMs only between their launches. */
+ * other work on the device shares the SMs only between their launches.
+ * Every device wait is bounded (1 s): a wait that runs out sets
+ * KVC_DEV_TIMEOUT and the kernel returns.  The environment variable
+ * KVC_TEST_SKIP_ARRIVE=1 (tests only) withholds one arrival in the first
+ * tensor-core pass to exercise that path. */
 int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *scores,
               void *ws, size_t ws_bytes, cudaStream_t stream);
 
