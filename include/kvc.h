@@ -72,7 +72,7 @@ extern "C" {
 typedef enum {
     KVC_OK = 0,
     KVC_ERR_INVALID_ARG = -1,  /* bad shape, pointer, size or alignment */
-    KVC_ERR_UNSUPPORTED = -2,  /* valid request this build cannot serve */
+    KVC_ERR_UNSUPPORTED = -2,  /* valid request the library cannot serve */
     KVC_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
     KVC_ERR_TIMEOUT = -4,      /* reserved: a device wait gave up */
     KVC_ERR_WORKSPACE = -5     /* workspace missing or smaller than required */
