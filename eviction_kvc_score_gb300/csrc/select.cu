@@ -566,7 +566,9 @@ __global__ void __launch_bounds__(kSelThreads)
     });
     bad = __syncthreads_or(bad);
     if (tid == 0 && bad) set_status(status, KVC_DEV_BAD_SCORE);
-    long long C = 0;   // elements strictly above the current bucket
+    // B is clamped to [0, P] above and P < 2^31: positions and counts from
+    // here on are 32-bit (64-bit integer arithmetic cost ~8% of the kernel)
+    int C = 0;   // elements strictly above the current bucket
     {
         uint32_t c4[4], cl = 0;
 #pragma unroll
@@ -610,10 +612,10 @@ __global__ void __launch_bounds__(kSelThreads)
         prefix = (prefix << bits) | (uint32_t)s_d;
     }
     const uint32_t vstar = prefix;
-    const long long need_eq = B - C;   // >= 1
+    const int need_eq = (int)B - C;   // >= 1
     // Ordered compaction: position of a kept j is G(j) + min(E(j), need_eq)
     // with G/E the numbers of elements above / equal to v* before j.
-    long long g_before = 0, e_before = 0;
+    int g_before = 0, e_before = 0;
     uint32_t nxt[4];   // next chunk's keys, loaded before this chunk's scan
 #pragma unroll
     for (int i = 0; i < 4; ++i) nxt[i] = 4 * tid + i < P ? __float_as_uint(src[4 * tid + i]) : 0u;
@@ -636,12 +638,12 @@ __global__ void __launch_bounds__(kSelThreads)
             nxt[i] = jn < P ? __float_as_uint(src[jn]) : 0u;
         }
         const uint32_t packed = block_excl_scan(ng | (ne << 16), warp_tot, &s_total);
-        long long G = g_before + (packed & 0xFFFFu);
-        long long E = e_before + (packed >> 16);
+        int G = g_before + (int)(packed & 0xFFFFu);
+        int E = e_before + (int)(packed >> 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (gt[i] || (eq[i] && E < need_eq)) {
-                const long long pos = G + (E < need_eq ? E : need_eq);
+                const int pos = G + (E < need_eq ? E : need_eq);
                 if (pos < B) out[pos] = j0 + i;   // always true for valid scores
             }
             G += gt[i];
