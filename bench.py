@@ -36,6 +36,9 @@ from eviction_kvc_score_gb300 import workloads as wk  # noqa: E402
 
 METRIC = "prompt tokens compressed/sec (score+budget+select+gather); % of HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# a timed region at least this long is compared with the sustained (power-
+# capped) tensor peak, a shorter one with the burst peak
+SUSTAINED_REGION_S = 2.0
 # kernels each C-ABI call launches
 LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
             "kvc_channel_prune": 1, "kvc_pool_scores": 1, "kvc_head_budget": 1,
@@ -52,7 +55,8 @@ def parse():
                     choices=sorted(wk.WORKLOADS) + ["ragged_mistral_batch"])
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the workload with this many layers")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-warmup", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool", type=int, default=0,
                     help="optional SnapKV pooling: odd kernel size of an average pool applied "
@@ -394,14 +398,20 @@ def run_kvc(args):
         score_ms = statistics.mean(a.elapsed_time(b) for a, b in sev)
         flops = score_flops(wl)
         achieved = flops / (score_ms / 1e3) / 1e12
-        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        # A kernel timed inside a short burst runs at full clock: compare it
+        # with the burst peak.  Only a timed region of seconds (power cap
+        # reached) is held against the sustained figure.
+        long_region = t_wall >= SUSTAINED_REGION_S
+        peak_key = "bf16_tflops_sustained" if long_region and "bf16_tflops_sustained" in pk \
+            else "bf16_tflops"
+        peak = pk[peak_key]
         traffic = traffic_for(os.path.join(ROOT, "eviction_kvc_score_gb300", "csrc", "score_tc.cu"),
                               args.workload if not args.layers else None)
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": "kvc_score (stats + merge + column-mean launches)",
                 "ms_per_launch": round(score_ms, 4), "flops_per_launch": flops,
-                "peak_source": f"{pk_src} bf16_tflops_sustained"}
+                "peak_source": f"{pk_src} {peak_key} (timed region {t_wall:.3f} s)"}
         if args.score == "keyformer":
             # The contraction runs on the tensor cores; the bound is the noise:
             # one Philox4x32-10 draw and two logarithms per visible logit and
@@ -511,7 +521,8 @@ def run_e2e(args, jobs, stream):
             if "k_pruned" in hout:
                 hout["k_pruned"].copy_(b.k_pruned, non_blocking=True)
 
-    e2e_step()
+    for _ in range(max(1, args.e2e_warmup)):
+        e2e_step()
     torch.cuda.synchronize()
     for _, _, b, _, _ in jobs:
         st = kvc.kvc_workspace_status(b.ws)
@@ -534,6 +545,7 @@ def run_e2e(args, jobs, stream):
     return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "v_rows_read_in_place_bytes_per_step": v_read, "steps": args.e2e_steps,
+            "warmup": max(1, args.e2e_warmup),
             "api": "kvc_compress_host"}
 
 
@@ -554,57 +566,73 @@ def _oracle_run(wl, x, n):
     return time.perf_counter() - t0
 
 
-def _sample_desc(wl, n, dt):
+def oracle_sample_layers(wl, cores):
+    """Layers of the prompt in one oracle sample: the fewest whole layers
+    that give every host thread at least two (layer, KV head) units (the
+    oracle runs its units in parallel, one per thread at a time), so that no
+    core idles and the two CPU legs time the same work."""
+    need = -(-2 * max(1, cores) // wl.n_kv_heads)
+    return max(1, min(wl.n_layers, need))
+
+
+def _sample_desc(wl, n, dt, reps):
     return (f"first {n} of {wl.n_layers} layers of one {wl.seq_len}-token prompt "
             f"({n * wl.n_kv_heads} (layer, KV head) units), whole path in fp64, "
-            f"{dt:.2f} s wall per sample, scaled to the prompt by {wl.n_layers}/{n}")
+            f"{dt:.3f} s wall per sample (mean of {reps}), tokens/s scaled to the prompt by "
+            f"{wl.n_layers}/{n}")
 
 
-def cpu_baseline(wl, x, target_s=15.0):
+def cpu_baseline(wl, x, reps=2):
     """The oracle as it stands, timed on this host's cores on a bounded sample
-    of the workload (layers doubled until one sample takes about target_s/4),
-    scaled to tokens/s of the whole prompt."""
+    of the workload (oracle_sample_layers), scaled to tokens/s of the whole
+    prompt."""
     from oracle import oracle as O
-    n, spent = 1, 0.0
-    while True:
-        dt = _oracle_run(wl, x, n)
-        spent += dt
-        if dt * 4 >= target_s or n >= wl.n_layers or spent + 2 * dt > target_s:
-            break
-        n = min(wl.n_layers, 2 * n)
-    return {"value": round(wl.seq_len / (dt * wl.n_layers / n), 3), "unit": "tokens/s",
-            "cores": O.num_threads(), "kind": "oracle", "sample": _sample_desc(wl, n, dt)}
+    cores = O.num_threads()
+    n = oracle_sample_layers(wl, cores)
+    dt = statistics.mean(_oracle_run(wl, x, n) for _ in range(reps))
+    return {"value": round(wl.seq_len * n / wl.n_layers / dt, 3), "unit": "tokens/s",
+            "cores": cores, "kind": "oracle", "sample": _sample_desc(wl, n, dt, reps),
+            "sample_s": round(dt, 4), "scale": f"{wl.n_layers}/{n}"}
 
 
 def run_reference(args):
-    """Reference arm: the fp64 CPU oracle, each step one fixed bounded sample
-    (the first layer of the prompt)."""
+    """Reference arm: the fp64 CPU oracle on this host's cores.  Every step is
+    one sample of the workload -- the same first layers the cpu_baseline leg
+    times (oracle_sample_layers) -- and ms_per_step is that sample's measured
+    wall time; tokens/s counts the sample's share of the prompt (n/L of its
+    tokens), so value = tokens per second of oracle work actually done."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from oracle import oracle as O
     O.build()
     wl = workload_list(args.workload, 0)[0]
-    n = 1   # only the sampled layers are generated
+    cores = O.num_threads()
+    n = oracle_sample_layers(wl, cores)
+    # only the sampled layers are generated
     x = wk.make_inputs(wl.scaled(n_layers=n), wk.seed_for(2), device="cpu")
     times = []
     for i in range(args.warmup + args.steps):
         dt = _oracle_run(wl, x, n)
         if i >= args.warmup:
             times.append(dt)
-    per_prompt_s = statistics.mean(times) * wl.n_layers / n
-    val = wl.seq_len / per_prompt_s
+    sample_s = statistics.mean(times)
+    val = wl.seq_len * n / wl.n_layers / sample_s
     out = {"impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(per_prompt_s * 1e3, 1), "higher_is_better": True,
+           "ms_per_step": round(sample_s * 1e3, 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded generators)",
            "config": {"workload": args.workload, "layers": wl.n_layers,
                       "q_heads": wl.n_q_heads, "kv_heads": wl.n_kv_heads,
                       "head_dim": wl.head_dim, "seq_len": wl.seq_len, "window": wl.window,
                       "think_lambda": wl.think_lambda},
-           "cpu_baseline": {"value": round(val, 3), "unit": "tokens/s", "cores": O.num_threads(),
-                            "kind": "oracle", "sample": _sample_desc(wl, n, statistics.mean(times))},
+           "step": (f"one sample = layers 0..{n - 1} of the prompt ({n * wl.n_kv_heads} units, "
+                    f"{wl.seq_len * n / wl.n_layers:.0f} prompt-token equivalents); "
+                    f"ms_per_step is its measured time, not extrapolated"),
+           "cpu_baseline": {"value": round(val, 3), "unit": "tokens/s", "cores": cores,
+                            "kind": "oracle", "sample": _sample_desc(wl, n, sample_s, len(times)),
+                            "sample_s": round(sample_s, 4), "scale": f"{wl.n_layers}/{n}"},
            "e2e": {"value": round(val, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 namespace kvc {
 
@@ -43,43 +44,6 @@ DeviceInfo device_info() {
     return cache[dev];
 }
 
-bool shape_ok(const kvc_shape *s, const char *fn) {
-    if (!s) return fail(KVC_ERR_INVALID_ARG, "%s: shape is NULL", fn), false;
-    if (s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1)
-        return fail(KVC_ERR_INVALID_ARG, "%s: layers and heads must be >= 1", fn), false;
-    if (s->n_q_heads % s->n_kv_heads)
-        return fail(KVC_ERR_INVALID_ARG, "%s: n_q_heads %% n_kv_heads != 0", fn), false;
-    if (s->head_dim < 1 || s->head_dim > 256)
-        return fail(KVC_ERR_INVALID_ARG, "%s: head_dim must be in 1..256", fn), false;
-    if (s->window < 1 || s->seq_len <= s->window)
-        return fail(KVC_ERR_INVALID_ARG, "%s: need 1 <= window < seq_len", fn), false;
-    if (s->dtype != KVC_F32 && s->dtype != KVC_BF16)
-        return fail(KVC_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, s->dtype), false;
-    if ((int64_t)s->n_layers * s->n_kv_heads > (1 << 30))
-        return fail(KVC_ERR_INVALID_ARG, "%s: too many heads", fn), false;
-    return true;
-}
-
-bool tc_eligible(const kvc_shape &s) {
-    const int G = s.n_q_heads / s.n_kv_heads;
-    return s.dtype == KVC_BF16 && (s.head_dim == 64 || s.head_dim == 128) &&
-           (int64_t)G * s.window <= kMaxRowsTC && device_info().major >= 10;
-}
-
-// "auto" (default), "simt" or "tc", from KVC_SCORE_IMPL.
-int score_impl_choice() {
-    const char *e = getenv("KVC_SCORE_IMPL");
-    if (!e || !*e || !strcmp(e, "auto")) return 0;
-    if (!strcmp(e, "simt")) return 1;
-    if (!strcmp(e, "tc")) return 2;
-    return -1;
-}
-
-ScoreSplit make_split(const kvc_shape &s, bool tc) {
-    const int sms = device_info().sms;
-    return make_score_split(s, tc, sms, tc ? score_tc_pairs(sms) : 0);
-}
-
 struct WsLayout {
     size_t partial_off, partial_bytes;
     size_t bias_off, bias_bytes;
@@ -112,7 +76,121 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 uint32_t *status_word(void *ws) { return static_cast<uint32_t *>(ws); }
 
+
+// Event sets of kvc_compress_host, one per (device, staging buffer); created
+// on first use and kept (at most kMaxEventSets idle sets; the oldest idle set
+// is destroyed when a new buffer needs one and the cache is full).
+struct EventSet {
+    int dev = -1;
+    const void *key = nullptr;
+    bool in_use = false;
+    unsigned long long last_use = 0;
+    std::vector<cudaEvent_t> layer;
+    cudaEvent_t last_done = nullptr;
+};
+constexpr size_t kMaxEventSets = 64;
+std::mutex g_ev_mu;
+std::vector<EventSet *> g_ev_sets;
+unsigned long long g_ev_clock = 0;
+
+// An evicted set is destroyed only after its last call has finished reading
+// its staging buffers, so a later call on the same buffers (which gets a
+// fresh set) cannot overwrite them early.
+void destroy_set(EventSet *e) {
+    if (e->last_done) cudaEventSynchronize(e->last_done);
+    for (cudaEvent_t x : e->layer) cudaEventDestroy(x);
+    if (e->last_done) cudaEventDestroy(e->last_done);
+    delete e;
+}
+
+int checkout_events(const void *key, int n_layer_events, EventSet **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaGetDevice failed");
+    std::lock_guard<std::mutex> lk(g_ev_mu);
+    EventSet *e = nullptr;
+    for (EventSet *c : g_ev_sets)
+        if (c->dev == dev && c->key == key) e = c;
+    if (e && e->in_use)
+        return fail(KVC_ERR_INVALID_ARG,
+                    "kvc_compress_host: another call is using these staging buffers right now");
+    if (!e) {
+        if (g_ev_sets.size() >= kMaxEventSets) {
+            size_t victim = g_ev_sets.size();
+            for (size_t i = 0; i < g_ev_sets.size(); ++i)
+                if (!g_ev_sets[i]->in_use &&
+                    (victim == g_ev_sets.size() || g_ev_sets[i]->last_use < g_ev_sets[victim]->last_use))
+                    victim = i;
+            if (victim < g_ev_sets.size()) {
+                destroy_set(g_ev_sets[victim]);
+                g_ev_sets.erase(g_ev_sets.begin() + (long)victim);
+            }
+        }
+        e = new EventSet;
+        e->dev = dev;
+        e->key = key;
+        if (cudaEventCreateWithFlags(&e->last_done, cudaEventDisableTiming) != cudaSuccess) {
+            delete e;
+            return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
+        }
+        g_ev_sets.push_back(e);
+    }
+    while ((int)e->layer.size() < n_layer_events) {
+        cudaEvent_t x;
+        if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess)
+            return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
+        e->layer.push_back(x);
+    }
+    e->in_use = true;
+    e->last_use = ++g_ev_clock;
+    *out = e;
+    return KVC_OK;
+}
+
+void checkin_events(EventSet *e) {
+    std::lock_guard<std::mutex> lk(g_ev_mu);
+    e->in_use = false;
+}
+
 }  // namespace
+
+// Shape validation and score-kernel choice, shared by every entry point that
+// scores (kvc_score, kvc_score_keyformer, kvc_score_noalloc).
+bool shape_ok(const kvc_shape *s, const char *fn) {
+    if (!s) return fail(KVC_ERR_INVALID_ARG, "%s: shape is NULL", fn), false;
+    if (s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1)
+        return fail(KVC_ERR_INVALID_ARG, "%s: layers and heads must be >= 1", fn), false;
+    if (s->n_q_heads % s->n_kv_heads)
+        return fail(KVC_ERR_INVALID_ARG, "%s: n_q_heads %% n_kv_heads != 0", fn), false;
+    if (s->head_dim < 1 || s->head_dim > 256)
+        return fail(KVC_ERR_INVALID_ARG, "%s: head_dim must be in 1..256", fn), false;
+    if (s->window < 1 || s->seq_len <= s->window)
+        return fail(KVC_ERR_INVALID_ARG, "%s: need 1 <= window < seq_len", fn), false;
+    if (s->dtype != KVC_F32 && s->dtype != KVC_BF16)
+        return fail(KVC_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, s->dtype), false;
+    if ((int64_t)s->n_layers * s->n_kv_heads > (1 << 30))
+        return fail(KVC_ERR_INVALID_ARG, "%s: too many heads", fn), false;
+    return true;
+}
+
+bool tc_eligible(const kvc_shape &s) {
+    const int G = s.n_q_heads / s.n_kv_heads;
+    return s.dtype == KVC_BF16 && (s.head_dim == 64 || s.head_dim == 128) &&
+           (int64_t)G * s.window <= kMaxRowsTC && device_info().major >= 10;
+}
+
+int score_impl_choice() {
+    const char *e = getenv("KVC_SCORE_IMPL");
+    if (!e || !*e || !strcmp(e, "auto")) return 0;
+    if (!strcmp(e, "simt")) return 1;
+    if (!strcmp(e, "tc")) return 2;
+    return -1;
+}
+
+ScoreSplit make_split(const kvc_shape &s, bool tc) {
+    const int sms = device_info().sms;
+    return make_score_split(s, tc, sms, tc ? score_tc_pairs(sms) : 0);
+}
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -212,49 +290,45 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     }
     const void *v_dev = pa.devicePointer;
     if (!aligned16(v_dev)) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_host: v_host must be 16-byte aligned");
-    // one event per layer (plus one for Q), created once per device
-    constexpr int kMaxEv = 1025;
-    static cudaEvent_t events[16][kMaxEv];
-    static int n_events[16] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 16 || s.n_layers + 1 > kMaxEv)
-        return fail(KVC_ERR_UNSUPPORTED, "kvc_compress_host: at most 1024 layers on devices 0..15");
-    while (n_events[dev] < s.n_layers + 1) {
-        if (cudaEventCreateWithFlags(&events[dev][n_events[dev]], cudaEventDisableTiming) != cudaSuccess)
-            return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
-        ++n_events[dev];
-    }
+    // One set of events per staging buffer (per device): an event per layer
+    // of K plus one for Q, and `last_done`, recorded after the call's last
+    // read of the staging buffers (its compaction).  Calls with distinct
+    // staging buffers never share an event, so they may run concurrently from
+    // any threads; the set is checked out for the duration of the call.
+    EventSet *ev = nullptr;
+    int rc0 = checkout_events(k_dev, s.n_layers + 1, &ev);
+    if (rc0) return rc0;
+    struct Release {
+        EventSet *e;
+        ~Release() { checkin_events(e); }
+    } release{ev};
     const size_t es = s.dtype == KVC_F32 ? 4 : 2;
     const size_t q_layer = (size_t)s.n_q_heads * s.window * s.head_dim * es;
     const size_t k_layer = (size_t)s.n_kv_heads * s.seq_len * s.head_dim * es;
-    // 0. last_done marks the end of the previous call's last read of the
+    // 0. last_done marks the end of the previous call's last read of these
     // staging buffers (its compaction); this call's copies start after it --
     // and only after it, so whatever the caller enqueued since (reading the
     // outputs back) overlaps with the next prompt's copies.  Waiting on an
     // event that was never recorded returns at once.
-    static cudaEvent_t last_done[16] = {};
-    if (!last_done[dev] && cudaEventCreateWithFlags(&last_done[dev], cudaEventDisableTiming) != cudaSuccess)
-        return fail(KVC_ERR_CUDA, "kvc_compress_host: cudaEventCreate failed");
-    cudaError_t e = cudaStreamWaitEvent(copy_stream, last_done[dev], 0);
+    cudaError_t e = cudaStreamWaitEvent(copy_stream, ev->last_done, 0);
     // 1. the copy stream moves Q, then K layer by layer, marking each layer
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(q_dev, q_host, q_layer * s.n_layers, cudaMemcpyHostToDevice,
                             copy_stream);
-    if (e == cudaSuccess) e = cudaEventRecord(events[dev][0], copy_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(ev->layer[0], copy_stream);
     for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
         e = cudaMemcpyAsync(static_cast<char *>(k_dev) + l * k_layer,
                             static_cast<const char *>(k_host) + l * k_layer, k_layer,
                             cudaMemcpyHostToDevice, copy_stream);
-        if (e == cudaSuccess) e = cudaEventRecord(events[dev][l + 1], copy_stream);
+        if (e == cudaSuccess) e = cudaEventRecord(ev->layer[l + 1], copy_stream);
     }
     if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_compress_host: copy: %s", cudaGetErrorString(e));
     // 2. each layer is scored as soon as its keys have landed
     kvc_shape s1 = s;
     s1.n_layers = 1;
-    e = cudaStreamWaitEvent(stream, events[dev][0], 0);
+    e = cudaStreamWaitEvent(stream, ev->layer[0], 0);
     for (int l = 0; l < s.n_layers; ++l) {
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, events[dev][l + 1], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev->layer[l + 1], 0);
         if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_compress_host: %s", cudaGetErrorString(e));
         const int rc = kvc_score(&s1, static_cast<const char *>(q_dev) + l * q_layer,
                                  static_cast<const char *>(k_dev) + l * k_layer,
@@ -270,7 +344,7 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     rc = kvc_compact(&s, k_dev, v_dev, idx, budget, k_max, k_out, v_out, out_rows, ws, ws_bytes,
                      stream);
     if (rc) return rc;
-    e = cudaEventRecord(last_done[dev], stream);
+    e = cudaEventRecord(ev->last_done, stream);
     if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_compress_host: %s", cudaGetErrorString(e));
     return KVC_OK;
 }

@@ -506,4 +506,13 @@ int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, c
 
 void set_error(const char *fmt, ...);
 
+// Shared by every scoring entry point (api.cu): shape validation (message in
+// kvc_last_error on failure), whether the tensor-core kernels can serve the
+// shape on the current device, the KVC_SCORE_IMPL choice (0 auto, 1 simt,
+// 2 tc, -1 invalid) and the work split for the current device.
+bool shape_ok(const kvc_shape *s, const char *fn);
+bool tc_eligible(const kvc_shape &s);
+int score_impl_choice();
+ScoreSplit make_split(const kvc_shape &s, bool tc);
+
 }  // namespace kvc

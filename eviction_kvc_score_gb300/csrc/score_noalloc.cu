@@ -72,20 +72,6 @@ int scratch_address(unsigned char **out) {
     return KVC_OK;
 }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
-int cc_major() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -95,17 +81,10 @@ using namespace kvc;
 
 extern "C" int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, const void *k,
                                  float *scores, uint32_t *dev_status, cudaStream_t stream) {
-    if (!shape) {
-        set_error("kvc_score_noalloc: shape is NULL");
-        return KVC_ERR_INVALID_ARG;
-    }
+    // Same shape rules, kernel choice (KVC_SCORE_IMPL included) and work
+    // split as kvc_score, so both entry points run the same kernels.
+    if (!shape_ok(shape, "kvc_score_noalloc")) return KVC_ERR_INVALID_ARG;
     const kvc_shape &s = *shape;
-    if (s.n_layers < 1 || s.n_q_heads < 1 || s.n_kv_heads < 1 || s.n_q_heads % s.n_kv_heads ||
-        s.head_dim < 1 || s.head_dim > 256 || s.window < 1 || s.seq_len <= s.window ||
-        (s.dtype != KVC_F32 && s.dtype != KVC_BF16)) {
-        set_error("kvc_score_noalloc: invalid shape");
-        return KVC_ERR_INVALID_ARG;
-    }
     if (!q_obs || !k || !scores) {
         set_error("kvc_score_noalloc: NULL tensor");
         return KVC_ERR_INVALID_ARG;
@@ -114,13 +93,24 @@ extern "C" int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, cons
         set_error("kvc_score_noalloc: q_obs and k must be 16-byte aligned");
         return KVC_ERR_INVALID_ARG;
     }
-    const int G = s.n_q_heads / s.n_kv_heads;
-    const bool tc = s.dtype == KVC_BF16 && (s.head_dim == 64 || s.head_dim == 128) &&
-                    (int64_t)G * s.window <= kMaxRowsTC && cc_major() >= 10;
-    const int sms = sm_count() > 0 ? sm_count() : 148;
-
-    // Same work split as kvc_score.
-    const ScoreSplit sp = make_score_split(s, tc, sms, tc ? score_tc_pairs(sms) : 0);
+    // the kernels OR status bits into *dev_status with 32-bit atomics
+    if (reinterpret_cast<uintptr_t>(dev_status) & 3) {
+        set_error("kvc_score_noalloc: dev_status must be 4-byte aligned");
+        return KVC_ERR_INVALID_ARG;
+    }
+    const int choice = score_impl_choice();
+    if (choice < 0) {
+        set_error("kvc_score_noalloc: KVC_SCORE_IMPL must be auto, simt or tc");
+        return KVC_ERR_INVALID_ARG;
+    }
+    const bool can_tc = tc_eligible(s);
+    if (choice == 2 && !can_tc) {
+        set_error("kvc_score_noalloc: tensor-core path needs bf16, head_dim 64/128, G*W <= 512 "
+                  "and an sm_100-family device");
+        return KVC_ERR_UNSUPPORTED;
+    }
+    const bool tc = can_tc && choice != 1;
+    const ScoreSplit sp = make_split(s, tc);
 
     const size_t partial_bytes = round256((size_t)sp.n_units * sp.max_slots * sp.rows_pad * sizeof(float2));
     const size_t bias_bytes = round256((size_t)sp.n_units * sp.rows_pad * sizeof(float));

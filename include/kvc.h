@@ -136,13 +136,17 @@ int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *s
  * plugin just its input and output buffers -- no workspace -- and forbid
  * cudaMalloc because their own allocator already holds the device memory
  * and an allocation would synchronise the device mid-schedule.  This call
- * computes exactly what kvc_score computes, with the same kernels, but keeps
- * its scratch in a fixed 8 MiB array inside the library's device memory
+ * computes exactly what kvc_score computes, with the same shape rules, the
+ * same kernel choice (KVC_SCORE_IMPL included) and the same kernels, but
+ * keeps its scratch in a fixed 8 MiB array inside the library's device memory
  * (held by every GPU that loads the library until the process exits).
  * Shapes whose scratch exceeds 8 MiB return KVC_ERR_UNSUPPORTED (the 32K and
  * 128K Llama-3-8B-shaped prompts need 2.5 MiB).  dev_status is an
- * optional DEVICE uint32 that is zeroed and then receives the KVC_DEV_* bits
- * (NULL: they go to a word inside the array).  The first call on each device
+ * optional 4-byte-aligned DEVICE uint32 that is zeroed and then receives the
+ * KVC_DEV_* bits (misaligned: KVC_ERR_INVALID_ARG).  With dev_status NULL the
+ * bits go to a word inside the array that no call reads back, so device-side
+ * errors (a timed-out wait) cannot be observed: callers that need them pass
+ * a word of their own.  The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress) and should be
  * made outside any stream capture.  All calls share the array: calls that
  * overlap on the GPU race and give undefined scores, so order them on one
@@ -185,10 +189,14 @@ int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k
  * from stream.  Outputs, capacities and the workspace are those of the four
  * calls it makes (see them); the call is asynchronous on both streams, and
  * the host buffers must stay valid until `stream` has finished.  A call's
- * copies wait only for the previous call's compaction on this device (the
- * last read of the staging buffers), so reading the outputs back overlaps
- * with the next prompt's copies.  At most 1024 layers; one event per layer
- * is created once per device and kept. */
+ * copies wait only for the compaction of the previous call on the same
+ * staging buffers (their last read), so reading the outputs back overlaps
+ * with the next prompt's copies.  Events: one per layer plus two, per staging
+ * buffer k_dev and device, created on first use and kept (up to 64 idle sets;
+ * beyond that the least recently used idle set is destroyed after the host
+ * has waited for its last call).  Calls with distinct staging buffers may run
+ * concurrently from any threads; a call whose k_dev is in use by a call still
+ * being issued on another thread returns KVC_ERR_INVALID_ARG. */
 int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_host,
                       const void *v_host, void *q_dev, void *k_dev, uint32_t mass_num,
                       uint32_t mass_den, int64_t total_budget, int32_t layer_floor, int32_t k_max,

@@ -608,6 +608,42 @@ def test_keyformer_single_row_is_noisy_softmax(tau):
         np.testing.assert_allclose(c[0, h], want, rtol=1e-9, atol=1e-300)
 
 
+@pytest.mark.parametrize("tau", [0.5, 2.0])
+def test_keyformer_grouped_window_equals_library_attention(tau):
+    """G > 1, W > 1, finite tau: the Keyformer score equals torch's own
+    scaled-dot-product attention with V = identity (the output IS the
+    probability matrix), the logits scaled by 1/(sqrt(D) tau), the noise
+    zeta/tau (scipy's Gumbel inverse CDF of the uniforms) as an additive
+    float mask with -inf on the causal part, the GQA mapping expanded with
+    repeat_interleave and the mean taken over each KV head's G*W rows.
+    Catches a wrong query-head -> KV-head map (kv + g*H_kv instead of kv*G + g),
+    a wrong row index in the noise counter (w instead of g*W + w), the noise
+    not divided by tau, and a wrong causal offset."""
+    from scipy.stats import gumbel_r
+    L, Hq, Hkv, D, T, W = 2, 6, 2, 8, 29, 4
+    G, P = Hq // Hkv, T - W
+    q, k = _rand_inputs(L, Hq, Hkv, D, T, W, 11, scale=1.5)
+    s = O.shape_of(L, Hq, Hkv, D, T, W, "f32")
+    seed = 1234
+    c = O.score_keyformer(s, q, k, seed, tau)
+    zeta = np.empty((L, Hq, W, T))
+    for l in range(L):
+        for h in range(Hq):
+            kv, g = divmod(h, G)
+            unit = l * Hkv + kv
+            for w in range(W):
+                u = [O.keyformer_uniform(seed, unit, g * W + w, j) for j in range(T)]
+                zeta[l, h, w] = gumbel_r.ppf(u)
+    visible = np.arange(T)[None, :] <= (P + np.arange(W))[:, None]     # [W][T]
+    mask = torch.from_numpy(np.where(visible[None, None], zeta / tau, -np.inf))
+    kk = k.double().repeat_interleave(G, dim=1)                          # [L][Hq][T][D]
+    eye = torch.eye(T, dtype=torch.float64).expand(L, Hq, T, T)
+    probs = torch.nn.functional.scaled_dot_product_attention(
+        q.double(), kk, eye, attn_mask=mask, scale=1.0 / (math.sqrt(D) * tau))
+    ref = probs.view(L, Hkv, G, W, T).mean(dim=(2, 3)).numpy()
+    np.testing.assert_allclose(c, ref, rtol=1e-10, atol=1e-300)
+
+
 def test_keyformer_rows_sum_to_one_and_hot_temperature_is_uniform():
     L, Hq, H, D, T, W = 2, 4, 2, 8, 40, 5
     q, k = _rand_inputs(L, Hq, H, D, T, W, 4)
