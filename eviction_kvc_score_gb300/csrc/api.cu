@@ -280,7 +280,17 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
     const WsLayout w = ws_layout(s);
     if (!ws_ok(ws, ws_bytes, w.total, "kvc_compress_host")) return KVC_ERR_WORKSPACE;
     // V is never copied: the compaction reads the kept rows through the
-    // device's mapping of the (pinned) host buffer
+    // device's mapping of the (pinned) host buffer.  The mapping is looked up
+    // in the calling thread's current context, which a thread that has not
+    // made a runtime call yet does not have: bind the current device's
+    // primary context first.
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(KVC_ERR_CUDA, "kvc_compress_host: no usable CUDA device");
+        }
+    }
     cudaPointerAttributes pa;
     if (cudaPointerGetAttributes(&pa, v_host) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
         pa.devicePointer == nullptr) {

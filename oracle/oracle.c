@@ -32,6 +32,9 @@
  *               pruned.
  *  [THINK-QD]   same page, "Greedy algorithm" and "Observation window":
  *               channel score = Frobenius norm of Q[-S_obs:, j] K[:, j]^T.
+ *  [THINK-V]    same page, appendix "Value cache pruning strategy": value
+ *               channel score = norm of column j of softmax(Q[-S_obs:] K^T /
+ *               sqrt(D)) V; keep the top T channels.
  *  [ZZ-HEAD]    ZigZagKV post: memory per attention head should follow the
  *               tokens that head needs; each head's K follows its quota.
  *  [KEYF]       "Keyformer: KV Cache reduction through key tokens selection"
@@ -565,6 +568,126 @@ int ora_channel_prune(const ora_shape *s, const void *k_out, const int32_t *budg
     }
     free(in_row);
     free(out_el);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Optional: ThinK value-channel pruning (THINKV)               [THINK-V]
+ *
+ * "ThinK: Thinner Key Cache by Query-Driven Pruning", appendix "Value cache
+ * pruning strategy": channel j of a head's value cache scores the norm of
+ * column j of the window queries' attention output,
+ *   Score_v[j] = || softmax(Q[-S_obs:] K^T / sqrt(D)) V[:, j] ||_F,
+ * and only the T channels with the largest scores are kept (T =
+ * floor((1-lambda) D), the same count as for keys).
+ * Readings: the attention is the window scoring's own (a1): window row i
+ * (position P+i) attends to the whole prompt's keys 0..P+i with
+ * softmax(q.k / sqrt(D)); with grouped-query attention the output column
+ * stacks the G*W window rows of the KV head's query heads (as for the
+ * query-driven key criterion); channels are ranked by the squared norm
+ * (monotone in the norm, no rounding sqrt), ties to the lower channel.
+ *
+ * ora_value_scores: score_v [L][H_kv][D] = sum over the unit's G*W rows of
+ * o_d^2, o = sum_j p_j v_j, one softmax row at a time.
+ * ------------------------------------------------------------------------- */
+int ora_value_scores(const ora_shape *s, const void *q, const void *k, const void *v,
+                     double *score_v)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t D = s->head_dim, T = s->seq_len, W = s->window;
+    const int64_t Hq = s->n_q_heads, Hkv = s->n_kv_heads, G = Hq / Hkv;
+    const int64_t P = T - W, units = (int64_t)s->n_layers * Hkv;
+    const double root_d = sqrt((double)D);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t u = 0; u < units; ++u) {
+        const int64_t layer = u / Hkv, kv_head = u % Hkv;
+        const int64_t kv_base = u * T * D;
+        double *x = (double *)malloc(sizeof(double) * (size_t)T);
+        double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+        double *o = (double *)malloc(sizeof(double) * (size_t)D);
+        double *sv = score_v + u * D;
+        if (!x || !qr || !o) { free(x); free(qr); free(o); bad = 1; continue; }
+        for (int64_t d = 0; d < D; ++d) sv[d] = 0.0;
+        for (int64_t g = 0; g < G; ++g) {
+            const int64_t h = kv_head * G + g;
+            for (int64_t i = 0; i < W; ++i) {
+                const int64_t q_base = ((layer * Hq + h) * W + i) * D;
+                for (int64_t d = 0; d < D; ++d) qr[d] = ora_elem(q, q_base + d, s->dtype);
+                const int64_t t = P + i;
+                double mu = -INFINITY;
+                for (int64_t j = 0; j <= t; ++j) {
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += qr[d] * ora_elem(k, kv_base + j * D + d, s->dtype);
+                    x[j] = dot / root_d;
+                    if (x[j] > mu) mu = x[j];
+                }
+                double z = 0.0;
+                for (int64_t j = 0; j <= t; ++j) {
+                    x[j] = exp(x[j] - mu);
+                    z += x[j];
+                }
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t j = 0; j <= t; ++j) {
+                    const double pj = x[j] / z;
+                    for (int64_t d = 0; d < D; ++d)
+                        o[d] += pj * ora_elem(v, kv_base + j * D + d, s->dtype);
+                }
+                for (int64_t d = 0; d < D; ++d) sv[d] += o[d] * o[d];
+            }
+        }
+        free(x);
+        free(qr);
+        free(o);
+    }
+    return bad ? -2 : 0;
+}
+
+/* THINKV selection and copy: for every head keep the `keep` channels with the
+ * largest score_v (ties to the lower channel), written ascending to chan
+ * [L][H_kv][keep], and copy those channels of the head's n_l kept prefix rows
+ * of the compacted values v_out (packed as kvc_compact writes them) to
+ * v_pruned (layer l holds [H_kv][n_l][keep]); window rows are not pruned. */
+int ora_channel_prune_value(const ora_shape *s, const double *score_v, const void *v_out,
+                            const int32_t *budget, double lambda, int32_t *chan, void *v_pruned)
+{
+    if (!ora_shape_ok(s)) return -1;
+    const int64_t D = s->head_dim, W = s->window, P = (int64_t)s->seq_len - W;
+    const int64_t Hkv = s->n_kv_heads, L = s->n_layers;
+    const int32_t keep = ora_keep_channels(lambda, (int32_t)D);
+    if (keep < 1 || keep > D) return -1;
+    const size_t es = s->dtype == 0 ? 4 : 2;
+    int64_t ir = 0, oe = 0;
+    for (int64_t l = 0; l < L; ++l) {
+        const int64_t n = ora_kept(budget[l], P);
+        for (int64_t h = 0; h < Hkv; ++h) {
+            const int64_t u = l * Hkv + h;
+            const int64_t row0 = ir + h * (n + W);
+            ora_chan *ch = (ora_chan *)malloc(sizeof(ora_chan) * (size_t)D);
+            if (!ch) return -2;
+            for (int64_t d = 0; d < D; ++d) {
+                ch[d].m = score_v[u * D + d];
+                ch[d].d = (int32_t)d;
+            }
+            qsort(ch, (size_t)D, sizeof(ora_chan), ora_cmp_chan);
+            int32_t *sel = chan + u * keep;
+            for (int32_t i = 0; i < keep; ++i) sel[i] = ch[i].d;
+            qsort(sel, (size_t)keep, sizeof(int32_t), ora_cmp_i32);
+            free(ch);
+            if (v_pruned) {
+                const unsigned char *src = (const unsigned char *)v_out;
+                unsigned char *dst = (unsigned char *)v_pruned;
+                const int64_t o0 = oe + h * n * keep;
+                for (int64_t r = 0; r < n; ++r)
+                    for (int32_t i = 0; i < keep; ++i)
+                        memcpy(dst + (size_t)(o0 + r * keep + i) * es,
+                               src + (size_t)((row0 + r) * D + sel[i]) * es, es);
+            }
+        }
+        ir += Hkv * (n + W);
+        oe += Hkv * n * keep;
+    }
     return 0;
 }
 

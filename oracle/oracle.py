@@ -77,6 +77,8 @@ def lib():
                 "ora_keep_channels": (i32, [d, i32]),
                 "ora_channel_prune": (C.c_int, [sp, p, p, d, p, p, p]),
                 "ora_channel_prune_query": (C.c_int, [sp, p, p, p, d, p, p, p]),
+                "ora_value_scores": (C.c_int, [sp, p, p, p, p]),
+                "ora_channel_prune_value": (C.c_int, [sp, p, p, p, d, p, p]),
                 "ora_compress": (C.c_int, [sp, p, p, p, u32, u32, i64, i64, d, i64,
                                            p, p, p, p, p, p, p, p]),
             }
@@ -311,6 +313,33 @@ def channel_prune_query(s: Shape, q, k_out, budget_l, lam: float):
     _check(lib().ora_channel_prune_query(C.byref(s), _ptr(qa), _ptr(ka), _ptr(b), float(lam),
                                          _ptr(chan), _ptr(sc), _ptr(kp)), "channel_prune_query")
     return chan, sc, kp
+
+
+def value_scores(s: Shape, q, k, v) -> np.ndarray:
+    """THINKV channel scores: [L][H_kv][D] fp64, the squared norm of each
+    column of the window rows' attention output softmax(QK^T/sqrt(D)) V."""
+    qa, ka, va = raw(q), raw(k), raw(v)
+    out = np.empty((s.n_layers, s.n_kv_heads, s.head_dim), dtype=np.float64)
+    _check(lib().ora_value_scores(C.byref(s), _ptr(qa), _ptr(ka), _ptr(va), _ptr(out)),
+           "value_scores")
+    return out
+
+
+def channel_prune_value(s: Shape, score_v, v_out, budget_l, lam: float):
+    """THINKV selection on given channel scores ([L][H_kv][D], fp64 or fp32
+    widened exactly) and copy of the kept prefix rows' channels.  Returns
+    (chan [L][H_kv][keep], v_pruned raw)."""
+    sv = np.ascontiguousarray(score_v, dtype=np.float64)
+    va = raw(v_out)
+    b = np.ascontiguousarray(budget_l, dtype=np.int32)
+    keep = keep_channels(lam, s.head_dim)
+    P = s.seq_len - s.window
+    n = np.clip(b, 0, P).astype(np.int64)
+    chan = np.empty((s.n_layers, s.n_kv_heads, max(keep, 1)), dtype=np.int32)
+    vp = np.empty(max(1, int(s.n_kv_heads * n.sum() * max(keep, 1))), dtype=va.dtype)
+    _check(lib().ora_channel_prune_value(C.byref(s), _ptr(sv), _ptr(va), _ptr(b), float(lam),
+                                         _ptr(chan), _ptr(vp)), "channel_prune_value")
+    return chan, vp[: int(s.n_kv_heads * n.sum() * keep)]
 
 
 def compress(s: Shape, q, k, v, total: int, floor: int, k_max: int,

@@ -566,6 +566,90 @@ def test_compact_heads_equals_fancy_indexing():
     assert np.array_equal(got, want)
 
 
+# ---------------------------------------------------- optional THINKV (values)
+@pytest.mark.parametrize("seed", [0, 1])
+def test_value_scores_equal_library_attention_output(seed):
+    """THINKV channel scores are the squared column norms of the window
+    rows' attention output: torch's own scaled-dot-product attention with the
+    real V, the causal window mask and the GQA mapping expanded explicitly,
+    then summed over each KV head's G*W rows.  Catches a wrong GQA map, mask
+    offset, scale, a missing normalisation, |o| instead of o^2 and a sum over
+    the wrong axis."""
+    L, Hq, Hkv, D, T, W = 2, 6, 2, 8, 31, 4
+    G, P = Hq // Hkv, T - W
+    q, k = _rand_inputs(L, Hq, Hkv, D, T, W, seed, scale=1.5)
+    v = torch.randn(L, Hkv, T, D, generator=torch.Generator().manual_seed(100 + seed))
+    s = O.shape_of(L, Hq, Hkv, D, T, W, "f32")
+    got = O.value_scores(s, q, k, v)
+    kk = k.double().repeat_interleave(G, dim=1)
+    vv = v.double().repeat_interleave(G, dim=1)
+    mask = torch.arange(T)[None, :] <= (P + torch.arange(W))[:, None]
+    out = torch.nn.functional.scaled_dot_product_attention(q.double(), kk, vv, attn_mask=mask)
+    want = (out ** 2).view(L, Hkv, G, W, D).sum(dim=(2, 3)).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-300)
+
+
+def test_value_scores_equal_keys_closed_form():
+    """All keys equal: window row i attends uniformly to keys 0..P+i, so its
+    output is the mean of those value rows and score_v[d] is the sum over
+    rows of that mean squared."""
+    L, H, D, T, W = 1, 2, 5, 17, 3
+    q, _ = _rand_inputs(L, H, H, D, T, W, 9)
+    k = torch.full((L, H, T, D), 0.25)
+    v = torch.randn(L, H, T, D, generator=torch.Generator().manual_seed(4))
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    got = O.value_scores(s, q, k, v)
+    P = T - W
+    for h in range(H):
+        vv = v[0, h].double().numpy()
+        want = sum(vv[: P + i + 1].mean(axis=0) ** 2 for i in range(W))
+        np.testing.assert_allclose(got[0, h], want, rtol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_channel_prune_value_selection_bruteforce(seed):
+    """Selection = the keep-subset with the largest scores, ties to the lower
+    channel (a stable full sort), written ascending; the pruned bytes are
+    those channels of each head's kept prefix rows (numpy fancy indexing)."""
+    rng = np.random.default_rng(seed)
+    L, H, D, T, W, lam = 2, 2, 6, 12, 3, 0.5
+    P = T - W
+    keep = O.keep_channels(lam, D)
+    sv = rng.integers(0, 4, size=(L, H, D)).astype(np.float64)   # many ties
+    bud = np.array([4, 9], dtype=np.int32)
+    rows = int(H * sum(min(b, P) + W for b in bud))
+    v_out = rng.standard_normal((rows, D)).astype(np.float32)
+    s = O.shape_of(L, H, H, D, T, W, "f32")
+    chan, vp = O.channel_prune_value(s, sv, v_out, bud, lam)
+    r0, parts = 0, []
+    for l in range(L):
+        n = min(int(bud[l]), P)
+        for h in range(H):
+            best = max(itertools.combinations(range(D), keep),
+                       key=lambda c: (sum(sv[l, h, list(c)]), [-x for x in c]))
+            assert chan[l, h].tolist() == list(best)
+            parts.append(v_out[r0: r0 + n][:, list(best)].ravel())
+            r0 += n + W
+    assert np.array_equal(vp, np.concatenate(parts))
+
+
+def test_value_scores_keep_a_dominant_value_channel():
+    """A value channel scaled x8 dominates every output column norm, so it is
+    always among the kept channels."""
+    L, Hq, H, D, T, W = 1, 4, 2, 16, 64, 8
+    q, k = _rand_inputs(L, Hq, H, D, T, W, 5)
+    g = torch.Generator().manual_seed(6)
+    v = torch.randn(L, H, T, D, generator=g) + 0.5
+    v[..., 11] *= 8.0
+    s = O.shape_of(L, Hq, H, D, T, W, "f32")
+    sv = O.value_scores(s, q, k, v)
+    bud = np.array([20], dtype=np.int32)
+    rows = H * (20 + W)
+    chan, _ = O.channel_prune_value(s, sv, np.zeros((rows, D), np.float32), bud, 0.75)
+    for h in range(H):
+        assert 11 in chan[0, h].tolist()
+
+
 # ----------------------------------------------------------- optional Keyformer
 def test_philox4x32_10_known_answers():
     """Known-answer vectors published with the Philox4x32-10 generator

@@ -112,7 +112,28 @@ def check_discrete_stages(wl, x, b, lam=None, heads=None):
                     assert abs(kth - nxt) <= 1e-9 * kth, f"ThinK channels layer {l} head {h}"
         if np.array_equal(gchan, chan):
             assert np.array_equal(kp, o.raw(b.k_pruned[: kp.size])), "pruned K"
+        else:   # a near-tie: the pruned bytes are still those of the GPU's channels
+            check_pruned_bytes(wl, b, o.raw(b.k_out[:rows]), bud)
     return bud
+
+
+def check_pruned_bytes(wl, b, kout, bud):
+    """k_pruned holds, per head, the GPU's kept channels of its kept prefix
+    rows (numpy fancy indexing of the compacted keys)."""
+    o = O()
+    P, W, keep = wl.prefix_len, wl.window, b.keep
+    gchan = b.chan.cpu().numpy()
+    n = np.clip(bud, 0, P).astype(np.int64)
+    row0 = np.concatenate([[0], np.cumsum(wl.n_kv_heads * (n + W))])
+    el0 = np.concatenate([[0], np.cumsum(wl.n_kv_heads * n * keep)])
+    gkp = o.raw(b.k_pruned)
+    for l in range(wl.n_layers):
+        for h in range(wl.n_kv_heads):
+            r0 = int(row0[l] + h * (n[l] + W))
+            want = kout[r0: r0 + n[l]][:, gchan[l, h]]
+            e0 = int(el0[l] + h * n[l] * keep)
+            got = gkp[e0: e0 + n[l] * keep].reshape(n[l], keep)
+            assert np.array_equal(got, want), f"pruned K layer {l} head {h}"
 
 
 # --------------------------------------------------------------------------
@@ -166,37 +187,18 @@ def test_simt_path_matches_oracle_on_bf16(name):
     check_discrete_stages(wl, x, b, lam=lam)
 
 
-def test_end_to_end_against_oracle_chain():
+@pytest.mark.parametrize("name", ["tc_d128_rows512_ragged", "tc_rows256_think",
+                                  "tc_d64_rows128"])
+def test_end_to_end_against_oracle_chain(name):
     """Oracle's own chain (its fp64 scores) vs the GPU chain, with the
     near-tie allowances."""
-    wl, _, seed = SMALL["tc_d128_rows512_ragged"]
+    wl, lam, seed = SMALL[name]
     x = wk.make_inputs(wl, seed, device="cuda")
-    b = run_gpu(wl, x)
-    o = O()
+    b = run_gpu(wl, x, lam=lam)
     total, floor = wl.budget_args()
-    ref = o.compress(oshape(wl), x["q"], x["k"], x["v"], total, floor, wl.k_max)
-    assert_scores_close(b.scores.cpu().numpy(), ref["scores"])
-    gm = b.mba.cpu().numpy()
-    for (l, h), m in np.ndenumerate(ref["mba"]):
-        if gm[l, h] != m:
-            c = np.sort(ref["scores"][l, h])[::-1]
-            cum = np.cumsum(c)
-            thr = 0.9 * cum[-1]
-            assert abs(cum[m - 1] - thr) <= 1e-5 * thr or abs(cum[gm[l, h] - 1] - thr) <= 1e-5 * thr
-    if np.array_equal(gm, ref["mba"]):
-        assert np.array_equal(b.budget.cpu().numpy(), ref["budget"])
-    bud = b.budget.cpu().numpy()
-    gi = b.idx.cpu().numpy()
-    P = wl.prefix_len
-    for l in range(wl.n_layers):
-        n = bud[l]
-        for h in range(wl.n_kv_heads):
-            oi = set(o.topk(ref["scores"][l, h, :P], P, n).tolist())
-            diff = oi ^ set(gi[l, h, :n].tolist())
-            if diff:
-                kth = np.sort(ref["scores"][l, h, :P])[::-1][n - 1]
-                for j in diff:
-                    assert abs(ref["scores"][l, h, j] - kth) <= 1e-3 * kth
+    ref = O().compress(oshape(wl), x["q"], x["k"], x["v"], total, floor, wl.k_max,
+                       wl.mass_num, wl.mass_den, lam=lam)
+    check_end_to_end(wl, x, b, ref, lam=lam)
 
 
 def test_runs_are_deterministic():
@@ -304,137 +306,127 @@ def test_rejects_undersized_workspace_before_launch():
 
 
 # --------------------------------------------------------------------------
-# full-size workloads, in the launch configuration the benchmark times
-def _sampled_units(wl, rng, n):
-    units = [(l, h) for l in range(wl.n_layers) for h in range(wl.n_kv_heads)]
-    pick = rng.choice(len(units), size=min(n, len(units)), replace=False)
-    return [units[i] for i in sorted(pick)]
+# full-size workloads, in the launch configuration the benchmark times: every
+# (layer, KV head) unit, the oracle's own fp64 chain end to end, and the
+# stage-isolated bit-exact check on the GPU's own scores
+MBA_RTOL = 1e-5      # crossing-mass window for an MBA difference
+TOPK_RTOL = 1e-3     # adjacent-score window for an index difference
 
 
-def _check_units(wl, x, b, units):
+def check_end_to_end(wl, x, b, ref, lam=None):
+    """GPU chain vs the oracle's own chain (its fp64 scores):
+    scores within SCORE_RTOL everywhere; an MBA may differ only where the
+    oracle's cumulative mass at the GPU's count is within MBA_RTOL of 0.9 U;
+    budgets equal the oracle's when every MBA agrees, else the oracle's
+    allocation of the GPU's MBAs; top-K indices may differ only at positions
+    whose oracle score is within TOPK_RTOL of the head's n-th largest oracle
+    score; compacted bytes equal the oracle's copy under the GPU's indices;
+    ThinK channels equal the oracle's on the GPU's compacted keys except at a
+    near-tie, and the pruned bytes are those channels' bytes either way."""
     o = O()
     s = oshape(wl)
-    sc = b.scores
-    for (l, h) in units:
-        q1 = x["q"][l: l + 1].cpu()
-        k1 = x["k"][l: l + 1].cpu()
-        s1 = o.shape_of(1, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len, wl.window,
-                        wl.dtype)
-        ref = o.score_unit(s1, q1, k1, 0, h)
-        assert_scores_close(sc[l, h].cpu().numpy(), ref)
-
-
-def _check_compaction_heads(wl, b, x, bud, heads):
-    """Compacted rows of the sampled heads equal the oracle's copy for that
-    head (its K/V, the GPU's indices)."""
-    o = O()
-    P, W = wl.prefix_len, wl.window
-    n = np.clip(bud, 0, P).astype(np.int64)
-    offs = np.concatenate([[0], np.cumsum(wl.n_kv_heads * (n + W))])
-    gi = b.idx
-    for (l, h) in heads:
-        s1 = o.shape_of(1, wl.group, 1, wl.head_dim, wl.seq_len, W, wl.dtype)
-        r0 = int(offs[l] + h * (n[l] + W))
-        idx1 = gi[l, h: h + 1].cpu().numpy()[None]
-        for name, out in (("k", b.k_out), ("v", b.v_out)):
-            src = x[name][l, h].cpu()[None, None]
-            ref = o.compact(s1, src, idx1, np.array([bud[l]], dtype=np.int32), wl.k_max)
-            assert np.array_equal(o.raw(out[r0: r0 + n[l] + W]), ref), (name, l, h)
-
-
-def test_full_llama3_8b_single_layer_16k():
-    wl = wk.LLAMA3_8B_LAYER
-    x = wk.make_inputs(wl, wk.seed_for(1), device="cuda")
-    b = run_gpu(wl, x)
-    _check_units(wl, x, b, [(0, h) for h in range(wl.n_kv_heads)])
-    check_discrete_stages(wl, x, b)
-
-
-def test_full_zigzag_32k_sampled():
-    wl = wk.ZIGZAG_32K
-    x = wk.make_inputs(wl, wk.seed_for(2), device="cuda")
-    b = run_gpu(wl, x)
-    rng = np.random.default_rng(2)
-    _check_units(wl, x, b, _sampled_units(wl, rng, 3))
-    o = O()
-    s = oshape(wl)
+    P = wl.prefix_len
+    gs = b.scores.cpu().numpy()
+    assert_scores_close(gs, ref["scores"])
+    np.testing.assert_allclose(gs.astype(np.float64).sum(-1), 1.0, atol=1e-5)
+    gm = b.mba.cpu().numpy()
+    n_mba_diff = 0
+    for (l, h), m in np.ndenumerate(ref["mba"]):
+        mg = int(gm[l, h])
+        if mg == m:
+            continue
+        n_mba_diff += 1
+        c = np.sort(ref["scores"][l, h])[::-1]
+        cum = np.concatenate([[0.0], np.cumsum(c)])
+        thr = wl.mass_num / wl.mass_den * cum[-1]
+        # the oracle's mass at the GPU's count sits at the crossing
+        if mg > m:
+            assert cum[mg - 1] - thr <= MBA_RTOL * thr, f"MBA layer {l} head {h}: {mg} vs {m}"
+        else:
+            assert thr - cum[mg] <= MBA_RTOL * thr, f"MBA layer {l} head {h}: {mg} vs {m}"
     total, floor = wl.budget_args()
-    sc = b.scores.cpu().numpy()
-    np.testing.assert_allclose(sc.astype(np.float64).sum(-1), 1.0, atol=1e-5)
-    mba = o.mba_all(s, sc)
-    assert np.array_equal(mba, b.mba.cpu().numpy())
-    bud = o.budget(mba, wl.prefix_len, total, floor)
-    assert np.array_equal(bud, b.budget.cpu().numpy())
-    assert bud.sum() == total and bud.min() >= floor and len(set(bud.tolist())) > 1
-    idx = o.topk_all(s, sc, bud, wl.k_max)
+    gb = b.budget.cpu().numpy()
+    if n_mba_diff == 0:
+        assert np.array_equal(gb, ref["budget"]), "budget"
+    else:
+        assert np.array_equal(gb, o.budget(gm, P, total, floor)), "budget of the GPU's MBAs"
     gi = b.idx.cpu().numpy()
+    n_idx_diff = 0
     for l in range(wl.n_layers):
-        assert np.array_equal(gi[l, :, : bud[l]], idx[l, :, : bud[l]])
-    _check_compaction_heads(wl, b, x, bud, _sampled_units(wl, rng, 4))
-
-
-def test_full_think_128k_sampled():
-    wl = wk.THINK_128K
-    x = wk.make_inputs(wl, wk.seed_for(4), device="cuda")
-    lam = wl.think_lambda
-    b = run_gpu(wl, x, lam=lam)
-    rng = np.random.default_rng(4)
-    _check_units(wl, x, b, _sampled_units(wl, rng, 1))
-    o = O()
-    s = oshape(wl)
-    total, floor = wl.budget_args()
-    sc = b.scores.cpu().numpy()
-    mba = o.mba_all(s, sc)
-    assert np.array_equal(mba, b.mba.cpu().numpy())
-    bud = o.budget(mba, wl.prefix_len, total, floor)
-    assert np.array_equal(bud, b.budget.cpu().numpy())
-    idx = o.topk_all(s, sc, bud, wl.k_max)
-    gi = b.idx.cpu().numpy()
-    for l in range(wl.n_layers):
-        assert np.array_equal(gi[l, :, : bud[l]], idx[l, :, : bud[l]])
-    heads = _sampled_units(wl, rng, 3)
-    _check_compaction_heads(wl, b, x, bud, heads)
-    # ThinK on the sampled heads: oracle over that head's compacted keys
-    P, W, D = wl.prefix_len, wl.window, wl.head_dim
-    n = np.clip(bud, 0, P).astype(np.int64)
-    offs = np.concatenate([[0], np.cumsum(wl.n_kv_heads * (n + W))])
-    keep = b.keep
-    gchan = b.chan.cpu().numpy()
-    poffs = np.concatenate([[0], np.cumsum(wl.n_kv_heads * n * keep)])
-    for (l, h) in heads:
-        r0 = int(offs[l] + h * (n[l] + W))
-        blk = o.raw(b.k_out[r0: r0 + n[l] + W])
-        s1 = o.shape_of(1, wl.group, 1, D, wl.seq_len, W, wl.dtype)
-        chan, norms, kp = o.channel_prune(s1, blk, np.array([bud[l]], dtype=np.int32), lam)
-        assert np.array_equal(chan[0, 0], gchan[l, h])
-        p0 = int(poffs[l] + h * n[l] * keep)
-        assert np.array_equal(kp, o.raw(b.k_pruned[p0: p0 + n[l] * keep]))
-    # the outlier channels (x8) are among the kept channels of every head
-    kf = x["k"]
-    for (l, h) in heads:
-        outl = torch.topk(kf[l, h, :P].float().abs().mean(0), wl.outlier_channels).indices
-        assert set(outl.tolist()) <= set(gchan[l, h].tolist())
-
-
-def test_ragged_mistral_batch_sampled():
-    batch = wk.ragged_mistral_batch(wk.seed_for(3))
-    rng = np.random.default_rng(3)
-    o = O()
-    for wl in (min(batch, key=lambda w: w.seq_len), max(batch, key=lambda w: w.seq_len)):
-        x = wk.make_inputs(wl, wk.seed_for(3) + wl.seq_len, device="cuda")
-        b = run_gpu(wl, x)
-        _check_units(wl, x, b, _sampled_units(wl, rng, 1))
-        s = oshape(wl)
-        total, floor = wl.budget_args()
-        sc = b.scores.cpu().numpy()
-        mba = o.mba_all(s, sc)
-        assert np.array_equal(mba, b.mba.cpu().numpy())
-        bud = o.budget(mba, wl.prefix_len, total, floor)
-        assert np.array_equal(bud, b.budget.cpu().numpy())
-        idx = o.topk_all(s, sc, bud, wl.k_max)
-        gi = b.idx.cpu().numpy()
+        n = int(min(max(gb[l], 0), P))
+        if n == 0:
+            continue
+        for h in range(wl.n_kv_heads):
+            sc = ref["scores"][l, h, :P]
+            oi = o.topk(sc, P, n)
+            gl = gi[l, h, :n]
+            if np.array_equal(oi, gl):
+                continue
+            assert np.all(np.diff(gl) > 0), f"indices not ascending, layer {l} head {h}"
+            diff = np.setxor1d(oi, gl)
+            kth = np.partition(sc, P - n)[P - n]
+            assert np.all(np.abs(sc[diff] - kth) <= TOPK_RTOL * kth), \
+                f"top-K layer {l} head {h}: {diff.size} differences outside the near-tie window"
+            n_idx_diff += diff.size
+    rows = o.compact_rows(s, gb)
+    assert np.array_equal(o.raw(b.k_out[:rows]), o.compact(s, x["k"], gi, gb, wl.k_max)), "K"
+    assert np.array_equal(o.raw(b.v_out[:rows]), o.compact(s, x["v"], gi, gb, wl.k_max)), "V"
+    if lam is not None:
+        kout = o.raw(b.k_out[:rows])
+        chan, norms, kp = o.channel_prune(s, kout, gb, lam)
+        gchan = b.chan.cpu().numpy()
+        keep = b.keep
         for l in range(wl.n_layers):
-            assert np.array_equal(gi[l, :, : bud[l]], idx[l, :, : bud[l]])
-        _check_compaction_heads(wl, b, x, bud, _sampled_units(wl, rng, 2))
+            for h in range(wl.n_kv_heads):
+                if not np.array_equal(gchan[l, h], chan[l, h]):
+                    srt = np.sort(norms[l, h])[::-1]
+                    kth, nxt = srt[keep - 1], srt[keep]
+                    assert abs(kth - nxt) <= 1e-9 * kth, f"ThinK channels layer {l} head {h}"
+        check_pruned_bytes(wl, b, kout, gb)
+    return n_mba_diff, n_idx_diff
+
+
+def _full_case(wl, seed, lam=None):
+    x = wk.make_inputs(wl, seed, device="cuda")
+    b = run_gpu(wl, x, lam=lam)
+    total, floor = wl.budget_args()
+    ref = O().compress(oshape(wl), x["q"], x["k"], x["v"], total, floor, wl.k_max,
+                       wl.mass_num, wl.mass_den, lam=lam)
+    diffs = check_end_to_end(wl, x, b, ref, lam=lam)
+    bud = check_discrete_stages(wl, x, b, lam=lam)
+    return x, b, bud, diffs
+
+
+def test_full_llama3_8b_single_layer_16k_all_units():
+    wl = wk.LLAMA3_8B_LAYER
+    _, b, bud, _ = _full_case(wl, wk.seed_for(1))
+    assert bud.tolist() == [wl.per_head_budget]
+
+
+def test_full_zigzag_32k_all_units():
+    wl = wk.ZIGZAG_32K
+    _, b, bud, _ = _full_case(wl, wk.seed_for(2))
+    total, floor = wl.budget_args()
+    assert bud.sum() == total and bud.min() >= floor and len(set(bud.tolist())) > 1
+
+
+def test_full_think_128k_all_units():
+    wl = wk.THINK_128K
+    x, b, bud, _ = _full_case(wl, wk.seed_for(4), lam=wl.think_lambda)
+    # the outlier channels (x8) are among the kept channels of every head
+    gchan = b.chan.cpu().numpy()
+    P = wl.prefix_len
+    for l in range(wl.n_layers):
+        for h in range(wl.n_kv_heads):
+            outl = torch.topk(x["k"][l, h, :P].float().abs().mean(0), wl.outlier_channels).indices
+            assert set(outl.tolist()) <= set(gchan[l, h].tolist()), (l, h)
+
+
+def test_full_ragged_mistral_batch_all_prompts():
+    batch = wk.ragged_mistral_batch(wk.seed_for(3))
+    for i, wl in enumerate(batch):
+        x, b, bud, _ = _full_case(wl, wk.seed_for(3, i + 1))
+        total, floor = wl.budget_args()
+        assert bud.sum() == min(total, wl.n_layers * wl.prefix_len) and bud.min() >= floor
         del x, b
         torch.cuda.empty_cache()
