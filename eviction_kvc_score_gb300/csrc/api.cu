@@ -47,6 +47,8 @@ DeviceInfo device_info() {
 struct WsLayout {
     size_t partial_off, partial_bytes;
     size_t bias_off, bias_bytes;
+    size_t vpart_off, vpart_bytes;   // THINKV per-part channel sums
+    size_t vscore_off, vscore_bytes; // THINKV channel scores when the caller passes none
     size_t total;
 };
 
@@ -58,7 +60,11 @@ WsLayout ws_layout(const kvc_shape &s) {
     w.partial_bytes = align256((size_t)a.n_units * slots * a.rows_pad * sizeof(float2));
     w.bias_off = w.partial_off + w.partial_bytes;
     w.bias_bytes = align256((size_t)a.n_units * a.rows_pad * sizeof(float));
-    w.total = w.bias_off + w.bias_bytes;
+    w.vpart_off = w.bias_off + w.bias_bytes;
+    w.vpart_bytes = align256((size_t)value_partial_floats(s) * sizeof(float));
+    w.vscore_off = w.vpart_off + w.vpart_bytes;
+    w.vscore_bytes = align256((size_t)a.n_units * s.head_dim * sizeof(float));
+    w.total = w.vscore_off + w.vscore_bytes;
     return w;
 }
 
@@ -519,6 +525,54 @@ int kvc_channel_prune(const kvc_shape *shape, const void *k_out, const int32_t *
     if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_channel_prune")) return KVC_ERR_WORKSPACE;
     return launch_channel_prune(*shape, nullptr, k_out, budget, keep, chan, k_pruned, pruned_elems,
                                 status_word(ws), stream);
+}
+
+int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const void *k,
+                            const void *v, const void *v_out, const int32_t *budget, double lambda,
+                            float *value_scores, int32_t *chan, void *v_pruned,
+                            int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (!shape_ok(shape, "kvc_channel_prune_value")) return KVC_ERR_INVALID_ARG;
+    const kvc_shape &s = *shape;
+    if (!q_obs || !k || !v || !v_out || !budget || !chan || !v_pruned)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: NULL tensor");
+    if (!aligned16(q_obs) || !aligned16(k) || !aligned16(v))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: q_obs, k and v must be 16-byte aligned");
+    const int32_t keep = kvc_keep_channels(lambda, s.head_dim);
+    if (keep < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: lambda keeps no channel");
+    if (pruned_elems < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: bad pruned_elems");
+    const WsLayout w = ws_layout(s);
+    if (!ws_ok(ws, ws_bytes, w.total, "kvc_channel_prune_value")) return KVC_ERR_WORKSPACE;
+    const int choice = score_impl_choice();
+    if (choice < 0)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: KVC_SCORE_IMPL must be auto, simt or tc");
+    const bool can_tc = tc_eligible(s);
+    if (choice == 2 && !can_tc)
+        return fail(KVC_ERR_UNSUPPORTED, "kvc_channel_prune_value: tensor-core path needs bf16, "
+                                         "head_dim 64/128, G*W <= 512 and an sm_100-family device");
+    const bool tc = can_tc && choice != 1;
+    const ScoreSplit sp = make_split(s, tc);
+    char *base = static_cast<char *>(ws);
+    // 1. the window rows' softmax normalisers (the score pass's first half)
+    ScoreArgs a;
+    a.q = q_obs;
+    a.k = k;
+    a.scores = nullptr;
+    a.partial = reinterpret_cast<float2 *>(base + w.partial_off);
+    a.neg_bias = reinterpret_cast<float *>(base + w.bias_off);
+    a.status = status_word(ws);
+    a.stats_only = true;
+    int rc = tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
+    if (rc) return rc;
+    // 2. per-channel squared norms of the window rows' attention output
+    float *sv = value_scores ? value_scores : reinterpret_cast<float *>(base + w.vscore_off);
+    rc = launch_value_scores(s, sp, q_obs, k, v, a.neg_bias,
+                             reinterpret_cast<float *>(base + w.vpart_off), sv,
+                             tc && value_tc_eligible(s), status_word(ws), stream);
+    if (rc) return rc;
+    // 3. keep the top channels and copy them out of the kept prefix rows
+    return launch_channel_prune(s, nullptr, v_out, budget, keep, chan, v_pruned, pruned_elems,
+                                status_word(ws), stream, sv);
 }
 
 int kvc_channel_prune_query(const kvc_shape *shape, const void *q_obs, const void *k_out,

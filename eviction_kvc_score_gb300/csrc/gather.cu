@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kPruneThreads)
     channel_prune_kernel(const T *__restrict__ k_out, const T *__restrict__ q, int Hq,
                          const int32_t *__restrict__ budget, int T_len, int W, int Hkv, int D,
                          int keep, int32_t *__restrict__ chan, T *__restrict__ k_pruned,
-                         int64_t pruned_elems, uint32_t *status) {
+                         int64_t pruned_elems, uint32_t *status, const float *__restrict__ given) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ FF part[kPruneThreads];
@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kPruneThreads)
         }
         __syncthreads();
     };
-    slice_sum(k_out, row0, r_lo, r_hi, slice_k);
-    if (q != nullptr) {
+    if (given == nullptr) slice_sum(k_out, row0, r_lo, r_hi, slice_k);
+    if (given == nullptr && q != nullptr) {
         // query-driven criterion: the W window rows of each of the head's G
         // query heads, split over the cluster like the key rows
         const int G = Hq / Hkv;
@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(kPruneThreads)
     cluster.sync();
 
     // 2. whole-head sums in rank order, then rank by (score desc, d asc)
-    if (tid < D) {
+    if (tid < D && given != nullptr) {
+        m[tid] = (double)given[(int64_t)head * D + tid];   // THINKV: scores supplied
+    } else if (tid < D) {
         FF tk = {0.f, 0.f}, tq = {0.f, 0.f};
         for (int rr = 0; rr < kPruneCluster; ++rr) {
             tk = ff_add(tk, cluster.map_shared_rank(slice_k, rr)[tid]);
@@ -268,7 +270,8 @@ __global__ void __launch_bounds__(kPruneThreads)
 template <typename T>
 cudaError_t launch_prune_t(const kvc_shape &s, const void *q, const void *k_out,
                            const int32_t *budget, int32_t keep, int32_t *chan, void *k_pruned,
-                           int64_t pruned_elems, uint32_t *status, cudaStream_t st) {
+                           int64_t pruned_elems, uint32_t *status, cudaStream_t st,
+                           const float *given) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(s.n_layers * s.n_kv_heads * kPruneCluster));
     cfg.blockDim = dim3(kPruneThreads);
@@ -283,7 +286,7 @@ cudaError_t launch_prune_t(const kvc_shape &s, const void *q, const void *k_out,
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, channel_prune_kernel<T>, (const T *)k_out, (const T *)q,
                               s.n_q_heads, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim,
-                              (int)keep, chan, (T *)k_pruned, pruned_elems, status);
+                              (int)keep, chan, (T *)k_pruned, pruned_elems, status, given);
 }
 
 }  // namespace
@@ -322,16 +325,16 @@ int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32
 
 int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, const int32_t *budget,
                          int32_t keep, int32_t *chan, void *k_pruned, int64_t pruned_elems,
-                         uint32_t *status, cudaStream_t st) {
+                         uint32_t *status, cudaStream_t st, const float *given) {
     if (s.head_dim > 256) {
         set_error("kvc_channel_prune: head_dim above 256 is not supported");
         return KVC_ERR_UNSUPPORTED;
     }
     cudaError_t e0 = s.dtype == KVC_F32
                          ? launch_prune_t<float>(s, q, k_out, budget, keep, chan, k_pruned,
-                                                 pruned_elems, status, st)
+                                                 pruned_elems, status, st, given)
                          : launch_prune_t<__nv_bfloat16>(s, q, k_out, budget, keep, chan, k_pruned,
-                                                         pruned_elems, status, st);
+                                                         pruned_elems, status, st, given);
     if (e0 != cudaSuccess) {
         set_error("kvc_channel_prune: launch failed: %s", cudaGetErrorString(e0));
         return KVC_ERR_CUDA;

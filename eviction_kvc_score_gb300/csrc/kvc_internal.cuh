@@ -319,6 +319,35 @@ __device__ __forceinline__ void tc_commit2(uint64_t *bar, uint16_t cta_mask) {
         : "memory");
 }
 
+// The SM-pair MMA with its A operand in TMEM (one 128-lane block per CTA at
+// the same TMEM address in both) and B from shared memory.
+__device__ __forceinline__ void tc_mma2_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 registers -> 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
@@ -469,11 +498,17 @@ struct ScoreArgs {
     float2 *partial;   // [units][max_slots][rows_pad] (running max, sum), log2 units
     float *neg_bias;   // [units][rows_pad] = -(max + log2(sum)), -inf for pad rows
     uint32_t *status;
+    bool stats_only = false;   // stop after pass 1 + merge (row biases only)
 };
 
 // CTA pairs of the tensor-core score kernels that the current device runs at
 // once (cached per device; half the SM count if the query fails).
 int score_tc_pairs(int sms);
+// 3-D bf16 TMA view [outer][mid][inner] with a (64, box_rows, 1) box and the
+// 128-byte swizzle; rows past `mid` read as zeros.  False if the driver
+// entry point is missing or the encoding is refused.
+bool make_tma_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer,
+                  uint32_t box_rows);
 int launch_score_tc(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cudaStream_t st);
 int launch_score_tc_keyformer(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
                               uint64_t seed, double tau, cudaStream_t st);
@@ -499,10 +534,25 @@ int launch_pool(const kvc_shape &s, const float *scores, int32_t kernel, int32_t
 int launch_compact(const kvc_shape &s, const void *k, const void *v, const int32_t *idx,
                    const int32_t *budget, int per_head, int32_t k_max, void *k_out, void *v_out,
                    int64_t out_rows, uint32_t *status, cudaStream_t st);
-// q == nullptr: magnitude criterion; otherwise the query-driven one.
+// q == nullptr: magnitude criterion; otherwise the query-driven one.  With
+// `given` ([L][H_kv][D] fp32) the channels are ranked by those scores instead
+// (THINKV), and k_out may be any packed cache (the compacted values).
 int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, const int32_t *budget,
                          int32_t keep, int32_t *chan, void *k_pruned, int64_t pruned_elems,
-                         uint32_t *status, cudaStream_t st);
+                         uint32_t *status, cudaStream_t st, const float *given = nullptr);
+// THINKV: per-channel value scores [L][H_kv][D] (fp32 sums of squared window
+// attention outputs) from the row biases that a stats-only score pass left
+// in a.neg_bias; `partial` is scratch of value_partial_floats() floats.
+constexpr int kValueTcParts = 4;   // (job, CTA) partial sums per unit, tensor-core kernel
+int64_t value_partial_floats(const kvc_shape &s);
+// The tensor-core THINKV kernel serves bf16, head_dim 128, G*W <= 512.
+bool value_tc_eligible(const kvc_shape &s);
+int launch_value_tc(const kvc_shape &s, const ScoreSplit &sp, const void *q, const void *k,
+                    const void *v, const float *neg_bias, float *partial, uint32_t *status,
+                    cudaStream_t st, int *parts_out);
+int launch_value_scores(const kvc_shape &s, const ScoreSplit &sp, const void *q, const void *k,
+                        const void *v, const float *neg_bias, float *partial, float *score_v,
+                        bool tc, uint32_t *status, cudaStream_t st);
 
 void set_error(const char *fmt, ...);
 

@@ -245,7 +245,7 @@ int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, 
         return KVC_ERR_CUDA;
     }
     int rc = launch_score_merge(s, sp, a, st);
-    if (rc) return rc;
+    if (rc || a.stats_only) return rc;
     score_colmean_simt<T, NOISE><<<sp.grid, kSimtThreads, sm2, st>>>(q, k, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {

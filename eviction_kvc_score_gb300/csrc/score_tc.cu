@@ -859,19 +859,28 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// 3-D bf16 view [outer][mid][inner] with a (64, 128, 1) box, 128-byte swizzle.
-// Rows past `mid` read as zeros.
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer) {
+}  // namespace
+
+bool make_tma_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer,
+                  uint32_t box_rows) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[3] = {inner, mid, outer};
     cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+// 3-D bf16 view [outer][mid][inner] with a (64, 128, 1) box, 128-byte swizzle.
+// Rows past `mid` read as zeros.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer) {
+    return make_tma_map(m, base, inner, mid, outer, 128);
 }
 
 constexpr size_t kSmemLimit = 232448;   // 227 KiB per CTA
@@ -960,7 +969,7 @@ int launch_kh(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a, cuda
         return KVC_ERR_CUDA;
     }
     int rc = launch_score_merge(s, sp, a, st);
-    if (rc) return rc;
+    if (rc || a.stats_only) return rc;
     p.skip_first_relay = 0;
     if (noise)
         score_colmean_tc<KH, kEWGNoise, true><<<ctas, cta_threads(kEWGNoise), smem, st>>>(tq, tk, p);

@@ -1,0 +1,464 @@
+// value_tc.cu -- THINKV value-channel scores on the sm_103a tensor cores.
+//
+// What is computed ("ThinK: Thinner Key Cache by Query-Driven Pruning",
+// appendix "Value cache pruning strategy"): for every unit = (layer, KV head)
+// and window row r (position P + w, w = r mod W) the attention output
+//   o_r = sum over keys j <= P + w of 2^(x_rj + nb_r) v_j,
+//   x_rj = q_r . k_j log2(e) / sqrt(D),  nb_r = -(m_r + log2 l_r)
+// (nb_r from the score pass's pass 1 + merge, so each probability is final
+// when formed), and score_v[d] = sum_r o_r[d]^2 over the unit's G*W rows.
+//
+// Work item = (unit, job): a job is 256 of the unit's window rows, the full
+// M of one SM-pair MMA.  Items are dealt round-robin to the pairs, so with two
+// jobs per unit and an even number of pairs, pairs 2m and 2m+1 run the two
+// jobs of the same unit side by side and the second reader of each K/V tile
+// finds it in L2.  Per 128-key tile of an item:
+//   MMA1  S = Q K^T           M = 256 rows, N = 128 keys, K = D = 128
+//         (A = the CTA's 128 Q rows, B = the CTA's 64 keys, both K-major,
+//          128-byte swizzled as TMA writes them) -> a TMEM slot
+//   epi   p = 2^(s log2(e)/sqrt(D) + nb_r), 0 where row r does not see key j,
+//         rounded to bf16 and stored back into the slot (tcgen05.st)
+//   MMA2  O += P V            M = 256 rows, N = 128 channels, K = 128 keys
+//         (A = P straight from TMEM, B = the CTA's 64 channels of the tile's
+//          128 value rows, channel-contiguous: the MN-major B layout)
+// O stays in TMEM for the whole item; at its end each epilogue thread squares
+// its row's 64 channels, a warp butterfly sums them over the warp's 32 rows
+// and the four warps of a warpgroup are added in order, giving one partial
+// per (unit, job, CTA) -- reduced in a fixed order afterwards, so the result
+// is deterministic.
+//
+// TMEM (512 columns per CTA): O in columns [0,128); three S/P slots of 128
+// columns at 128, 256, 384.  Within a slot, epilogue warpgroup e reads S
+// columns [64e, 64e+64) (keys 64e..) and writes its bf16 P words into the
+// first 32 of those columns, so no thread overwrites another's unread S.
+//
+// Roles per CTA: warp 0 TMA producer (Q rows of the item; per tile its 64
+// keys and its 64 value channels of the tile's 128 keys), warp 1 the MMA
+// issuer (even CTA) or the relay of load completions (odd CTA), warps 2..9
+// two epilogue warpgroups.  Every wait is bounded (kvc_internal.cuh).
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kVStages = 4;
+constexpr int kVSlots = 3;
+constexpr int kVTileKeys = 128;                 // keys per pair tile
+constexpr int kVEWG = 2;                        // epilogue warpgroups
+constexpr int kVThreadsTC = 64 + 128 * kVEWG;
+constexpr uint32_t kVTmemCols = 512;
+constexpr uint32_t kOCol = 0;                   // O accumulator columns [0,128)
+constexpr uint32_t kSlotCol0 = 128;             // slot s at 128 + 128 s
+constexpr int kQBox = 128 * 128;                // 128 rows x 64 bf16
+constexpr int kKBox = 64 * 128;                 // 64 keys x 64 bf16
+constexpr int kVBox = 128 * 128;                // 128 keys x 64 channels
+constexpr int kStageBytes = 2 * kKBox + kVBox;  // head_dim 128: two K boxes + one V box
+
+struct VtcParams {
+    int64_t n_units;
+    int njob;             // jobs (256-row blocks) per unit
+    int64_t n_items;      // n_units * njob
+    int pairs;
+    int T, P, W, rows, rows_pad, n_tiles;
+    float cs;             // log2(e) / sqrt(D)
+    const float *neg_bias;
+    float *partial;       // [units][kValueTcParts][128]
+    uint32_t *status;
+};
+
+struct VSmem {
+    uint8_t *q;        // [2][128 rows][128 B]
+    uint8_t *kv;       // [stages][K box 0 | K box 1 | V box]
+    float *red;        // [2 warpgroups][4 quarters][64]
+    uint64_t *full, *empty, *pfull;     // [stages]
+    uint64_t *q_full, *q_empty, *q_pfull;
+    uint64_t *s_full, *p_full, *slot_empty;   // [slots]
+    uint64_t *o_full, *o_empty, *drain;
+    uint32_t *tmem_base;
+    volatile int *abort_flag;
+};
+
+constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kVStages * kStageBytes +
+                               kVEWG * 4 * 64 * sizeof(float) + (3 * kVStages + 3 * kVSlots + 8) * 8 +
+                               16;
+
+__device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
+    VSmem s;
+    uint8_t *b = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.q = b;
+    b += 2 * kQBox;
+    s.kv = b;
+    b += (size_t)kVStages * kStageBytes;
+    s.red = reinterpret_cast<float *>(b);
+    b += kVEWG * 4 * 64 * sizeof(float);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(b);
+    s.full = bars;
+    s.empty = bars + kVStages;
+    s.pfull = bars + 2 * kVStages;
+    s.q_full = bars + 3 * kVStages;
+    s.q_empty = s.q_full + 1;
+    s.q_pfull = s.q_full + 2;
+    s.s_full = s.q_full + 3;
+    s.p_full = s.s_full + kVSlots;
+    s.slot_empty = s.p_full + kVSlots;
+    s.o_full = s.slot_empty + kVSlots;
+    s.o_empty = s.o_full + 1;
+    s.drain = s.o_full + 2;
+    s.tmem_base = reinterpret_cast<uint32_t *>(s.drain + 1);
+    s.abort_flag = reinterpret_cast<volatile int *>(s.tmem_base + 1);
+    return s;
+}
+
+// Items of pair c: c, c + pairs, c + 2 pairs, ...
+struct Item {
+    int64_t u;
+    int job;
+};
+__device__ __forceinline__ Item item_of(int64_t i, int njob) {
+    Item it;
+    it.u = i / njob;
+    it.job = (int)(i % njob);
+    return it;
+}
+
+// K-major 128-byte swizzled operand (8-row groups 1024 bytes apart), as TMA
+// writes a box whose inner extent is 128 bytes.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(lbo >> 4) << 16;
+    d |= static_cast<uint64_t>(sbo >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
+    value_out_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, VtcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const VSmem s = vcarve(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank();
+    const int64_t c = cluster_id_x();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);
+            mbar_init(&s.pfull[i], 1);
+        }
+        mbar_init(s.q_full, 1);
+        mbar_init(s.q_empty, 1);
+        mbar_init(s.q_pfull, 1);
+        for (int i = 0; i < kVSlots; ++i) {
+            mbar_init(&s.s_full[i], 1);
+            mbar_init(&s.p_full[i], 2 * 4 * kVEWG);   // every epilogue warp of both CTAs
+            mbar_init(&s.slot_empty[i], 1);
+        }
+        mbar_init(s.o_full, 1);
+        mbar_init(s.o_empty, 2 * 4 * kVEWG);
+        mbar_init(s.drain, 1);
+        *s.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc2(s.tmem_base, kVTmemCols);
+        tmem_relinquish2();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *s.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            uint32_t gt = 0, qi = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+                const Item it = item_of(i, p.njob);
+                if (qi > 0 && !mbar_wait(s.q_empty, (qi - 1) & 1, s.abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(s.q_full, 2u * kQBox);
+                for (int kh = 0; kh < 2; ++kh)
+                    tma_load_3d(&tq, s.q_full, s.q + kh * kQBox, kh * 64, it.job * 256 + rank * 128,
+                                (int)it.u);
+                ++qi;
+                for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                    const uint32_t st = gt % kVStages, ph = (gt / kVStages) & 1;
+                    if (!mbar_wait(&s.empty[st], ph ^ 1, s.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *stage = s.kv + (size_t)st * kStageBytes;
+                    mbar_arrive_expect_tx(&s.full[st], (uint32_t)kStageBytes);
+                    for (int kh = 0; kh < 2; ++kh)
+                        tma_load_3d(&tk, &s.full[st], stage + kh * kKBox, kh * 64,
+                                    t * kVTileKeys + rank * 64, (int)it.u);
+                    tma_load_3d(&tv, &s.full[st], stage + 2 * kKBox, rank * 64, t * kVTileKeys,
+                                (int)it.u);
+                    ++issued;
+                }
+            }
+            if (*s.abort_flag) {   // unwind: every copy started must land
+                for (uint32_t g = issued > kVStages ? issued - kVStages : 0; g < issued; ++g)
+                    mbar_drain(&s.full[g % kVStages], (g / kVStages) & 1);
+                if (qi > 0) mbar_drain(s.q_full, (qi - 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 1) {
+            // ------------------------------------------------ relay (odd CTA)
+            const uint32_t r_pfull = mapa_shared(smem_u32(s.pfull), 0);
+            const uint32_t r_qpfull = mapa_shared(smem_u32(s.q_pfull), 0);
+            uint32_t gt = 0, qi = 0;
+            bool ok = true;
+            for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+                if (!mbar_wait(s.q_full, qi & 1, s.abort_flag, p.status)) break;
+                mbar_arrive_remote(r_qpfull);
+                ++qi;
+                for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                    const uint32_t st = gt % kVStages, ph = (gt / kVStages) & 1;
+                    if (!mbar_wait(&s.full[st], ph, s.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote(r_pfull + st * 8u);
+                }
+            }
+        } else if (lane == 0) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            constexpr uint16_t kBoth = 3;
+            const uint32_t idesc1 = idesc_bf16_f32(256, 128);              // both K-major
+            const uint32_t idesc2 = idesc_bf16_f32(256, 128) | (1u << 16);  // B MN-major
+            uint32_t gt = 0, qi = 0, items = 0;
+            bool ok = true;
+            // O += P V for tile g of the current item (first: overwrite O)
+            auto mma2 = [&](uint32_t g, bool first) -> bool {
+                const uint32_t slot = g % kVSlots, use = g / kVSlots;
+                const uint32_t st = g % kVStages;
+                if (!mbar_wait_cl(&s.p_full[slot], use & 1, s.abort_flag, p.status)) return false;
+                if (first && !mbar_wait(s.o_empty, (items & 1) ^ 1, s.abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t scol = tmem + kSlotCol0 + slot * 128;
+                const uint32_t vbase = smem_u32(s.kv + (size_t)st * kStageBytes + 2 * kKBox);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    // keys 16 ks ..: P words of warpgroup ks / 4 at columns
+                    // 64 (ks / 4) + 8 (ks % 4); value rows 16 ks .. of the box
+                    const uint32_t acol = scol + (uint32_t)((ks >> 2) * 64 + (ks & 3) * 8);
+                    const uint64_t b = desc_sw128(vbase + (uint32_t)ks * 2048u, 1024u, 1024u);
+                    tc_mma2_bf16_tmem_a(tmem + kOCol, acol, b, idesc2, (first && ks == 0) ? 0u : 1u);
+                }
+                tc_commit2(&s.slot_empty[slot], kBoth);
+                tc_commit2(&s.empty[st], kBoth);
+                return true;
+            };
+            for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+                if (!mbar_wait(s.q_full, qi & 1, s.abort_flag, p.status)) break;
+                if (!mbar_wait(s.q_pfull, qi & 1, s.abort_flag, p.status)) break;
+                ++qi;
+                for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                    const uint32_t st = gt % kVStages, ph = (gt / kVStages) & 1;
+                    const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
+                    if (!mbar_wait(&s.full[st], ph, s.abort_flag, p.status) ||
+                        !mbar_wait(&s.pfull[st], ph, s.abort_flag, p.status) ||
+                        !mbar_wait(&s.slot_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = smem_u32(s.kv + (size_t)st * kStageBytes);
+                    const uint32_t qbase = smem_u32(s.q);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int kh = ks >> 2, off = (ks & 3) * 32;
+                        const uint64_t a = desc_sw128(qbase + kh * kQBox + off, 16u, 1024u);
+                        const uint64_t b = desc_sw128(kbase + kh * kKBox + off, 16u, 1024u);
+                        tc_mma2_bf16(tmem + kSlotCol0 + slot * 128, a, b, idesc1, ks > 0);
+                    }
+                    tc_commit2(&s.s_full[slot], kBoth);
+                    if (t == p.n_tiles - 1) tc_commit2(s.q_empty, kBoth);
+                    // the previous tile's P V runs behind this tile's Q K^T
+                    if (t > 0 && !mma2(gt - 1, t == 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) break;
+                if (!mma2(gt - 1, p.n_tiles == 1)) break;
+                tc_commit2(s.o_full, kBoth);
+                ++items;
+            }
+            tc_commit2(s.drain, 1);
+            mbar_drain(s.drain, 0);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int ewg = (warp - 2) >> 2;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t r_pfull = mapa_shared(smem_u32(s.p_full), 0);
+        const uint32_t r_oempty = mapa_shared(smem_u32(s.o_empty), 0);
+        uint32_t gt = 0, items = 0;
+        bool ok = true;
+        for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+            const Item it = item_of(i, p.njob);
+            const int r = it.job * 256 + rank * 128 + quarter * 32 + lane;
+            const bool real = r < p.rows;
+            const float nb = real ? p.neg_bias[it.u * p.rows_pad + r] : -INFINITY;
+            const int lim_row = p.P + (real ? r % p.W : 0);   // last key the row sees
+            for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
+                if (!mbar_wait(&s.s_full[slot], use & 1, s.abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t scol = tmem + lane_base + kSlotCol0 + slot * 128 + ewg * 64;
+                float v[2][32];
+                tmem_ld32(scol, v[0]);
+                tmem_ld32(scol + 32, v[1]);
+                tmem_ld_wait();
+                reg_fence(v[0]);
+                reg_fence(v[1]);
+                const int j0 = t * kVTileKeys + ewg * 64;   // key of column 0
+                const int lim = lim_row - j0;                // columns <= lim are visible
+                uint32_t w32[32];
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const int c0 = 2 * i2, c1 = 2 * i2 + 1;
+                    const float p0 = c0 <= lim ? ex2(fmaf(v[c0 >> 5][c0 & 31], p.cs, nb)) : 0.f;
+                    const float p1 = c1 <= lim ? ex2(fmaf(v[c1 >> 5][c1 & 31], p.cs, nb)) : 0.f;
+                    uint32_t wd;
+                    // lower 16 bits: the even key (first along K)
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(wd) : "f"(p1), "f"(p0));
+                    w32[i2] = wd;
+                }
+                tmem_st32(scol, w32);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                // the MMA in the even CTA reads these TMEM words: release
+                // at cluster scope
+                if (lane == 0) mbar_arrive_remote_cluster(r_pfull + slot * 8u);
+            }
+            if (!ok) break;
+            // item done: this thread's row of O, channels [64 ewg, +64)
+            if (!mbar_wait(s.o_full, items & 1, s.abort_flag, p.status)) break;
+            tc_fence_after();
+            float o[2][32];
+            const uint32_t ocol = tmem + lane_base + kOCol + ewg * 64;
+            tmem_ld32(ocol, o[0]);
+            tmem_ld32(ocol + 32, o[1]);
+            tmem_ld_wait();
+            reg_fence(o[0]);
+            reg_fence(o[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(r_oempty);   // O may be overwritten
+            ++items;
+            // squares summed over the warp's 32 rows: a butterfly that halves
+            // the vector each step leaves lane l with channels 2l, 2l + 1
+            float a[64];
+#pragma unroll
+            for (int k = 0; k < 64; ++k) a[k] = o[k >> 5][k & 31] * o[k >> 5][k & 31];
+#pragma unroll
+            for (int half = 32; half >= 2; half >>= 1) {
+                const int bit = half / 2;   // lane bit that chooses the kept half
+                const bool upper = (lane & bit) != 0;
+#pragma unroll
+                for (int k = 0; k < half; ++k) {
+                    const float send = upper ? a[k] : a[k + half];
+                    const float keep = upper ? a[k + half] : a[k];
+                    a[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+                }
+            }
+            float *red = s.red + ewg * 4 * 64;
+            red[quarter * 64 + 2 * lane] = a[0];
+            red[quarter * 64 + 2 * lane + 1] = a[1];
+            named_bar_sync(1 + ewg, 128);
+            if (quarter == 0) {
+                const int ch = 2 * lane;
+                float s0 = red[ch], s1 = red[ch + 1];
+                for (int qq = 1; qq < 4; ++qq) {
+                    s0 += red[qq * 64 + ch];
+                    s1 += red[qq * 64 + ch + 1];
+                }
+                float *dst = p.partial + (it.u * kValueTcParts + it.job * 2 + rank) * 128 + ewg * 64;
+                dst[ch] = s0;
+                dst[ch + 1] = s1;
+            }
+            named_bar_sync(1 + ewg, 128);   // red is rewritten by the next item
+        }
+    }
+    // teardown: no MMA, load or remote arrive of the pair is left
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc2(tmem, kVTmemCols);
+    }
+    cluster_sync_all();
+}
+
+}  // namespace
+
+bool value_tc_eligible(const kvc_shape &s) {
+    const int G = s.n_q_heads / s.n_kv_heads;
+    return s.dtype == KVC_BF16 && s.head_dim == 128 && (int64_t)G * s.window <= kMaxRowsTC;
+}
+
+int launch_value_tc(const kvc_shape &s, const ScoreSplit &sp, const void *q, const void *k,
+                    const void *v, const float *neg_bias, float *partial, uint32_t *status,
+                    cudaStream_t st, int *parts_out) {
+    if (!value_tc_eligible(s) || sp.rows_pad % 256 || sp.rows_pad > kMaxRowsTC) {
+        set_error("kvc_channel_prune_value: tensor-core kernel needs bf16, head_dim 128 and "
+                  "G*W <= 512 with the tensor-core row split");
+        return KVC_ERR_UNSUPPORTED;
+    }
+    const int G = s.n_q_heads / s.n_kv_heads;
+    CUtensorMap tq, tk, tv;
+    const uint64_t units = (uint64_t)sp.n_units;
+    if (!make_tma_map(&tq, q, 128, (uint64_t)G * s.window, units, 128) ||
+        !make_tma_map(&tk, k, 128, (uint64_t)s.seq_len, units, 64) ||
+        !make_tma_map(&tv, v, 128, (uint64_t)s.seq_len, units, 128)) {
+        set_error("kvc_channel_prune_value: cuTensorMapEncodeTiled failed (alignment or driver)");
+        return KVC_ERR_CUDA;
+    }
+    VtcParams p;
+    p.n_units = sp.n_units;
+    p.njob = sp.rows_pad / 256;
+    p.n_items = sp.n_units * p.njob;
+    const int pairs = score_tc_pairs(0);
+    p.pairs = (int)(p.n_items < pairs ? p.n_items : pairs);
+    p.T = s.seq_len;
+    p.P = s.seq_len - s.window;
+    p.W = s.window;
+    p.rows = sp.rows;
+    p.rows_pad = sp.rows_pad;
+    p.n_tiles = (s.seq_len + kVTileKeys - 1) / kVTileKeys;
+    p.cs = (float)(kLog2e / sqrt(128.0));
+    p.neg_bias = neg_bias;
+    p.partial = partial;
+    p.status = status;
+    cudaFuncSetAttribute(value_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kVSmemBytes);
+    value_out_tc<<<2 * p.pairs, kVThreadsTC, kVSmemBytes, st>>>(tq, tk, tv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("kvc_channel_prune_value: tensor-core launch failed: %s", cudaGetErrorString(e));
+        return KVC_ERR_CUDA;
+    }
+    *parts_out = 2 * p.njob;
+    return KVC_OK;
+}
+
+}  // namespace kvc

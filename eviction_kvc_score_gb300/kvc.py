@@ -65,6 +65,8 @@ _SIGS = {
     "kvc_compact": (C.c_int, [_sp, _p, _p, _p, _p, _i32, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune": (C.c_int, [_sp, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune_query": (C.c_int, [_sp, _p, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
+    "kvc_channel_prune_value": (C.c_int, [_sp, _p, _p, _p, _p, _p, _d, _p, _p, _p, _i64, _p, _sz,
+                                          _p]),
     "kvc_keep_channels": (_i32, [_d, _i32]),
     "kvc_status_string": (C.c_char_p, [C.c_int]),
     "kvc_last_error": (C.c_char_p, []),
@@ -240,6 +242,17 @@ def kvc_channel_prune_query(s: KvcShape, q_obs, k_out, budget, lam: float, chan,
     _check("kvc_channel_prune_query", _lib.kvc_channel_prune_query(
         C.byref(s), _ptr(q_obs), _ptr(k_out), _ptr(budget), float(lam), _ptr(chan),
         _ptr(k_pruned), k_pruned.numel(), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def kvc_channel_prune_value(s: KvcShape, q_obs, k, v, v_out, budget, lam: float, chan, v_pruned,
+                            ws, value_scores=None, stream=None) -> None:
+    """THINKV: rank value channels by the squared column norms of the window
+    rows' attention output and keep the top floor((1-lam) D) of the kept
+    prefix rows of v_out (see kvc.h)."""
+    _check("kvc_channel_prune_value", _lib.kvc_channel_prune_value(
+        C.byref(s), _ptr(q_obs), _ptr(k), _ptr(v), _ptr(v_out), _ptr(budget), float(lam),
+        _ptr(value_scores), _ptr(chan), _ptr(v_pruned), v_pruned.numel(), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def kvc_keep_channels(lam: float, head_dim: int) -> int:

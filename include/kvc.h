@@ -323,6 +323,31 @@ int kvc_channel_prune_query(const kvc_shape *shape, const void *q_obs, const voi
                             const int32_t *budget, double lambda, int32_t *chan, void *k_pruned,
                             int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Optional variant of a6 for the VALUE cache -- THINKV ("ThinK: Thinner Key
+ * Cache by Query-Driven Pruning", appendix "Value cache pruning strategy":
+ * channel j of a head's value cache scores the norm of column j of the window
+ * queries' attention output, || softmax(Q_obs K^T / sqrt(D)) V[:, j] ||, and
+ * the top floor((1-lambda) D) channels are kept).  Per head (l, k):
+ *   value_scores[l][k][j] = sum over the G*W window rows r of o_r[j]^2,
+ *   o_r = sum over the keys t row r sees (t <= T-W+w, as in kvc_score) of
+ *         softmax_t(q_r . k_t / sqrt(D)) v_t
+ * (the squared norm; rows stack the KV head's G query heads); the `keep`
+ * channels with the largest value_scores (ties to the lower channel) are
+ * written ascending to chan [L][H_kv][keep] and copied out of the n_l kept
+ * prefix rows of v_out (kvc_compact's packed values) into v_pruned, packed
+ * like k_pruned (layer l: [H_kv][n_l][keep]); window rows stay full width in
+ * v_out.  q_obs, k, v are the full prompt tensors of kvc_score (16-byte
+ * aligned); value_scores is an optional DEVICE output [L][H_kv][D] fp32
+ * (NULL: kept in the workspace).  The call recomputes the window rows'
+ * softmax normalisers itself (the first half of kvc_score's work) and then
+ * forms o on the tensor cores for bf16 with head_dim 128 and G*W <= 512
+ * (probabilities rounded to bf16, fp32 accumulation), on the CUDA cores in
+ * fp32 otherwise; the workspace is kvc_workspace_size()'s. */
+int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const void *k,
+                            const void *v, const void *v_out, const int32_t *budget, double lambda,
+                            float *value_scores, int32_t *chan, void *v_pruned,
+                            int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* floor((1 - lambda) * head_dim) computed in double; 0 if lambda is outside
  * [0,1). */
 int32_t kvc_keep_channels(double lambda, int32_t head_dim);

@@ -1,0 +1,178 @@
+"""GPU parity of the optional THINKV value-channel criterion
+(kvc_channel_prune_value; ThinK page, appendix "Value cache pruning
+strategy") against the oracle, on every (layer, KV head) unit:
+
+  value scores   |s_gpu - s_ora| <= VALUE_RTOL * s_ora per channel, s_ora the
+                 oracle's fp64 squared column norms of the window rows'
+                 attention output (VALUE_RTOL per path, see below);
+  stage-isolated the oracle's selection on the GPU's own fp32 value scores
+                 gives the GPU's channels and pruned bytes bit for bit;
+  end to end     the GPU's channels equal the oracle's (from its fp64 scores)
+                 except where a channel in the symmetric difference has an
+                 oracle score within VALUE_RTOL of the head's keep-th score.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from eviction_kvc_score_gb300 import workloads as wk
+
+pytestmark = pytest.mark.gpu
+
+# CUDA cores: fp32 products and sums over at most a few 10^5 terms per output
+# (relative error ~ sqrt(T) 2^-24 < 1e-4).  Tensor cores: probabilities are
+# rounded to bf16 (relative 2^-9 each) before the fp32-accumulated product
+# with V; the rounding errors of different keys and rows are independent, so
+# a squared norm over 512 rows moves by ~2 * 2^-9 / sqrt(rows) ~ 2e-4 -- the
+# bound used is 2e-3, the worst case of a head attending to one key.
+VALUE_RTOL = {"simt": 1e-4, "tc": 2e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def K():
+    from eviction_kvc_score_gb300 import kvc
+    return kvc
+
+
+def O():
+    from oracle import oracle
+    return oracle
+
+
+def oshape(wl):
+    return O().shape_of(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len,
+                        wl.window, wl.dtype)
+
+
+CASES = {
+    # tensor-core shape: bf16, D=128, 512 window rows, ragged last tile
+    "bf16_d128_rows512": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=2, n_q_heads=8, seq_len=1500, total_budget=2 * 300,
+        layer_floor=40, temperature=(0.3, 3.0), think_lambda=0.4), 41),
+    # 384 rows: the second 256-row job is half padding
+    "bf16_d128_rows384": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=2, n_q_heads=8, seq_len=2000, window=96,
+        total_budget=2 * 380, layer_floor=30, temperature=None, think_lambda=0.3), 42),
+    # 48 rows, one tile only partly visible
+    "bf16_d128_rows48": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=2, n_q_heads=6, seq_len=300, window=16, total_budget=2 * 50,
+        layer_floor=5, temperature=None, think_lambda=0.5), 43),
+    # CUDA-core shapes
+    "bf16_d64": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=3, n_q_heads=6, head_dim=64, seq_len=777, window=64,
+        total_budget=2 * 100, layer_floor=20, think_lambda=0.4), 44),
+    "f32_mha": (wk.TINY.scaled(think_lambda=0.25), 45),
+    "f32_d80": (wk.ZIGZAG_32K.scaled(
+        n_layers=2, n_kv_heads=2, n_q_heads=4, head_dim=80, seq_len=333, window=8,
+        total_budget=2 * 60, layer_floor=10, temperature=None, dtype="f32",
+        think_lambda=0.25), 46),
+}
+
+
+def path_of(wl):
+    tc = (wl.dtype == "bf16" and wl.head_dim == 128 and wl.group * wl.window <= 512
+          and os.environ.get("KVC_SCORE_IMPL", "auto") != "simt")
+    return "tc" if tc else "simt"
+
+
+def run_value(wl, x):
+    """Default chain, then THINKV on its compacted values."""
+    kvc = K()
+    lam = wl.think_lambda
+    total, floor = wl.budget_args()
+    b = kvc.alloc_buffers(kvc.shape_of(wl), total, wl.k_max)
+    kvc.compress(b, x["q"], x["k"], x["v"], total, floor, wl.mass_num, wl.mass_den)
+    L, H, D = wl.n_layers, wl.n_kv_heads, wl.head_dim
+    keep = kvc.kvc_keep_channels(lam, D)
+    kept_rows = min(total, L * wl.prefix_len)
+    b.v_scores = torch.full((L, H, D), float("nan"), device="cuda")
+    b.v_chan = torch.full((L, H, keep), -1, dtype=torch.int32, device="cuda")
+    b.v_pruned = torch.empty(max(1, H * kept_rows * keep), dtype=x["v"].dtype, device="cuda")
+    kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget, lam,
+                                b.v_chan, b.v_pruned, b.ws, value_scores=b.v_scores)
+    torch.cuda.synchronize()
+    assert kvc.kvc_workspace_status(b.ws) == 0
+    b.v_keep = keep
+    return b
+
+
+def check_value(wl, x, b, ref_scores, rtol):
+    o = O()
+    s = oshape(wl)
+    lam = wl.think_lambda
+    gs = b.v_scores.double().cpu().numpy()
+    bad = np.abs(gs - ref_scores) > rtol * ref_scores
+    assert not bad.any(), (f"{bad.sum()} value scores out of tolerance, worst relative "
+                           f"{(np.abs(gs - ref_scores) / ref_scores).max():.2e}")
+    bud = b.budget.cpu().numpy()
+    rows = o.compact_rows(s, bud)
+    v_out = o.raw(b.v_out[:rows])
+    # stage-isolated: the oracle's selection on the GPU's own scores
+    chan_g, vp_g = o.channel_prune_value(s, b.v_scores.cpu().numpy(), v_out, bud, lam)
+    gchan = b.v_chan.cpu().numpy()
+    assert np.array_equal(gchan, chan_g), "channels on the GPU's scores"
+    assert np.array_equal(o.raw(b.v_pruned[: vp_g.size]), vp_g), "pruned V bytes"
+    # end to end: the oracle's own fp64 scores, near-ties allowed
+    chan_o, _ = o.channel_prune_value(s, ref_scores, v_out, bud, lam)
+    keep = b.v_keep
+    n_diff = 0
+    for l in range(wl.n_layers):
+        for h in range(wl.n_kv_heads):
+            diff = np.setxor1d(gchan[l, h], chan_o[l, h])
+            if diff.size:
+                kth = np.sort(ref_scores[l, h])[::-1][keep - 1]
+                assert np.all(np.abs(ref_scores[l, h, diff] - kth) <= rtol * kth), (l, h)
+                n_diff += diff.size
+    return n_diff
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_value_channels_match_oracle(name):
+    wl, seed = CASES[name]
+    x = wk.make_inputs(wl, seed, device="cuda")
+    b = run_value(wl, x)
+    ref = O().value_scores(oshape(wl), x["q"], x["k"], x["v"])
+    check_value(wl, x, b, ref, VALUE_RTOL[path_of(wl)])
+
+
+def test_value_cuda_core_path_on_tensor_core_shape():
+    wl, seed = CASES["bf16_d128_rows512"]
+    x = wk.make_inputs(wl, seed, device="cuda")
+    old = os.environ.get("KVC_SCORE_IMPL")
+    os.environ["KVC_SCORE_IMPL"] = "simt"
+    try:
+        b = run_value(wl, x)
+    finally:
+        if old is None:
+            os.environ.pop("KVC_SCORE_IMPL", None)
+        else:
+            os.environ["KVC_SCORE_IMPL"] = old
+    ref = O().value_scores(oshape(wl), x["q"], x["k"], x["v"])
+    check_value(wl, x, b, ref, VALUE_RTOL["simt"])
+
+
+def test_value_full_llama3_layer_16k_all_units():
+    wl = wk.LLAMA3_8B_LAYER.scaled(think_lambda=0.3)
+    x = wk.make_inputs(wl, wk.seed_for(1), device="cuda")
+    b = run_value(wl, x)
+    ref = O().value_scores(oshape(wl), x["q"], x["k"], x["v"])
+    check_value(wl, x, b, ref, VALUE_RTOL[path_of(wl)])
+
+
+def test_value_runs_are_deterministic():
+    wl, seed = CASES["bf16_d128_rows512"]
+    x = wk.make_inputs(wl, seed, device="cuda")
+    a = run_value(wl, x)
+    b = run_value(wl, x)
+    assert torch.equal(a.v_scores, b.v_scores) and torch.equal(a.v_chan, b.v_chan)
+    assert torch.equal(a.v_pruned, b.v_pruned)
