@@ -42,7 +42,7 @@ SUSTAINED_REGION_S = 2.0
 # kernels each C-ABI call launches
 LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
             "kvc_channel_prune": 1, "kvc_pool_scores": 1, "kvc_head_budget": 1,
-            "kvc_threshold_select": 1}
+            "kvc_threshold_select": 1, "kvc_channel_prune_value": 5}
 
 
 def parse():
@@ -63,6 +63,9 @@ def parse():
                          "to the scores before top-K (0 = off)")
     ap.add_argument("--think-criterion", default="magnitude", choices=["magnitude", "query"],
                     help="ThinK key-channel criterion on workloads that prune channels")
+    ap.add_argument("--think-value", type=float, default=0.0,
+                    help="optional THINKV: also prune value channels (ratio lambda, e.g. 0.3) "
+                         "by the window rows' attention-output norms after compaction")
     ap.add_argument("--select", default="layer", choices=["layer", "head", "threshold"],
                     help="token selection: per-layer budgets (default), per-head budgets split "
                          "by MBA inside each layer, or every prefix token scoring >= tau")
@@ -267,6 +270,13 @@ def run_kvc(args):
         b = kvc.alloc_buffers(kvc.shape_of(wl), total, wl.k_max, lam=wl.think_lambda)
         if args.pool > 1:
             b.pooled = torch.empty_like(b.scores)
+        if args.think_value > 0:
+            keep_v = kvc.kvc_keep_channels(args.think_value, wl.head_dim)
+            kept = min(total, wl.n_layers * (wl.seq_len - wl.window))
+            b.v_chan = torch.empty((wl.n_layers, wl.n_kv_heads, keep_v), dtype=torch.int32,
+                                   device=dev)
+            b.v_pruned = torch.empty(max(1, wl.n_kv_heads * kept * keep_v), dtype=b.v_out.dtype,
+                                     device=dev)
         if args.select != "layer":
             L, H, P = wl.n_layers, wl.n_kv_heads, wl.seq_len - wl.window
             b.head_counts = torch.empty((L, H), dtype=torch.int32, device=dev)
@@ -332,6 +342,10 @@ def run_kvc(args):
                 kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
                                 b.v_out, b.ws)
                 mark("kvc_compact")
+            if args.think_value > 0:
+                kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                            args.think_value, b.v_chan, b.v_pruned, b.ws)
+                mark("kvc_channel_prune_value")
             if wl.think_lambda is not None:
                 if args.think_criterion == "query":
                     kvc.kvc_channel_prune_query(b.shape, x["q"], b.k_out, b.budget,
@@ -442,6 +456,7 @@ def run_kvc(args):
                    "window": jobs[0][0].window, "think_lambda": jobs[0][0].think_lambda,
                    "think_criterion": (args.think_criterion if jobs[0][0].think_lambda is not None
                                        else None),
+                   "think_value_lambda": args.think_value if args.think_value > 0 else None,
                    "pool_kernel": args.pool if args.pool > 1 else None,
                    "select": args.select,
                    "score": args.score,
@@ -465,7 +480,8 @@ def run_kvc(args):
                                        "kvc_compact"))
              + (LAUNCHES["kvc_head_budget"] if args.select == "head" else 0)
              + (LAUNCHES["kvc_pool_scores"] if args.pool > 1 else 0))
-            + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)),
+            + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)
+            + (LAUNCHES["kvc_channel_prune_value"] if args.think_value > 0 else 0)),
         "stages_ms": {k: round(v / len(jobs), 4) for k, v in stages.items()},
         "wall_s_timed": round(t_wall, 3),
     }

@@ -17,20 +17,26 @@
 //         (A = the CTA's 128 Q rows, B = the CTA's 64 keys, both K-major,
 //          128-byte swizzled as TMA writes them) -> a TMEM slot
 //   epi   p = 2^(s log2(e)/sqrt(D) + nb_r), 0 where row r does not see key j,
-//         rounded to bf16 and stored back into the slot (tcgen05.st)
-//   MMA2  O += P V            M = 256 rows, N = 128 channels, K = 128 keys
+//         split into bf16 p_hi = bf16(p) and p_lo = bf16(p - p_hi) (about 16
+//         significant bits together) and stored back into the slot (tcgen05.st)
+//   MMA2  O += P_hi V + P_lo V   M = 256 rows, N = 128 channels, K = 128 keys
 //         (A = P straight from TMEM, B = the CTA's 64 channels of the tile's
 //          128 value rows, channel-contiguous: the MN-major B layout)
-// O stays in TMEM for the whole item; at its end each epilogue thread squares
-// its row's 64 channels, a warp butterfly sums them over the warp's 32 rows
+// A single bf16 P (8 bits) moved the squared norms of a head with few window
+// rows by up to 3e-3; the two-term split brings every score within 1e-4 of
+// the fp64 definition at the price of a second P V product.
+// O accumulates in TMEM over chunks of kChunkTiles tiles, each chunk added
+// into fp32 registers by the epilogue; at the item's end each epilogue thread
+// squares its row's 64 channels, a warp butterfly sums them over the warp's 32 rows
 // and the four warps of a warpgroup are added in order, giving one partial
 // per (unit, job, CTA) -- reduced in a fixed order afterwards, so the result
 // is deterministic.
 //
 // TMEM (512 columns per CTA): O in columns [0,128); three S/P slots of 128
 // columns at 128, 256, 384.  Within a slot, epilogue warpgroup e reads S
-// columns [64e, 64e+64) (keys 64e..) and writes its bf16 P words into the
-// first 32 of those columns, so no thread overwrites another's unread S.
+// columns [64e, 64e+64) (keys 64e..) in two halves of 32 columns and writes
+// each half's 16 P_hi and 16 P_lo words back into that half's own columns,
+// so no thread overwrites S that it or another thread has not yet read.
 //
 // Roles per CTA: warp 0 TMA producer (Q rows of the item; per tile its 64
 // keys and its 64 value channels of the tile's 128 keys), warp 1 the MMA
@@ -45,6 +51,11 @@ namespace {
 constexpr int kVStages = 4;
 constexpr int kVSlots = 3;
 constexpr int kVTileKeys = 128;                 // keys per pair tile
+// O is accumulated in TMEM over chunks of this many tiles (2048 keys, 256
+// MMAs) and each chunk is added into fp32 registers by the epilogue: the
+// tensor core's fp32 accumulation loses about half an ulp per MMA in one
+// direction, which over a 32K-key item (4096 MMAs) moved O by ~2.5e-4.
+constexpr int kChunkTiles = 16;
 constexpr int kVEWG = 2;                        // epilogue warpgroups
 constexpr int kVThreadsTC = 64 + 128 * kVEWG;
 constexpr uint32_t kVTmemCols = 512;
@@ -236,28 +247,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             constexpr uint16_t kBoth = 3;
             const uint32_t idesc1 = idesc_bf16_f32(256, 128);              // both K-major
             const uint32_t idesc2 = idesc_bf16_f32(256, 128) | (1u << 16);  // B MN-major
-            uint32_t gt = 0, qi = 0, items = 0;
+            uint32_t gt = 0, qi = 0;
             bool ok = true;
-            // O += P V for tile g of the current item (first: overwrite O)
-            auto mma2 = [&](uint32_t g, bool first) -> bool {
+            uint32_t chunks = 0;   // chunks of O handed to the epilogue so far
+            // O += P V for tile g, the item's tile t (a chunk's first tile
+            // overwrites O; its last hands O to the epilogue)
+            auto mma2 = [&](uint32_t g, int t) -> bool {
                 const uint32_t slot = g % kVSlots, use = g / kVSlots;
                 const uint32_t st = g % kVStages;
+                const bool first = t % kChunkTiles == 0;
+                const bool last = t % kChunkTiles == kChunkTiles - 1 || t == p.n_tiles - 1;
                 if (!mbar_wait_cl(&s.p_full[slot], use & 1, s.abort_flag, p.status)) return false;
-                if (first && !mbar_wait(s.o_empty, (items & 1) ^ 1, s.abort_flag, p.status))
+                if (first && !mbar_wait(s.o_empty, (chunks & 1) ^ 1, s.abort_flag, p.status))
                     return false;
                 tc_fence_after();
                 const uint32_t scol = tmem + kSlotCol0 + slot * 128;
                 const uint32_t vbase = smem_u32(s.kv + (size_t)st * kStageBytes + 2 * kKBox);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    // keys 16 ks ..: P words of warpgroup ks / 4 at columns
-                    // 64 (ks / 4) + 8 (ks % 4); value rows 16 ks .. of the box
-                    const uint32_t acol = scol + (uint32_t)((ks >> 2) * 64 + (ks & 3) * 8);
+                    // keys 16 ks ..: warpgroup e = ks / 4, half h = (ks / 2) % 2
+                    // of its 64 keys; the half's P_hi words at columns
+                    // 64 e + 32 h + 8 (ks % 2), its P_lo words 16 further;
+                    // value rows 16 ks .. of the box
+                    const uint32_t acol =
+                        scol + (uint32_t)((ks >> 2) * 64 + ((ks >> 1) & 1) * 32 + (ks & 1) * 8);
                     const uint64_t b = desc_sw128(vbase + (uint32_t)ks * 2048u, 1024u, 1024u);
                     tc_mma2_bf16_tmem_a(tmem + kOCol, acol, b, idesc2, (first && ks == 0) ? 0u : 1u);
+                    tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 16u, b, idesc2, 1u);
                 }
                 tc_commit2(&s.slot_empty[slot], kBoth);
                 tc_commit2(&s.empty[st], kBoth);
+                if (last) {
+                    tc_commit2(s.o_full, kBoth);
+                    ++chunks;
+                }
                 return true;
             };
             for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
@@ -286,15 +309,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     tc_commit2(&s.s_full[slot], kBoth);
                     if (t == p.n_tiles - 1) tc_commit2(s.q_empty, kBoth);
                     // the previous tile's P V runs behind this tile's Q K^T
-                    if (t > 0 && !mma2(gt - 1, t == 1)) {
+                    if (t > 0 && !mma2(gt - 1, t - 1)) {
                         ok = false;
                         break;
                     }
                 }
                 if (!ok) break;
-                if (!mma2(gt - 1, p.n_tiles == 1)) break;
-                tc_commit2(s.o_full, kBoth);
-                ++items;
+                if (!mma2(gt - 1, p.n_tiles - 1)) break;
             }
             tc_commit2(s.drain, 1);
             mbar_drain(s.drain, 0);
@@ -306,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t r_pfull = mapa_shared(smem_u32(s.p_full), 0);
         const uint32_t r_oempty = mapa_shared(smem_u32(s.o_empty), 0);
-        uint32_t gt = 0, items = 0;
+        uint32_t gt = 0, chunks = 0;
         bool ok = true;
         for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
             const Item it = item_of(i, p.njob);
@@ -314,6 +335,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             const bool real = r < p.rows;
             const float nb = real ? p.neg_bias[it.u * p.rows_pad + r] : -INFINITY;
             const int lim_row = p.P + (real ? r % p.W : 0);   // last key the row sees
+            float acc[64];   // this row's O, channels [64 ewg, +64), summed over chunks
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
             for (int t = 0; t < p.n_tiles; ++t, ++gt) {
                 const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
                 if (!mbar_wait(&s.s_full[slot], use & 1, s.abort_flag, p.status)) {
@@ -321,54 +345,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t scol = tmem + lane_base + kSlotCol0 + slot * 128 + ewg * 64;
-                float v[2][32];
-                tmem_ld32(scol, v[0]);
-                tmem_ld32(scol + 32, v[1]);
-                tmem_ld_wait();
-                reg_fence(v[0]);
-                reg_fence(v[1]);
-                const int j0 = t * kVTileKeys + ewg * 64;   // key of column 0
-                const int lim = lim_row - j0;                // columns <= lim are visible
-                uint32_t w32[32];
+                // this warpgroup's 64 keys in two halves of 32: a half's P
+                // words (16 hi, then 16 lo) go into its own S columns once
+                // they are in registers
 #pragma unroll
-                for (int i2 = 0; i2 < 32; ++i2) {
-                    const int c0 = 2 * i2, c1 = 2 * i2 + 1;
-                    const float p0 = c0 <= lim ? ex2(fmaf(v[c0 >> 5][c0 & 31], p.cs, nb)) : 0.f;
-                    const float p1 = c1 <= lim ? ex2(fmaf(v[c1 >> 5][c1 & 31], p.cs, nb)) : 0.f;
-                    uint32_t wd;
-                    // lower 16 bits: the even key (first along K)
-                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(wd) : "f"(p1), "f"(p0));
-                    w32[i2] = wd;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t scol = tmem + lane_base + kSlotCol0 + slot * 128 + ewg * 64 + h * 32;
+                    float v[32];
+                    tmem_ld32(scol, v);
+                    tmem_ld_wait();
+                    reg_fence(v);
+                    const int lim = lim_row - (t * kVTileKeys + ewg * 64 + h * 32);
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i2 = 0; i2 < 16; ++i2) {
+                        const int c0 = 2 * i2, c1 = 2 * i2 + 1;
+                        const float p0 = c0 <= lim ? ex2(fmaf(v[c0], p.cs, nb)) : 0.f;
+                        const float p1 = c1 <= lim ? ex2(fmaf(v[c1], p.cs, nb)) : 0.f;
+                        uint32_t hi, lo;
+                        // lower 16 bits: the even key (first along K)
+                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(p1), "f"(p0));
+                        const float h0 = __uint_as_float(hi << 16);
+                        const float h1 = __uint_as_float(hi & 0xFFFF0000u);
+                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(p1 - h1), "f"(p0 - h0));
+                        w[i2] = hi;
+                        w[16 + i2] = lo;
+                    }
+                    tmem_st32(scol, w);
                 }
-                tmem_st32(scol, w32);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 // the MMA in the even CTA reads these TMEM words: release
                 // at cluster scope
                 if (lane == 0) mbar_arrive_remote_cluster(r_pfull + slot * 8u);
+                if (t % kChunkTiles == kChunkTiles - 1 || t == p.n_tiles - 1) {
+                    // a chunk of O is complete: add it to the registers
+                    if (!mbar_wait(s.o_full, chunks & 1, s.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    ++chunks;
+                    tc_fence_after();
+                    const uint32_t ocol = tmem + lane_base + kOCol + ewg * 64;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float o[32];
+                        tmem_ld32(ocol + h * 32, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) acc[h * 32 + k] += o[k];
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(r_oempty);   // O may be overwritten
+                }
             }
             if (!ok) break;
-            // item done: this thread's row of O, channels [64 ewg, +64)
-            if (!mbar_wait(s.o_full, items & 1, s.abort_flag, p.status)) break;
-            tc_fence_after();
-            float o[2][32];
-            const uint32_t ocol = tmem + lane_base + kOCol + ewg * 64;
-            tmem_ld32(ocol, o[0]);
-            tmem_ld32(ocol + 32, o[1]);
-            tmem_ld_wait();
-            reg_fence(o[0]);
-            reg_fence(o[1]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(r_oempty);   // O may be overwritten
-            ++items;
             // squares summed over the warp's 32 rows: a butterfly that halves
             // the vector each step leaves lane l with channels 2l, 2l + 1
             float a[64];
 #pragma unroll
-            for (int k = 0; k < 64; ++k) a[k] = o[k >> 5][k & 31] * o[k >> 5][k & 31];
+            for (int k = 0; k < 64; ++k) a[k] = acc[k] * acc[k];
 #pragma unroll
             for (int half = 32; half >= 2; half >>= 1) {
                 const int bit = half / 2;   // lane bit that chooses the kept half
