@@ -17,8 +17,9 @@
 //         (A = the CTA's 128 Q rows, B = the CTA's 64 keys, both K-major,
 //          128-byte swizzled as TMA writes them) -> a TMEM slot
 //   epi   p = 2^(s log2(e)/sqrt(D) + nb_r), 0 where row r does not see key j,
-//         split into bf16 p_hi = bf16(p) and p_lo = bf16(p - p_hi) (about 16
-//         significant bits together) and stored back into the slot (tcgen05.st)
+//         split into bf16 p_hi = p truncated to its top 16 bits and p_lo =
+//         bf16(p - p_hi) (about 16 significant bits together) and stored back
+//         into the slot (tcgen05.st)
 //   MMA2  O += P_hi V + P_lo V   M = 256 rows, N = 128 channels, K = 128 keys
 //         (A = P straight from TMEM, B = the CTA's 64 channels of the tile's
 //          128 value rows, channel-contiguous: the MN-major B layout)
@@ -27,21 +28,23 @@
 // the fp64 definition at the price of a second P V product.
 // O accumulates in TMEM over chunks of kChunkTiles tiles, each chunk added
 // into fp32 registers by the epilogue; at the item's end each epilogue thread
-// squares its row's 64 channels, a warp butterfly sums them over the warp's 32 rows
+// squares its row's 32 channels, a warp butterfly sums them over the warp's 32 rows
 // and the four warps of a warpgroup are added in order, giving one partial
 // per (unit, job, CTA) -- reduced in a fixed order afterwards, so the result
 // is deterministic.
 //
 // TMEM (512 columns per CTA): O in columns [0,128); three S/P slots of 128
 // columns at 128, 256, 384.  Within a slot, epilogue warpgroup e reads S
-// columns [64e, 64e+64) (keys 64e..) in two halves of 32 columns and writes
-// each half's 16 P_hi and 16 P_lo words back into that half's own columns,
-// so no thread overwrites S that it or another thread has not yet read.
+// columns [32e, 32e+32) (keys 32e..) in two halves of 16 and writes each
+// half's 8 P_hi and 8 P_lo words back into its own 16 columns (one MMA K-step
+// of P: hi words, then lo words), so no thread overwrites S that it or
+// another thread has not yet read; it also owns O channels [32e, 32e+32).
 //
 // Roles per CTA: warp 0 TMA producer (Q rows of the item; per tile its 64
 // keys and its 64 value channels of the tile's 128 keys), warp 1 the MMA
-// issuer (even CTA) or the relay of load completions (odd CTA), warps 2..9
-// two epilogue warpgroups.  Every wait is bounded (kvc_internal.cuh).
+// issuer (even CTA) or the relay of load completions (odd CTA), warps 2..17
+// four epilogue warpgroups (four warps per SM sub-partition hide the
+// exponentials' latency; two left the kernel at 40% of its MMA time).  Every wait is bounded (kvc_internal.cuh).
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -56,7 +59,8 @@ constexpr int kVTileKeys = 128;                 // keys per pair tile
 // tensor core's fp32 accumulation loses about half an ulp per MMA in one
 // direction, which over a 32K-key item (4096 MMAs) moved O by ~2.5e-4.
 constexpr int kChunkTiles = 16;
-constexpr int kVEWG = 2;                        // epilogue warpgroups
+constexpr int kVEWG = 4;                        // epilogue warpgroups
+constexpr int kVKeysWG = kVTileKeys / kVEWG;    // S columns (keys) and O channels per warpgroup
 constexpr int kVThreadsTC = 64 + 128 * kVEWG;
 constexpr uint32_t kVTmemCols = 512;
 constexpr uint32_t kOCol = 0;                   // O accumulator columns [0,128)
@@ -91,7 +95,7 @@ struct VSmem {
 };
 
 constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kVStages * kStageBytes +
-                               kVEWG * 4 * 64 * sizeof(float) + (3 * kVStages + 3 * kVSlots + 8) * 8 +
+                               kVEWG * 4 * kVKeysWG * sizeof(float) + (3 * kVStages + 3 * kVSlots + 8) * 8 +
                                16;
 
 __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
@@ -102,7 +106,7 @@ __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
     s.kv = b;
     b += (size_t)kVStages * kStageBytes;
     s.red = reinterpret_cast<float *>(b);
-    b += kVEWG * 4 * 64 * sizeof(float);
+    b += kVEWG * 4 * kVKeysWG * sizeof(float);
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
     s.full = bars;
     s.empty = bars + kVStages;
@@ -257,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                 const uint32_t st = g % kVStages;
                 const bool first = t % kChunkTiles == 0;
                 const bool last = t % kChunkTiles == kChunkTiles - 1 || t == p.n_tiles - 1;
-                if (!mbar_wait_cl(&s.p_full[slot], use & 1, s.abort_flag, p.status)) return false;
+                if (!mbar_wait(&s.p_full[slot], use & 1, s.abort_flag, p.status)) return false;
                 if (first && !mbar_wait(s.o_empty, (chunks & 1) ^ 1, s.abort_flag, p.status))
                     return false;
                 tc_fence_after();
@@ -265,15 +269,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                 const uint32_t vbase = smem_u32(s.kv + (size_t)st * kStageBytes + 2 * kKBox);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    // keys 16 ks ..: warpgroup e = ks / 4, half h = (ks / 2) % 2
-                    // of its 64 keys; the half's P_hi words at columns
-                    // 64 e + 32 h + 8 (ks % 2), its P_lo words 16 further;
-                    // value rows 16 ks .. of the box
-                    const uint32_t acol =
-                        scol + (uint32_t)((ks >> 2) * 64 + ((ks >> 1) & 1) * 32 + (ks & 1) * 8);
+                    // keys 16 ks ..: the P_hi words of that half of warpgroup
+                    // ks / 2's keys at columns 16 ks, its P_lo words 8
+                    // further; value rows 16 ks .. of the box
+                    const uint32_t acol = scol + (uint32_t)(ks * 16);
                     const uint64_t b = desc_sw128(vbase + (uint32_t)ks * 2048u, 1024u, 1024u);
                     tc_mma2_bf16_tmem_a(tmem + kOCol, acol, b, idesc2, (first && ks == 0) ? 0u : 1u);
-                    tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 16u, b, idesc2, 1u);
+                    tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 8u, b, idesc2, 1u);
                 }
                 tc_commit2(&s.slot_empty[slot], kBoth);
                 tc_commit2(&s.empty[st], kBoth);
@@ -335,9 +337,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             const bool real = r < p.rows;
             const float nb = real ? p.neg_bias[it.u * p.rows_pad + r] : -INFINITY;
             const int lim_row = p.P + (real ? r % p.W : 0);   // last key the row sees
-            float acc[64];   // this row's O, channels [64 ewg, +64), summed over chunks
+            float acc[kVKeysWG];   // this row's O, channels [32 ewg, +32), summed over chunks
 #pragma unroll
-            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
+            for (int k = 0; k < kVKeysWG; ++k) acc[k] = 0.f;
             for (int t = 0; t < p.n_tiles; ++t, ++gt) {
                 const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
                 if (!mbar_wait(&s.s_full[slot], use & 1, s.abort_flag, p.status)) {
@@ -345,40 +347,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     break;
                 }
                 tc_fence_after();
-                // this warpgroup's 64 keys in two halves of 32: a half's P
-                // words (16 hi, then 16 lo) go into its own S columns once
-                // they are in registers
+                // this warpgroup's 32 keys in two halves of 16 (one MMA K-step
+                // each): a half's P words (8 hi, then 8 lo) go back into its
+                // own 16 S columns once read
+                const unsigned long long cs2 = f2_pack(p.cs, p.cs), nb2 = f2_pack(nb, nb);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t scol = tmem + lane_base + kSlotCol0 + slot * 128 + ewg * 64 + h * 32;
-                    float v[32];
-                    tmem_ld32(scol, v);
+                    const uint32_t scol =
+                        tmem + lane_base + kSlotCol0 + slot * 128 + ewg * kVKeysWG + h * 16;
+                    float v[16];
+                    tmem_ld16(scol, v);
                     tmem_ld_wait();
-                    reg_fence(v);
-                    const int lim = lim_row - (t * kVTileKeys + ewg * 64 + h * 32);
-                    uint32_t w[32];
+                    asm volatile("" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]),
+                                 "+f"(v[5]), "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]),
+                                 "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
+                                 "+f"(v[15]));
+                    const int lim = lim_row - (t * kVTileKeys + ewg * kVKeysWG + h * 16);
+                    if (lim < 15) {   // the window's causal edge: mask invisible keys
 #pragma unroll
-                    for (int i2 = 0; i2 < 16; ++i2) {
-                        const int c0 = 2 * i2, c1 = 2 * i2 + 1;
-                        const float p0 = c0 <= lim ? ex2(fmaf(v[c0], p.cs, nb)) : 0.f;
-                        const float p1 = c1 <= lim ? ex2(fmaf(v[c1], p.cs, nb)) : 0.f;
+                        for (int i = 0; i < 16; ++i)
+                            if (i > lim) v[i] = -INFINITY;   // 2^-inf = +0
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) {
+                        float y0, y1;
+                        f2_unpack(f2_fma(f2_pack(v[2 * i2], v[2 * i2 + 1]), cs2, nb2), y0, y1);
+                        const float p0 = ex2(y0), p1 = ex2(y1);
+                        // p = hi + lo: hi keeps the top 16 bits (truncated, a
+                        // bf16), lo = p - hi is exact and rounded to bf16
+                        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                        const unsigned long long lo2 = f2_add(
+                            f2_pack(p0, p1), f2_pack(-__uint_as_float(b0 & 0xFFFF0000u),
+                                                     -__uint_as_float(b1 & 0xFFFF0000u)));
+                        float l0, l1;
+                        f2_unpack(lo2, l0, l1);
                         uint32_t hi, lo;
                         // lower 16 bits: the even key (first along K)
-                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(p1), "f"(p0));
-                        const float h0 = __uint_as_float(hi << 16);
-                        const float h1 = __uint_as_float(hi & 0xFFFF0000u);
-                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(p1 - h1), "f"(p0 - h0));
+                        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(b0), "r"(b1));
+                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(l1), "f"(l0));
                         w[i2] = hi;
-                        w[16 + i2] = lo;
+                        w[8 + i2] = lo;
                     }
-                    tmem_st32(scol, w);
+                    tmem_st16(scol, w);
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                // the MMA in the even CTA reads these TMEM words: release
-                // at cluster scope
-                if (lane == 0) mbar_arrive_remote_cluster(r_pfull + slot * 8u);
+                // the stores are complete (wait::st) and fenced for the
+                // thread sync: hand the slot to the MMA issuer
+                if (lane == 0) mbar_arrive_remote(r_pfull + slot * 8u);
                 if (t % kChunkTiles == kChunkTiles - 1 || t == p.n_tiles - 1) {
                     // a chunk of O is complete: add it to the registers
                     if (!mbar_wait(s.o_full, chunks & 1, s.abort_flag, p.status)) {
@@ -387,15 +405,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     }
                     ++chunks;
                     tc_fence_after();
-                    const uint32_t ocol = tmem + lane_base + kOCol + ewg * 64;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    const uint32_t ocol = tmem + lane_base + kOCol + ewg * kVKeysWG;
+                    {
                         float o[32];
-                        tmem_ld32(ocol + h * 32, o);
+                        tmem_ld32(ocol, o);
                         tmem_ld_wait();
                         reg_fence(o);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) acc[h * 32 + k] += o[k];
+                        for (int k = 0; k < 32; ++k) acc[k] += o[k];
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -404,35 +421,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             }
             if (!ok) break;
             // squares summed over the warp's 32 rows: a butterfly that halves
-            // the vector each step leaves lane l with channels 2l, 2l + 1
-            float a[64];
+            // the vector each step leaves lane l with channel l
+            float a[32];
 #pragma unroll
-            for (int k = 0; k < 64; ++k) a[k] = acc[k] * acc[k];
+            for (int k = 0; k < 32; ++k) a[k] = acc[k] * acc[k];
 #pragma unroll
-            for (int half = 32; half >= 2; half >>= 1) {
-                const int bit = half / 2;   // lane bit that chooses the kept half
-                const bool upper = (lane & bit) != 0;
+            for (int half = 16; half >= 1; half >>= 1) {
+                const bool upper = (lane & half) != 0;   // lane bit that chooses the kept half
 #pragma unroll
                 for (int k = 0; k < half; ++k) {
                     const float send = upper ? a[k] : a[k + half];
                     const float keep = upper ? a[k + half] : a[k];
-                    a[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+                    a[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
                 }
             }
-            float *red = s.red + ewg * 4 * 64;
-            red[quarter * 64 + 2 * lane] = a[0];
-            red[quarter * 64 + 2 * lane + 1] = a[1];
+            float *red = s.red + ewg * 4 * kVKeysWG;
+            red[quarter * kVKeysWG + lane] = a[0];
             named_bar_sync(1 + ewg, 128);
             if (quarter == 0) {
-                const int ch = 2 * lane;
-                float s0 = red[ch], s1 = red[ch + 1];
-                for (int qq = 1; qq < 4; ++qq) {
-                    s0 += red[qq * 64 + ch];
-                    s1 += red[qq * 64 + ch + 1];
-                }
-                float *dst = p.partial + (it.u * kValueTcParts + it.job * 2 + rank) * 128 + ewg * 64;
-                dst[ch] = s0;
-                dst[ch + 1] = s1;
+                float s0 = red[lane];
+                for (int qq = 1; qq < 4; ++qq) s0 += red[qq * kVKeysWG + lane];
+                p.partial[(it.u * kValueTcParts + it.job * 2 + rank) * 128 + ewg * kVKeysWG + lane] = s0;
             }
             named_bar_sync(1 + ewg, 128);   // red is rewritten by the next item
         }
