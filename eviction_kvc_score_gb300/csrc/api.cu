@@ -218,6 +218,7 @@ size_t kvc_workspace_size(const kvc_shape *shape, int32_t k_max) {
 }
 
 int kvc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_workspace_init");
     g_err[0] = 0;
     if (!ws || ws_bytes < kWsHeader) return fail(KVC_ERR_WORKSPACE, "kvc_workspace_init: bad workspace");
     cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
@@ -226,6 +227,7 @@ int kvc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
 }
 
 int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_workspace_status");
     g_err[0] = 0;
     if (!ws || ws_bytes < kWsHeader || !status)
         return fail(KVC_ERR_INVALID_ARG, "kvc_workspace_status: bad arguments");
@@ -239,6 +241,7 @@ int kvc_workspace_status(const void *ws, size_t ws_bytes, uint32_t *status, cuda
 
 int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *scores, void *ws,
               size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_score");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_score")) return KVC_ERR_INVALID_ARG;
     if (!q_obs || !k || !scores) return fail(KVC_ERR_INVALID_ARG, "kvc_score: NULL tensor");
@@ -272,6 +275,7 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
                       float *scores, int32_t *mba, int32_t *budget, int32_t *idx, void *k_out,
                       void *v_out, int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream,
                       cudaStream_t copy_stream) {
+    NvtxRange nvtx_range("kvc_compress_host");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_compress_host")) return KVC_ERR_INVALID_ARG;
     const kvc_shape &s = *shape;
@@ -367,6 +371,7 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
 
 int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k, uint64_t seed,
                         double tau, float *scores, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_score_keyformer");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_score_keyformer")) return KVC_ERR_INVALID_ARG;
     if (!q_obs || !k || !scores) return fail(KVC_ERR_INVALID_ARG, "kvc_score_keyformer: NULL tensor");
@@ -400,6 +405,7 @@ int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k
 int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_num, uint32_t mass_den,
                    int64_t total_budget, int32_t layer_floor, int32_t *mba, int32_t *budget, void *ws,
                    size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_mba_budget");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_mba_budget")) return KVC_ERR_INVALID_ARG;
     const kvc_shape &s = *shape;
@@ -419,6 +425,7 @@ int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_nu
 
 int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *budget, int32_t k_max,
                     int32_t *idx, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_topk_select");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_topk_select")) return KVC_ERR_INVALID_ARG;
     if (!scores || !budget || !idx) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: NULL tensor");
@@ -429,6 +436,7 @@ int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *
 
 int kvc_head_budget(const kvc_shape *shape, const int32_t *mba, const int32_t *budget,
                     int32_t *head_budget, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_head_budget");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_head_budget")) return KVC_ERR_INVALID_ARG;
     if (!mba || !budget || !head_budget) return fail(KVC_ERR_INVALID_ARG, "kvc_head_budget: NULL tensor");
@@ -439,6 +447,7 @@ int kvc_head_budget(const kvc_shape *shape, const int32_t *mba, const int32_t *b
 int kvc_topk_select_heads(const kvc_shape *shape, const float *scores, const int32_t *head_budget,
                           int32_t k_max, int32_t *idx, void *ws, size_t ws_bytes,
                           cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_topk_select_heads");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_topk_select_heads")) return KVC_ERR_INVALID_ARG;
     if (!scores || !head_budget || !idx)
@@ -451,6 +460,7 @@ int kvc_topk_select_heads(const kvc_shape *shape, const float *scores, const int
 int kvc_threshold_select(const kvc_shape *shape, const float *scores, float tau, int32_t k_max,
                          int32_t *idx, int32_t *counts, void *ws, size_t ws_bytes,
                          cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_threshold_select");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_threshold_select")) return KVC_ERR_INVALID_ARG;
     if (!scores || !idx || !counts)
@@ -464,6 +474,7 @@ int kvc_threshold_select(const kvc_shape *shape, const float *scores, float tau,
 int kvc_compact_heads(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
                       const int32_t *counts, int32_t k_max, void *k_out, void *v_out,
                       int64_t out_rows, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_compact_heads");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_compact_heads")) return KVC_ERR_INVALID_ARG;
     if (!k || !v || !idx || !counts || !k_out || !v_out)
@@ -479,6 +490,7 @@ int kvc_compact_heads(const kvc_shape *shape, const void *k, const void *v, cons
 
 int kvc_pool_scores(const kvc_shape *shape, const float *scores, int32_t kernel, int32_t mode,
                     float *pooled, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_pool_scores");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_pool_scores")) return KVC_ERR_INVALID_ARG;
     if (!scores || !pooled) return fail(KVC_ERR_INVALID_ARG, "kvc_pool_scores: NULL tensor");
@@ -495,6 +507,7 @@ int kvc_pool_scores(const kvc_shape *shape, const float *scores, int32_t kernel,
 int kvc_compact(const kvc_shape *shape, const void *k, const void *v, const int32_t *idx,
                 const int32_t *budget, int32_t k_max, void *k_out, void *v_out, int64_t out_rows,
                 void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_compact");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_compact")) return KVC_ERR_INVALID_ARG;
     if (!k || !v || !idx || !budget || !k_out || !v_out)
@@ -515,6 +528,7 @@ int32_t kvc_keep_channels(double lambda, int32_t head_dim) {
 int kvc_channel_prune(const kvc_shape *shape, const void *k_out, const int32_t *budget, double lambda,
                       int32_t *chan, void *k_pruned, int64_t pruned_elems, void *ws, size_t ws_bytes,
                       cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_channel_prune");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_channel_prune")) return KVC_ERR_INVALID_ARG;
     if (!k_out || !budget || !chan || !k_pruned)
@@ -531,6 +545,7 @@ int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const voi
                             const void *v, const void *v_out, const int32_t *budget, double lambda,
                             float *value_scores, int32_t *chan, void *v_pruned,
                             int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_channel_prune_value");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_channel_prune_value")) return KVC_ERR_INVALID_ARG;
     const kvc_shape &s = *shape;
@@ -578,6 +593,7 @@ int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const voi
 int kvc_channel_prune_query(const kvc_shape *shape, const void *q_obs, const void *k_out,
                             const int32_t *budget, double lambda, int32_t *chan, void *k_pruned,
                             int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_channel_prune_query");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_channel_prune_query")) return KVC_ERR_INVALID_ARG;
     if (!q_obs || !k_out || !budget || !chan || !k_pruned)

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/kvc.h"
@@ -565,6 +566,17 @@ int launch_value_scores(const kvc_shape &s, const ScoreSplit &sp, const void *q,
                         bool tc, uint32_t *status, cudaStream_t st);
 
 void set_error(const char *fmt, ...);
+
+// One NVTX range per C-ABI call, named after the call, around its host-side
+// work (validation and enqueueing): a profiler's timeline shows which call
+// launched which kernels.  Without a profiler attached the push and pop are a
+// check of an unset function pointer.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Shared by every scoring entry point (api.cu): shape validation (message in
 // kvc_last_error on failure), whether the tensor-core kernels can serve the

@@ -81,6 +81,7 @@ using namespace kvc;
 
 extern "C" int kvc_score_noalloc(const kvc_shape *shape, const void *q_obs, const void *k,
                                  float *scores, uint32_t *dev_status, cudaStream_t stream) {
+    NvtxRange nvtx_range("kvc_score_noalloc");
     // Same shape rules, kernel choice (KVC_SCORE_IMPL included) and work
     // split as kvc_score, so both entry points run the same kernels.
     if (!shape_ok(shape, "kvc_score_noalloc")) return KVC_ERR_INVALID_ARG;
