@@ -443,6 +443,18 @@ def run_kvc(args):
                     "tensor_tflops": round(achieved, 1),
                     "peak_source": "derived: SMs x 128 lanes x max SM clock"}
 
+    think_value = None
+    if args.think_value > 0 and single and "kvc_channel_prune_value" in stages:
+        # THINKV's contractions: the row statistics (pass 1, 2 H_q W D T per
+        # layer), Q K^T again in the value kernel, and P V as two bf16 terms
+        wl = jobs[0][0]
+        unit = 2 * wl.n_q_heads * wl.window * wl.head_dim * wl.seq_len * wl.n_layers
+        fl = 4 * unit
+        ms_v = stages["kvc_channel_prune_value"] / len(jobs)
+        think_value = {"ms": round(ms_v, 4), "flops": fl,
+                       "tflops": round(fl / (ms_v / 1e3) / 1e12, 1),
+                       "frac_of_bf16_burst": round(fl / (ms_v / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+                       "note": "pass 1 + Q K^T + P_hi V + P_lo V; stage event time"}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -483,6 +495,7 @@ def run_kvc(args):
             + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)
             + (LAUNCHES["kvc_channel_prune_value"] if args.think_value > 0 else 0)),
         "stages_ms": {k: round(v / len(jobs), 4) for k, v in stages.items()},
+        "think_value": think_value,
         "wall_s_timed": round(t_wall, 3),
     }
     # the end-to-end leg runs the public compress() call, i.e. the default selection

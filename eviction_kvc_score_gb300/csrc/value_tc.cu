@@ -51,7 +51,7 @@ namespace kvc {
 
 namespace {
 
-constexpr int kVStages = 4;
+constexpr int kVStages = 3;
 constexpr int kVSlots = 3;
 constexpr int kVTileKeys = 128;                 // keys per pair tile
 // O is accumulated in TMEM over chunks of this many tiles (2048 keys, 256
@@ -85,7 +85,8 @@ struct VtcParams {
 struct VSmem {
     uint8_t *q;        // [2][128 rows][128 B]
     uint8_t *kv;       // [stages][K box 0 | K box 1 | V box]
-    float *red;        // [2 warpgroups][4 quarters][64]
+    float *red;        // [warpgroups][4 quarters][32]
+    float *oacc;       // [16 epilogue warps][32 channels][32 lanes]: O summed over chunks
     uint64_t *full, *empty, *pfull;     // [stages]
     uint64_t *q_full, *q_empty, *q_pfull;
     uint64_t *s_full, *p_full, *slot_empty;   // [slots]
@@ -94,7 +95,8 @@ struct VSmem {
     volatile int *abort_flag;
 };
 
-constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kVStages * kStageBytes +
+constexpr size_t kOaccBytes = (size_t)4 * kVEWG * kVKeysWG * 32 * sizeof(float);
+constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kVStages * kStageBytes + kOaccBytes +
                                kVEWG * 4 * kVKeysWG * sizeof(float) + (3 * kVStages + 3 * kVSlots + 8) * 8 +
                                16;
 
@@ -105,6 +107,8 @@ __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
     b += 2 * kQBox;
     s.kv = b;
     b += (size_t)kVStages * kStageBytes;
+    s.oacc = reinterpret_cast<float *>(b);
+    b += kOaccBytes;
     s.red = reinterpret_cast<float *>(b);
     b += kVEWG * 4 * kVKeysWG * sizeof(float);
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
@@ -253,7 +257,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             const uint32_t idesc2 = idesc_bf16_f32(256, 128) | (1u << 16);  // B MN-major
             uint32_t gt = 0, qi = 0;
             bool ok = true;
-            uint32_t chunks = 0;   // chunks of O handed to the epilogue so far
+            uint32_t chunks = 0;
+            const uint64_t qd0 = desc_sw128(smem_u32(s.q), 16u, 1024u);   // chunks of O handed to the epilogue so far
             // O += P V for tile g, the item's tile t (a chunk's first tile
             // overwrites O; its last hands O to the epilogue)
             auto mma2 = [&](uint32_t g, int t) -> bool {
@@ -266,14 +271,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     return false;
                 tc_fence_after();
                 const uint32_t scol = tmem + kSlotCol0 + slot * 128;
-                const uint32_t vbase = smem_u32(s.kv + (size_t)st * kStageBytes + 2 * kKBox);
+                // one descriptor per stage; a K-step only moves the start
+                // address field (bits [0,14), in 16-byte units)
+                const uint64_t b0 =
+                    desc_sw128(smem_u32(s.kv + (size_t)st * kStageBytes + 2 * kKBox), 1024u, 1024u);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     // keys 16 ks ..: the P_hi words of that half of warpgroup
                     // ks / 2's keys at columns 16 ks, its P_lo words 8
-                    // further; value rows 16 ks .. of the box
+                    // further; value rows 16 ks .. of the box (2048 bytes on)
                     const uint32_t acol = scol + (uint32_t)(ks * 16);
-                    const uint64_t b = desc_sw128(vbase + (uint32_t)ks * 2048u, 1024u, 1024u);
+                    const uint64_t b = b0 + (uint64_t)(ks * (2048 >> 4));
                     tc_mma2_bf16_tmem_a(tmem + kOCol, acol, b, idesc2, (first && ks == 0) ? 0u : 1u);
                     tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 8u, b, idesc2, 1u);
                 }
@@ -299,13 +307,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t kbase = smem_u32(s.kv + (size_t)st * kStageBytes);
-                    const uint32_t qbase = smem_u32(s.q);
+                    const uint64_t kd0 = desc_sw128(smem_u32(s.kv + (size_t)st * kStageBytes), 16u, 1024u);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
+                        // K-steps 0-3 in the first 64-column box, 4-7 in the
+                        // second; 32 bytes each
                         const int kh = ks >> 2, off = (ks & 3) * 32;
-                        const uint64_t a = desc_sw128(qbase + kh * kQBox + off, 16u, 1024u);
-                        const uint64_t b = desc_sw128(kbase + kh * kKBox + off, 16u, 1024u);
+                        const uint64_t a = qd0 + (uint64_t)((kh * kQBox + off) >> 4);
+                        const uint64_t b = kd0 + (uint64_t)((kh * kKBox + off) >> 4);
                         tc_mma2_bf16(tmem + kSlotCol0 + slot * 128, a, b, idesc1, ks > 0);
                     }
                     tc_commit2(&s.s_full[slot], kBoth);
@@ -337,9 +346,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             const bool real = r < p.rows;
             const float nb = real ? p.neg_bias[it.u * p.rows_pad + r] : -INFINITY;
             const int lim_row = p.P + (real ? r % p.W : 0);   // last key the row sees
-            float acc[kVKeysWG];   // this row's O, channels [32 ewg, +32), summed over chunks
+            // this row's O, channels [32 ewg, +32), summed over chunks in
+            // shared memory (registers stay free for a whole tile of S)
+            float *acc = s.oacc + (size_t)(warp - 2) * kVKeysWG * 32 + lane;
 #pragma unroll
-            for (int k = 0; k < kVKeysWG; ++k) acc[k] = 0.f;
+            for (int k = 0; k < kVKeysWG; ++k) acc[k * 32] = 0.f;
             for (int t = 0; t < p.n_tiles; ++t, ++gt) {
                 const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
                 if (!mbar_wait(&s.s_full[slot], use & 1, s.abort_flag, p.status)) {
@@ -347,50 +358,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     break;
                 }
                 tc_fence_after();
-                // this warpgroup's 32 keys in two halves of 16 (one MMA K-step
-                // each): a half's P words (8 hi, then 8 lo) go back into its
-                // own 16 S columns once read
-                const unsigned long long cs2 = f2_pack(p.cs, p.cs), nb2 = f2_pack(nb, nb);
+                // this warpgroup's 32 keys, read at once; each half of 16 (one
+                // MMA K-step) gets its P words (8 hi, then 8 lo) written back
+                // into its own 16 S columns, both halves in one store
+                const uint32_t scol = tmem + lane_base + kSlotCol0 + slot * 128 + ewg * kVKeysWG;
+                float v[32];
+                tmem_ld32(scol, v);
+                tmem_ld_wait();
+                reg_fence(v);
+                const int lim = lim_row - (t * kVTileKeys + ewg * kVKeysWG);
+                if (lim < kVKeysWG - 1) {   // the window's causal edge: mask invisible keys
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t scol =
-                        tmem + lane_base + kSlotCol0 + slot * 128 + ewg * kVKeysWG + h * 16;
-                    float v[16];
-                    tmem_ld16(scol, v);
-                    tmem_ld_wait();
-                    asm volatile("" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]),
-                                 "+f"(v[5]), "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]),
-                                 "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
-                                 "+f"(v[15]));
-                    const int lim = lim_row - (t * kVTileKeys + ewg * kVKeysWG + h * 16);
-                    if (lim < 15) {   // the window's causal edge: mask invisible keys
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (i > lim) v[i] = -INFINITY;   // 2^-inf = +0
-                    }
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2) {
-                        float y0, y1;
-                        f2_unpack(f2_fma(f2_pack(v[2 * i2], v[2 * i2 + 1]), cs2, nb2), y0, y1);
-                        const float p0 = ex2(y0), p1 = ex2(y1);
-                        // p = hi + lo: hi keeps the top 16 bits (truncated, a
-                        // bf16), lo = p - hi is exact and rounded to bf16
-                        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-                        const unsigned long long lo2 = f2_add(
-                            f2_pack(p0, p1), f2_pack(-__uint_as_float(b0 & 0xFFFF0000u),
-                                                     -__uint_as_float(b1 & 0xFFFF0000u)));
-                        float l0, l1;
-                        f2_unpack(lo2, l0, l1);
-                        uint32_t hi, lo;
-                        // lower 16 bits: the even key (first along K)
-                        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(b0), "r"(b1));
-                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(l1), "f"(l0));
-                        w[i2] = hi;
-                        w[8 + i2] = lo;
-                    }
-                    tmem_st16(scol, w);
+                    for (int i = 0; i < 32; ++i)
+                        if (i > lim) v[i] = -INFINITY;   // 2^-inf = +0
                 }
+                const unsigned long long cs2 = f2_pack(p.cs, p.cs), nb2 = f2_pack(nb, nb);
+                uint32_t w[32];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    float y0, y1;
+                    f2_unpack(f2_fma(f2_pack(v[2 * i2], v[2 * i2 + 1]), cs2, nb2), y0, y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    // p = hi + lo: hi keeps the top 16 bits (truncated, a
+                    // bf16), lo = p - hi is exact and rounded to bf16
+                    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                    const unsigned long long lo2 = f2_add(
+                        f2_pack(p0, p1), f2_pack(-__uint_as_float(b0 & 0xFFFF0000u),
+                                                 -__uint_as_float(b1 & 0xFFFF0000u)));
+                    float l0, l1;
+                    f2_unpack(lo2, l0, l1);
+                    uint32_t hi, lo;
+                    // lower 16 bits: the even key (first along K)
+                    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(b0), "r"(b1));
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(l1), "f"(l0));
+                    // half i2 / 8: hi words at 16 half + i2 % 8, lo words 8 further
+                    w[(i2 >> 3) * 16 + (i2 & 7)] = hi;
+                    w[(i2 >> 3) * 16 + 8 + (i2 & 7)] = lo;
+                }
+                tmem_st32(scol, w);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -412,7 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                         tmem_ld_wait();
                         reg_fence(o);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) acc[k] += o[k];
+                        for (int k = 0; k < 32; ++k) acc[k * 32] += o[k];
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -424,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
             // the vector each step leaves lane l with channel l
             float a[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) a[k] = acc[k] * acc[k];
+            for (int k = 0; k < 32; ++k) a[k] = acc[k * 32] * acc[k * 32];
 #pragma unroll
             for (int half = 16; half >= 1; half >>= 1) {
                 const bool upper = (lane & half) != 0;   // lane bit that chooses the kept half
