@@ -420,7 +420,7 @@ int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_nu
     if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_mba_budget")) return KVC_ERR_WORKSPACE;
     int rc = launch_mba(s, scores, mass_num, mass_den, mba, status_word(ws), stream);
     if (rc) return rc;
-    return launch_budget(s, mba, total_budget, layer_floor, budget, stream);
+    return launch_budget(s, mba, total_budget, layer_floor, budget, status_word(ws), stream);
 }
 
 int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *budget, int32_t k_max,

@@ -88,6 +88,9 @@ __global__ void __launch_bounds__(kCopyThreads)
                 set_status(status, KVC_DEV_BAD_BUDGET);
                 continue;
             }
+            // kept prefix positions strictly ascending and inside the prefix
+            if (kDebugBounds && e == 0 && r < n && (t >= P || (r > 0 && sel[r - 1] >= t)))
+                set_status(status, KVC_DEV_INVARIANT);
             k_out[orow * vec_per_row + e] = ks[(int64_t)t * vec_per_row + e];
             v_out[orow * vec_per_row + e] = vs[(int64_t)t * vec_per_row + e];
         }
@@ -250,6 +253,9 @@ __global__ void __launch_bounds__(kPruneThreads)
     }
     // no CTA may leave while another still reads its slice sums
     cluster.sync();
+    if (kDebugBounds && rank == 0 && tid < keep &&
+        (sel[tid] < 0 || sel[tid] >= D || (tid > 0 && sel[tid - 1] >= sel[tid])))
+        set_status(status, KVC_DEV_INVARIANT);   // keep channels, strictly ascending
 
     // 3. copy the kept channels of this CTA's rows
     const int64_t o0 = s_o0 + (int64_t)r_lo * keep;

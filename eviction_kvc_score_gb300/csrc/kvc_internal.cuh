@@ -75,6 +75,15 @@ inline ScoreSplit make_score_split(const kvc_shape &s, bool tc, int sms, int pai
     return sp;
 }
 
+// Bounds-checking build (nvcc -DKVC_DEBUG_BOUNDS): kernels verify their
+// outputs' invariants and OR KVC_DEV_INVARIANT into the status word on a
+// failure, without trapping; the checks compile away otherwise.
+#ifdef KVC_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
 // ---------------------------------------------------------------- status word
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
     atomicOr(status, bits);
@@ -532,7 +541,7 @@ int launch_score_keyformer(const kvc_shape &s, const ScoreSplit &sp, const Score
 int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
                uint32_t *status, cudaStream_t st);
 int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,
-                  int32_t *budget, cudaStream_t st);
+                  int32_t *budget, uint32_t *status, cudaStream_t st);
 // per_head == 0: budget[L] per layer; 1: budget[L][H_kv] per head.
 int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int per_head,
                 int32_t k_max, int32_t *idx, uint32_t *status, cudaStream_t st);

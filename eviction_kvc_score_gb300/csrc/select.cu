@@ -342,13 +342,15 @@ __global__ void __launch_bounds__(kSelThreads)
         const unsigned long long ustar = fixed56f(__uint_as_float(prefix));
         const unsigned __int128 have = (unsigned __int128)den * A;
         const unsigned __int128 step = (unsigned __int128)den * ustar;
+        long long m;
         if (step == 0 || have >= need) {
             set_status(status, KVC_DEV_BAD_SCORE);   // unreachable for valid scores
-            mba[blockIdx.x] = (int32_t)C;
+            m = C;
         } else {
-            const long long k = (long long)((need - have + step - 1) / step);
-            mba[blockIdx.x] = (int32_t)(C + k);
+            m = C + (long long)((need - have + step - 1) / step);
         }
+        if (kDebugBounds && (m < 0 || m > T)) set_status(status, KVC_DEV_INVARIANT);
+        mba[blockIdx.x] = (int32_t)m;
     }
 }
 
@@ -417,7 +419,7 @@ __device__ long long lr_split(int L, const long long *S, const unsigned char *el
 
 __global__ void __launch_bounds__(kMaxLayers)
     budget_kernel(const int32_t *__restrict__ mba, int L, int Hkv, long long P, long long total,
-                  long long floor_, int32_t *__restrict__ budget) {
+                  long long floor_, int32_t *__restrict__ budget, uint32_t *status) {
     __shared__ long long S[kMaxLayers], rem[kMaxLayers];
     __shared__ unsigned char elig[kMaxLayers];
     __shared__ unsigned long long red[3];
@@ -451,6 +453,17 @@ __global__ void __launch_bounds__(kMaxLayers)
         B += lr_split(L, S, elig, (long long)excess, rem, red);
     }
     if (act) budget[l] = (int32_t)B;
+    if (kDebugBounds) {   // sum = total (every layer at P if total >= L P), floor <= B <= P
+        __syncthreads();
+        if (l == 0) red[0] = 0;
+        __syncthreads();
+        if (act) {
+            atomicAdd(&red[0], (unsigned long long)B);
+            if (B < floor_ || B > P) set_status(status, KVC_DEV_INVARIANT);
+        }
+        __syncthreads();
+        if (l == 0 && (long long)red[0] != total) set_status(status, KVC_DEV_INVARIANT);
+    }
 }
 
 // Per-head budgets: block l splits the layer's H_kv * B_l tokens over its
@@ -655,6 +668,13 @@ __global__ void __launch_bounds__(kSelThreads)
         if (g_before + (e_before < need_eq ? e_before : need_eq) >= B) break;
         __syncthreads();
     }
+    if (kDebugBounds) {   // B positions, strictly ascending, inside the prefix
+        __syncthreads();
+        for (int i = tid; i < B; i += kSelThreads) {
+            const int32_t x = out[i];
+            if (x < 0 || x >= P || (i > 0 && out[i - 1] >= x)) set_status(status, KVC_DEV_INVARIANT);
+        }
+    }
 }
 
 // Threshold selection: per head, every prefix position with score >= tau,
@@ -693,6 +713,14 @@ __global__ void __launch_bounds__(kSelThreads)
     if (tid == 0) {
         counts[head] = (int32_t)min(before, (long long)INT32_MAX);
         if (before > k_max) set_status(status, KVC_DEV_BAD_BUDGET);
+    }
+    if (kDebugBounds) {   // written positions strictly ascending, inside the prefix
+        __syncthreads();
+        const long long n = before < k_max ? before : k_max;
+        for (long long i = tid; i < n; i += kSelThreads) {
+            const int32_t x = out[i];
+            if (x < 0 || x >= P || (i > 0 && out[i - 1] >= x)) set_status(status, KVC_DEV_INVARIANT);
+        }
     }
 }
 
@@ -748,14 +776,14 @@ int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t d
 }
 
 int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,
-                  int32_t *budget, cudaStream_t st) {
+                  int32_t *budget, uint32_t *status, cudaStream_t st) {
     if (s.n_layers > kMaxLayers) {
         set_error("kvc_mba_budget: at most %d layers", kMaxLayers);
         return KVC_ERR_UNSUPPORTED;
     }
     budget_kernel<<<1, (s.n_layers + 31) / 32 * 32, 0, st>>>(mba, s.n_layers, s.n_kv_heads,
                                     (long long)s.seq_len - s.window, (long long)total,
-                                    (long long)floor_, budget);
+                                    (long long)floor_, budget, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_mba_budget: budget launch failed: %s", cudaGetErrorString(e));

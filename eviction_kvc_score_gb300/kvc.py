@@ -18,7 +18,9 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvc.so")
+# KVC_LIBRARY selects another build of the same ABI, e.g. the bounds-checking
+# libkvc_debug.so
+LIB_PATH = os.environ.get("KVC_LIBRARY") or os.path.join(_HERE, "libkvc.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -30,6 +32,7 @@ _lib = C.CDLL(LIB_PATH)
 KVC_OK = 0
 KVC_F32, KVC_BF16 = 0, 1
 DEV_TIMEOUT, DEV_BAD_SCORE, DEV_BAD_BUDGET, DEV_OUT_CAPACITY = 0x1, 0x2, 0x4, 0x8
+DEV_INVARIANT = 0x10   # bounds-checking builds only
 
 
 class KvcError(RuntimeError):

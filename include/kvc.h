@@ -88,6 +88,16 @@ typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
                                       budget[l] was negative; clamped */
 #define KVC_DEV_OUT_CAPACITY 0x8u  /* packed output larger than the buffer;
                                       rows past the end were not written */
+#define KVC_DEV_INVARIANT    0x10u /* bounds-checking builds only (compiled with
+                                      KVC_DEBUG_BOUNDS): an output invariant
+                                      failed -- kept or compacted indices not
+                                      strictly ascending or outside [0, T-W),
+                                      an MBA outside [0, T], budgets not summing
+                                      to min(total, L (T-W)) or outside
+                                      [floor, T-W], kept channels not strictly
+                                      ascending or outside [0, D).  The check
+                                      records the bit and the kernel goes on; it
+                                      never traps. */
 
 typedef struct {
     int32_t n_layers;    /* L >= 1 */

@@ -35,6 +35,14 @@ def test_every_declared_symbol_is_exported(lib):
     assert not missing, missing
 
 
+def test_bounds_checking_build_exports_the_same_abi():
+    """The KVC_DEBUG_BOUNDS variant is the same C ABI with extra device checks."""
+    from eviction_kvc_score_gb300 import build
+    dbg = C.CDLL(build.build(debug_bounds=True))
+    missing = [s for s in declared_symbols() if not hasattr(dbg, s)]
+    assert not missing, missing
+
+
 def test_binding_exposes_the_same_names(lib):
     from eviction_kvc_score_gb300 import kvc
     for s in declared_symbols():
