@@ -563,7 +563,7 @@ int launch_channel_prune(const kvc_shape &s, const void *q, const void *k_out, c
 // THINKV: per-channel value scores [L][H_kv][D] (fp32 sums of squared window
 // attention outputs) from the row biases that a stats-only score pass left
 // in a.neg_bias; `partial` is scratch of value_partial_floats() floats.
-constexpr int kValueTcParts = 4;   // (job, CTA) partial sums per unit, tensor-core kernel
+constexpr int kValueTcParts = 16;  // (job, CTA, warp) partial sums per unit, tensor-core kernel
 int64_t value_partial_floats(const kvc_shape &s);
 // The tensor-core THINKV kernel serves bf16, head_dim 128, G*W <= 512.
 bool value_tc_eligible(const kvc_shape &s);

@@ -27,11 +27,10 @@
 // rows by up to 3e-3; the two-term split brings every score within 1e-4 of
 // the fp64 definition at the price of a second P V product.
 // O accumulates in TMEM over chunks of kChunkTiles tiles, each chunk added
-// into fp32 registers by the epilogue; at the item's end each epilogue thread
-// squares its row's 32 channels, a warp butterfly sums them over the warp's 32 rows
-// and the four warps of a warpgroup are added in order, giving one partial
-// per (unit, job, CTA) -- reduced in a fixed order afterwards, so the result
-// is deterministic.
+// into fp32 sums in shared memory by the epilogue; at the item's end each
+// epilogue thread squares its row's 32 channels and a warp butterfly sums them
+// over the warp's 32 rows, giving one partial per (unit, job, CTA, warp) --
+// reduced in a fixed order afterwards, so the result is deterministic.
 //
 // TMEM (512 columns per CTA): O in columns [0,128); three S/P slots of 128
 // columns at 128, 256, 384.  Within a slot, epilogue warpgroup e reads S
@@ -78,14 +77,13 @@ struct VtcParams {
     int T, P, W, rows, rows_pad, n_tiles;
     float cs;             // log2(e) / sqrt(D)
     const float *neg_bias;
-    float *partial;       // [units][kValueTcParts][128]
+    float *partial;       // [units][kValueTcParts = (job, CTA, warp)][128]
     uint32_t *status;
 };
 
 struct VSmem {
     uint8_t *q;        // [2][128 rows][128 B]
     uint8_t *kv;       // [stages][K box 0 | K box 1 | V box]
-    float *red;        // [warpgroups][4 quarters][32]
     float *oacc;       // [16 epilogue warps][32 channels][32 lanes]: O summed over chunks
     uint64_t *full, *empty, *pfull;     // [stages]
     uint64_t *q_full, *q_empty, *q_pfull;
@@ -97,7 +95,7 @@ struct VSmem {
 
 constexpr size_t kOaccBytes = (size_t)4 * kVEWG * kVKeysWG * 32 * sizeof(float);
 constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kVStages * kStageBytes + kOaccBytes +
-                               kVEWG * 4 * kVKeysWG * sizeof(float) + (3 * kVStages + 3 * kVSlots + 8) * 8 +
+                               (3 * kVStages + 3 * kVSlots + 8) * 8 +
                                16;
 
 __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
@@ -109,8 +107,6 @@ __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
     b += (size_t)kVStages * kStageBytes;
     s.oacc = reinterpret_cast<float *>(b);
     b += kOaccBytes;
-    s.red = reinterpret_cast<float *>(b);
-    b += kVEWG * 4 * kVKeysWG * sizeof(float);
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
     s.full = bars;
     s.empty = bars + kVStages;
@@ -440,15 +436,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                     a[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
                 }
             }
-            float *red = s.red + ewg * 4 * kVKeysWG;
-            red[quarter * kVKeysWG + lane] = a[0];
-            named_bar_sync(1 + ewg, 128);
-            if (quarter == 0) {
-                float s0 = red[lane];
-                for (int qq = 1; qq < 4; ++qq) s0 += red[qq * kVKeysWG + lane];
-                p.partial[(it.u * kValueTcParts + it.job * 2 + rank) * 128 + ewg * kVKeysWG + lane] = s0;
-            }
-            named_bar_sync(1 + ewg, 128);   // red is rewritten by the next item
+            // one partial per (job, CTA, warp): no barrier between warps, so
+            // a warp that gave up on a wait cannot leave another one waiting
+            p.partial[(it.u * kValueTcParts + (it.job * 2 + rank) * 4 + quarter) * 128 +
+                      ewg * kVKeysWG + lane] = a[0];
         }
     }
     // teardown: no MMA, load or remote arrive of the pair is left
@@ -510,7 +501,7 @@ int launch_value_tc(const kvc_shape &s, const ScoreSplit &sp, const void *q, con
         set_error("kvc_channel_prune_value: tensor-core launch failed: %s", cudaGetErrorString(e));
         return KVC_ERR_CUDA;
     }
-    *parts_out = 2 * p.njob;
+    *parts_out = 8 * p.njob;   // the first 8 njob of the kValueTcParts slots
     return KVC_OK;
 }
 
