@@ -25,6 +25,7 @@ namespace {
 constexpr int kVThreads = 128;
 constexpr int kVRows = 16;   // window rows per block
 constexpr int kVKeys = 32;   // keys per shared-memory tile
+constexpr int kVParts = 16;  // blocks (partial sums) per unit at most
 
 template <typename T>
 __device__ __forceinline__ float to_f(T x);
@@ -35,16 +36,18 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return _
 
 struct VParams {
     int T, P, W, D, rows, rows_pad, chunks;
+    int parts;                // blocks per unit: block b takes chunks b, b + parts, ...
     float cs;                 // log2(e) / sqrt(D)
     const float *neg_bias;    // [units][rows_pad]
-    float *partial;           // [units][chunks][D]
+    float *partial;           // [units][parts][D]
 };
 
-// Block (chunk, unit): the chunk's 16 window rows over all T keys.  Keys and
-// values stream through shared memory 32 at a time; thread (key j, row group)
-// forms 4 logits, then thread d accumulates o_r[d] for the 16 rows (and d +
-// 128 when D > 128).  At the end each thread writes the sum over the chunk's
-// rows of o_r[d]^2.
+// Block (part, unit) handles the unit's 16-row chunks part, part + parts, ...
+// in that order; for each chunk the keys and values stream through shared
+// memory 32 at a time, thread (key j, row group) forms 4 logits, then thread d
+// accumulates o_r[d] for the 16 rows (and d + 128 when D > 128) and adds
+// o_r[d]^2 to its running sum.  At the end each thread writes its sum: one
+// partial per (unit, part), at most kVParts per unit.
 template <typename T>
 __global__ void __launch_bounds__(kVThreads)
     value_out_simt(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
@@ -56,74 +59,76 @@ __global__ void __launch_bounds__(kVThreads)
     float *vs = ks + kVKeys * DK;                    // [32][D]
     float *ps = vs + kVKeys * D;                     // [16][32]
     float *nb = ps + kVRows * kVKeys;                // [16]
-    const int chunk = blockIdx.x;
     const int64_t u = blockIdx.y;
-    const int r0 = chunk * kVRows;
     const int tid = threadIdx.x;
-    for (int e = tid; e < kVRows * D; e += kVThreads) {
-        const int r = r0 + e / D;
-        qs[e] = r < p.rows ? to_f(q[(u * p.rows + r) * (int64_t)D + e % D]) : 0.f;
-    }
-    if (tid < kVRows) {
-        const int r = r0 + tid;
-        nb[tid] = r < p.rows ? p.neg_bias[u * p.rows_pad + r] : -INFINITY;
-    }
-    // the last window position a row of this chunk sees
-    const int r_last = min(r0 + kVRows, p.rows) - 1;
-    int w_max = 0;
-    for (int r = r0; r <= r_last; ++r) w_max = max(w_max, r % p.W);
-    const int j_end = min(p.T, p.P + w_max + 1);
-    const int jk = tid & 31, rg = tid >> 5;          // logits: key jk, rows 4 rg .. 4 rg + 3
-    float acc[kVRows][2];
-#pragma unroll
-    for (int r = 0; r < kVRows; ++r) acc[r][0] = acc[r][1] = 0.f;
-    const T *ku = k + u * (int64_t)p.T * D;
-    const T *vu = v + u * (int64_t)p.T * D;
-    for (int j0 = 0; j0 < j_end; j0 += kVKeys) {
-        __syncthreads();
-        for (int e = tid; e < kVKeys * D; e += kVThreads) {
-            const int jj = j0 + e / D, d = e % D;
-            const bool in = jj < p.T;
-            ks[(e / D) * DK + d] = in ? to_f(ku[(int64_t)jj * D + d]) : 0.f;
-            vs[e] = in ? to_f(vu[(int64_t)jj * D + d]) : 0.f;
+    float sq[2] = {0.f, 0.f};
+    for (int chunk = blockIdx.x; chunk < p.chunks; chunk += p.parts) {
+        const int r0 = chunk * kVRows;
+        __syncthreads();   // the previous chunk's shared memory is no longer read
+        for (int e = tid; e < kVRows * D; e += kVThreads) {
+            const int r = r0 + e / D;
+            qs[e] = r < p.rows ? to_f(q[(u * p.rows + r) * (int64_t)D + e % D]) : 0.f;
         }
-        __syncthreads();
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int d = 0; d < D; ++d) {
-            const float kd = ks[jk * DK + d];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s4[i] = fmaf(qs[(rg * 4 + i) * D + d], kd, s4[i]);
+        if (tid < kVRows) {
+            const int r = r0 + tid;
+            nb[tid] = r < p.rows ? p.neg_bias[u * p.rows_pad + r] : -INFINITY;
         }
-        const int j = j0 + jk;
+        // the last window position a row of this chunk sees
+        const int r_last = min(r0 + kVRows, p.rows) - 1;
+        int w_max = 0;
+        for (int r = r0; r <= r_last; ++r) w_max = max(w_max, r % p.W);
+        const int j_end = min(p.T, p.P + w_max + 1);
+        const int jk = tid & 31, rg = tid >> 5;          // logits: key jk, rows 4 rg .. 4 rg + 3
+        float acc[kVRows][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int rl = rg * 4 + i, r = r0 + rl;
-            const bool vis = r < p.rows && j < p.T && j <= p.P + r % p.W;
-            ps[rl * kVKeys + jk] = vis ? ex2(fmaf(s4[i], p.cs, nb[rl])) : 0.f;
-        }
-        __syncthreads();
+        for (int r = 0; r < kVRows; ++r) acc[r][0] = acc[r][1] = 0.f;
+        const T *ku = k + u * (int64_t)p.T * D;
+        const T *vu = v + u * (int64_t)p.T * D;
+        for (int j0 = 0; j0 < j_end; j0 += kVKeys) {
+            __syncthreads();
+            for (int e = tid; e < kVKeys * D; e += kVThreads) {
+                const int jj = j0 + e / D, d = e % D;
+                const bool in = jj < p.T;
+                ks[(e / D) * DK + d] = in ? to_f(ku[(int64_t)jj * D + d]) : 0.f;
+                vs[e] = in ? to_f(vu[(int64_t)jj * D + d]) : 0.f;
+            }
+            __syncthreads();
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int d = 0; d < D; ++d) {
+                const float kd = ks[jk * DK + d];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int d = tid + h * kVThreads;
-            if (d < D) {
+                for (int i = 0; i < 4; ++i) s4[i] = fmaf(qs[(rg * 4 + i) * D + d], kd, s4[i]);
+            }
+            const int j = j0 + jk;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rl = rg * 4 + i, r = r0 + rl;
+                const bool vis = r < p.rows && j < p.T && j <= p.P + r % p.W;
+                ps[rl * kVKeys + jk] = vis ? ex2(fmaf(s4[i], p.cs, nb[rl])) : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int d = tid + h * kVThreads;
+                if (d < D) {
 #pragma unroll 4
-                for (int jj = 0; jj < kVKeys; ++jj) {
-                    const float vd = vs[jj * D + d];
+                    for (int jj = 0; jj < kVKeys; ++jj) {
+                        const float vd = vs[jj * D + d];
 #pragma unroll
-                    for (int r = 0; r < kVRows; ++r) acc[r][h] = fmaf(ps[r * kVKeys + jj], vd, acc[r][h]);
+                        for (int r = 0; r < kVRows; ++r) acc[r][h] = fmaf(ps[r * kVKeys + jj], vd, acc[r][h]);
+                    }
                 }
             }
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int r = 0; r < kVRows; ++r) sq[h] = fmaf(acc[r][h], acc[r][h], sq[h]);
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int d = tid + h * kVThreads;
-        if (d < D) {
-            float sq = 0.f;
-#pragma unroll
-            for (int r = 0; r < kVRows; ++r) sq = fmaf(acc[r][h], acc[r][h], sq);
-            p.partial[(u * p.chunks + chunk) * (int64_t)D + d] = sq;
-        }
+        if (d < D) p.partial[(u * p.parts + blockIdx.x) * (int64_t)D + d] = sq[h];
     }
 }
 
@@ -153,29 +158,28 @@ int launch_simt_t(const kvc_shape &s, const ScoreSplit &sp, const void *q, const
     p.rows = sp.rows;
     p.rows_pad = sp.rows_pad;
     p.chunks = (sp.rows + kVRows - 1) / kVRows;
+    p.parts = p.chunks < kVParts ? p.chunks : kVParts;
     p.cs = (float)(kLog2e / sqrt((double)s.head_dim));
     p.neg_bias = neg_bias;
     p.partial = partial;
     const size_t smem = sizeof(float) * ((size_t)kVRows * p.D + (size_t)kVKeys * (p.D + 1) +
                                          (size_t)kVKeys * p.D + kVRows * kVKeys + kVRows);
     cudaFuncSetAttribute(value_out_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    value_out_simt<T><<<dim3((unsigned)p.chunks, (unsigned)sp.n_units), kVThreads, smem, st>>>(
+    value_out_simt<T><<<dim3((unsigned)p.parts, (unsigned)sp.n_units), kVThreads, smem, st>>>(
         static_cast<const T *>(q), static_cast<const T *>(k), static_cast<const T *>(v), p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_channel_prune_value: value-output launch failed: %s", cudaGetErrorString(e));
         return KVC_ERR_CUDA;
     }
-    *parts_out = p.chunks;
+    *parts_out = p.parts;
     return KVC_OK;
 }
 
 }  // namespace
 
 int64_t value_partial_floats(const kvc_shape &s) {
-    const int64_t rows = (int64_t)(s.n_q_heads / s.n_kv_heads) * s.window;
-    const int64_t chunks = (rows + kVRows - 1) / kVRows;
-    const int64_t parts = chunks > kValueTcParts ? chunks : kValueTcParts;
+    const int64_t parts = kVParts > kValueTcParts ? kVParts : kValueTcParts;
     return (int64_t)s.n_layers * s.n_kv_heads * parts * s.head_dim;
 }
 

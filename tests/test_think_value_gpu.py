@@ -186,3 +186,29 @@ def test_value_full_zigzag_32k_all_units():
     b = run_value(wl, x)
     ref = O().value_scores(oshape(wl), x["q"], x["k"], x["v"])
     check_value(wl, x, b, ref, VALUE_RTOL[path_of(wl)])
+
+
+def test_value_full_think_128k_sampled_layers():
+    """The 128K prompt (32 layers, the benchmark's launch configuration): the
+    GPU runs every layer; two layers' value scores (all their heads) are
+    checked against the oracle run on those layers alone, and the channels and
+    pruned bytes of every head against the oracle's selection on the GPU's own
+    scores."""
+    wl = wk.THINK_128K.scaled(think_lambda=0.3)
+    x = wk.make_inputs(wl, wk.seed_for(4), device="cuda")
+    b = run_value(wl, x)
+    o = O()
+    gs = b.v_scores.double().cpu().numpy()
+    for l in (0, 17):
+        s1 = o.shape_of(1, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.seq_len, wl.window,
+                        wl.dtype)
+        ref = o.value_scores(s1, x["q"][l:l + 1], x["k"][l:l + 1], x["v"][l:l + 1])[0]
+        rtol = VALUE_RTOL[path_of(wl)]
+        assert np.all(np.abs(gs[l] - ref) <= rtol * ref), l
+    s = oshape(wl)
+    bud = b.budget.cpu().numpy()
+    rows = o.compact_rows(s, bud)
+    chan_g, vp_g = o.channel_prune_value(s, b.v_scores.cpu().numpy(), o.raw(b.v_out[:rows]), bud,
+                                         wl.think_lambda)
+    assert np.array_equal(b.v_chan.cpu().numpy(), chan_g)
+    assert np.array_equal(o.raw(b.v_pruned[: vp_g.size]), vp_g)
