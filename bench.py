@@ -18,6 +18,7 @@ max-over-ranks time.  Rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -73,6 +74,10 @@ def parse():
                     help="window scores: SnapKV (default) or Keyformer's Gumbel-noised, "
                          "temperature-softened scores (CUDA-core fp32 kernels)")
     ap.add_argument("--keyformer-tau", type=float, default=1.0)
+    ap.add_argument("--streams", type=int, default=4,
+                    help="workloads of several prompts (the ragged batch): run the prompts' "
+                         "call chains on this many streams (1: one after another); a single "
+                         "prompt always runs on one stream")
     ap.add_argument("--tau-mult", type=float, default=4.0,
                     help="threshold selection: tau = tau_mult / seq_len (mean score x tau_mult)")
     return ap.parse_args()
@@ -293,6 +298,8 @@ def run_kvc(args):
         jobs.append((wl, x, b, total, floor))
     torch.cuda.synchronize()
 
+    streams = [torch.cuda.Stream() for _ in range(max(1, args.streams))]
+
     def step(score_ev=None, stage_ev=None):
         def mark(name):
             if stage_ev is not None:
@@ -300,61 +307,74 @@ def run_kvc(args):
                 e.record(stream)
                 stage_ev.append((name, e))
 
-        for wl, x, b, total, floor in jobs:
-            mark("start")
-            if score_ev is not None:
-                score_ev[0].record(stream)
-            if args.score == "keyformer":
-                kvc.kvc_score_keyformer(b.shape, x["q"], x["k"], 0x5EED, args.keyformer_tau,
-                                        b.scores, b.ws)
-            else:
-                kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
-            if score_ev is not None:
-                score_ev[1].record(stream)
-            mark("kvc_score_keyformer" if args.score == "keyformer" else "kvc_score")
-            if args.select == "threshold":
-                kvc.kvc_threshold_select(b.shape, b.scores, args.tau_mult / wl.seq_len, b.k_max,
-                                         b.idx, b.head_counts, b.ws)
-                mark("kvc_threshold_select")
-                kvc.kvc_compact_heads(b.shape, x["k"], x["v"], b.idx, b.head_counts, b.k_max,
-                                      b.k_out, b.v_out, b.ws)
-                mark("kvc_compact_heads")
-                continue
-            kvc.kvc_mba_budget(b.shape, b.scores, wl.mass_num, wl.mass_den, total, floor,
-                               b.mba, b.budget, b.ws)
-            mark("kvc_mba_budget")
-            sel = b.scores
-            if args.pool > 1:
-                kvc.kvc_pool_scores(b.shape, b.scores, args.pool, 0, b.pooled, b.ws)
-                sel = b.pooled
-                mark("kvc_pool_scores")
-            if args.select == "head":
-                kvc.kvc_head_budget(b.shape, b.mba, b.budget, b.head_counts, b.ws)
-                mark("kvc_head_budget")
-                kvc.kvc_topk_select_heads(b.shape, sel, b.head_counts, b.k_max, b.idx, b.ws)
-                mark("kvc_topk_select_heads")
-                kvc.kvc_compact_heads(b.shape, x["k"], x["v"], b.idx, b.head_counts, b.k_max,
-                                      b.k_out, b.v_out, b.ws)
-                mark("kvc_compact_heads")
-            else:
-                kvc.kvc_topk_select(b.shape, sel, b.budget, b.k_max, b.idx, b.ws)
-                mark("kvc_topk_select")
-                kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
-                                b.v_out, b.ws)
-                mark("kvc_compact")
-            if args.think_value > 0:
-                kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
-                                            args.think_value, b.v_chan, b.v_pruned, b.ws)
-                mark("kvc_channel_prune_value")
-            if wl.think_lambda is not None:
-                if args.think_criterion == "query":
-                    kvc.kvc_channel_prune_query(b.shape, x["q"], b.k_out, b.budget,
-                                                wl.think_lambda, b.chan, b.k_pruned, b.ws)
-                    mark("kvc_channel_prune_query")
+        side = (args.streams > 1 and len(jobs) > 1 and stage_ev is None and score_ev is None)
+        if side:   # prompts spread over several streams, joined at the end
+            start = torch.cuda.Event()
+            start.record(stream)
+        for j, (wl, x, b, total, floor) in enumerate(jobs):
+            if side:
+                js = streams[j % len(streams)]
+                js.wait_event(start)
+            with (torch.cuda.stream(js) if side else contextlib.nullcontext()):
+                mark("start")
+                if score_ev is not None:
+                    score_ev[0].record(stream)
+                if args.score == "keyformer":
+                    kvc.kvc_score_keyformer(b.shape, x["q"], x["k"], 0x5EED, args.keyformer_tau,
+                                            b.scores, b.ws)
                 else:
-                    kvc.kvc_channel_prune(b.shape, b.k_out, b.budget, wl.think_lambda, b.chan,
-                                          b.k_pruned, b.ws)
-                    mark("kvc_channel_prune")
+                    kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
+                if score_ev is not None:
+                    score_ev[1].record(stream)
+                mark("kvc_score_keyformer" if args.score == "keyformer" else "kvc_score")
+                if args.select == "threshold":
+                    kvc.kvc_threshold_select(b.shape, b.scores, args.tau_mult / wl.seq_len, b.k_max,
+                                             b.idx, b.head_counts, b.ws)
+                    mark("kvc_threshold_select")
+                    kvc.kvc_compact_heads(b.shape, x["k"], x["v"], b.idx, b.head_counts, b.k_max,
+                                          b.k_out, b.v_out, b.ws)
+                    mark("kvc_compact_heads")
+                    continue
+                kvc.kvc_mba_budget(b.shape, b.scores, wl.mass_num, wl.mass_den, total, floor,
+                                   b.mba, b.budget, b.ws)
+                mark("kvc_mba_budget")
+                sel = b.scores
+                if args.pool > 1:
+                    kvc.kvc_pool_scores(b.shape, b.scores, args.pool, 0, b.pooled, b.ws)
+                    sel = b.pooled
+                    mark("kvc_pool_scores")
+                if args.select == "head":
+                    kvc.kvc_head_budget(b.shape, b.mba, b.budget, b.head_counts, b.ws)
+                    mark("kvc_head_budget")
+                    kvc.kvc_topk_select_heads(b.shape, sel, b.head_counts, b.k_max, b.idx, b.ws)
+                    mark("kvc_topk_select_heads")
+                    kvc.kvc_compact_heads(b.shape, x["k"], x["v"], b.idx, b.head_counts, b.k_max,
+                                          b.k_out, b.v_out, b.ws)
+                    mark("kvc_compact_heads")
+                else:
+                    kvc.kvc_topk_select(b.shape, sel, b.budget, b.k_max, b.idx, b.ws)
+                    mark("kvc_topk_select")
+                    kvc.kvc_compact(b.shape, x["k"], x["v"], b.idx, b.budget, b.k_max, b.k_out,
+                                    b.v_out, b.ws)
+                    mark("kvc_compact")
+                if args.think_value > 0:
+                    kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                                args.think_value, b.v_chan, b.v_pruned, b.ws)
+                    mark("kvc_channel_prune_value")
+                if wl.think_lambda is not None:
+                    if args.think_criterion == "query":
+                        kvc.kvc_channel_prune_query(b.shape, x["q"], b.k_out, b.budget,
+                                                    wl.think_lambda, b.chan, b.k_pruned, b.ws)
+                        mark("kvc_channel_prune_query")
+                    else:
+                        kvc.kvc_channel_prune(b.shape, b.k_out, b.budget, wl.think_lambda, b.chan,
+                                              b.k_pruned, b.ws)
+                        mark("kvc_channel_prune")
+        if side:
+            for js in streams:
+                done = torch.cuda.Event()
+                done.record(js)
+                stream.wait_event(done)
 
     for _ in range(args.warmup):
         step()
@@ -478,7 +498,8 @@ def run_kvc(args):
                        v for hc in heads for row in hc for v in row), 1)
                        if args.select != "layer" else None),
                    "l2": "inputs larger than the 129 MB L2 (K and V resident in HBM); no flush",
-                   "parallelism": f"replica x{world} (one prompt per GPU)"},
+                   "parallelism": f"replica x{world} (one prompt per GPU)",
+                   "streams": args.streams if len(jobs) > 1 else 1},
         "hbm_roofline": {"algorithmic_bytes_per_step": alg_bytes,
                          "achieved_gbs": round(alg_bytes / (ms_local / 1e3) / 1e9, 1),
                          "peak_gbs": pk["hbm_gbs"], "frac": round(hbm_frac, 4),
