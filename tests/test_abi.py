@@ -85,6 +85,29 @@ def test_host_side_validation_rejects_bad_arguments(lib):
                                4096, nul) == -1
 
 
+def test_value_channel_prune_rejects_bad_arguments(lib):
+    """kvc_channel_prune_value refuses NULL tensors, misaligned inputs, a
+    lambda that keeps no channel and a small workspace before any launch."""
+    from eviction_kvc_score_gb300 import kvc
+    L = kvc._lib
+    nul = C.c_void_p(0)
+    fake = C.c_void_p(0x1000)
+    s = _shape(kvc)
+
+    def call(q=fake, k=fake, v=fake, v_out=fake, bud=fake, lam=0.3, chan=fake, vp=fake, ws=fake,
+             ws_bytes=1 << 30):
+        return L.kvc_channel_prune_value(C.byref(s), q, k, v, v_out, bud, C.c_double(lam), nul,
+                                         chan, vp, 1 << 20, ws, ws_bytes, nul)
+    assert call(q=nul) == -1
+    assert call(v=nul) == -1
+    assert call(chan=nul) == -1
+    assert call(k=C.c_void_p(0x1008)) == -1                 # not 16-byte aligned
+    assert call(lam=1.0) == -1 and call(lam=-0.1) == -1     # keeps no channel / invalid
+    assert call(ws_bytes=64) == -5
+    assert call(ws=C.c_void_p(0x1010)) == -5                # workspace not 256-byte aligned
+    assert "kvc_channel_prune_value" in kvc.kvc_last_error()
+
+
 def test_keep_channels_and_workspace_size(lib):
     from eviction_kvc_score_gb300 import kvc
     assert kvc.kvc_keep_channels(0.4, 128) == 76
