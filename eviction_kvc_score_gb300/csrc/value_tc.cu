@@ -39,18 +39,30 @@
 // of P: hi words, then lo words), so no thread overwrites S that it or
 // another thread has not yet read; it also owns O channels [32e, 32e+32).
 //
-// Roles per CTA: warp 0 TMA producer (Q rows of the item; per tile its 64
-// keys and its 64 value channels of the tile's 128 keys), warp 1 the MMA
-// issuer (even CTA) or the relay of load completions (odd CTA), warps 2..17
-// four epilogue warpgroups (four warps per SM sub-partition hide the
-// exponentials' latency; two left the kernel at 40% of its MMA time).  Every wait is bounded (kvc_internal.cuh).
+// Roles per CTA: warp 0 loads Q rows (per item) and K (per tile, its 64
+// keys) into a four-stage K ring; warp 19 loads V (its 64 channels of the
+// tile's 128 keys) into a four-stage V ring; warp 1 issues S = Q K^T (even
+// CTA) or relays Q/K load completions to the even CTA (odd CTA); warp 18
+// issues O += P V (even CTA) or relays V completions (odd CTA); warps 2..17
+// are four epilogue warpgroups (four warps per SM sub-partition hide the
+// exponentials' latency; two left the kernel at 40% of its MMA time).
+// Two issuing threads because one thread's issue loop, not the tensor
+// pipe, set the pace: measured on the 32K prompt, a single issuer spent
+// ~2,300 clocks per tile issuing its 24 MMAs (1,536 clocks of tensor time);
+// split, `kvc_channel_prune_value` went from 3.84 to 3.20 ms with identical
+// scores.  The K ring is freed as soon as a tile's S is computed (it used to
+// wait for the tile's P V, which left the S issuer idle ~1,200 clocks per
+// tile waiting for K): 3.13 ms.  Per accumulator the MMAs keep their order,
+// so the result does not depend on the split.  Every wait is bounded
+// (kvc_internal.cuh).
 #include "kvc_internal.cuh"
 
 namespace kvc {
 
 namespace {
 
-constexpr int kVStages = 3;
+constexpr int kKStages = 4;   // K ring: freed when a tile's S = Q K^T completes
+constexpr int kVvStages = 4;  // V ring: freed when a tile's O += P V completes
 constexpr int kVSlots = 3;
 constexpr int kVTileKeys = 128;                 // keys per pair tile
 // O is accumulated in TMEM over chunks of this many tiles (2048 keys, 256
@@ -60,14 +72,17 @@ constexpr int kVTileKeys = 128;                 // keys per pair tile
 constexpr int kChunkTiles = 16;
 constexpr int kVEWG = 4;                        // epilogue warpgroups
 constexpr int kVKeysWG = kVTileKeys / kVEWG;    // S columns (keys) and O channels per warpgroup
-constexpr int kVThreadsTC = 64 + 128 * kVEWG;
+constexpr int kVThreadsTC = 64 + 128 * kVEWG + 64;   // + the P V issuer and V loader warps
+constexpr int kPVWarp = 2 + 4 * kVEWG;                // P V issuer (even CTA) / V relay (odd)
+constexpr int kVLoadWarp = kPVWarp + 1;               // V loader
 constexpr uint32_t kVTmemCols = 512;
 constexpr uint32_t kOCol = 0;                   // O accumulator columns [0,128)
 constexpr uint32_t kSlotCol0 = 128;             // slot s at 128 + 128 s
 constexpr int kQBox = 128 * 128;                // 128 rows x 64 bf16
 constexpr int kKBox = 64 * 128;                 // 64 keys x 64 bf16
 constexpr int kVBox = 128 * 128;                // 128 keys x 64 channels
-constexpr int kStageBytes = 2 * kKBox + kVBox;  // head_dim 128: two K boxes + one V box
+constexpr int kKStageBytes = 2 * kKBox;          // head_dim 128: two K boxes
+constexpr int kVStageBytes = kVBox;
 
 struct VtcParams {
     int64_t n_units;
@@ -83,19 +98,22 @@ struct VtcParams {
 
 struct VSmem {
     uint8_t *q;        // [2][128 rows][128 B]
-    uint8_t *kv;       // [stages][K box 0 | K box 1 | V box]
+    uint8_t *k;        // [kKStages][K box 0 | K box 1]
+    uint8_t *v;        // [kVvStages][V box]
     float *oacc;       // [16 epilogue warps][32 channels][32 lanes]: O summed over chunks
-    uint64_t *full, *empty, *pfull;     // [stages]
+    uint64_t *kf, *ke, *kp;   // K ring [kKStages]: loaded, free, peer's loaded (even CTA)
+    uint64_t *vf, *ve, *vp;   // V ring [kVvStages]
     uint64_t *q_full, *q_empty, *q_pfull;
     uint64_t *s_full, *p_full, *slot_empty;   // [slots]
-    uint64_t *o_full, *o_empty, *drain;
+    uint64_t *o_full, *o_empty, *drain, *drain2;
     uint32_t *tmem_base;
     volatile int *abort_flag;
 };
 
 constexpr size_t kOaccBytes = (size_t)4 * kVEWG * kVKeysWG * 32 * sizeof(float);
-constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kVStages * kStageBytes + kOaccBytes +
-                               (3 * kVStages + 3 * kVSlots + 8) * 8 +
+constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kKStages * kKStageBytes +
+                               (size_t)kVvStages * kVStageBytes + kOaccBytes +
+                               (3 * kKStages + 3 * kVvStages + 3 * kVSlots + 9) * 8 +
                                16;
 
 __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
@@ -103,15 +121,20 @@ __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
     uint8_t *b = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.q = b;
     b += 2 * kQBox;
-    s.kv = b;
-    b += (size_t)kVStages * kStageBytes;
+    s.k = b;
+    b += (size_t)kKStages * kKStageBytes;
+    s.v = b;
+    b += (size_t)kVvStages * kVStageBytes;
     s.oacc = reinterpret_cast<float *>(b);
     b += kOaccBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
-    s.full = bars;
-    s.empty = bars + kVStages;
-    s.pfull = bars + 2 * kVStages;
-    s.q_full = bars + 3 * kVStages;
+    s.kf = bars;
+    s.ke = bars + kKStages;
+    s.kp = bars + 2 * kKStages;
+    s.vf = bars + 3 * kKStages;
+    s.ve = s.vf + kVvStages;
+    s.vp = s.vf + 2 * kVvStages;
+    s.q_full = s.vf + 3 * kVvStages;
     s.q_empty = s.q_full + 1;
     s.q_pfull = s.q_full + 2;
     s.s_full = s.q_full + 3;
@@ -120,7 +143,8 @@ __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
     s.o_full = s.slot_empty + kVSlots;
     s.o_empty = s.o_full + 1;
     s.drain = s.o_full + 2;
-    s.tmem_base = reinterpret_cast<uint32_t *>(s.drain + 1);
+    s.drain2 = s.o_full + 3;
+    s.tmem_base = reinterpret_cast<uint32_t *>(s.drain2 + 1);
     s.abort_flag = reinterpret_cast<volatile int *>(s.tmem_base + 1);
     return s;
 }
@@ -149,7 +173,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     value_out_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, VtcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -158,10 +182,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
     const int rank = (int)cluster_ctarank();
     const int64_t c = cluster_id_x();
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kVStages; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);
-            mbar_init(&s.pfull[i], 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&s.kf[i], 1);
+            mbar_init(&s.ke[i], 1);
+            mbar_init(&s.kp[i], 1);
+        }
+        for (int i = 0; i < kVvStages; ++i) {
+            mbar_init(&s.vf[i], 1);
+            mbar_init(&s.ve[i], 1);
+            mbar_init(&s.vp[i], 1);
         }
         mbar_init(s.q_full, 1);
         mbar_init(s.q_empty, 1);
@@ -174,6 +203,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
         mbar_init(s.o_full, 1);
         mbar_init(s.o_empty, 2 * 4 * kVEWG);
         mbar_init(s.drain, 1);
+        mbar_init(s.drain2, 1);
         *s.abort_flag = 0;
         fence_barrier_init();
     }
@@ -205,31 +235,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                                 (int)it.u);
                 ++qi;
                 for (int t = 0; t < p.n_tiles; ++t, ++gt) {
-                    const uint32_t st = gt % kVStages, ph = (gt / kVStages) & 1;
-                    if (!mbar_wait(&s.empty[st], ph ^ 1, s.abort_flag, p.status)) {
+                    const uint32_t st = gt % kKStages, ph = (gt / kKStages) & 1;
+                    if (!mbar_wait(&s.ke[st], ph ^ 1, s.abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *stage = s.kv + (size_t)st * kStageBytes;
-                    mbar_arrive_expect_tx(&s.full[st], (uint32_t)kStageBytes);
+                    uint8_t *stage = s.k + (size_t)st * kKStageBytes;
+                    mbar_arrive_expect_tx(&s.kf[st], (uint32_t)kKStageBytes);
                     for (int kh = 0; kh < 2; ++kh)
-                        tma_load_3d(&tk, &s.full[st], stage + kh * kKBox, kh * 64,
+                        tma_load_3d(&tk, &s.kf[st], stage + kh * kKBox, kh * 64,
                                     t * kVTileKeys + rank * 64, (int)it.u);
-                    tma_load_3d(&tv, &s.full[st], stage + 2 * kKBox, rank * 64, t * kVTileKeys,
-                                (int)it.u);
                     ++issued;
                 }
             }
             if (*s.abort_flag) {   // unwind: every copy started must land
-                for (uint32_t g = issued > kVStages ? issued - kVStages : 0; g < issued; ++g)
-                    mbar_drain(&s.full[g % kVStages], (g / kVStages) & 1);
+                for (uint32_t g = issued > kKStages ? issued - kKStages : 0; g < issued; ++g)
+                    mbar_drain(&s.kf[g % kKStages], (g / kKStages) & 1);
                 if (qi > 0) mbar_drain(s.q_full, (qi - 1) & 1);
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 1) {
             // ------------------------------------------------ relay (odd CTA)
-            const uint32_t r_pfull = mapa_shared(smem_u32(s.pfull), 0);
+            const uint32_t r_pfull = mapa_shared(smem_u32(s.kp), 0);
             const uint32_t r_qpfull = mapa_shared(smem_u32(s.q_pfull), 0);
             uint32_t gt = 0, qi = 0;
             bool ok = true;
@@ -238,8 +266,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                 mbar_arrive_remote(r_qpfull);
                 ++qi;
                 for (int t = 0; t < p.n_tiles; ++t, ++gt) {
-                    const uint32_t st = gt % kVStages, ph = (gt / kVStages) & 1;
-                    if (!mbar_wait(&s.full[st], ph, s.abort_flag, p.status)) {
+                    const uint32_t st = gt % kKStages, ph = (gt / kKStages) & 1;
+                    if (!mbar_wait(&s.kf[st], ph, s.abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -247,63 +275,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                 }
             }
         } else if (lane == 0) {
-            // ------------------------------------------------ MMA issuer (even CTA)
+            // ------------------------------------------------ S = Q K^T issuer (even CTA)
             constexpr uint16_t kBoth = 3;
-            const uint32_t idesc1 = idesc_bf16_f32(256, 128);              // both K-major
-            const uint32_t idesc2 = idesc_bf16_f32(256, 128) | (1u << 16);  // B MN-major
+            const uint32_t idesc1 = idesc_bf16_f32(256, 128);   // both K-major
             uint32_t gt = 0, qi = 0;
             bool ok = true;
-            uint32_t chunks = 0;
-            const uint64_t qd0 = desc_sw128(smem_u32(s.q), 16u, 1024u);   // chunks of O handed to the epilogue so far
-            // O += P V for tile g, the item's tile t (a chunk's first tile
-            // overwrites O; its last hands O to the epilogue)
-            auto mma2 = [&](uint32_t g, int t) -> bool {
-                const uint32_t slot = g % kVSlots, use = g / kVSlots;
-                const uint32_t st = g % kVStages;
-                const bool first = t % kChunkTiles == 0;
-                const bool last = t % kChunkTiles == kChunkTiles - 1 || t == p.n_tiles - 1;
-                if (!mbar_wait(&s.p_full[slot], use & 1, s.abort_flag, p.status)) return false;
-                if (first && !mbar_wait(s.o_empty, (chunks & 1) ^ 1, s.abort_flag, p.status))
-                    return false;
-                tc_fence_after();
-                const uint32_t scol = tmem + kSlotCol0 + slot * 128;
-                // one descriptor per stage; a K-step only moves the start
-                // address field (bits [0,14), in 16-byte units)
-                const uint64_t b0 =
-                    desc_sw128(smem_u32(s.kv + (size_t)st * kStageBytes + 2 * kKBox), 1024u, 1024u);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    // keys 16 ks ..: the P_hi words of that half of warpgroup
-                    // ks / 2's keys at columns 16 ks, its P_lo words 8
-                    // further; value rows 16 ks .. of the box (2048 bytes on)
-                    const uint32_t acol = scol + (uint32_t)(ks * 16);
-                    const uint64_t b = b0 + (uint64_t)(ks * (2048 >> 4));
-                    tc_mma2_bf16_tmem_a(tmem + kOCol, acol, b, idesc2, (first && ks == 0) ? 0u : 1u);
-                    tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 8u, b, idesc2, 1u);
-                }
-                tc_commit2(&s.slot_empty[slot], kBoth);
-                tc_commit2(&s.empty[st], kBoth);
-                if (last) {
-                    tc_commit2(s.o_full, kBoth);
-                    ++chunks;
-                }
-                return true;
-            };
+            const uint64_t qd0 = desc_sw128(smem_u32(s.q), 16u, 1024u);
             for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
                 if (!mbar_wait(s.q_full, qi & 1, s.abort_flag, p.status)) break;
                 if (!mbar_wait(s.q_pfull, qi & 1, s.abort_flag, p.status)) break;
                 ++qi;
                 for (int t = 0; t < p.n_tiles; ++t, ++gt) {
-                    const uint32_t st = gt % kVStages, ph = (gt / kVStages) & 1;
+                    const uint32_t st = gt % kKStages, ph = (gt / kKStages) & 1;
                     const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
-                    if (!mbar_wait(&s.full[st], ph, s.abort_flag, p.status) ||
-                        !mbar_wait(&s.pfull[st], ph, s.abort_flag, p.status) ||
+                    if (!mbar_wait(&s.kf[st], ph, s.abort_flag, p.status) ||
+                        !mbar_wait(&s.kp[st], ph, s.abort_flag, p.status) ||
                         !mbar_wait(&s.slot_empty[slot], (use & 1) ^ 1, s.abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t kd0 = desc_sw128(smem_u32(s.kv + (size_t)st * kStageBytes), 16u, 1024u);
+                    const uint64_t kd0 = desc_sw128(smem_u32(s.k + (size_t)st * kKStageBytes), 16u, 1024u);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         // K-steps 0-3 in the first 64-column box, 4-7 in the
@@ -314,18 +306,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kVThreadsTC, 1)
                         tc_mma2_bf16(tmem + kSlotCol0 + slot * 128, a, b, idesc1, ks > 0);
                     }
                     tc_commit2(&s.s_full[slot], kBoth);
+                    tc_commit2(&s.ke[st], kBoth);   // K stage free for the loaders
                     if (t == p.n_tiles - 1) tc_commit2(s.q_empty, kBoth);
-                    // the previous tile's P V runs behind this tile's Q K^T
-                    if (t > 0 && !mma2(gt - 1, t - 1)) {
-                        ok = false;
-                        break;
-                    }
                 }
-                if (!ok) break;
-                if (!mma2(gt - 1, p.n_tiles - 1)) break;
             }
             tc_commit2(s.drain, 1);
             mbar_drain(s.drain, 0);
+        }
+    } else if (warp == kPVWarp) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ O += P V issuer (even CTA)
+            // A second issuing thread, with its own V ring.
+            constexpr uint16_t kBoth = 3;
+            const uint32_t idesc2 = idesc_bf16_f32(256, 128) | (1u << 16);  // B MN-major
+            uint32_t gt = 0, chunks = 0;
+            bool ok = true;
+            for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+                for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                    const uint32_t slot = gt % kVSlots, use = gt / kVSlots;
+                    const uint32_t st = gt % kVvStages, ph = (gt / kVvStages) & 1;
+                    const bool first = t % kChunkTiles == 0;
+                    const bool last = t % kChunkTiles == kChunkTiles - 1 || t == p.n_tiles - 1;
+                    if (!mbar_wait(&s.vf[st], ph, s.abort_flag, p.status) ||
+                        !mbar_wait(&s.vp[st], ph, s.abort_flag, p.status) ||
+                        !mbar_wait(&s.p_full[slot], use & 1, s.abort_flag, p.status) ||
+                        (first && !mbar_wait(s.o_empty, (chunks & 1) ^ 1, s.abort_flag, p.status))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t scol = tmem + kSlotCol0 + slot * 128;
+                    const uint64_t b0 = desc_sw128(smem_u32(s.v + (size_t)st * kVStageBytes), 1024u, 1024u);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        // keys 16 ks ..: the P_hi words of that half of warpgroup
+                        // ks / 2's keys at columns 16 ks, its P_lo words 8
+                        // further; value rows 16 ks .. of the box (2048 bytes on)
+                        const uint32_t acol = scol + (uint32_t)(ks * 16);
+                        const uint64_t b = b0 + (uint64_t)(ks * (2048 >> 4));
+                        tc_mma2_bf16_tmem_a(tmem + kOCol, acol, b, idesc2, (first && ks == 0) ? 0u : 1u);
+                        tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 8u, b, idesc2, 1u);
+                    }
+                    tc_commit2(&s.slot_empty[slot], kBoth);
+                    tc_commit2(&s.ve[st], kBoth);   // V stage free for the loaders
+                    if (last) {
+                        tc_commit2(s.o_full, kBoth);
+                        ++chunks;
+                    }
+                }
+            }
+            tc_commit2(s.drain2, 1);
+            mbar_drain(s.drain2, 0);
+        } else if (lane == 0) {
+            // ------------------------------------------------ V relay (odd CTA)
+            const uint32_t r_vp = mapa_shared(smem_u32(s.vp), 0);
+            uint32_t gt = 0;
+            bool ok = true;
+            for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+                for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                    const uint32_t st = gt % kVvStages, ph = (gt / kVvStages) & 1;
+                    if (!mbar_wait(&s.vf[st], ph, s.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote(r_vp + st * 8u);
+                }
+            }
+        }
+    } else if (warp == kVLoadWarp) {
+        if (lane == 0) {
+            // ------------------------------------------------ V loader
+            tma_prefetch_desc(&tv);
+            uint32_t gt = 0, issued = 0;
+            bool ok = true;
+            for (int64_t i = c; i < p.n_items && ok; i += p.pairs) {
+                const Item it = item_of(i, p.njob);
+                for (int t = 0; t < p.n_tiles; ++t, ++gt) {
+                    const uint32_t st = gt % kVvStages, ph = (gt / kVvStages) & 1;
+                    if (!mbar_wait(&s.ve[st], ph ^ 1, s.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.vf[st], (uint32_t)kVStageBytes);
+                    tma_load_3d(&tv, &s.vf[st], s.v + (size_t)st * kVStageBytes, rank * 64,
+                                t * kVTileKeys, (int)it.u);
+                    ++issued;
+                }
+            }
+            if (*s.abort_flag) {   // unwind: every copy started must land
+                for (uint32_t g = issued > kVvStages ? issued - kVvStages : 0; g < issued; ++g)
+                    mbar_drain(&s.vf[g % kVvStages], (g / kVvStages) & 1);
+            }
         }
     } else {
         // ---------------------------------------------------- epilogue
