@@ -40,8 +40,8 @@
 // another thread has not yet read; it also owns O channels [32e, 32e+32).
 //
 // Roles per CTA: warp 0 loads Q rows (per item) and K (per tile, its 64
-// keys) into a four-stage K ring; warp 19 loads V (its 64 channels of the
-// tile's 128 keys) into a four-stage V ring; warp 1 issues S = Q K^T (even
+// keys) into a three-stage K ring; warp 19 loads V (its 64 channels of the
+// tile's 128 keys) into a three-stage V ring; warp 1 issues S = Q K^T (even
 // CTA) or relays Q/K load completions to the even CTA (odd CTA); warp 18
 // issues O += P V (even CTA) or relays V completions (odd CTA); warps 2..17
 // are four epilogue warpgroups (four warps per SM sub-partition hide the
@@ -50,10 +50,11 @@
 // pipe, set the pace: measured on the 32K prompt, a single issuer spent
 // ~2,300 clocks per tile issuing its 24 MMAs (1,536 clocks of tensor time);
 // split, `kvc_channel_prune_value` went from 3.84 to 3.20 ms with identical
-// scores.  The K ring is freed as soon as a tile's S is computed (it used to
-// wait for the tile's P V, which left the S issuer idle ~1,200 clocks per
-// tile waiting for K): 3.13 ms.  Per accumulator the MMAs keep their order,
-// so the result does not depend on the split.  Every wait is bounded
+// scores.  K and V have rings of their own, K freed as soon as a tile's S is
+// computed (a shared stage freed only after the tile's P V left the S issuer
+// idle ~1,200 clocks per tile waiting for K): 3.13 ms; the rings' free
+// signals folded into the slot barriers: 3.06 ms.  Per accumulator the MMAs
+// keep their order, so the result does not depend on the split.  Every wait is bounded
 // (kvc_internal.cuh).
 #include "kvc_internal.cuh"
 
@@ -61,8 +62,12 @@ namespace kvc {
 
 namespace {
 
-constexpr int kKStages = 4;   // K ring: freed when a tile's S = Q K^T completes
-constexpr int kVvStages = 4;  // V ring: freed when a tile's O += P V completes
+// K and V rings of as many stages as there are S/P slots and indexed like
+// them, so a slot's barriers also free its stages: K stage s when the slot's
+// S is computed (s_full), V stage s when its P V is done (slot_empty) -- one
+// commit per issuer and tile fewer than rings of their own.
+constexpr int kKStages = 3;
+constexpr int kVvStages = 3;
 constexpr int kVSlots = 3;
 constexpr int kVTileKeys = 128;                 // keys per pair tile
 // O is accumulated in TMEM over chunks of this many tiles (2048 keys, 256
@@ -101,8 +106,8 @@ struct VSmem {
     uint8_t *k;        // [kKStages][K box 0 | K box 1]
     uint8_t *v;        // [kVvStages][V box]
     float *oacc;       // [16 epilogue warps][32 channels][32 lanes]: O summed over chunks
-    uint64_t *kf, *ke, *kp;   // K ring [kKStages]: loaded, free, peer's loaded (even CTA)
-    uint64_t *vf, *ve, *vp;   // V ring [kVvStages]
+    uint64_t *kf, *kp;   // K ring [kKStages]: loaded, peer's loaded (even CTA)
+    uint64_t *vf, *vp;   // V ring [kVvStages]
     uint64_t *q_full, *q_empty, *q_pfull;
     uint64_t *s_full, *p_full, *slot_empty;   // [slots]
     uint64_t *o_full, *o_empty, *drain, *drain2;
@@ -113,7 +118,7 @@ struct VSmem {
 constexpr size_t kOaccBytes = (size_t)4 * kVEWG * kVKeysWG * 32 * sizeof(float);
 constexpr size_t kVSmemBytes = 1024 + 2 * kQBox + (size_t)kKStages * kKStageBytes +
                                (size_t)kVvStages * kVStageBytes + kOaccBytes +
-                               (3 * kKStages + 3 * kVvStages + 3 * kVSlots + 9) * 8 +
+                               (2 * kKStages + 2 * kVvStages + 3 * kVSlots + 9) * 8 +
                                16;
 
 __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
@@ -129,12 +134,10 @@ __device__ __forceinline__ VSmem vcarve(uint8_t *raw) {
     b += kOaccBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(b);
     s.kf = bars;
-    s.ke = bars + kKStages;
-    s.kp = bars + 2 * kKStages;
-    s.vf = bars + 3 * kKStages;
-    s.ve = s.vf + kVvStages;
-    s.vp = s.vf + 2 * kVvStages;
-    s.q_full = s.vf + 3 * kVvStages;
+    s.kp = bars + kKStages;
+    s.vf = bars + 2 * kKStages;
+    s.vp = s.vf + kVvStages;
+    s.q_full = s.vf + 2 * kVvStages;
     s.q_empty = s.q_full + 1;
     s.q_pfull = s.q_full + 2;
     s.s_full = s.q_full + 3;
@@ -184,12 +187,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&s.kf[i], 1);
-            mbar_init(&s.ke[i], 1);
             mbar_init(&s.kp[i], 1);
         }
         for (int i = 0; i < kVvStages; ++i) {
             mbar_init(&s.vf[i], 1);
-            mbar_init(&s.ve[i], 1);
             mbar_init(&s.vp[i], 1);
         }
         mbar_init(s.q_full, 1);
@@ -236,7 +237,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                 ++qi;
                 for (int t = 0; t < p.n_tiles; ++t, ++gt) {
                     const uint32_t st = gt % kKStages, ph = (gt / kKStages) & 1;
-                    if (!mbar_wait(&s.ke[st], ph ^ 1, s.abort_flag, p.status)) {
+                    // stage st is free once the slot-st S of three tiles ago is
+                    // computed (its s_full phase); the first round needs no wait
+                    if (gt >= (uint32_t)kKStages &&
+                        !mbar_wait(&s.s_full[st], ph ^ 1, s.abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -306,7 +310,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                         tc_mma2_bf16(tmem + kSlotCol0 + slot * 128, a, b, idesc1, ks > 0);
                     }
                     tc_commit2(&s.s_full[slot], kBoth);
-                    tc_commit2(&s.ke[st], kBoth);   // K stage free for the loaders
                     if (t == p.n_tiles - 1) tc_commit2(s.q_empty, kBoth);
                 }
             }
@@ -316,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     } else if (warp == kPVWarp) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------ O += P V issuer (even CTA)
-            // A second issuing thread, with its own V ring.
+            // The second issuing thread.
             constexpr uint16_t kBoth = 3;
             const uint32_t idesc2 = idesc_bf16_f32(256, 128) | (1u << 16);  // B MN-major
             uint32_t gt = 0, chunks = 0;
@@ -348,7 +351,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                         tc_mma2_bf16_tmem_a(tmem + kOCol, acol + 8u, b, idesc2, 1u);
                     }
                     tc_commit2(&s.slot_empty[slot], kBoth);
-                    tc_commit2(&s.ve[st], kBoth);   // V stage free for the loaders
                     if (last) {
                         tc_commit2(s.o_full, kBoth);
                         ++chunks;
@@ -383,7 +385,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                 const Item it = item_of(i, p.njob);
                 for (int t = 0; t < p.n_tiles; ++t, ++gt) {
                     const uint32_t st = gt % kVvStages, ph = (gt / kVvStages) & 1;
-                    if (!mbar_wait(&s.ve[st], ph ^ 1, s.abort_flag, p.status)) {
+                    // free once the slot-st P V of three tiles ago is done
+                    if (!mbar_wait(&s.slot_empty[st], ph ^ 1, s.abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
