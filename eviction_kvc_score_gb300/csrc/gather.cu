@@ -138,17 +138,92 @@ __device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16 *p, int
 }
 
 constexpr int kPruneThreads = 512;
+constexpr int kPruneWarps = kPruneThreads / 32;
 constexpr int kPruneCluster = 8;   // CTAs per head, one cluster
+
+// x^2 added to a float-float sum.  A bf16 value has 8 significant bits, so
+// its square is exact in fp32; an fp32 square carries its FMA-recovered
+// rounding error.
+template <typename T>
+__device__ __forceinline__ FF ff_add_sq_t(FF a, float x) {
+    if constexpr (sizeof(T) == 2) {
+        float s, e;
+        two_sum(a.hi, x * x, s, e);
+        e += a.lo;
+        FF r;
+        two_sum(s, e, r.hi, r.lo);
+        return r;
+    } else {
+        return ff_add_sq(a, x);
+    }
+}
+
+// Per-channel float-float sums of squares over rows [lo, hi) of the
+// row-major [rows][D] block starting at row first_row of base: warp w takes
+// rows lo + w, lo + w + 16, ...; lane l owns channels l + 32 k, so each load
+// instruction of a warp reads consecutive elements of one row.  The warps'
+// partial sums are added in warp order (a fixed order: every CTA of a head
+// gets the same bits for the same slice).
+template <typename T, int CPL>
+__device__ void slice_sums(const T *__restrict__ base, int64_t first_row, int lo, int hi, int D,
+                           FF *wpart, FF *out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    FF a[CPL];
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) a[k] = {0.f, 0.f};
+    int r = lo + warp;
+    // four rows' loads in flight before their (dependent) sums: the warp's
+    // rows are few and HBM latency, not bandwidth, would set the pace
+    constexpr int kRowsInFlight = 4;
+    for (; r + (kRowsInFlight - 1) * kPruneWarps < hi; r += kRowsInFlight * kPruneWarps) {
+        float x[kRowsInFlight][CPL];
+#pragma unroll
+        for (int i = 0; i < kRowsInFlight; ++i) {
+            const T *ri = base + (first_row + r + (int64_t)i * kPruneWarps) * D;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                const int c = lane + 32 * k;
+                x[i][k] = c < D ? ld_f(ri, c) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsInFlight; ++i)
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) a[k] = ff_add_sq_t<T>(a[k], x[i][k]);
+    }
+    for (; r < hi; r += kPruneWarps) {
+        const T *r0 = base + (first_row + r) * D;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int c = lane + 32 * k;
+            if (c < D) a[k] = ff_add_sq_t<T>(a[k], ld_f(r0, c));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const int c = lane + 32 * k;
+        if (c < D) wpart[warp * D + c] = a[k];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kPruneThreads) {
+        FF t = wpart[c];
+        for (int w = 1; w < kPruneWarps; ++w) t = ff_add(t, wpart[w * D + c]);
+        out[c] = t;
+    }
+    __syncthreads();
+}
 
 // One cluster of kPruneCluster CTAs per head: CTA `rank` owns a contiguous
 // slice of the head's kept prefix rows (and of its window-query rows for the
 // query-driven criterion).  Each CTA forms float-float per-channel sums of
-// squares over its slice (thread = channel x row group, two interleaved
-// accumulators per thread); after a cluster barrier every CTA adds the
-// slices' sums in rank order from distributed shared memory -- the same
-// fixed order in every CTA, so all of them rank the channels identically --
-// and copies the chosen channels of its own rows.
-template <typename T>
+// squares over its slice; after a cluster barrier every CTA adds the slices'
+// sums in rank order from distributed shared memory -- the same fixed order
+// in every CTA, so all of them rank the channels identically -- and copies
+// the chosen channels of its own rows: a warp per row, lane l writing output
+// positions l + 32 k from source channels fixed for the head (coalesced
+// stores, no per-element index arithmetic).  CPL = channels per lane
+// (D <= 32 CPL).
+template <typename T, int CPL>
 __global__ void __launch_bounds__(kPruneThreads)
     channel_prune_kernel(const T *__restrict__ k_out, const T *__restrict__ q, int Hq,
                          const int32_t *__restrict__ budget, int T_len, int W, int Hkv, int D,
@@ -156,11 +231,11 @@ __global__ void __launch_bounds__(kPruneThreads)
                          int64_t pruned_elems, uint32_t *status, const float *__restrict__ given) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
-    __shared__ FF part[kPruneThreads];
-    __shared__ FF slice_k[256], slice_q[256];
-    __shared__ double m[256];
-    __shared__ int sel[256];
-    __shared__ int flag[256];
+    __shared__ FF wpart[kPruneWarps * 32 * CPL];
+    __shared__ FF slice_k[32 * CPL], slice_q[32 * CPL];
+    __shared__ unsigned long long m[32 * CPL];   // channel scores as ordered keys
+    __shared__ int sel[32 * CPL];
+    __shared__ int flag[32 * CPL];
     __shared__ int64_t s_row0, s_o0;
     __shared__ int s_n;
     const int rank = (int)cluster.block_rank();
@@ -168,65 +243,48 @@ __global__ void __launch_bounds__(kPruneThreads)
     const int l = head / Hkv, h = head % Hkv;
     const int P = T_len - W;
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        const int64_t n = kept(budget[l], P);
-        s_n = (int)n;
-        s_row0 = layer_row_offset(budget, l, Hkv, P, W) + (int64_t)h * (n + W);
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        // kept prefix rows of the layers before l, summed by the warp (the
+        // loads in parallel, not one dependent load per layer)
         int64_t o = 0;
-        for (int i = 0; i < l; ++i) o += kept(budget[i], P);
-        s_o0 = ((int64_t)Hkv * o + (int64_t)h * n) * keep;
+        for (int i = lane; i < l; i += 32) o += kept(budget[i], P);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) o += __shfl_xor_sync(0xffffffffu, o, off);
+        if (lane == 0) {
+            const int64_t n = kept(budget[l], P);
+            s_n = (int)n;
+            // each earlier layer holds Hkv heads of (kept + W) rows
+            s_row0 = (int64_t)Hkv * (o + (int64_t)l * W) + (int64_t)h * (n + W);
+            s_o0 = ((int64_t)Hkv * o + (int64_t)h * n) * keep;
+        }
     }
     __syncthreads();
     const int n = s_n;
     const int64_t row0 = s_row0;
     const int r_lo = (int)((int64_t)n * rank / kPruneCluster);
     const int r_hi = (int)((int64_t)n * (rank + 1) / kPruneCluster);
-    const int groups = kPruneThreads / D;
-    const int d = tid % D, g = tid / D;
 
     // 1. this CTA's slice: per-channel sums of squares of its rows
-    auto slice_sum = [&](const T *base, int64_t first_row, int lo, int hi, FF *out) {
-        FF a0 = {0.f, 0.f}, a1 = {0.f, 0.f};
-        if (g < groups) {
-            // eight rows' loads in flight before their sums (the rows come
-            // from global memory; the sums are a dependent chain)
-            int r = lo + g;
-            for (; r + 7 * groups < hi; r += 8 * groups) {
-                float x[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) x[k] = ld_f(base, (first_row + r + k * groups) * D + d);
-#pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    a0 = ff_add_sq(a0, x[k]);
-                    a1 = ff_add_sq(a1, x[k + 1]);
-                }
-            }
-            for (; r < hi; r += groups) a0 = ff_add_sq(a0, ld_f(base, (first_row + r) * D + d));
-        }
-        part[tid] = ff_add(a0, a1);
-        __syncthreads();
-        if (tid < D) {
-            FF tot = part[tid];
-            for (int gg = 1; gg < groups; ++gg) tot = ff_add(tot, part[gg * D + tid]);
-            out[tid] = tot;
-        }
-        __syncthreads();
-    };
-    if (given == nullptr) slice_sum(k_out, row0, r_lo, r_hi, slice_k);
+    if (given == nullptr) slice_sums<T, CPL>(k_out, row0, r_lo, r_hi, D, wpart, slice_k);
     if (given == nullptr && q != nullptr) {
         // query-driven criterion: the W window rows of each of the head's G
         // query heads, split over the cluster like the key rows
         const int G = Hq / Hkv;
         const int qrows = G * W;
-        slice_sum(q, ((int64_t)l * Hq + (int64_t)h * G) * W,
-                  (int)((int64_t)qrows * rank / kPruneCluster),
-                  (int)((int64_t)qrows * (rank + 1) / kPruneCluster), slice_q);
+        slice_sums<T, CPL>(q, ((int64_t)l * Hq + (int64_t)h * G) * W,
+                           (int)((int64_t)qrows * rank / kPruneCluster),
+                           (int)((int64_t)qrows * (rank + 1) / kPruneCluster), D, wpart, slice_q);
     }
     cluster.sync();
 
-    // 2. whole-head sums in rank order, then rank by (score desc, d asc)
+    // 2. whole-head sums in rank order, then rank by (score desc, d asc).
+    // The scores are non-negative doubles, whose bit patterns order like the
+    // values as 64-bit integers: the D x D comparisons run on integer units
+    // (this part's FP64 rate is a small fraction of its FP32 rate).
     if (tid < D && given != nullptr) {
-        m[tid] = (double)given[(int64_t)head * D + tid];   // THINKV: scores supplied
+        const double mg = (double)given[(int64_t)head * D + tid];   // THINKV: scores supplied
+        m[tid] = (unsigned long long)__double_as_longlong(mg > 0.0 ? mg : 0.0);
     } else if (tid < D) {
         FF tk = {0.f, 0.f}, tq = {0.f, 0.f};
         for (int rr = 0; rr < kPruneCluster; ++rr) {
@@ -235,11 +293,11 @@ __global__ void __launch_bounds__(kPruneThreads)
         }
         double mk = (double)tk.hi + (double)tk.lo;
         if (q != nullptr) mk *= (double)tq.hi + (double)tq.lo;
-        m[tid] = mk;
+        m[tid] = (unsigned long long)__double_as_longlong(mk > 0.0 ? mk : 0.0);
     }
     __syncthreads();
     if (tid < D) {
-        const double mine = m[tid];
+        const unsigned long long mine = m[tid];
         int rk = 0;
         for (int o = 0; o < D; ++o) rk += (m[o] > mine) || (m[o] == mine && o < tid);
         flag[tid] = rk < keep;
@@ -257,19 +315,25 @@ __global__ void __launch_bounds__(kPruneThreads)
         (sel[tid] < 0 || sel[tid] >= D || (tid > 0 && sel[tid - 1] >= sel[tid])))
         set_status(status, KVC_DEV_INVARIANT);   // keep channels, strictly ascending
 
-    // 3. copy the kept channels of this CTA's rows
-    const int64_t o0 = s_o0 + (int64_t)r_lo * keep;
-    int total = (r_hi - r_lo) * keep;
-    if (o0 + total > pruned_elems) {   // output too small: copy what fits, report it
-        if (tid == 0) set_status(status, KVC_DEV_OUT_CAPACITY);
-        total = (int)max((int64_t)0, pruned_elems - o0);
+    // 3. copy the kept channels of this CTA's rows: warp per row
+    int src[CPL];
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const int j = lane + 32 * k;
+        src[k] = j < keep ? sel[j] : -1;
     }
-    const T *src = k_out + (row0 + r_lo) * D;
-    T *dst = k_pruned + o0;
+    if (s_o0 + (int64_t)r_hi * keep > pruned_elems && tid == 0)
+        set_status(status, KVC_DEV_OUT_CAPACITY);   // output too small: copy what fits
 #pragma unroll 4
-    for (int i = tid; i < total; i += kPruneThreads) {
-        const int r = i / keep;
-        dst[i] = src[(int64_t)r * D + sel[i - r * keep]];
+    for (int r = r_lo + warp; r < r_hi; r += kPruneWarps) {
+        const T *s_row = k_out + (row0 + r) * D;
+        const int64_t o = s_o0 + (int64_t)r * keep;
+        T *d_row = k_pruned + o;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int j = lane + 32 * k;
+            if (src[k] >= 0 && o + j < pruned_elems) d_row[j] = s_row[src[k]];
+        }
     }
 }
 
@@ -290,9 +354,15 @@ cudaError_t launch_prune_t(const kvc_shape &s, const void *q, const void *k_out,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, channel_prune_kernel<T>, (const T *)k_out, (const T *)q,
-                              s.n_q_heads, budget, s.seq_len, s.window, s.n_kv_heads, s.head_dim,
-                              (int)keep, chan, (T *)k_pruned, pruned_elems, status, given);
+    auto go = [&](auto kernel) {
+        return cudaLaunchKernelEx(&cfg, kernel, (const T *)k_out, (const T *)q, s.n_q_heads, budget,
+                                  s.seq_len, s.window, s.n_kv_heads, s.head_dim, (int)keep, chan,
+                                  (T *)k_pruned, pruned_elems, status, given);
+    };
+    // channels per lane of the sums and the copy
+    if (s.head_dim <= 64) return go(channel_prune_kernel<T, 2>);
+    if (s.head_dim <= 128) return go(channel_prune_kernel<T, 4>);
+    return go(channel_prune_kernel<T, 8>);
 }
 
 }  // namespace
