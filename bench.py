@@ -43,7 +43,10 @@ SUSTAINED_REGION_S = 2.0
 # kernels each C-ABI call launches
 LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
             "kvc_channel_prune": 1, "kvc_pool_scores": 1, "kvc_head_budget": 1,
-            "kvc_threshold_select": 1, "kvc_channel_prune_value": 5}
+            "kvc_threshold_select": 1,
+            # value kernel, merge, channel copy (+ stats pass and merge unless
+            # the step's kvc_score statistics are reused)
+            "kvc_channel_prune_value": 3}
 
 
 def parse():
@@ -358,8 +361,12 @@ def run_kvc(args):
                                     b.v_out, b.ws)
                     mark("kvc_compact")
                 if args.think_value > 0:
+                    # the step's own kvc_score on this workspace left the window
+                    # rows' softmax statistics: THINKV reuses them (Keyformer's
+                    # noisy statistics are not THINKV's)
                     kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
-                                                args.think_value, b.v_chan, b.v_pruned, b.ws)
+                                                args.think_value, b.v_chan, b.v_pruned, b.ws,
+                                                reuse_score_stats=args.score == "snapkv")
                     mark("kvc_channel_prune_value")
                 if wl.think_lambda is not None:
                     if args.think_criterion == "query":
@@ -465,16 +472,20 @@ def run_kvc(args):
 
     think_value = None
     if args.think_value > 0 and single and "kvc_channel_prune_value" in stages:
-        # THINKV's contractions: the row statistics (pass 1, 2 H_q W D T per
-        # layer), Q K^T again in the value kernel, and P V as two bf16 terms
+        # THINKV's contractions: Q K^T again in the value kernel and P V as two
+        # bf16 terms (2 H_q W D T per layer each); the row statistics come
+        # from the step's kvc_score
         wl = jobs[0][0]
         unit = 2 * wl.n_q_heads * wl.window * wl.head_dim * wl.seq_len * wl.n_layers
-        fl = 4 * unit
+        reused = args.score == "snapkv"
+        fl = (3 if reused else 4) * unit
         ms_v = stages["kvc_channel_prune_value"] / len(jobs)
         think_value = {"ms": round(ms_v, 4), "flops": fl,
                        "tflops": round(fl / (ms_v / 1e3) / 1e12, 1),
                        "frac_of_bf16_burst": round(fl / (ms_v / 1e3) / 1e12 / pk["bf16_tflops"], 4),
-                       "note": "pass 1 + Q K^T + P_hi V + P_lo V; stage event time"}
+                       "note": ("Q K^T + P_hi V + P_lo V (row statistics reused from kvc_score)"
+                                if reused else "pass 1 + Q K^T + P_hi V + P_lo V")
+                               + "; stage event time"}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -514,7 +525,8 @@ def run_kvc(args):
              + (LAUNCHES["kvc_head_budget"] if args.select == "head" else 0)
              + (LAUNCHES["kvc_pool_scores"] if args.pool > 1 else 0))
             + (LAUNCHES["kvc_channel_prune"] if wls[0].think_lambda is not None else 0)
-            + (LAUNCHES["kvc_channel_prune_value"] if args.think_value > 0 else 0)),
+            + ((LAUNCHES["kvc_channel_prune_value"] + (0 if args.score == "snapkv" else 2))
+               if args.think_value > 0 else 0)),
         "stages_ms": {k: round(v / len(jobs), 4) for k, v in stages.items()},
         "think_value": think_value,
         "wall_s_timed": round(t_wall, 3),

@@ -158,6 +158,67 @@ void checkin_events(EventSet *e) {
     e->in_use = false;
 }
 
+// The window rows' softmax statistics a plain score pass leaves in a
+// workspace (the merge's -(m_r + log2 l_r)), recorded per workspace with what
+// they were computed from, so that kvc_channel_prune_value_ex can reuse them
+// on request.  Host-side and per process; a record is replaced by the next
+// plain score pass over the workspace and dropped by anything else that
+// rewrites the statistics (a Keyformer score, a workspace reset).
+struct StatsRecord {
+    const void *ws;
+    kvc_shape s;
+    const void *q, *k;
+    bool tc;
+    int device;
+};
+std::mutex g_stats_mu;
+std::vector<StatsRecord> g_stats;
+
+bool same_shape(const kvc_shape &a, const kvc_shape &b) {
+    return a.n_layers == b.n_layers && a.n_q_heads == b.n_q_heads && a.n_kv_heads == b.n_kv_heads &&
+           a.head_dim == b.head_dim && a.seq_len == b.seq_len && a.window == b.window &&
+           a.dtype == b.dtype;
+}
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) {
+        cudaGetLastError();
+        d = -1;
+    }
+    return d;
+}
+
+void stats_forget(const void *ws) {
+    std::lock_guard<std::mutex> lk(g_stats_mu);
+    for (size_t i = 0; i < g_stats.size(); ++i)
+        if (g_stats[i].ws == ws) {
+            g_stats[i] = g_stats.back();
+            g_stats.pop_back();
+            return;
+        }
+}
+
+void stats_record(const void *ws, const kvc_shape &s, const void *q, const void *k, bool tc) {
+    const StatsRecord r{ws, s, q, k, tc, current_device()};
+    std::lock_guard<std::mutex> lk(g_stats_mu);
+    for (auto &e : g_stats)
+        if (e.ws == ws) {
+            e = r;
+            return;
+        }
+    g_stats.push_back(r);
+}
+
+bool stats_match(const void *ws, const kvc_shape &s, const void *q, const void *k, bool tc) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_stats_mu);
+    for (const auto &e : g_stats)
+        if (e.ws == ws)
+            return same_shape(e.s, s) && e.q == q && e.k == k && e.tc == tc && e.device == dev;
+    return false;
+}
+
 }  // namespace
 
 // Shape validation and score-kernel choice, shared by every entry point that
@@ -221,6 +282,7 @@ int kvc_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
     NvtxRange nvtx_range("kvc_workspace_init");
     g_err[0] = 0;
     if (!ws || ws_bytes < kWsHeader) return fail(KVC_ERR_WORKSPACE, "kvc_workspace_init: bad workspace");
+    stats_forget(ws);
     cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
     if (e != cudaSuccess) return fail(KVC_ERR_CUDA, "kvc_workspace_init: %s", cudaGetErrorString(e));
     return KVC_OK;
@@ -265,7 +327,12 @@ int kvc_score(const kvc_shape *shape, const void *q_obs, const void *k, float *s
     a.partial = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.partial_off);
     a.neg_bias = reinterpret_cast<float *>(static_cast<char *>(ws) + w.bias_off);
     a.status = status_word(ws);
-    return tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
+    const int rc = tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
+    if (rc == KVC_OK)
+        stats_record(ws, s, q_obs, k, tc);
+    else
+        stats_forget(ws);
+    return rc;
 }
 
 // Host-resident prompt, whole default path (see kvc.h).
@@ -398,6 +465,7 @@ int kvc_score_keyformer(const kvc_shape *shape, const void *q_obs, const void *k
     a.partial = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.partial_off);
     a.neg_bias = reinterpret_cast<float *>(static_cast<char *>(ws) + w.bias_off);
     a.status = status_word(ws);
+    stats_forget(ws);   // the noisy statistics replace the plain ones
     return tc ? launch_score_tc_keyformer(s, sp, a, seed, tau, stream)
               : launch_score_keyformer(s, sp, a, seed, tau, stream);
 }
@@ -545,6 +613,15 @@ int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const voi
                             const void *v, const void *v_out, const int32_t *budget, double lambda,
                             float *value_scores, int32_t *chan, void *v_pruned,
                             int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return kvc_channel_prune_value_ex(shape, q_obs, k, v, v_out, budget, lambda, value_scores, chan,
+                                      v_pruned, pruned_elems, 0u, ws, ws_bytes, stream);
+}
+
+int kvc_channel_prune_value_ex(const kvc_shape *shape, const void *q_obs, const void *k,
+                               const void *v, const void *v_out, const int32_t *budget,
+                               double lambda, float *value_scores, int32_t *chan, void *v_pruned,
+                               int64_t pruned_elems, uint32_t flags, void *ws, size_t ws_bytes,
+                               cudaStream_t stream) {
     NvtxRange nvtx_range("kvc_channel_prune_value");
     g_err[0] = 0;
     if (!shape_ok(shape, "kvc_channel_prune_value")) return KVC_ERR_INVALID_ARG;
@@ -556,6 +633,8 @@ int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const voi
     const int32_t keep = kvc_keep_channels(lambda, s.head_dim);
     if (keep < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: lambda keeps no channel");
     if (pruned_elems < 0) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value: bad pruned_elems");
+    if (flags & ~KVC_VALUE_REUSE_SCORE_STATS)
+        return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune_value_ex: unknown flags %#x", flags);
     const WsLayout w = ws_layout(s);
     if (!ws_ok(ws, ws_bytes, w.total, "kvc_channel_prune_value")) return KVC_ERR_WORKSPACE;
     const int choice = score_impl_choice();
@@ -568,7 +647,8 @@ int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const voi
     const bool tc = can_tc && choice != 1;
     const ScoreSplit sp = make_split(s, tc);
     char *base = static_cast<char *>(ws);
-    // 1. the window rows' softmax normalisers (the score pass's first half)
+    // 1. the window rows' softmax normalisers (the score pass's first half),
+    // or those the last kvc_score over the same shape, q_obs and k left here
     ScoreArgs a;
     a.q = q_obs;
     a.k = k;
@@ -577,8 +657,20 @@ int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const voi
     a.neg_bias = reinterpret_cast<float *>(base + w.bias_off);
     a.status = status_word(ws);
     a.stats_only = true;
-    int rc = tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
-    if (rc) return rc;
+    int rc = KVC_OK;
+    if (flags & KVC_VALUE_REUSE_SCORE_STATS) {
+        if (!stats_match(ws, s, q_obs, k, tc))
+            return fail(KVC_ERR_INVALID_ARG,
+                        "kvc_channel_prune_value_ex: no kvc_score over this shape, q_obs and k is "
+                        "recorded for this workspace");
+    } else {
+        rc = tc ? launch_score_tc(s, sp, a, stream) : launch_score_simt(s, sp, a, stream);
+        if (rc) {
+            stats_forget(ws);
+            return rc;
+        }
+        stats_record(ws, s, q_obs, k, tc);
+    }
     // 2. per-channel squared norms of the window rows' attention output
     float *sv = value_scores ? value_scores : reinterpret_cast<float *>(base + w.vscore_off);
     rc = launch_value_scores(s, sp, q_obs, k, v, a.neg_bias,

@@ -32,6 +32,7 @@ _lib = C.CDLL(LIB_PATH)
 KVC_OK = 0
 KVC_F32, KVC_BF16 = 0, 1
 DEV_TIMEOUT, DEV_BAD_SCORE, DEV_BAD_BUDGET, DEV_OUT_CAPACITY = 0x1, 0x2, 0x4, 0x8
+VALUE_REUSE_SCORE_STATS = 0x1   # kvc_channel_prune_value_ex flag
 DEV_INVARIANT = 0x10   # bounds-checking builds only
 
 
@@ -70,6 +71,8 @@ _SIGS = {
     "kvc_channel_prune_query": (C.c_int, [_sp, _p, _p, _p, _d, _p, _p, _i64, _p, _sz, _p]),
     "kvc_channel_prune_value": (C.c_int, [_sp, _p, _p, _p, _p, _p, _d, _p, _p, _p, _i64, _p, _sz,
                                           _p]),
+    "kvc_channel_prune_value_ex": (C.c_int, [_sp, _p, _p, _p, _p, _p, _d, _p, _p, _p, _i64,
+                                             C.c_uint32, _p, _sz, _p]),
     "kvc_keep_channels": (_i32, [_d, _i32]),
     "kvc_status_string": (C.c_char_p, [C.c_int]),
     "kvc_last_error": (C.c_char_p, []),
@@ -248,14 +251,29 @@ def kvc_channel_prune_query(s: KvcShape, q_obs, k_out, budget, lam: float, chan,
 
 
 def kvc_channel_prune_value(s: KvcShape, q_obs, k, v, v_out, budget, lam: float, chan, v_pruned,
-                            ws, value_scores=None, stream=None) -> None:
+                            ws, value_scores=None, stream=None, reuse_score_stats=False) -> None:
     """THINKV: rank value channels by the squared column norms of the window
     rows' attention output and keep the top floor((1-lam) D) of the kept
-    prefix rows of v_out (see kvc.h)."""
+    prefix rows of v_out (see kvc.h).  reuse_score_stats: take the window
+    rows' softmax normalisers the last kvc_score over the same shape, q_obs
+    and k left in ws (kvc_channel_prune_value_ex, KVC_VALUE_REUSE_SCORE_STATS)."""
+    if reuse_score_stats:
+        kvc_channel_prune_value_ex(s, q_obs, k, v, v_out, budget, lam, chan, v_pruned,
+                                   VALUE_REUSE_SCORE_STATS, ws, value_scores, stream)
+        return
     _check("kvc_channel_prune_value", _lib.kvc_channel_prune_value(
         C.byref(s), _ptr(q_obs), _ptr(k), _ptr(v), _ptr(v_out), _ptr(budget), float(lam),
         _ptr(value_scores), _ptr(chan), _ptr(v_pruned), v_pruned.numel(), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def kvc_channel_prune_value_ex(s: KvcShape, q_obs, k, v, v_out, budget, lam: float, chan,
+                               v_pruned, flags: int, ws, value_scores=None, stream=None) -> None:
+    """kvc_channel_prune_value with flags (VALUE_REUSE_SCORE_STATS; see kvc.h)."""
+    _check("kvc_channel_prune_value_ex", _lib.kvc_channel_prune_value_ex(
+        C.byref(s), _ptr(q_obs), _ptr(k), _ptr(v), _ptr(v_out), _ptr(budget), float(lam),
+        _ptr(value_scores), _ptr(chan), _ptr(v_pruned), v_pruned.numel(), int(flags), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def kvc_keep_channels(lam: float, head_dim: int) -> int:

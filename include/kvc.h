@@ -351,12 +351,33 @@ int kvc_channel_prune_query(const kvc_shape *shape, const void *q_obs, const voi
  * (NULL: kept in the workspace).  The call recomputes the window rows'
  * softmax normalisers itself (the first half of kvc_score's work) and then
  * forms o on the tensor cores for bf16 with head_dim 128 and G*W <= 512
- * (probabilities rounded to bf16, fp32 accumulation), on the CUDA cores in
- * fp32 otherwise; the workspace is kvc_workspace_size()'s. */
+ * (each probability as the sum of two bf16 terms, about 16 significant bits;
+ * fp32 accumulation), on the CUDA cores in fp32 otherwise; the workspace is
+ * kvc_workspace_size()'s.  Same as kvc_channel_prune_value_ex with flags 0. */
 int kvc_channel_prune_value(const kvc_shape *shape, const void *q_obs, const void *k,
                             const void *v, const void *v_out, const int32_t *budget, double lambda,
                             float *value_scores, int32_t *chan, void *v_pruned,
                             int64_t pruned_elems, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* kvc_channel_prune_value with flags.  KVC_VALUE_REUSE_SCORE_STATS: take the
+ * window rows' softmax normalisers from the workspace, where the most recent
+ * kvc_score on it over the same shape, q_obs and k (and the same kernel
+ * choice, on the same device) left them, instead of recomputing them -- one
+ * pass of the score's two fewer when THINKV follows the default path.  The
+ * library keeps a host-side record per workspace of the last such call (per
+ * process; replaced by the next kvc_score or kvc_channel_prune_value on the
+ * workspace, dropped by kvc_score_keyformer and kvc_workspace_init, whose
+ * statistics differ) and returns KVC_ERR_INVALID_ARG, launching nothing, when
+ * there is none that matches.  The caller guarantees that q_obs and k were not
+ * rewritten since and that the kvc_score work is ordered before this call on
+ * the device (the same stream, or an event).  Results are identical to the
+ * call without the flag.  Other flag bits: KVC_ERR_INVALID_ARG. */
+#define KVC_VALUE_REUSE_SCORE_STATS 0x1u
+int kvc_channel_prune_value_ex(const kvc_shape *shape, const void *q_obs, const void *k,
+                               const void *v, const void *v_out, const int32_t *budget,
+                               double lambda, float *value_scores, int32_t *chan, void *v_pruned,
+                               int64_t pruned_elems, uint32_t flags, void *ws, size_t ws_bytes,
+                               cudaStream_t stream);
 
 /* floor((1 - lambda) * head_dim) computed in double; 0 if lambda is outside
  * [0,1). */

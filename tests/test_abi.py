@@ -106,6 +106,10 @@ def test_value_channel_prune_rejects_bad_arguments(lib):
     assert call(ws_bytes=64) == -5
     assert call(ws=C.c_void_p(0x1010)) == -5                # workspace not 256-byte aligned
     assert "kvc_channel_prune_value" in kvc.kvc_last_error()
+    # the flags entry point: unknown flag bits are refused before anything else runs
+    assert L.kvc_channel_prune_value_ex(C.byref(s), fake, fake, fake, fake, fake, C.c_double(0.3),
+                                        nul, fake, fake, 1 << 20, 0x2, fake, 1 << 30, nul) == -1
+    assert "flags" in kvc.kvc_last_error()
 
 
 def test_keep_channels_and_workspace_size(lib):

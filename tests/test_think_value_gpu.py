@@ -293,3 +293,42 @@ def test_value_edge_cases(case):
                                          wl.think_lambda)
     assert np.array_equal(chan.cpu().numpy(), chan_g)
     assert np.array_equal(o.raw(vp[: vp_g.size]), vp_g)
+
+
+def test_value_reuses_the_score_statistics():
+    """kvc_channel_prune_value_ex with KVC_VALUE_REUSE_SCORE_STATS after the
+    default path's kvc_score gives bit-identical value scores, channels and
+    pruned bytes without its own statistics pass; with no matching kvc_score
+    recorded for the workspace (a fresh workspace, a Keyformer score, a reset)
+    it is refused."""
+    kvc = K()
+    wl, seed = CASES["bf16_d128_rows512"]
+    x = wk.make_inputs(wl, seed, device="cuda")
+    b = run_value(wl, x)   # compress (kvc_score on b.ws), then THINKV with its own statistics
+    kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)   # the record for b.ws
+    vs = torch.full_like(b.v_scores, float("nan"))
+    ch = torch.full_like(b.v_chan, -1)
+    vp = torch.zeros_like(b.v_pruned)
+    kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                wl.think_lambda, ch, vp, b.ws, value_scores=vs,
+                                reuse_score_stats=True)
+    torch.cuda.synchronize()
+    assert kvc.kvc_workspace_status(b.ws) == 0
+    assert torch.equal(vs, b.v_scores) and torch.equal(ch, b.v_chan)
+    assert torch.equal(vp, b.v_pruned)
+    # another shape's or another tensor's statistics are not taken
+    with pytest.raises(RuntimeError):
+        kvc.kvc_channel_prune_value(b.shape, x["q"].clone(), x["k"], x["v"], b.v_out, b.budget,
+                                    wl.think_lambda, ch, vp, b.ws, reuse_score_stats=True)
+    # a Keyformer score rewrites the statistics: refused until the next kvc_score
+    kvc.kvc_score_keyformer(b.shape, x["q"], x["k"], 7, 1.0, b.scores, b.ws)
+    with pytest.raises(RuntimeError):
+        kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                    wl.think_lambda, ch, vp, b.ws, reuse_score_stats=True)
+    # a fresh workspace has no statistics
+    ws2 = torch.empty_like(b.ws)
+    kvc.kvc_workspace_init(ws2)
+    with pytest.raises(RuntimeError):
+        kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                    wl.think_lambda, ch, vp, ws2, reuse_score_stats=True)
+
