@@ -199,11 +199,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# Lane operations of one Keyformer draw: Philox4x32-10 is 10 rounds of two
-# 32x32 -> 64-bit multiplies (high and low halves: 4 operations), 4 XORs and
-# 2 key additions (100); the 24-bit uniform, two logarithms and the scaling
+# Lane operations of one Keyformer draw: a Philox4x32-10 block is 10 rounds
+# of two 32x32 -> 64-bit multiplies (high and low halves: 4 operations), 4
+# XORs and 2 key additions (100), and serves four draws (four consecutive keys
+# of a row): 25 per draw; the 24-bit uniform, two logarithms and the scaling
 # add about 10.
-KEYFORMER_OPS_PER_DRAW = 110
+KEYFORMER_OPS_PER_DRAW = 35
 
 
 def keyformer_draws(wl):

@@ -472,11 +472,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // ---------------------------------------------------------------- Keyformer noise
-// (both score paths draw the same numbers for the same (unit, row, key))
-// Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2,
-// 3", SC 2011), word 0 of the output block for counter (c0, c1, c2, 0).
-__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2,
-                                                 uint32_t k0, uint32_t k1) {
+// (both score paths draw the same numbers for the same (unit, row, key)):
+// key j of row r takes word j mod 4 of the Philox4x32-10 block (Salmon et
+// al., "Parallel random numbers: as easy as 1, 2, 3", SC 2011) at counter
+// (j / 4, r, unit, 0), so one block serves four consecutive keys of a row.
+__device__ __forceinline__ void philox4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t k0,
+                                        uint32_t k1, uint32_t (&o)[4]) {
     uint32_t c3 = 0;
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
@@ -489,16 +490,24 @@ __device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint3
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
-    return c0;
+    o[0] = c0;
+    o[1] = c1;
+    o[2] = c2;
+    o[3] = c3;
 }
 
-// Gumbel draw for (unit, row, key): u = (b + 1/2) 2^-24 from the top 24 bits
+// Word s (0..3, a run-time value) of a block.
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&o)[4], uint32_t s) {
+    const uint32_t a = (s & 1) ? o[1] : o[0], b = (s & 1) ? o[3] : o[2];
+    return (s & 2) ? b : a;
+}
+
+// Gumbel draw from a 32-bit word: u = (b + 1/2) 2^-24 from its top 24 bits
 // b, zeta = -ln(-ln u).  -ln u is formed from whichever of u and 1 - u is
 // exact in fp32 (log1p near 1), so the rare draws close to 1 -- the large
 // zeta that dominate a row -- come out accurately.
-__device__ __forceinline__ float gumbel(uint32_t unit, uint32_t row, uint32_t key, uint32_t k0,
-                                        uint32_t k1) {
-    const uint32_t b = philox_word0(key, row, unit, k0, k1) >> 8;
+__device__ __forceinline__ float gumbel_bits(uint32_t w) {
+    const uint32_t b = w >> 8;
     float nlu;
     if (b >= (1u << 23)) {
         const float v = ((float)((1u << 24) - 1u - b) + 0.5f) * 0x1p-24f;   // 1 - u, exact
@@ -508,6 +517,15 @@ __device__ __forceinline__ float gumbel(uint32_t unit, uint32_t row, uint32_t ke
         nlu = -logf(u);
     }
     return -logf(nlu);
+}
+
+// One draw for (unit, row, key) (a whole block for one word: the CUDA-core
+// path; the tensor-core epilogues use every word of each block).
+__device__ __forceinline__ float gumbel(uint32_t unit, uint32_t row, uint32_t key, uint32_t k0,
+                                        uint32_t k1) {
+    uint32_t o[4];
+    philox4(key >> 2, row, unit, k0, k1, o);
+    return gumbel_bits(pick4(o, key & 3));
 }
 
 // ---------------------------------------------------------------- host side

@@ -508,6 +508,12 @@ __device__ __forceinline__ void col_sums64(const float (&v)[2][32], float cs, fl
     for (int i = 0; i < 8; ++i) a8[i] += t[i];
 }
 
+// v[base + s] for a run-time s in 0..3 (selects, no local memory).
+__device__ __forceinline__ float pick4f(const float (&v)[8], int base, int s) {
+    const float a = (s & 1) ? v[base + 1] : v[base], b = (s & 1) ? v[base + 3] : v[base + 2];
+    return (s & 2) ? b : a;
+}
+
 // Causal mask inside the window for pass 2: row r = g*W + w sees the key iff
 // w >= dj.  w advances with the column and wraps at W; it carries over
 // between consecutive chunks.
@@ -615,13 +621,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                     float v8[8];
                     load_cols8(taddr + ch * 8, v8);
                     if (ch == cols / 8 - 1) release_slot(r_tempty + slot * 8u, lane);
+                    // the chunk's 8 keys are two whole Philox blocks of row r
+                    uint32_t w[2][4];
+                    const uint32_t blk = (uint32_t)(j0 + ch * 8) >> 2;
+                    philox4(blk, (uint32_t)r, (uint32_t)u, p.key0, p.key1, w[0]);
+                    philox4(blk + 1u, (uint32_t)r, (uint32_t)u, p.key0, p.key1, w[1]);
                     float mx = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int col = ch * 8 + i;
-                        v8[i] = col <= lim ? fmaf(gumbel((uint32_t)u, (uint32_t)r, (uint32_t)(j0 + col),
-                                                         p.key0, p.key1),
-                                                  p.noise_scale, v8[i] * p.cs)
+                        v8[i] = col <= lim ? fmaf(gumbel_bits(w[i >> 2][i & 3]), p.noise_scale,
+                                                  v8[i] * p.cs)
                                            : -INFINITY;
                         mx = fmaxf(mx, v8[i]);
                     }
@@ -788,20 +798,37 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(max_regs(EWG))
                     const uint32_t taddr8 =
                         tmem + ((uint32_t)(quarter * 32) << 16) + slot * kSlotCols + c0;
                     const int nch = (cn + 7) / 8;
+                    // Draws: the four lanes of a key block (keys 4m..4m+3, m =
+                    // j / 4) each compute the Philox block of one of four rows,
+                    // then a 4 x 4 transpose by xor-shuffles hands every lane
+                    // its own key's word of each row: in round x lane b sends
+                    // word b ^ x and receives, from lane b ^ x, its key's word
+                    // of row b ^ x.
+                    const uint32_t bq = (uint32_t)lane & 3u;
 #pragma unroll 1
                     for (int ch = 0; ch < nch; ++ch) {
                         float v8[8];
                         load_cols8(taddr8 + ch * 8, v8);
                         if (ch == nch - 1) release_slot(r_tempty + slot * 8u, lane);
+                        const int row0 = nc * 256 + c0 + ch * 8;   // rows row0 .. row0 + 7
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int col = ch * 8 + i;
-                            const int row = nc * 256 + c0 + col;
-                            const bool vis = col < cn && (!masked || row % p.W >= dj);
-                            if (vis)
-                                a8[i] += ex2(fmaf(gumbel((uint32_t)u, (uint32_t)row, (uint32_t)j,
-                                                         p.key0, p.key1),
-                                                  p.noise_scale, v8[i] * p.cs));
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t w[4];
+                            philox4((uint32_t)j >> 2, (uint32_t)(row0 + 4 * c) + bq, (uint32_t)u,
+                                    p.key0, p.key1, w);
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const uint32_t send = pick4(w, bq ^ (uint32_t)x);
+                                const uint32_t got =
+                                    x == 0 ? send : __shfl_xor_sync(0xffffffffu, send, x);
+                                const int i = 4 * c + (int)(bq ^ (uint32_t)x);   // this draw's column
+                                const float vi = (i & 4) ? pick4f(v8, 4, i & 3) : pick4f(v8, 0, i & 3);
+                                const int row = row0 + i;
+                                const bool vis = ch * 8 + i < cn && (!masked || row % p.W >= dj);
+                                if (vis)
+                                    a8[4 * c + x] += ex2(fmaf(gumbel_bits(got), p.noise_scale,
+                                                              vi * p.cs));
+                            }
                         }
                     }
                     continue;

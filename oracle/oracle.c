@@ -937,16 +937,17 @@ void ora_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint3
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The uniform draw for (unit u, row r, key j): word 0 of Philox4x32-10 at
- * counter (j, r, u, 0) with key (seed low, seed high); its top 24 bits b give
+/* The uniform draw for (unit u, row r, key j): word j mod 4 of Philox4x32-10
+ * at counter (floor(j / 4), r, u, 0) with key (seed low, seed high) -- one
+ * output block serves four consecutive keys of a row; its top 24 bits b give
  * u = (b + 1/2) * 2^-24, exactly representable and strictly inside (0,1). */
 double ora_keyformer_uniform(uint64_t seed, int64_t unit, int64_t row, int64_t key)
 {
-    const uint32_t ctr[4] = {(uint32_t)key, (uint32_t)row, (uint32_t)unit, 0u};
+    const uint32_t ctr[4] = {(uint32_t)(key >> 2), (uint32_t)row, (uint32_t)unit, 0u};
     const uint32_t k[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t o[4];
     ora_philox4x32_10(ctr, k, o);
-    return ((double)(o[0] >> 8) + 0.5) * (1.0 / 16777216.0);
+    return ((double)(o[key & 3] >> 8) + 0.5) * (1.0 / 16777216.0);
 }
 
 int ora_score_keyformer(const ora_shape *s, const void *q, const void *k, uint64_t seed,

@@ -676,6 +676,23 @@ def test_keyformer_uniforms_and_gumbel_moments():
     assert O.keyformer_uniform(7, 1, 2, 3) != O.keyformer_uniform(8, 1, 2, 3)
 
 
+def test_keyformer_uniforms_of_a_block_are_its_four_words():
+    """Four consecutive keys of a row share one Philox4x32-10 block, one word
+    each (the published generator is pinned by its known answers above): the
+    draws for keys 4m..4m+3 are the block's four words in order, the four
+    differ, and neighbouring keys are uncorrelated."""
+    seed, unit, row = 0x1234567890ABCDEF, 5, 17
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    for m in (0, 1, 1000):
+        words = O.philox4x32_10((m, row, unit, 0), key)
+        u = [O.keyformer_uniform(seed, unit, row, 4 * m + i) for i in range(4)]
+        assert u == [((w >> 8) + 0.5) / 2 ** 24 for w in words]
+        assert len(set(u)) == 4
+    x = np.array([O.keyformer_uniform(seed, unit, row, j) for j in range(4000)])
+    assert abs(np.corrcoef(x[:-1], x[1:])[0, 1]) < 0.05
+    assert abs(np.corrcoef(x[0::4], x[1::4])[0, 1]) < 0.08
+
+
 @pytest.mark.parametrize("tau", [0.5, 1.0, 3.0])
 def test_keyformer_single_row_is_noisy_softmax(tau):
     """W = 1, G = 1: the score is one softmax of (q.k/sqrt(D) + zeta)/tau over
