@@ -60,6 +60,17 @@ CASES = {
     "bf16_odd_dim": (wk.ZIGZAG_32K.scaled(
         n_layers=2, n_kv_heads=2, n_q_heads=4, head_dim=80, seq_len=333, window=8,
         total_budget=2 * 60, layer_floor=10, temperature=None), 103),
+    # tensor-core path, 400 window rows (W = 100, not a multiple of 4): the
+    # second 256-row job is partly padding and the causal edge crosses the
+    # four-row groups whose noise blocks pass 2 shares across lanes; ragged
+    # last tile
+    "bf16_rows400_w100": (wk.ZIGZAG_32K.scaled(
+        n_layers=1, n_kv_heads=2, n_q_heads=8, seq_len=3001, window=100,
+        total_budget=2 * 500, layer_floor=40, temperature=None), 105),
+    # 384 rows, D = 64: the odd CTA's rows of the second job are all padding
+    "bf16_d64_rows384": (wk.ZIGZAG_32K.scaled(
+        n_layers=1, n_kv_heads=2, n_q_heads=16, head_dim=64, seq_len=1000, window=48,
+        total_budget=2 * 200, layer_floor=20, temperature=None), 106),
 }
 
 
