@@ -82,14 +82,21 @@ __global__ void __launch_bounds__(kSimtThreads)
                 if (NOISE) {
                     // base-2 noisy logits (x / sqrt(D) + zeta) / tau, logits
                     // beyond the causal limit stay out of the max and sum
+                    // the sub-tile's keys are whole noise blocks of row r (four
+                    // keys each)
+                    static_assert(kSub % 4 == 0, "whole Philox blocks per sub-tile");
 #pragma unroll
-                    for (int i = 0; i < kSub; ++i)
-                        if (i <= lim && j0 + i < p.T)
-                            s[i] = fmaf(gumbel((uint32_t)u, (uint32_t)r, (uint32_t)(j0 + i),
-                                               p.key0, p.key1),
-                                        p.noise_scale, s[i] * p.cs);
-                        else
-                            s[i] = -INFINITY;
+                    for (int i4 = 0; i4 < kSub; i4 += 4) {
+                        uint32_t wb[4];
+                        philox4((uint32_t)(j0 + i4) >> 2, (uint32_t)r, (uint32_t)u, p.key0,
+                                p.key1, wb);
+#pragma unroll
+                        for (int i = i4; i < i4 + 4; ++i)
+                            if (i <= lim && j0 + i < p.T)
+                                s[i] = fmaf(gumbel_bits(wb[i & 3]), p.noise_scale, s[i] * p.cs);
+                            else
+                                s[i] = -INFINITY;
+                    }
                     float mxn = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < kSub; ++i) mxn = fmaxf(mxn, s[i]);
