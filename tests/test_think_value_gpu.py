@@ -331,4 +331,32 @@ def test_value_reuses_the_score_statistics():
     with pytest.raises(RuntimeError):
         kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
                                     wl.think_lambda, ch, vp, ws2, reuse_score_stats=True)
+    # the CUDA-core path reuses its own statistics, and statistics of the
+    # other path (another row split) are refused
+    old = os.environ.get("KVC_SCORE_IMPL")
+    try:
+        os.environ["KVC_SCORE_IMPL"] = "simt"
+        with pytest.raises(RuntimeError):   # the record is the tensor-core score's... none now
+            kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                        wl.think_lambda, ch, vp, b.ws, reuse_score_stats=True)
+        kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
+        ref_s = torch.empty_like(vs)
+        kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                    wl.think_lambda, ch, vp, b.ws, value_scores=ref_s)
+        kvc.kvc_score(b.shape, x["q"], x["k"], b.scores, b.ws)
+        vs2 = torch.full_like(vs, float("nan"))
+        kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                    wl.think_lambda, ch, vp, b.ws, value_scores=vs2,
+                                    reuse_score_stats=True)
+        torch.cuda.synchronize()
+        assert torch.equal(vs2, ref_s)
+        os.environ["KVC_SCORE_IMPL"] = "tc"
+        with pytest.raises(RuntimeError):   # recorded for the CUDA-core split
+            kvc.kvc_channel_prune_value(b.shape, x["q"], x["k"], x["v"], b.v_out, b.budget,
+                                        wl.think_lambda, ch, vp, b.ws, reuse_score_stats=True)
+    finally:
+        if old is None:
+            os.environ.pop("KVC_SCORE_IMPL", None)
+        else:
+            os.environ["KVC_SCORE_IMPL"] = old
 
