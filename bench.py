@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capped) tensor peak, a shorter one with the burst peak
 SUSTAINED_REGION_S = 2.0
 # kernels each C-ABI call launches
-LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 2, "kvc_topk_select": 1, "kvc_compact": 1,
+LAUNCHES = {"kvc_score": 3, "kvc_mba_budget": 1, "kvc_topk_select": 1, "kvc_compact": 1,
             "kvc_channel_prune": 1, "kvc_pool_scores": 1, "kvc_head_budget": 1,
             "kvc_threshold_select": 1,
             # value kernel, merge, channel copy (+ stats pass and merge unless

@@ -81,6 +81,8 @@ bool ws_ok(void *ws, size_t ws_bytes, size_t need, const char *fn) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 uint32_t *status_word(void *ws) { return static_cast<uint32_t *>(ws); }
+// Completion counter of the MBA launch (zero between launches).
+uint32_t *mba_done_word(void *ws) { return static_cast<uint32_t *>(ws) + 1; }
 
 
 // Event sets of kvc_compress_host, one per (device, staging buffer); created
@@ -486,9 +488,8 @@ int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_nu
     if (total_budget < (int64_t)s.n_layers * layer_floor)
         return fail(KVC_ERR_INVALID_ARG, "kvc_mba_budget: total_budget below n_layers * layer_floor");
     if (!ws_ok(ws, ws_bytes, kWsHeader, "kvc_mba_budget")) return KVC_ERR_WORKSPACE;
-    int rc = launch_mba(s, scores, mass_num, mass_den, mba, status_word(ws), stream);
-    if (rc) return rc;
-    return launch_budget(s, mba, total_budget, layer_floor, budget, status_word(ws), stream);
+    return launch_mba_budget(s, scores, mass_num, mass_den, total_budget, layer_floor, mba, budget,
+                             mba_done_word(ws), status_word(ws), stream);
 }
 
 int kvc_topk_select(const kvc_shape *shape, const float *scores, const int32_t *budget, int32_t k_max,

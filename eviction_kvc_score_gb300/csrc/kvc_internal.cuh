@@ -17,7 +17,7 @@ namespace kvc {
 constexpr int kTileKeys = 128;          // keys per score tile of the CUDA-core path
 constexpr int kPairKeys = 256;          // keys per SM-pair tile of the tensor-core path
 constexpr int kMaxRowsTC = 512;         // G*W handled by the tensor-core path
-constexpr size_t kWsHeader = 256;       // status word + padding
+constexpr size_t kWsHeader = 256;       // status word, MBA completion counter, padding
 constexpr double kLog2e = 1.4426950408889634;
 
 // Every pipeline wait gives up after this many nanoseconds of %globaltimer,
@@ -556,10 +556,11 @@ int launch_score_merge(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs
                        cudaStream_t st);
 int launch_score_keyformer(const kvc_shape &s, const ScoreSplit &sp, const ScoreArgs &a,
                            uint64_t seed, double tau, cudaStream_t st);
-int launch_mba(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den, int32_t *mba,
-               uint32_t *status, cudaStream_t st);
-int launch_budget(const kvc_shape &s, const int32_t *mba, int64_t total, int32_t floor_,
-                  int32_t *budget, uint32_t *status, cudaStream_t st);
+// MBA of every head and the layer budgets in one launch; done is a workspace
+// word that is zero between launches.
+int launch_mba_budget(const kvc_shape &s, const float *scores, uint32_t num, uint32_t den,
+                      int64_t total, int32_t floor_, int32_t *mba, int32_t *budget, uint32_t *done,
+                      uint32_t *status, cudaStream_t st);
 // per_head == 0: budget[L] per layer; 1: budget[L][H_kv] per head.
 int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, int per_head,
                 int32_t k_max, int32_t *idx, uint32_t *status, cudaStream_t st);
