@@ -89,6 +89,12 @@ __device__ __forceinline__ V block_sum(V v, V *warp_tot, V *total) {
     return *total;
 }
 
+// Order key of a score: its bit pattern without the sign bit.  Non-negative
+// floats order like their bit patterns, and -0.0 becomes +0.0 (the two
+// compare equal); a negative score, already reported as invalid, takes its
+// magnitude's key in every pass alike, and no key's bucket leaves [0, 4096).
+__device__ __forceinline__ uint32_t skey(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
 // floor(c * 2^56) for 0 <= c <= 1, from the bits: a normal c is
 // m 2^(e - 150) with m its 24-bit significand, so the floor is m shifted by
 // e - 94 (left, or right with the dropped bits truncated); a subnormal c is
@@ -367,7 +373,7 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
         const bool valid = in && v >= 0.f && v <= 1.f;
         if (in && !valid) bad = 1;
         if (!valid) return;
-        const uint32_t key = __float_as_uint(v);
+        const uint32_t key = skey(v);
         W.add((int)(key >> 19), unit_mass(key));
     };
     if (cached && (reinterpret_cast<uintptr_t>(c) & 15) == 0)
@@ -436,7 +442,7 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
     WarpList wl{list + (tid >> 5) * seg, seg, 0};
     uint32_t cg = 0;
     for_scores4(src, T, vec, [&](int, float v, bool in) {
-        const uint32_t key = __float_as_uint(v);
+        const uint32_t key = skey(v);
         const int d = in ? (int)(key >> 19) : -1;
         cg += d > d1;
         wl.append(d == d1, key);
@@ -464,7 +470,7 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
             for (int i = lane; i < wl.n; i += 32) add(wl.slot[i]);
         } else {
             for_scores4(src, T, vec, [&](int, float v, bool in) {
-                if (in) add(__float_as_uint(v));
+                if (in) add(skey(v));
             });
         }
         __syncthreads();
@@ -614,10 +620,13 @@ __device__ __forceinline__ unsigned long long warp_add(unsigned long long v) {
     return v;
 }
 
-// lr_split for L <= 32 by one warp (lane l is layer l): register shuffles only.
-__device__ long long lr_split_warp(int L, long long S, bool e, long long R) {
-    const int l = threadIdx.x & 31;
-    e = e && l < L;
+// lr_split for L <= 32 by the whole 1024-thread block: lane l of every warp
+// holds layer l and every warp computes the sums alike; warp w ranks layer w's
+// remainder with one ballot, and the ranks meet in shared memory (rk: 32
+// words).  The same arithmetic as lr_split.
+__device__ long long lr_split_small(int L, long long S, bool e, long long R, long long *rk) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    e = e && lane < L;
     unsigned long long sumw = warp_add(e ? (unsigned long long)S : 0ull);
     const unsigned long long n_el = warp_add(e ? 1ull : 0ull);
     if (n_el == 0 || R <= 0) return 0;
@@ -625,47 +634,55 @@ __device__ long long lr_split_warp(int L, long long S, bool e, long long R) {
     if (equal) sumw = n_el;
     unsigned long long q = 0, r = 0;
     if (e) muldiv((unsigned long long)R, equal ? 1ull : (unsigned long long)S, sumw, q, r);
-    long long add = (long long)q;
     const long long left = R - (long long)warp_add(q);
-    long long rank = 0;
-#pragma unroll 4
-    for (int o = 0; o < 32; ++o) {
-        const unsigned long long ro = __shfl_sync(0xffffffffu, r, o);
-        const bool eo = __shfl_sync(0xffffffffu, e, o);
-        rank += eo && (ro > r || (ro == r && o < l));
-    }
+    // layers ranked before layer `warp`: larger remainder, or equal and lower index
+    const unsigned long long rw = __shfl_sync(0xffffffffu, r, warp);
+    const unsigned before = __ballot_sync(0xffffffffu, e && (r > rw || (r == rw && lane < warp)));
+    if (lane == 0) rk[warp] = __popc(before);
+    __syncthreads();
+    const long long rank = rk[lane];
+    __syncthreads();   // rk is rewritten by the next call
+    long long add = (long long)q;
     if (e && left > 0 && rank < left) add += 1;
     return add;
 }
 
-// layer_budgets for L <= 32 by one warp, the same arithmetic.
-__device__ void layer_budgets_warp(const int32_t *mba, int L, int Hkv, long long P, long long total,
-                                   long long floor_, int32_t *__restrict__ budget,
-                                   uint32_t *status) {
-    const int l = threadIdx.x & 31;
-    const bool act = l < L;
+// layer_budgets for L <= 32 by the whole 1024-thread block (lane l of every
+// warp is layer l), the same arithmetic.  sh: 64 words of shared memory.
+__device__ void layer_budgets_small(const int32_t *mba, int L, int Hkv, long long P,
+                                    long long total, long long floor_,
+                                    int32_t *__restrict__ budget, uint32_t *status, long long *sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool act = lane < L;
     if (total >= (long long)L * P) {
-        if (act) budget[l] = (int32_t)P;
+        if (threadIdx.x < L) budget[threadIdx.x] = (int32_t)P;
         return;
     }
-    long long S = 0;
-    if (act)
-        for (int k = 0; k < Hkv; ++k) S += __ldcg(mba + (int64_t)l * Hkv + k);
+    // S_l: warp l sums layer l's heads over its lanes
+    if (warp < L) {
+        unsigned long long acc = 0;
+        for (int k = lane; k < Hkv; k += 32)
+            acc += (unsigned long long)__ldcg(mba + (int64_t)warp * Hkv + k);
+        acc = warp_add(acc);
+        if (lane == 0) sh[32 + warp] = (long long)acc;
+    }
+    __syncthreads();
+    const long long S = act ? sh[32 + lane] : 0;
     bool elig = act;
-    long long B = floor_ + lr_split_warp(L, S, elig, total - (long long)L * floor_);
+    long long B = floor_ + lr_split_small(L, S, elig, total - (long long)L * floor_, sh);
     while (true) {
         const long long over = act && B > P ? B - P : 0;
         if (over) B = P;
         const unsigned long long excess = warp_add((unsigned long long)over);
         if (excess == 0) break;
         elig = act && B < P;
-        B += lr_split_warp(L, S, elig, (long long)excess);
+        B += lr_split_small(L, S, elig, (long long)excess, sh);
     }
-    if (act) budget[l] = (int32_t)B;
-    if (kDebugBounds) {   // sum = total, floor <= B <= P
+    if (threadIdx.x < L) budget[threadIdx.x] = (int32_t)B;
+    if (kDebugBounds && warp == 0) {   // sum = total, floor <= B <= P
         const unsigned long long sum = warp_add(act ? (unsigned long long)B : 0ull);
         if (act && (B < floor_ || B > P)) set_status(status, KVC_DEV_INVARIANT);
-        if (l == 0 && (long long)sum != total) set_status(status, KVC_DEV_INVARIANT);
+        if (lane == 0 && (long long)sum != total) set_status(status, KVC_DEV_INVARIANT);
     }
 }
 
@@ -693,7 +710,8 @@ __global__ void __launch_bounds__(kSelThreads)
     if (!s_last) return;
     __threadfence();
     if (L <= 32) {
-        if (threadIdx.x < 32) layer_budgets_warp(mba, L, Hkv, P, total, floor_, budget, status);
+        layer_budgets_small(mba, L, Hkv, P, total, floor_, budget, status,
+                            reinterpret_cast<long long *>(sel_smem));
         if (threadIdx.x == 0) *done = 0u;
         return;
     }
@@ -830,7 +848,7 @@ __global__ void __launch_bounds__(kSelThreads)
     const auto body = [&](int, float v, bool in) {
         if (!in) return;
         if (!(v >= 0.f)) bad = 1;
-        atomicAdd(&cnt[(__float_as_uint(v) >> 19) & (kB0 - 1)], 1u);
+        atomicAdd(&cnt[(skey(v) >> 19) & (kB0 - 1)], 1u);
     };
     if (cached && (reinterpret_cast<uintptr_t>(c) & 15) == 0)
         for_scores4_async(c, cache, P, body);
@@ -886,10 +904,10 @@ __global__ void __launch_bounds__(kSelThreads)
                 for (int i = 0; i < 8; ++i) {
                     const int q = (i + tid) & 7;   // rotated: distinct banks for 8 neighbours
                     const float4 v = s4[q];
-                    const uint32_t e0 = __float_as_uint(v.x) >> 19,
-                                   e1 = __float_as_uint(v.y) >> 19,
-                                   e2 = __float_as_uint(v.z) >> 19,
-                                   e3 = __float_as_uint(v.w) >> 19;
+                    const uint32_t e0 = skey(v.x) >> 19,
+                                   e1 = skey(v.y) >> 19,
+                                   e2 = skey(v.z) >> 19,
+                                   e3 = skey(v.w) >> 19;
                     ab |= ((uint32_t)(e0 > d1) | ((uint32_t)(e1 > d1) << 1) |
                            ((uint32_t)(e2 > d1) << 2) | ((uint32_t)(e3 > d1) << 3)) << (4 * q);
                     in |= ((uint32_t)(e0 == d1) | ((uint32_t)(e1 == d1) << 1) |
@@ -898,7 +916,7 @@ __global__ void __launch_bounds__(kSelThreads)
             } else {
                 for (int i = 0; i < 32; ++i) {
                     if (j0 + i < P) {
-                        const uint32_t e = __float_as_uint(cache[j0 + i]) >> 19;
+                        const uint32_t e = skey(cache[j0 + i]) >> 19;
                         ab |= (uint32_t)(e > d1) << i;
                         in |= (uint32_t)(e == d1) << i;
                     }
@@ -917,13 +935,13 @@ __global__ void __launch_bounds__(kSelThreads)
                 }
                 int slot = wl.n + incl - n_in;
                 for (uint32_t m = in; m; m &= m - 1u, ++slot)
-                    if (slot < seg) wl.slot[slot] = __float_as_uint(cache[j0 + __ffs(m) - 1]);
+                    if (slot < seg) wl.slot[slot] = skey(cache[j0 + __ffs(m) - 1]);
                 wl.n += __shfl_sync(0xffffffffu, incl, 31);
             }
         }
     } else {
         for_scores4(src, P, vec, [&](int, float v, bool in) {
-            const uint32_t key = __float_as_uint(v);
+            const uint32_t key = skey(v);
             wl.append(in && (key >> 19) == d1, key);
         });
     }
@@ -940,7 +958,7 @@ __global__ void __launch_bounds__(kSelThreads)
             for (int i = lane; i < wl.n; i += 32) add(wl.slot[i]);
         } else {   // a list overflowed: every score again
             for_scores4(src, P, vec, [&](int, float v, bool in) {
-                if (in) add(__float_as_uint(v));
+                if (in) add(skey(v));
             });
         }
         __syncthreads();
@@ -974,7 +992,7 @@ __global__ void __launch_bounds__(kSelThreads)
             gt = base == 0 ? above[0] : above[1];
             for (uint32_t m = base == 0 ? inside[0] : inside[1]; m; m &= m - 1u) {
                 const int i = __ffs(m) - 1;
-                const uint32_t key = __float_as_uint(cache[j0 + i]);
+                const uint32_t key = skey(cache[j0 + i]);
                 gt |= (uint32_t)(key > vstar) << i;
                 eq |= (uint32_t)(key == vstar) << i;
             }
@@ -1003,8 +1021,8 @@ __global__ void __launch_bounds__(kSelThreads)
                 for (int i = 0; i < 8; ++i) {
                     const int q = (i + tid) & 7;
                     const float4 r = s4[q];
-                    const uint32_t k0 = __float_as_uint(r.x), k1 = __float_as_uint(r.y),
-                                   k2 = __float_as_uint(r.z), k3 = __float_as_uint(r.w);
+                    const uint32_t k0 = skey(r.x), k1 = skey(r.y),
+                                   k2 = skey(r.z), k3 = skey(r.w);
                     gt |= ((uint32_t)(k0 > vstar) | ((uint32_t)(k1 > vstar) << 1) |
                            ((uint32_t)(k2 > vstar) << 2) | ((uint32_t)(k3 > vstar) << 3))
                           << (4 * q);
@@ -1016,7 +1034,7 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll 8
                 for (int i = 0; i < 32; ++i) {
                     if (r0 + i < n) {
-                        const uint32_t key = __float_as_uint(rs[r0 + i]);
+                        const uint32_t key = skey(rs[r0 + i]);
                         gt |= (uint32_t)(key > vstar) << i;
                         eq |= (uint32_t)(key == vstar) << i;
                     }

@@ -176,3 +176,45 @@ def test_mba_crossing_on_a_bucket_boundary():
     for l in range(L):
         B = int(want_bud[l])
         assert np.array_equal(got[l, 0, :B], o.topk(c[l, 0], P, B)), l
+
+
+@pytest.mark.parametrize("T", [3000, 40000])
+def test_negative_zero_scores_count_as_zero(T):
+    """-0.0 and +0.0 are the same score: MBA with the whole mass counts the
+    positive scores, and a budget reaching into the zeros keeps the
+    lowest-index zeros whatever their sign."""
+    kvc, o = K(), O()
+    L, H, W = 2, 1, 8
+    P = T - W
+    g = np.random.default_rng(T + 5)
+    x = np.zeros((L, H, T), dtype=np.float32)
+    npos = 500
+    for l in range(L):
+        pos = g.choice(P, size=npos, replace=False)
+        v = np.exp(g.normal(0.0, 1.0, size=npos))
+        x[l, 0, pos] = (v / v.sum()).astype(np.float32)
+    neg = (x == 0) & (g.random(x.shape) < 0.5)
+    x[neg] = np.float32(-0.0)
+    assert np.signbit(x).sum() > 0
+    s = kvc.shape(L, H, H, 64, T, W, "f32")
+    ws = torch.empty(kvc.kvc_workspace_size(s, P), dtype=torch.uint8, device="cuda")
+    kvc.kvc_workspace_init(ws)
+    scd = torch.from_numpy(x).cuda()
+    c = x.astype(np.float64)
+    for num, den in ((1, 1), (9, 10)):
+        mba = torch.empty((L, H), dtype=torch.int32, device="cuda")
+        bud = torch.empty(L, dtype=torch.int32, device="cuda")
+        kvc.kvc_mba_budget(s, scd, num, den, L * 100, 10, mba, bud, ws)
+        torch.cuda.synchronize()
+        want = [o.mba(c[l, 0], num, den) for l in range(L)]
+        assert mba[:, 0].tolist() == want, (num, den)
+    assert want[0] <= npos
+    budgets = [npos + 300, npos - 1]
+    idx = torch.full((L, H, P), -1, dtype=torch.int32, device="cuda")
+    kvc.kvc_topk_select(s, scd, torch.tensor(budgets, dtype=torch.int32, device="cuda"), P, idx,
+                        ws)
+    torch.cuda.synchronize()
+    assert kvc.kvc_workspace_status(ws) == 0
+    got = idx.cpu().numpy()
+    for l, B in enumerate(budgets):
+        assert np.array_equal(got[l, 0, :B], o.topk(c[l, 0], P, B)), (T, B)
