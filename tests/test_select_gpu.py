@@ -218,3 +218,60 @@ def test_negative_zero_scores_count_as_zero(T):
     got = idx.cpu().numpy()
     for l, B in enumerate(budgets):
         assert np.array_equal(got[l, 0, :B], o.topk(c[l, 0], P, B)), (T, B)
+
+
+@pytest.mark.parametrize("L,H,T", [(32, 2, 600), (33, 2, 600), (40, 3, 700), (1024, 1, 300)])
+def test_budgets_across_layer_counts(L, H, T):
+    """The layer budgets are computed by the last MBA block: one lane per
+    layer for up to 32 layers, block-wide sums beyond (up to the 1024-layer
+    limit).  Budgets tight enough that the cap at P and the largest-remainder
+    leftovers both occur; MBA, budgets and top-K against the oracle."""
+    kvc, o = K(), O()
+    W = 8
+    P = T - W
+    sc = _rows("lognormal", L, H, T, seed=L * 7 + H)
+    s = kvc.shape(L, H, H, 64, T, W, "f32")
+    floor = 5
+    for total in (L * floor + 7, (L * P * 3) // 4 + 1):
+        ws = torch.empty(kvc.kvc_workspace_size(s, P), dtype=torch.uint8, device="cuda")
+        kvc.kvc_workspace_init(ws)
+        scd = sc.cuda()
+        mba = torch.empty((L, H), dtype=torch.int32, device="cuda")
+        bud = torch.empty(L, dtype=torch.int32, device="cuda")
+        kvc.kvc_mba_budget(s, scd, 9, 10, total, floor, mba, bud, ws)
+        idx = torch.full((L, H, P), -1, dtype=torch.int32, device="cuda")
+        kvc.kvc_topk_select(s, scd, bud, P, idx, ws)
+        torch.cuda.synchronize()
+        assert kvc.kvc_workspace_status(ws) == 0
+        c = sc.double().numpy()
+        want_mba = np.array([[o.mba(c[l, h], 9, 10) for h in range(H)] for l in range(L)])
+        assert np.array_equal(mba.cpu().numpy(), want_mba), (L, total)
+        want_bud = o.budget(want_mba, P, total, floor)
+        got_bud = bud.cpu().numpy()
+        assert np.array_equal(got_bud, want_bud), (L, total)
+        assert int(got_bud.sum()) == total
+        got = idx.cpu().numpy()
+        for l in range(0, L, max(1, L // 16)):
+            B = int(want_bud[l])
+            for h in range(H):
+                assert np.array_equal(got[l, h, :B], o.topk(c[l, h], P, B)), (L, total, l, h)
+
+
+@pytest.mark.parametrize("Hkv", [8, 40])
+def test_head_budgets_beyond_one_warp(Hkv):
+    """kvc_head_budget runs one thread per KV head: 40 heads take two warps of
+    block-wide sums."""
+    kvc, o = K(), O()
+    L, T, W = 3, 800, 16
+    P = T - W
+    g = np.random.default_rng(Hkv)
+    mba = torch.from_numpy(g.integers(0, P, size=(L, Hkv)).astype(np.int32)).cuda()
+    bud = torch.from_numpy(np.array([P // 3, P - 1, 7], dtype=np.int32)).cuda()
+    s = kvc.shape(L, Hkv, Hkv, 64, T, W, "f32")
+    ws = torch.empty(kvc.kvc_workspace_size(s, P), dtype=torch.uint8, device="cuda")
+    kvc.kvc_workspace_init(ws)
+    hb = torch.empty((L, Hkv), dtype=torch.int32, device="cuda")
+    kvc.kvc_head_budget(s, mba, bud, hb, ws)
+    torch.cuda.synchronize()
+    want = o.head_budget(mba.cpu().numpy(), bud.cpu().numpy(), P)
+    assert np.array_equal(hb.cpu().numpy(), want)
