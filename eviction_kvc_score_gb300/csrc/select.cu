@@ -21,13 +21,14 @@
 // keeps everything above it and the lowest-index ties, writing positions in
 // ascending order.
 //
-// One 1024-thread block per head.  The first pass copies the head's scores
-// into shared memory (cp.async, when they fit: T <= 36,864) for the later
+// One block per head: 1024 threads, or for MBA 512 threads two per SM when
+// the heads exceed one wave of 1024-thread blocks.  The first pass copies the
+// head's scores into shared memory (cp.async, when they fit) for the later
 // passes; a second pass gathers the crossing bucket's keys into per-warp
 // shared lists, so that the two remaining digits never reread the row (for
 // top-K on a held row that pass is also the compaction's classification).
 // The last MBA block to finish computes the layer budgets.  Bucket searches
-// are block-wide scans with one to four buckets per thread; only native
+// are block-wide scans with one to eight buckets per thread; only native
 // 32-bit shared atomics are used on the usual path (64-bit shared atomics are
 // emulated and several times slower).
 #include "kvc_internal.cuh"
@@ -65,14 +66,15 @@ __device__ __forceinline__ V block_scan_excl(V v, V *warp_tot, V *total) {
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const V w = warp_tot[lane];
+        const int nw = (int)(blockDim.x >> 5);
+        const V w = lane < nw ? warp_tot[lane] : V{};
         V wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const V a = shfl_up(wi, o);
             if (lane >= o) wi += a;
         }
-        warp_tot[lane] = wi - w;
+        if (lane < nw) warp_tot[lane] = wi - w;
         if (lane == 31) *total = wi;
     }
     __syncthreads();
@@ -114,27 +116,27 @@ __device__ __forceinline__ unsigned long long fixed56f(float c) {
 // sixteen loads issued before any is used (latency hidden when the scores come
 // from global memory).  f(k, v, in) is called for every lane, with in false
 // past the end, so warp-wide votes inside f stay uniform.
-template <typename F>
+template <int NT = kSelThreads, typename F>
 __device__ __forceinline__ void for_scores(const float *__restrict__ src, int n, F f) {
     constexpr int kBatch = 16;
     const int tid = threadIdx.x;
-    for (int base = 0; base < n; base += kBatch * kSelThreads) {
+    for (int base = 0; base < n; base += kBatch * NT) {
         float r[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             r[i] = k < n ? src[k] : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             f(k, r[i], k < n);
         }
     }
 }
 
 // ------------------------------------------------------------------ MBA
-// Per head (one 1024-thread block):
+// Per head (one block of NT threads):
 //  1. one pass over the scores (copying them into shared memory when they
 //     fit, for the later passes) builds a 4096-bucket histogram of the top 12
 //     key bits holding each bucket's EXACT mass: every score of a bucket has
@@ -201,25 +203,25 @@ struct WSum {
 // aligned: thread tid reads vectors tid, tid + 1024, ... (coalesced), four in
 // flight.  f(k, v, in) is called for every lane, with in false past the end,
 // so warp-wide votes inside f stay uniform.
-template <typename F>
+template <int NT = kSelThreads, typename F>
 __device__ __forceinline__ void for_scores4(const float *__restrict__ src, int n, bool vec, F f) {
     if (!vec) {
-        for_scores(src, n, f);
+        for_scores<NT>(src, n, f);
         return;
     }
     const int tid = threadIdx.x;
     const int n4 = n >> 2;
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
-    for (int base = 0; base < n4; base += 4 * kSelThreads) {
+    for (int base = 0; base < n4; base += 4 * NT) {
         float4 r[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             r[i] = k < n4 ? s4[k] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             const bool in = k < n4;
             f(4 * k, r[i].x, in);
             f(4 * k + 1, r[i].y, in);
@@ -233,12 +235,12 @@ __device__ __forceinline__ void for_scores4(const float *__restrict__ src, int n
 
 // for_scores4 over global g that also copies every score into cache[0..n):
 // the staging copy rides on the first histogram pass.
-template <typename F>
+template <int NT = kSelThreads, typename F>
 __device__ __forceinline__ void for_scores4_stage(const float *__restrict__ g, float *cache, int n,
                                                   F f) {
     const int tid = threadIdx.x;
     if ((reinterpret_cast<uintptr_t>(g) & 15) != 0) {
-        for_scores(g, n, [&](int k, float v, bool in) {
+        for_scores<NT>(g, n, [&](int k, float v, bool in) {
             if (in) cache[k] = v;
             f(k, v, in);
         });
@@ -247,16 +249,16 @@ __device__ __forceinline__ void for_scores4_stage(const float *__restrict__ g, f
     const int n4 = n >> 2;
     const float4 *g4 = reinterpret_cast<const float4 *>(g);
     float4 *c4 = reinterpret_cast<float4 *>(cache);
-    for (int base = 0; base < n4; base += 4 * kSelThreads) {
+    for (int base = 0; base < n4; base += 4 * NT) {
         float4 r[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             r[i] = k < n4 ? g4[k] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             const bool in = k < n4;
             if (in) c4[k] = r[i];
             f(4 * k, r[i].x, in);
@@ -290,17 +292,17 @@ __device__ __forceinline__ void cp_async_wait() {
 // eight in flight, one commit group per vector, and visits each as soon as
 // its group has landed (a thread reads only what it copied itself, so no
 // barrier is needed before the block's next one).
-template <typename F>
+template <int NT = kSelThreads, typename F>
 __device__ __forceinline__ void for_scores4_async(const float *__restrict__ g, float *cache, int n,
                                                   F f) {
     const int tid = threadIdx.x;
     const int n4 = n >> 2;
     const float4 *g4 = reinterpret_cast<const float4 *>(g);
     float4 *c4 = reinterpret_cast<float4 *>(cache);
-    for (int base = 0; base < n4; base += 8 * kSelThreads) {
+    for (int base = 0; base < n4; base += 8 * NT) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             if (k < n4) cp_async16(c4 + k, g4 + k);
             cp_async_commit();
         }
@@ -314,7 +316,7 @@ __device__ __forceinline__ void for_scores4_async(const float *__restrict__ g, f
             if (i == 5) cp_async_wait<2>();
             if (i == 6) cp_async_wait<1>();
             if (i == 7) cp_async_wait<0>();
-            const int k = base + i * kSelThreads + tid;
+            const int k = base + i * NT + tid;
             const bool in = k < n4;
             const float4 r = in ? c4[k] : make_float4(0.f, 0.f, 0.f, 0.f);
             f(4 * k, r.x, in);
@@ -347,7 +349,7 @@ struct WarpList {
 };
 
 // One head's MBA into mba[blockIdx.x] (written by thread 0 on every path).
-template <bool kWide>
+template <bool kWide, int NT>
 __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restrict__ scores, int T,
                                          uint32_t num, uint32_t den, int cached, int list_cap,
                                          int32_t *__restrict__ mba, uint32_t *status) {
@@ -365,7 +367,7 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
 
     // 1. exact bucket masses (and the staging copy)
     WSum<kWide> W{hist, kB0};
-    for (int i = tid; i < 2 * kB0; i += kSelThreads) hist[i] = 0u;
+    for (int i = tid; i < 2 * kB0; i += NT) hist[i] = 0u;
     if (tid == 0) s_d = -1;
     __syncthreads();
     int bad = 0;
@@ -377,22 +379,22 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
         W.add((int)(key >> 19), unit_mass(key));
     };
     if (cached && (reinterpret_cast<uintptr_t>(c) & 15) == 0)
-        for_scores4_async(c, cache, T, body);
+        for_scores4_async<NT>(c, cache, T, body);
     else if (cached)
-        for_scores4_stage(c, cache, T, body);
+        for_scores4_stage<NT>(c, cache, T, body);
     else
-        for_scores4(c, T, vec, body);
+        for_scores4<NT>(c, T, vec, body);
     __syncthreads();
 
     // 2. crossing bucket: thread t holds buckets 4095-4t .. 4092-4t (descending).
     // An invalid score adds 2^61, so one exact 128-bit total catches both it
     // and a head summing above 16.
-    u128 m4[4], ml = bad ? (u128)1 << 61 : (u128)0;
+    constexpr int kPer = kB0 / NT;   // buckets per thread
+    u128 ml = bad ? (u128)1 << 61 : (u128)0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int d = kB0 - 1 - 4 * tid - i;
-        m4[i] = shifted_mass(W.get(d), d >> 4);
-        ml += m4[i];
+    for (int i = 0; i < kPer; ++i) {
+        const int d = kB0 - 1 - kPer * tid - i;
+        ml += shifted_mass(W.get(d), d >> 4);
     }
     const u128 mpre = block_scan_excl(ml, wt128, &s_tot128);
     const u128 U128 = s_tot128;
@@ -413,10 +415,11 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
         // every partial sum is at most U <= 2^60 here
         unsigned long long run = (unsigned long long)mpre;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const unsigned long long mi = (unsigned long long)m4[i];
+        for (int i = 0; i < kPer; ++i) {
+            const int d = kB0 - 1 - kPer * tid - i;
+            const unsigned long long mi = (unsigned long long)shifted_mass(W.get(d), d >> 4);
             if (mi > 0 && (u128)den * run < need && (u128)den * (run + mi) >= need) {
-                s_d = kB0 - 1 - 4 * tid - i;
+                s_d = d;
                 s_add = run;
             }
             run += mi;
@@ -438,10 +441,10 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
     // remaining digits (bits 18..9, 8..0) from the gathered keys
     uint32_t *cnt = hist;   // [1024] counts, then the w sums [2 * 1024]
     WSum<kWide> W2{hist + 1024, 1024};
-    const int seg = list_cap / kSelWarps;
+    const int seg = list_cap / (NT / 32);
     WarpList wl{list + (tid >> 5) * seg, seg, 0};
     uint32_t cg = 0;
-    for_scores4(src, T, vec, [&](int, float v, bool in) {
+    for_scores4<NT>(src, T, vec, [&](int, float v, bool in) {
         const uint32_t key = skey(v);
         const int d = in ? (int)(key >> 19) : -1;
         cg += d > d1;
@@ -458,7 +461,7 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
         const int bits = pass == 1 ? 10 : 9, shift = pass == 1 ? 9 : 0, nb = 1 << bits;
         // the digit's counts and masses from the gathered keys (all scores
         // if a list overflowed)
-        for (int i = tid; i < 3 * 1024; i += kSelThreads) hist[i] = 0u;
+        for (int i = tid; i < 3 * 1024; i += NT) hist[i] = 0u;
         __syncthreads();
         const auto add = [&](uint32_t key) {
             if ((key >> (shift + bits)) != prefix) return;
@@ -469,21 +472,31 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
         if (lists_ok) {
             for (int i = lane; i < wl.n; i += 32) add(wl.slot[i]);
         } else {
-            for_scores4(src, T, vec, [&](int, float v, bool in) {
+            for_scores4<NT>(src, T, vec, [&](int, float v, bool in) {
                 if (in) add(skey(v));
             });
         }
         __syncthreads();
-        // thread t holds bucket nb-1-t (descending), its count in the high
-        // 64 bits and its mass (at most 2^60) in the low 64 bits
-        const int b = nb - 1 - tid;
-        const u128 pb = b >= 0 ? shifted_mass(W2.get(b), e1) | ((u128)cnt[b] << 64) : (u128)0;
-        const u128 pp = block_scan_excl(pb, wt128, &s_tot128);
-        const unsigned long long mb = (unsigned long long)pb, mp = (unsigned long long)pp;
-        if (mb > 0 && (u128)den * (A + mp) < need && (u128)den * (A + mp + mb) >= need) {
-            s_d = b;
-            s_add = mp;
-            s_cadd = (uint32_t)(pp >> 64);
+        // thread t holds buckets nb-1-per*t .. nb-per*(t+1) (descending),
+        // each as its count in the high 64 bits and its mass (at most 2^60)
+        // in the low 64 bits
+        const int per = (nb + NT - 1) / NT;
+        u128 pt = 0;
+        for (int q = 0; q < per; ++q) {
+            const int b = nb - 1 - per * tid - q;
+            if (b >= 0) pt += shifted_mass(W2.get(b), e1) | ((u128)cnt[b] << 64);
+        }
+        u128 pp = block_scan_excl(pt, wt128, &s_tot128);
+        for (int q = 0; q < per; ++q) {
+            const int b = nb - 1 - per * tid - q;
+            const u128 pb = b >= 0 ? shifted_mass(W2.get(b), e1) | ((u128)cnt[b] << 64) : (u128)0;
+            const unsigned long long mb = (unsigned long long)pb, mp = (unsigned long long)pp;
+            if (mb > 0 && (u128)den * (A + mp) < need && (u128)den * (A + mp + mb) >= need) {
+                s_d = b;
+                s_add = mp;
+                s_cadd = (uint32_t)(pp >> 64);
+            }
+            pp += pb;
         }
         __syncthreads();
         A += s_add;
@@ -635,10 +648,12 @@ __device__ long long lr_split_small(int L, long long S, bool e, long long R, lon
     unsigned long long q = 0, r = 0;
     if (e) muldiv((unsigned long long)R, equal ? 1ull : (unsigned long long)S, sumw, q, r);
     const long long left = R - (long long)warp_add(q);
-    // layers ranked before layer `warp`: larger remainder, or equal and lower index
-    const unsigned long long rw = __shfl_sync(0xffffffffu, r, warp);
-    const unsigned before = __ballot_sync(0xffffffffu, e && (r > rw || (r == rw && lane < warp)));
-    if (lane == 0) rk[warp] = __popc(before);
+    // layers ranked before layer lw: larger remainder, or equal and lower index
+    for (int lw = warp; lw < 32; lw += (int)(blockDim.x >> 5)) {
+        const unsigned long long rw = __shfl_sync(0xffffffffu, r, lw);
+        const unsigned before = __ballot_sync(0xffffffffu, e && (r > rw || (r == rw && lane < lw)));
+        if (lane == 0) rk[lw] = __popc(before);
+    }
     __syncthreads();
     const long long rank = rk[lane];
     __syncthreads();   // rk is rewritten by the next call
@@ -659,12 +674,12 @@ __device__ void layer_budgets_small(const int32_t *mba, int L, int Hkv, long lon
         return;
     }
     // S_l: warp l sums layer l's heads over its lanes
-    if (warp < L) {
+    for (int lw = warp; lw < L; lw += (int)(blockDim.x >> 5)) {
         unsigned long long acc = 0;
         for (int k = lane; k < Hkv; k += 32)
-            acc += (unsigned long long)__ldcg(mba + (int64_t)warp * Hkv + k);
+            acc += (unsigned long long)__ldcg(mba + (int64_t)lw * Hkv + k);
         acc = warp_add(acc);
-        if (lane == 0) sh[32 + warp] = (long long)acc;
+        if (lane == 0) sh[32 + lw] = (long long)acc;
     }
     __syncthreads();
     const long long S = act ? sh[32 + lane] : 0;
@@ -689,15 +704,15 @@ __device__ void layer_budgets_small(const int32_t *mba, int L, int Hkv, long lon
 // MBA of every head (one block each), then the layer budgets: the last block
 // to finish (a completion counter in the workspace, reset by that block for
 // the next launch; nothing waits on it) computes them from all heads' MBA.
-template <bool kWide>
-__global__ void __launch_bounds__(kSelThreads)
+template <bool kWide, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT)
     mba_budget_kernel(const float *__restrict__ scores, int T, uint32_t num, uint32_t den,
                       int cached, int list_cap, int32_t *__restrict__ mba, int L, int Hkv,
                       long long P, long long total, long long floor_,
                       int32_t *__restrict__ budget, uint32_t *done, uint32_t *status) {
     extern __shared__ __align__(16) uint8_t sel_smem[];
     __shared__ int s_last;
-    mba_head<kWide>(sel_smem, scores, T, num, den, cached, list_cap, mba, status);
+    mba_head<kWide, NT>(sel_smem, scores, T, num, den, cached, list_cap, mba, status);
     __syncthreads();   // the head is done with shared memory; thread 0 wrote its MBA
     if (threadIdx.x == 0) {
         // release: this block's MBA is visible before the count moves;
@@ -1110,27 +1125,40 @@ __global__ void __launch_bounds__(kSelThreads)
 
 }  // namespace
 
-// Per device: the dynamic shared memory a selection block may use (the
-// block opt-in limit less 2 KiB for the kernels' static shared memory); the
-// first call on a device raises the selection kernels' limit to it.
-int sel_smem_limit() {
+// Per device: the SM count and the dynamic shared memory a selection block
+// may use alone on an SM (the block opt-in limit) or as one of two (half the
+// SM's shared memory), each less 3 KiB for the kernels' static shared memory
+// and the per-block reservation; the first call on a device raises the
+// selection kernels' limit.
+struct SelDevice {
+    int sms = 0, smem_one = 0, smem_two_per_sm = 0;
+};
+
+SelDevice sel_device() {
     static std::mutex mu;
-    static int cache[64];
+    static SelDevice cache[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SelDevice{};
     std::lock_guard<std::mutex> lk(mu);
-    if (cache[dev] == 0) {
-        int optin = 0;
+    SelDevice &d = cache[dev];
+    if (d.smem_one == 0) {
+        int optin = 0, per_sm = 0, sms = 0;
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         const int lim = optin > 4096 ? optin - 2048 : 0;
-        cudaFuncSetAttribute(mba_budget_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             lim);
-        cudaFuncSetAttribute(mba_budget_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             lim);
+        cudaFuncSetAttribute(mba_budget_kernel<false, 1024>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+        cudaFuncSetAttribute(mba_budget_kernel<true, 1024>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+        cudaFuncSetAttribute(mba_budget_kernel<false, 512>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-        cache[dev] = lim;
+        d.sms = sms;
+        d.smem_two_per_sm = per_sm / 2 > 3072 ? min(per_sm / 2 - 3072, lim) : 0;
+        d.smem_one = lim;
     }
-    return cache[dev];
+    return d;
 }
 
 int launch_head_budget(const kvc_shape &s, const int32_t *mba, const int32_t *budget,
@@ -1171,7 +1199,14 @@ int launch_mba_budget(const kvc_shape &s, const float *scores, uint32_t num, uin
     }
     const int heads = s.n_layers * s.n_kv_heads;
     const int T = s.seq_len;
-    const int lim = sel_smem_limit();
+    const SelDevice dev = sel_device();
+    // Heads beyond one wave of 1024-thread blocks (one per SM): 512-thread
+    // blocks, two per SM, with the rows read from L2 on each pass, when the
+    // rows are short enough that 1024-thread blocks would hold them in shared
+    // memory (longer rows: the 1024-thread form is faster) and the last block
+    // has a thread per layer for the budgets.
+    const bool half = heads > dev.sms && T <= kCacheFloats && s.n_layers <= 512;
+    const int lim = half ? dev.smem_two_per_sm : dev.smem_one;
     const int hist = 2 * kB0 * 4;
     const int cached = T <= kCacheFloats && hist + T * 4 + kMinList * 4 <= lim;
     const int fixed = hist + (cached ? T * 4 : 0);
@@ -1182,14 +1217,17 @@ int launch_mba_budget(const kvc_shape &s, const float *scores, uint32_t num, uin
     const int list_cap = min(((lim - fixed) / 4) & ~3, (T + 3) & ~3);
     const size_t smem = (size_t)fixed + (size_t)list_cap * 4;
     const long long P = (long long)T - s.window;
-    if (T <= kSplitMaxT)
-        mba_budget_kernel<false><<<heads, kSelThreads, smem, st>>>(
-            scores, T, num, den, cached, list_cap, mba, s.n_layers, s.n_kv_heads, P,
-            (long long)total, (long long)floor_, budget, done, status);
+    const bool wide = T > kSplitMaxT;
+#define KVC_MBA_ARGS                                                                             \
+    scores, T, num, den, cached, list_cap, mba, s.n_layers, s.n_kv_heads, P, (long long)total, \
+        (long long)floor_, budget, done, status
+    if (half)
+        mba_budget_kernel<false, 512><<<heads, 512, smem, st>>>(KVC_MBA_ARGS);
+    else if (!wide)
+        mba_budget_kernel<false, 1024><<<heads, 1024, smem, st>>>(KVC_MBA_ARGS);
     else
-        mba_budget_kernel<true><<<heads, kSelThreads, smem, st>>>(
-            scores, T, num, den, cached, list_cap, mba, s.n_layers, s.n_kv_heads, P,
-            (long long)total, (long long)floor_, budget, done, status);
+        mba_budget_kernel<true, 1024><<<heads, 1024, smem, st>>>(KVC_MBA_ARGS);
+#undef KVC_MBA_ARGS
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_mba_budget: launch failed: %s", cudaGetErrorString(e));
@@ -1202,7 +1240,7 @@ int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, 
                 int32_t k_max, int32_t *idx, uint32_t *status, cudaStream_t st) {
     const int heads = s.n_layers * s.n_kv_heads;
     const int P = s.seq_len - s.window;
-    const int lim = sel_smem_limit();
+    const int lim = sel_device().smem_one;
     const int hist = kB0 * 4;
     const int cached = P <= kCacheFloats && hist + P * 4 + kMinList * 4 <= lim;
     const int fixed = hist + (cached ? P * 4 : 0);

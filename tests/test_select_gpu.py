@@ -275,3 +275,38 @@ def test_head_budgets_beyond_one_warp(Hkv):
     torch.cuda.synchronize()
     want = o.head_budget(mba.cpu().numpy(), bud.cpu().numpy(), P)
     assert np.array_equal(hb.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("L,H,T", [(25, 8, 3000), (50, 4, 3000), (25, 8, 30000), (50, 4, 30000)])
+def test_more_heads_than_sms(L, H, T):
+    """200 heads: more than one wave of 1024-thread blocks on a GB300 (152
+    SMs), so MBA runs as 512-thread blocks, two per SM, for rows up to 36,864
+    scores (rows of 3,000 held in shared memory, rows of 30,000 read from L2);
+    one lane per layer (25) and block-wide sums (50) for the budgets."""
+    kvc, o = K(), O()
+    W = 16
+    P = T - W
+    sc = _rows("lognormal", L, H, T, seed=L * H + T)
+    s = kvc.shape(L, H, H, 64, T, W, "f32")
+    floor = 8
+    total = L * floor + (L * P - L * floor) // 5
+    ws = torch.empty(kvc.kvc_workspace_size(s, P), dtype=torch.uint8, device="cuda")
+    kvc.kvc_workspace_init(ws)
+    scd = sc.cuda()
+    mba = torch.empty((L, H), dtype=torch.int32, device="cuda")
+    bud = torch.empty(L, dtype=torch.int32, device="cuda")
+    kvc.kvc_mba_budget(s, scd, 9, 10, total, floor, mba, bud, ws)
+    idx = torch.full((L, H, P), -1, dtype=torch.int32, device="cuda")
+    kvc.kvc_topk_select(s, scd, bud, P, idx, ws)
+    torch.cuda.synchronize()
+    assert kvc.kvc_workspace_status(ws) == 0
+    c = sc.double().numpy()
+    want_mba = np.array([[o.mba(c[l, h], 9, 10) for h in range(H)] for l in range(L)])
+    assert np.array_equal(mba.cpu().numpy(), want_mba)
+    want_bud = o.budget(want_mba, P, total, floor)
+    assert np.array_equal(bud.cpu().numpy(), want_bud)
+    got = idx.cpu().numpy()
+    for l in range(0, L, 3):
+        B = int(want_bud[l])
+        for h in range(H):
+            assert np.array_equal(got[l, h, :B], o.topk(c[l, h], P, B)), (l, h)
