@@ -52,8 +52,9 @@ __device__ __forceinline__ unsigned __int128 shfl_up(unsigned __int128 v, int o)
     return ((unsigned __int128)hi << 64) | lo;
 }
 
-// Block-wide exclusive scan of one value per thread (1024 threads); *total
-// receives the block sum.  warp_tot must hold 32 values.
+// Block-wide exclusive scan of one value per thread (a block of any multiple
+// of 32 threads up to 1024); *total receives the block sum.  warp_tot must
+// hold 32 values.
 template <typename V>
 __device__ __forceinline__ V block_scan_excl(V v, V *warp_tot, V *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -112,7 +113,8 @@ __device__ __forceinline__ unsigned long long fixed56f(float c) {
     return sh >= 0 ? (m << sh) : (sh > -64 ? (m >> -sh) : 0ull);
 }
 
-// Visit scores 0..n-1 of one head: thread tid gets k = base + i*1024 + tid,
+// Visit scores 0..n-1 of one head (NT-thread block): thread tid gets
+// k = base + i*NT + tid,
 // sixteen loads issued before any is used (latency hidden when the scores come
 // from global memory).  f(k, v, in) is called for every lane, with in false
 // past the end, so warp-wide votes inside f stay uniform.
@@ -200,7 +202,7 @@ struct WSum {
 };
 
 // Visit scores 0..n-1 of one head with 16-byte loads when src is 16-byte
-// aligned: thread tid reads vectors tid, tid + 1024, ... (coalesced), four in
+// aligned: thread tid reads vectors tid, tid + NT, ... (coalesced), four in
 // flight.  f(k, v, in) is called for every lane, with in false past the end,
 // so warp-wide votes inside f stay uniform.
 template <int NT = kSelThreads, typename F>
@@ -288,7 +290,7 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // for_scores4_stage with the copy done by cp.async: each thread copies its own
-// 16-byte vectors (tid, tid + 1024, ...) of a 16-byte aligned g into cache,
+// 16-byte vectors (tid, tid + NT, ...) of a 16-byte aligned g into cache,
 // eight in flight, one commit group per vector, and visits each as soon as
 // its group has landed (a thread reads only what it copied itself, so no
 // barrier is needed before the block's next one).
@@ -523,7 +525,8 @@ __device__ __forceinline__ void mba_head(uint8_t *sel_smem, const float *__restr
 }
 
 // ------------------------------------------------------------------ budgets
-// One block, one thread per layer (L <= 1024).  Integer arithmetic only.
+// Computed by the last MBA block to finish, one thread per layer (L up to the
+// block's threads, at most 1024).  Integer arithmetic only.
 constexpr int kMaxLayers = 1024;
 
 // floor(a*b/c) and the remainder, exact (64-bit when the product fits).
@@ -633,9 +636,9 @@ __device__ __forceinline__ unsigned long long warp_add(unsigned long long v) {
     return v;
 }
 
-// lr_split for L <= 32 by the whole 1024-thread block: lane l of every warp
-// holds layer l and every warp computes the sums alike; warp w ranks layer w's
-// remainder with one ballot, and the ranks meet in shared memory (rk: 32
+// lr_split for L <= 32 by the whole block: lane l of every warp holds layer l
+// and every warp computes the sums alike; warp w ranks layers w, w + (warps),
+// ... with one ballot each, and the ranks meet in shared memory (rk: 32
 // words).  The same arithmetic as lr_split.
 __device__ long long lr_split_small(int L, long long S, bool e, long long R, long long *rk) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -662,8 +665,8 @@ __device__ long long lr_split_small(int L, long long S, bool e, long long R, lon
     return add;
 }
 
-// layer_budgets for L <= 32 by the whole 1024-thread block (lane l of every
-// warp is layer l), the same arithmetic.  sh: 64 words of shared memory.
+// layer_budgets for L <= 32 by the whole block (lane l of every warp is layer
+// l), the same arithmetic.  sh: 64 words of shared memory.
 __device__ void layer_budgets_small(const int32_t *mba, int L, int Hkv, long long P,
                                     long long total, long long floor_,
                                     int32_t *__restrict__ budget, uint32_t *status, long long *sh) {
