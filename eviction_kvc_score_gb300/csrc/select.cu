@@ -824,11 +824,13 @@ __device__ __forceinline__ void write_kept(uint32_t gt, uint32_t eq, int j0, int
 __global__ void __launch_bounds__(kSelThreads)
     topk_kernel(const float *__restrict__ scores, int T, int P, int Hkv,
                 const int32_t *__restrict__ budget, int per_head, int k_max, int cached,
-                int list_cap, int32_t *__restrict__ idx, uint32_t *status) {
+                int staged, int list_cap, int32_t *__restrict__ idx, uint32_t *status) {
     extern __shared__ __align__(16) uint8_t sel_smem[];
     uint32_t *cnt = reinterpret_cast<uint32_t *>(sel_smem);   // [4096]
     uint32_t *list = cnt + kB0;                                 // [list_cap] keys of d1
-    float *cache = reinterpret_cast<float *>(list + list_cap);  // [P] when cached
+    // the row ([P], when cached) or one compaction round of it ([32 * 1024],
+    // when staged)
+    float *cache = reinterpret_cast<float *>(list + list_cap);
     __shared__ uint32_t warp_tot[32];
     __shared__ uint32_t s_total, s_cadd;
     __shared__ unsigned long long wt64[32], s_tot64;
@@ -902,22 +904,38 @@ __global__ void __launch_bounds__(kSelThreads)
     uint32_t prefix = d1;
     const int seg = list_cap / kSelWarps;
     WarpList wl{list + (tid >> 5) * seg, seg, 0};
-    // Rows held in shared memory (at most two compaction rounds, see below):
-    // one pass marks every position as above the chosen bucket (kept whatever
-    // v* is) or inside it (decided once v* is known) in per-thread bit masks
-    // and gathers the inside keys on the way; other rows gather in a pass of
-    // their own.
+    // Rows held in shared memory, and rows of at most four compaction rounds
+    // (see below) copied round by round into a staging buffer: one pass marks
+    // every position as above the chosen bucket (kept whatever v* is) or
+    // inside it (decided once v* is known) in per-thread bit masks and gathers
+    // the inside keys on the way.  Longer rows gather in a pass of their own.
     constexpr int kRound = 32 * kSelThreads;
-    const bool merged = cached && P <= 2 * kRound;
-    uint32_t above[2] = {0u, 0u}, inside[2] = {0u, 0u};
+    constexpr int kMaxRounds = 4;
+    const bool merged = cached || (staged && P <= kMaxRounds * kRound);
+    uint32_t above[kMaxRounds] = {0u, 0u, 0u, 0u}, inside[kMaxRounds] = {0u, 0u, 0u, 0u};
     if (merged) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < kMaxRounds; ++r) {
             if (r * kRound >= P) break;
-            const int j0 = r * kRound + 32 * tid;
+            const int n = min(P - r * kRound, kRound);   // positions of this round
+            const float *rs = cache + r * kRound;
+            if (!cached) {
+                const float *g = c + r * kRound;
+                if (vec) {
+                    const float4 *g4 = reinterpret_cast<const float4 *>(g);
+                    float4 *r4 = reinterpret_cast<float4 *>(cache);
+                    for (int k = tid; k < (n >> 2); k += kSelThreads) r4[k] = g4[k];
+                    for (int k = 4 * (n >> 2) + tid; k < n; k += kSelThreads) cache[k] = g[k];
+                } else {
+                    for (int k = tid; k < n; k += kSelThreads) cache[k] = g[k];
+                }
+                __syncthreads();
+                rs = cache;
+            }
+            const int j0 = 32 * tid;   // within the round
             uint32_t ab = 0u, in = 0u;
-            if (j0 + 32 <= P) {
-                const float4 *s4 = reinterpret_cast<const float4 *>(cache + j0);
+            if (j0 + 32 <= n) {
+                const float4 *s4 = reinterpret_cast<const float4 *>(rs + j0);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int q = (i + tid) & 7;   // rotated: distinct banks for 8 neighbours
@@ -933,8 +951,8 @@ __global__ void __launch_bounds__(kSelThreads)
                 }
             } else {
                 for (int i = 0; i < 32; ++i) {
-                    if (j0 + i < P) {
-                        const uint32_t e = skey(cache[j0 + i]) >> 19;
+                    if (j0 + i < n) {
+                        const uint32_t e = skey(rs[j0 + i]) >> 19;
                         ab |= (uint32_t)(e > d1) << i;
                         in |= (uint32_t)(e == d1) << i;
                     }
@@ -953,9 +971,10 @@ __global__ void __launch_bounds__(kSelThreads)
                 }
                 int slot = wl.n + incl - n_in;
                 for (uint32_t m = in; m; m &= m - 1u, ++slot)
-                    if (slot < seg) wl.slot[slot] = skey(cache[j0 + __ffs(m) - 1]);
+                    if (slot < seg) wl.slot[slot] = skey(rs[j0 + __ffs(m) - 1]);
                 wl.n += __shfl_sync(0xffffffffu, incl, 31);
             }
+            if (!cached) __syncthreads();   // the next round's copy overwrites the buffer
         }
     } else {
         for_scores4(src, P, vec, [&](int, float v, bool in) {
@@ -1007,10 +1026,13 @@ __global__ void __launch_bounds__(kSelThreads)
         const int j0 = base + 32 * tid;
         uint32_t gt = 0u, eq = 0u;
         if (merged) {
-            gt = base == 0 ? above[0] : above[1];
-            for (uint32_t m = base == 0 ? inside[0] : inside[1]; m; m &= m - 1u) {
+            const int r = base / kRound;
+            gt = r == 0 ? above[0] : r == 1 ? above[1] : r == 2 ? above[2] : above[3];
+            const uint32_t in =
+                r == 0 ? inside[0] : r == 1 ? inside[1] : r == 2 ? inside[2] : inside[3];
+            for (uint32_t m = in; m; m &= m - 1u) {
                 const int i = __ffs(m) - 1;
-                const uint32_t key = skey(cache[j0 + i]);
+                const uint32_t key = skey(cached ? cache[j0 + i] : c[j0 + i]);
                 gt |= (uint32_t)(key > vstar) << i;
                 eq |= (uint32_t)(key == vstar) << i;
             }
@@ -1246,7 +1268,11 @@ int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, 
     const int lim = sel_device().smem_one;
     const int hist = kB0 * 4;
     const int cached = P <= kCacheFloats && hist + P * 4 + kMinList * 4 <= lim;
-    const int fixed = hist + (cached ? P * 4 : 0);
+    // rows of at most four compaction rounds that are not held whole: a
+    // one-round staging buffer
+    const int round = 32 * kSelThreads;
+    const int staged = !cached && P <= 4 * round && hist + round * 4 + kMinList * 4 <= lim;
+    const int fixed = hist + (cached ? P * 4 : staged ? round * 4 : 0);
     if (fixed + kMinList * 4 > lim) {
         set_error("kvc_topk_select: %d bytes of shared memory per block are too few", lim);
         return KVC_ERR_UNSUPPORTED;
@@ -1254,7 +1280,8 @@ int launch_topk(const kvc_shape &s, const float *scores, const int32_t *budget, 
     const int list_cap = min(((lim - fixed) / 4) & ~3, (P + 3) & ~3);
     const size_t smem = (size_t)fixed + (size_t)list_cap * 4;
     topk_kernel<<<heads, kSelThreads, smem, st>>>(scores, s.seq_len, P, s.n_kv_heads, budget,
-                                                   per_head, k_max, cached, list_cap, idx, status);
+                                                   per_head, k_max, cached, staged, list_cap, idx,
+                                                   status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kvc_topk_select: launch failed: %s", cudaGetErrorString(e));
