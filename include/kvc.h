@@ -225,8 +225,12 @@ int kvc_compress_host(const kvc_shape *shape, const void *q_host, const void *k_
  *             layers still below T-W until none exceeds it.  If total_budget
  *             >= L*(T-W) every layer gets T-W.
  * Requires 0 <= layer_floor <= T-W, total_budget >= L*layer_floor,
- * 0 < mass_den, mass_num <= mass_den.  Scores must lie in [0,1] and sum to
- * at most 16 per head (KVC_DEV_BAD_SCORE otherwise). */
+ * 0 < mass_den, mass_num <= mass_den, L <= 1024 (KVC_ERR_UNSUPPORTED
+ * otherwise).  Scores must lie in [0,1] (-0.0 counts as 0) and sum to at
+ * most 16 per head (KVC_DEV_BAD_SCORE otherwise).  One launch: the last
+ * head to finish computes the budgets, counting finished heads in a word of
+ * the workspace header that is zero between calls (kvc_workspace_init zeroes
+ * it), so the workspace of a call in flight must not serve another. */
 int kvc_mba_budget(const kvc_shape *shape, const float *scores, uint32_t mass_num,
                    uint32_t mass_den, int64_t total_budget, int32_t layer_floor,
                    int32_t *mba, int32_t *budget, void *ws, size_t ws_bytes,
