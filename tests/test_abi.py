@@ -81,6 +81,11 @@ def test_host_side_validation_rejects_bad_arguments(lib):
     assert L.kvc_mba_budget(C.byref(s), fake, 11, 10, 1000, 64, fake, fake, fake, 4096, nul) == -1
     assert L.kvc_mba_budget(C.byref(s), fake, 9, 0, 1000, 64, fake, fake, fake, 4096, nul) == -1
     assert L.kvc_topk_select(C.byref(s), fake, fake, 0, fake, fake, 4096, nul) == -1
+    # more layers than the budgets' one-thread-per-layer block holds
+    big = _shape(kvc, n_layers=1025)
+    assert L.kvc_mba_budget(C.byref(big), fake, 9, 10, 100_000, 64, fake, fake, fake, 4096,
+                            nul) == -2
+    assert "1024" in kvc.kvc_last_error()
     assert L.kvc_channel_prune(C.byref(s), fake, fake, C.c_double(1.0), fake, fake, 10, fake,
                                4096, nul) == -1
 

@@ -150,6 +150,21 @@ def test_mba_permutation_invariant_and_rejects_bad_scores():
         O.mba(np.array([0.5, np.nan]))
 
 
+def test_negative_zero_is_the_score_zero():
+    """-0.0 compares equal to +0.0: MBA counts it as no mass and top-K ranks it
+    as a zero (ties to the lower position), against the brute-force
+    definitions."""
+    c = np.zeros(10)
+    c[[2, 5, 8]] = [0.5, 0.3, 0.2]
+    neg = c.copy()
+    neg[[0, 3, 4, 9]] = -0.0
+    assert np.signbit(neg).sum() == 4
+    for num, den in ((9, 10), (1, 1)):
+        assert O.mba(neg, num, den) == O.mba(c, num, den) == _mba_bruteforce(c, num, den)
+    for B in (2, 3, 5, 10):
+        assert O.topk(neg, 10, B).tolist() == O.topk(c, 10, B).tolist() == _topk_bruteforce(c, B)
+
+
 # --------------------------------------------------------------------------- a3
 def _hamilton_ok(S, R, a):
     """a is a largest-remainder apportionment of R by weights S: every entry
