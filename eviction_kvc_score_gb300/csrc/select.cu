@@ -1178,6 +1178,10 @@ SelDevice sel_device() {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
         cudaFuncSetAttribute(mba_budget_kernel<false, 512>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+        // two of its blocks share an SM's shared memory
+        cudaFuncSetAttribute(mba_budget_kernel<false, 512>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
         d.sms = sms;
         d.smem_two_per_sm = per_sm / 2 > 3072 ? min(per_sm / 2 - 3072, lim) : 0;
