@@ -277,12 +277,14 @@ def test_head_budgets_beyond_one_warp(Hkv):
     assert np.array_equal(hb.cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("L,H,T", [(25, 8, 3000), (50, 4, 3000), (25, 8, 30000), (50, 4, 30000)])
+@pytest.mark.parametrize("L,H,T", [(25, 8, 3000), (50, 4, 3000), (25, 8, 30000), (50, 4, 30000),
+                                   (25, 8, 3001), (25, 8, 30001)])
 def test_more_heads_than_sms(L, H, T):
     """200 heads: more than one wave of 1024-thread blocks on a GB300 (152
     SMs), so MBA runs as 512-thread blocks, two per SM, for rows up to 36,864
     scores (rows of 3,000 held in shared memory, rows of 30,000 read from L2);
-    one lane per layer (25) and block-wide sums (50) for the budgets."""
+    one lane per layer (25) and block-wide sums (50) for the budgets; rows
+    whose length is not a multiple of four take the scalar visits."""
     kvc, o = K(), O()
     W = 16
     P = T - W
